@@ -1,0 +1,359 @@
+"""Pins of the fp64 oracle against things other than itself (no GPU).
+
+Each test checks the oracle against a hand-worked fixture, a closed form, an
+invariant of the mathematics, an independent brute-force loop written here,
+or a library routine (torch's CPU scaled_dot_product_attention in float64).
+The cases are chosen so that a dropped term, a wrong sign, a wrong index or
+pairing, or a transposed operand in the oracle fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+
+def _fixture(name):
+    rows = {}
+    with open(os.path.join(GOLD, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, rest = line.split(None, 1)
+            rows[key] = rest
+    return rows
+
+
+def _eval(expr):
+    return eval(expr, {"__builtins__": {}}, {"cos": math.cos, "sin": math.sin,
+                                               "sqrt": math.sqrt})
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+
+def test_rope_rotate_half_hand_case():
+    fx = _fixture("rope_rotate_half_d4.txt")
+    x = np.array([float(t) for t in fx["x"].split()]).reshape(1, 1, 1, 4)
+    p = int(fx["p"])
+    cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=4, theta=10000.0)
+    y = oracle.rotate(x, [p], cfg).reshape(-1)
+    want = [_eval(fx[f"y{i}"]) for i in range(4)]
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-14)
+
+
+def test_rope_partial_rotary_hand_case():
+    fx = _fixture("rope_partial_d8_r4.txt")
+    x = np.array([float(t) for t in fx["x"].split()]).reshape(1, 1, 1, 8)
+    cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=8, rope_dim=4, theta=100.0)
+    y = oracle.rotate(x, [int(fx["p"])], cfg).reshape(-1)
+    want = [_eval(fx[f"y{i}"]) for i in range(8)]
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("D,R", [(16, 16), (64, 32), (128, 64)])
+def test_rope_preserves_norm_and_position_zero_is_identity(D, R):
+    L = 7
+    x = RNG.standard_normal((2, 3, L, D))
+    cfg = oracle.Cfg(B=2, H=3, Hkv=3, L=L, D=D, rope_dim=R, theta=5e5,
+                     scaling=("llama3", 8.0, 1.0, 4.0, 8192))
+    y = oracle.rotate(x, [0, 11], cfg)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1),
+                               rtol=1e-13)
+    np.testing.assert_allclose(y[0, :, 0], x[0, :, 0], rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("scaling", [None, ("linear", 4.0), ("llama3", 8.0, 1.0, 4.0, 64)])
+def test_rope_relative_position_invariance(scaling):
+    """rope(q, p+d) . rope(k, m+d) == rope(q, p) . rope(k, m): the dot product
+    depends only on p - m ("Core Layers -- Deep Reference", RoPE)."""
+    D = 32
+    q = RNG.standard_normal((1, 1, 1, D))
+    k = RNG.standard_normal((1, 1, 1, D))
+    cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=D, theta=1e4, scaling=scaling)
+
+    def dot(p, m):
+        return float((oracle.rotate(q, [p], cfg) * oracle.rotate(k, [m], cfg)).sum())
+
+    base = dot(9, 4)
+    for d in (1, 17, 300, 4095):
+        assert abs(dot(9 + d, 4 + d) - base) < 1e-9
+    assert abs(dot(9, 5) - base) > 1e-6     # it does depend on p - m
+
+
+def test_rope_linear_scaling_is_position_division():
+    D, f = 16, 4.0
+    x = RNG.standard_normal((1, 2, 1, D))
+    lin = oracle.Cfg(B=1, H=2, Hkv=2, L=1, D=D, theta=1e4, scaling=("linear", f))
+    plain = oracle.Cfg(B=1, H=2, Hkv=2, L=1, D=D, theta=1e4)
+    for k in (1, 5, 250):
+        np.testing.assert_allclose(oracle.rotate(x, [int(f) * k], lin),
+                                   oracle.rotate(x, [k], plain), rtol=0, atol=1e-12)
+
+
+def test_llama3_scaling_special_cases():
+    """The Llama-3 ramp: factor 1 is no scaling; short wavelengths are kept;
+    long ones are divided by the factor; the ramp is continuous at both ends."""
+    D, theta = 128, 5e5
+    plain = oracle.inv_freq(oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=D, theta=theta))
+    one = oracle.inv_freq(oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=D, theta=theta,
+                                     scaling=("llama3", 1.0, 1.0, 4.0, 8192)))
+    np.testing.assert_allclose(one, plain, rtol=1e-15)
+
+    orig, lo, hi, fac = 8192.0, 1.0, 4.0, 8.0
+    sc = oracle.inv_freq(oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=D, theta=theta,
+                                    scaling=("llama3", fac, lo, hi, orig)))
+    wl = 2 * math.pi / plain
+    short = wl < orig / hi
+    long_ = wl > orig / lo
+    assert short.any() and long_.any() and (~short & ~long_).any()
+    np.testing.assert_array_equal(sc[short], plain[short])
+    np.testing.assert_allclose(sc[long_], plain[long_] / fac, rtol=1e-15)
+    mid = ~short & ~long_
+    # inside the ramp the frequency lies between the two branches
+    assert np.all(sc[mid] <= plain[mid]) and np.all(sc[mid] >= plain[mid] / fac)
+
+    # continuity: move the base so one frequency's wavelength crosses each end
+    for edge in (orig / hi, orig / lo):
+        i = 1
+        # theta such that 2*pi / theta^(-2i/D) == edge
+        th_edge = (edge / (2 * math.pi)) ** (D / (2 * i))
+        vals = []
+        for th in (th_edge * (1 - 1e-9), th_edge * (1 + 1e-9)):
+            cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=D, theta=th,
+                             scaling=("llama3", fac, lo, hi, orig))
+            vals.append(oracle.inv_freq(cfg)[i])
+        assert abs(vals[0] - vals[1]) <= 1e-7 * abs(vals[0])
+
+
+# ----------------------------------------------------------------------------- RMSNorm
+
+
+def test_rmsnorm_hand_case():
+    fx = _fixture("rmsnorm_d2.txt")
+    x = np.array([float(t) for t in fx["x"].split()]).reshape(1, 1, 1, 2)
+    w = np.array([float(t) for t in fx["w"].split()])
+    cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=2, rope_dim=0, norm_eps=0.0)
+    y = oracle.rotate(x, [0], cfg, norm_w=w).reshape(-1)
+    np.testing.assert_allclose(y, [_eval(fx["y0"]), _eval(fx["y1"])], rtol=1e-15)
+
+
+def test_rmsnorm_unit_rms_and_scale_invariance():
+    D = 64
+    x = RNG.standard_normal((1, 2, 3, D))
+    w = 1.0 + 0.1 * RNG.standard_normal(D)
+    cfg = oracle.Cfg(B=1, H=2, Hkv=2, L=3, D=D, rope_dim=0, norm_eps=0.0)
+    y = oracle.rotate(x, [0], cfg, norm_w=w)
+    np.testing.assert_allclose(np.sqrt(np.mean((y / w) ** 2, axis=-1)), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle.rotate(37.5 * x, [0], cfg, norm_w=w), y, rtol=1e-13)
+
+
+def test_norm_comes_before_rope():
+    """q/k RMSNorm runs before RoPE ("mojolearn.transformer", qk_norm)."""
+    D = 8
+    x = RNG.standard_normal((1, 1, 1, D))
+    w = np.arange(1, D + 1, dtype=np.float64)       # not rotation-symmetric
+    cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=D, theta=10.0, norm_eps=0.0)
+    y = oracle.rotate(x, [5], cfg, norm_w=w)
+    normed = x / np.sqrt(np.mean(x ** 2)) * w
+    rot_only = oracle.rotate(normed, [5], cfg)
+    np.testing.assert_allclose(y, rot_only, rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------- attention
+
+
+def brute_force(q, k, v, start, H, Hkv, window=0, softcap=0.0, scale=None):
+    """Independent per-query loop: explicit repeat-KV, a materialised mask."""
+    B, _, L, D = q.shape
+    G = H // Hkv
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = np.zeros_like(q)
+    for b in range(B):
+        pos = [start[b] + j for j in range(L)]
+        mask = [[(pos[j] <= pos[i]) and (window == 0 or pos[j] > pos[i] - window)
+                 for j in range(L)] for i in range(L)]
+        for h in range(H):
+            kk = [list(k[b, h // G, j]) for j in range(L)]        # repeat-KV
+            vv = [list(v[b, h // G, j]) for j in range(L)]
+            for i in range(L):
+                qi = list(q[b, h, i])
+                logits = []
+                for j in range(L):
+                    s = sum(a * c for a, c in zip(qi, kk[j])) * scale
+                    if softcap > 0:
+                        s = softcap * math.tanh(s / softcap)
+                    logits.append(s if mask[i][j] else -math.inf)
+                m = max(logits)
+                e = [math.exp(s - m) if s != -math.inf else 0.0 for s in logits]
+                z = sum(e)
+                for d in range(D):
+                    out[b, h, i, d] = sum(e[j] * vv[j][d] for j in range(L)) / z
+    return out
+
+
+@pytest.mark.parametrize("H,Hkv,L,D,window,softcap,start", [
+    (4, 2, 9, 4, 0, 0.0, (0,)),
+    (4, 2, 9, 6, 3, 0.0, (0,)),
+    (6, 2, 8, 4, 0, 2.0, (0, 5)),
+    (4, 1, 7, 8, 2, 1.5, (3,)),
+    (2, 2, 5, 2, 1, 0.0, (0,)),
+])
+def test_attention_matches_brute_force(H, Hkv, L, D, window, softcap, start):
+    B = len(start)
+    q = 2.0 * RNG.standard_normal((B, H, L, D))
+    k = 2.0 * RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=window, softcap=softcap)
+    got = oracle.attention(q, k, v, list(start), cfg)
+    want = brute_force(q, k, v, list(start), H, Hkv, window, softcap)
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,D", [(2, 8, 2, 37, 16), (1, 4, 4, 20, 32), (1, 8, 1, 33, 8)])
+def test_attention_matches_torch_sdpa(B, H, Hkv, L, D):
+    q = RNG.standard_normal((B, H, L, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D)
+    got = oracle.attention(q, k, v, [0] * B, cfg)
+    want = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), is_causal=True,
+        enable_gqa=True).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+def test_explicit_scale_matches_torch_sdpa():
+    B, H, Hkv, L, D = 1, 4, 2, 12, 8
+    q, k, v = (RNG.standard_normal((B, n, L, D)) for n in (H, Hkv, Hkv))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, scale=0.3)
+    got = oracle.attention(q, k, v, [0], cfg)
+    want = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), is_causal=True,
+        enable_gqa=True, scale=0.3).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+def test_gqa_equals_mha_over_repeated_kv():
+    B, H, Hkv, L, D = 1, 8, 2, 11, 8
+    q = RNG.standard_normal((B, H, L, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    gqa = oracle.attention(q, k, v, [0], oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=4,
+                                                    softcap=3.0))
+    krep, vrep = np.repeat(k, H // Hkv, axis=1), np.repeat(v, H // Hkv, axis=1)
+    mha = oracle.attention(q, krep, vrep, [0], oracle.Cfg(B=B, H=H, Hkv=H, L=L, D=D, window=4,
+                                                          softcap=3.0))
+    np.testing.assert_allclose(gqa, mha, rtol=0, atol=0)
+
+
+def test_special_cases():
+    B, H, Hkv, L, D = 1, 4, 2, 10, 8
+    q = 3 * RNG.standard_normal((B, H, L, D))
+    k = 3 * RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    causal = oracle.attention(q, k, v, [0], oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D))
+    # position 0 sees only itself
+    for h in range(H):
+        np.testing.assert_array_equal(causal[0, h, 0], v[0, h // 2, 0])
+    # window 1: every query sees only itself
+    w1 = oracle.attention(q, k, v, [0], oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=1))
+    for h in range(H):
+        np.testing.assert_array_equal(w1[0, h], v[0, h // 2])
+    # a window as long as the sequence is plain causal
+    wl = oracle.attention(q, k, v, [0], oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=L))
+    np.testing.assert_array_equal(wl, causal)
+    # a huge softcap is no softcap
+    big = oracle.attention(q, k, v, [0], oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D,
+                                                    softcap=1e9))
+    np.testing.assert_allclose(big, causal, rtol=1e-9, atol=1e-12)
+    # a small softcap does change the result
+    small = oracle.attention(q, k, v, [0], oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D,
+                                                      softcap=0.5))
+    assert np.abs(small - causal).max() > 1e-3
+
+
+def test_window_width_fixture():
+    fx = _fixture("window_mean_l8_w3.txt")
+    ps = [int(t) for t in fx["p"].split()]
+    want = [float(t) for t in fx["mean"].split()]
+    L, D = len(ps), 2
+    q = RNG.standard_normal((1, 1, L, D))
+    k = np.ones((1, 1, L, D))                     # every key equal
+    v = np.zeros((1, 1, L, D))
+    v[0, 0, :, 0] = np.arange(L)
+    out = oracle.attention(q, k, v, [0], oracle.Cfg(B=1, H=1, Hkv=1, L=L, D=D, window=3))
+    np.testing.assert_allclose(out[0, 0, :, 0], want, rtol=0, atol=1e-14)
+
+
+def test_softcap_two_key_closed_form():
+    """Two keys: softmax of c*tanh(s/c) written out by hand."""
+    D, c = 2, 1.5
+    q = np.array([[[[2.0, 0.0], [1.0, -1.0]]]])
+    k = np.array([[[[0.5, 1.0], [3.0, 2.0]]]])
+    v = np.array([[[[1.0, 0.0], [0.0, 1.0]]]])
+    out = oracle.attention(q, k, v, [0], oracle.Cfg(B=1, H=1, Hkv=1, L=2, D=D, softcap=c))
+    sc = 1 / math.sqrt(2)
+    s0 = c * math.tanh((1.0 * 0.5 - 1.0 * 1.0) * sc / c)
+    s1 = c * math.tanh((1.0 * 3.0 - 1.0 * 2.0) * sc / c)
+    w1 = math.exp(s1) / (math.exp(s0) + math.exp(s1))
+    np.testing.assert_allclose(out[0, 0, 1], [1 - w1, w1], rtol=1e-14)
+
+
+# ----------------------------------------------------------------------------- cache and decode
+
+
+@pytest.mark.parametrize("window,L", [(0, 12), (5, 12), (4, 3), (12, 12)])
+def test_carried_decode_equals_prefill(window, L):
+    """Token-by-token decode over a carried cache gives the prefill's rows
+    ("mojolearn.transformer": step is forward with L = 1 at cached_tokens)."""
+    B, H, Hkv, D = 2, 4, 2, 8
+    q = RNG.standard_normal((B, H, L, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    full = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, theta=100.0, window=window, softcap=2.0)
+    want, qr, kr = oracle.prefill(q, k, v, [0] * B, full)
+    cap = window if window else L
+    one = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=1, D=D, theta=100.0, window=window, softcap=2.0)
+    kc = vc = wr = None
+    for t in range(L):
+        kt = oracle.rotate(k[:, :, t:t + 1], [t] * B, one)
+        qt = oracle.rotate(q[:, :, t:t + 1], [t] * B, one)
+        kc, vc, wr = oracle.append(kt, v[:, :, t:t + 1], [t] * B, one, cap, kc, vc, wr)
+        got = oracle.decode(qt, kc, vc, [t + 1] * B, one)
+        np.testing.assert_allclose(got[:, :, 0], want[:, :, t], rtol=1e-12, atol=1e-13)
+
+
+def test_ring_slots_hold_the_last_window_positions():
+    """Under a window the cache is a ring of W slots, slot = position % W
+    ("mojolearn.transformer", TransformerState)."""
+    B, Hkv, L, D, W = 1, 2, 11, 4, 4
+    kr = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    cfg = oracle.Cfg(B=B, H=Hkv, Hkv=Hkv, L=L, D=D, window=W)
+    kc, vc, wr = oracle.append(kr, v, [0], cfg, W)
+    for s in range(W):
+        m = max(p for p in range(L) if p % W == s)
+        assert (wr[0, :, s] == m).all()
+        np.testing.assert_array_equal(vc[0, :, s], v[0, :, m])
+    # in ascending position order, the slots are the last W positions
+    order = sorted(range(W), key=lambda s: wr[0, 0, s])
+    assert [wr[0, 0, s] for s in order] == list(range(L - W, L))
+
+
+def test_append_full_cache_positions():
+    B, Hkv, L, D = 2, 1, 5, 4
+    kr = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    cfg = oracle.Cfg(B=B, H=1, Hkv=Hkv, L=L, D=D)
+    kc, vc, wr = oracle.append(kr, v, [0, 3], cfg, 9)
+    assert list(wr[0, 0]) == [0, 1, 2, 3, 4, -1, -1, -1, -1]
+    assert list(wr[1, 0]) == [-1, -1, -1, 3, 4, 5, 6, 7, -1]
+    np.testing.assert_array_equal(kc[1, 0, 3:8], kr[1, 0])
