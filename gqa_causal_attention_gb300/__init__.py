@@ -1,0 +1,243 @@
+"""Python binding of libgqa_attn.so: grouped-query causal attention on GB300.
+
+Every function here has the name of the C entry point it wraps (see
+``include/gqa_attn.h``) and does argument marshalling only: it checks dtypes,
+devices and contiguity, passes device pointers and the current CUDA stream,
+and raises ``AttnError`` on a non-zero return code. All arithmetic runs in the
+library's CUDA kernels; there is no fallback of any kind. If the library is
+missing or cannot load, every call raises.
+
+PyTorch provides device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "AttnError", "RopeParams", "load", "library_path",
+    "attn_rope_table_bytes", "attn_rope_table_init", "attn_rope_apply", "kv_cache_append",
+    "gqa_attn_prefill", "gqa_attn_decode_workspace_size", "gqa_attn_decode",
+    "attn_status_string", "attn_version", "rope_table", "ROPE_SCALING",
+    "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
+]
+
+DEV_POSITION, DEV_CAPACITY, DEV_LENGTH, DEV_TIMEOUT = 1, 2, 4, 8
+ROPE_SCALING = {None: 0, "none": 0, "linear": 1, "llama3": 2}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        super().__init__(f"{fn}: {attn_status_string(code)} (code {code})")
+        self.code = code
+
+
+class RopeParams(ctypes.Structure):
+    """Mirror of ``attn_rope_params``."""
+    _fields_ = [
+        ("theta", ctypes.c_double),
+        ("rope_dim", ctypes.c_int32),
+        ("max_positions", ctypes.c_int32),
+        ("scaling_type", ctypes.c_int32),
+        ("original_max_positions", ctypes.c_int32),
+        ("factor", ctypes.c_double),
+        ("low_freq_factor", ctypes.c_double),
+        ("high_freq_factor", ctypes.c_double),
+    ]
+
+    @classmethod
+    def make(cls, theta=10000.0, rope_dim=0, max_positions=8192, scaling=None):
+        """scaling: None, ("linear", f) or ("llama3", factor, low, high, original_max)."""
+        p = cls(theta=float(theta), rope_dim=int(rope_dim), max_positions=int(max_positions),
+                scaling_type=0, original_max_positions=0, factor=1.0, low_freq_factor=1.0,
+                high_freq_factor=1.0)
+        if scaling is not None:
+            p.scaling_type = ROPE_SCALING[scaling[0]]
+            if scaling[0] == "linear":
+                p.factor = float(scaling[1])
+            elif scaling[0] == "llama3":
+                p.factor, p.low_freq_factor, p.high_freq_factor = map(float, scaling[1:4])
+                p.original_max_positions = int(scaling[4])
+        return p
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libgqa_attn.so (building it first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB
+        lib = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        rp = ctypes.POINTER(RopeParams)
+        f = ctypes.c_float
+        sig = {
+            "attn_rope_table_bytes": (sz, [rp, i32]),
+            "attn_rope_table_init": (i32, [rp, i32, vp, sz, vp]),
+            "attn_rope_apply": (i32, [vp, i32, i32, i32, i32, vp, ctypes.c_int32, rp, vp, vp, f,
+                                      vp, vp]),
+            "kv_cache_append": (i32, [vp, vp, i32, i32, i32, i32, vp, ctypes.c_int32, rp, vp,
+                                      vp, f, vp, vp, i32, i32, vp, vp]),
+            "gqa_attn_prefill": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f, f, vp,
+                                       vp]),
+            "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+            "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
+                                      i32, i32, f, f, vp, sz, vp, vp]),
+            "attn_status_string": (ctypes.c_char_p, [i32]),
+            "attn_version": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _ptr(t) -> ctypes.c_void_p | None:
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _f32(name: str, t, ndim: int | None = None):
+    if t is None:
+        return
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+
+
+def _i32(name: str, t):
+    if t is None:
+        return
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise TypeError(f"{name} must be a contiguous CUDA int32 tensor")
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise AttnError(fn, rc)
+
+
+def attn_status_string(code: int) -> str:
+    return load().attn_status_string(int(code)).decode()
+
+
+def attn_version() -> str:
+    return load().attn_version().decode()
+
+
+def attn_rope_table_bytes(params: RopeParams, D: int) -> int:
+    return int(load().attn_rope_table_bytes(ctypes.byref(params), int(D)))
+
+
+def attn_rope_table_init(params: RopeParams, D: int, table: torch.Tensor, stream=None) -> None:
+    _f32("table", table)
+    rc = load().attn_rope_table_init(ctypes.byref(params), int(D), _ptr(table),
+                                     table.numel() * 4, _stream(stream))
+    _check("attn_rope_table_init", rc)
+
+
+def rope_table(params: RopeParams, D: int, device="cuda", stream=None) -> torch.Tensor:
+    """Allocate (with torch) and fill the cos/sin table for ``params``."""
+    n = attn_rope_table_bytes(params, D)
+    if n == 0:
+        raise AttnError("attn_rope_table_bytes", -7)
+    t = torch.empty(n // 4, dtype=torch.float32, device=device)
+    attn_rope_table_init(params, D, t, stream)
+    return t
+
+
+def attn_rope_apply(x, start, max_start: int, params: RopeParams, table, norm_w=None,
+                    norm_eps: float = 1e-6, status=None, stream=None) -> None:
+    """In place on x [B, Hx, L, D]: optional RMSNorm (norm_w), then RoPE at start[b] + l."""
+    _f32("x", x, 4); _f32("table", table); _f32("norm_w", norm_w); _i32("start", start)
+    _i32("status", status)
+    B, Hx, L, D = x.shape
+    rc = load().attn_rope_apply(_ptr(x), B, Hx, L, D, _ptr(start), int(max_start),
+                                ctypes.byref(params), _ptr(table), _ptr(norm_w),
+                                float(norm_eps), _ptr(status), _stream(stream))
+    _check("attn_rope_apply", rc)
+
+
+def kv_cache_append(k, v, start, max_start: int, params, table, k_norm_w, norm_eps, k_cache,
+                    v_cache, window: int = 0, status=None, stream=None) -> None:
+    """Rotate k [B, Hkv, L, D] in place (if params) and store k, v at their cache slots."""
+    _f32("k", k, 4); _f32("v", v, 4); _f32("k_cache", k_cache, 4); _f32("v_cache", v_cache, 4)
+    _f32("table", table); _f32("k_norm_w", k_norm_w); _i32("start", start)
+    _i32("status", status)
+    B, Hkv, L, D = k.shape
+    if tuple(v.shape) != (B, Hkv, L, D) or k_cache.shape != v_cache.shape \
+            or tuple(k_cache.shape[:2]) != (B, Hkv) or k_cache.shape[3] != D:
+        raise ValueError("kv_cache_append: inconsistent shapes")
+    rc = load().kv_cache_append(_ptr(k), _ptr(v), B, Hkv, L, D, _ptr(start), int(max_start),
+                                None if params is None else ctypes.byref(params), _ptr(table),
+                                _ptr(k_norm_w), float(norm_eps), _ptr(k_cache), _ptr(v_cache),
+                                int(k_cache.shape[2]), int(window), _ptr(status),
+                                _stream(stream))
+    _check("kv_cache_append", rc)
+
+
+def gqa_attn_prefill(q, k, v, out, window: int = 0, softcap: float = 0.0, scale: float = 0.0,
+                     status=None, stream=None) -> None:
+    """out [B, H, L, D] = causal (or windowed) GQA attention of rotated q, k and v."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _f32(n, t, 4)
+    _i32("status", status)
+    B, H, L, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, L, D) or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("gqa_attn_prefill: inconsistent shapes")
+    rc = load().gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, L, D,
+                                 int(window), float(softcap), float(scale), _ptr(status),
+                                 _stream(stream))
+    _check("gqa_attn_prefill", rc)
+
+
+def gqa_attn_decode_workspace_size(B: int, H: int, Hkv: int, D: int, max_cache_len: int,
+                                   window: int = 0) -> int:
+    return int(load().gqa_attn_decode_workspace_size(B, H, Hkv, D, int(max_cache_len),
+                                                     int(window)))
+
+
+def gqa_attn_decode(q, k_cache, v_cache, cache_len, max_cache_len: int, out, window: int = 0,
+                    softcap: float = 0.0, scale: float = 0.0, workspace=None, status=None,
+                    stream=None) -> None:
+    """out [B, H, 1, D]: one query per row against the first cache_len[b] positions."""
+    _f32("q", q, 4); _f32("out", out, 4); _f32("k_cache", k_cache, 4)
+    _f32("v_cache", v_cache, 4); _i32("cache_len", cache_len); _i32("status", status)
+    B, H, one, D = q.shape
+    Bc, Hkv, cap, Dc = k_cache.shape
+    if one != 1 or Bc != B or Dc != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("gqa_attn_decode: inconsistent shapes")
+    if workspace is not None and (not workspace.is_cuda or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load().gqa_attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
+                                int(max_cache_len), _ptr(out), B, H, Hkv, D, cap, int(window),
+                                float(softcap), float(scale), _ptr(workspace), wbytes,
+                                _ptr(status), _stream(stream))
+    _check("gqa_attn_decode", rc)

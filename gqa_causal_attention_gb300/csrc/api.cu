@@ -1,0 +1,213 @@
+// C ABI of libgqa_attn.so: argument checks on the host, then kernel launches.
+// Nothing here allocates device memory or synchronises a stream.
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/gqa_attn.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr double kPi = 3.14159265358979323846;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int max_pos_of(const attn_rope_params* rp) {
+  return rp->max_positions > 0 ? rp->max_positions : 8192;
+}
+
+int rope_dim_of(const attn_rope_params* rp, int D) { return rp->rope_dim > 0 ? rp->rope_dim : D; }
+
+bool rope_params_ok(const attn_rope_params* rp, int D) {
+  if (!rp) return false;
+  if (!(rp->theta > 0.0) || !isfinite(rp->theta)) return false;
+  if (rp->rope_dim < 0 || rp->max_positions < 0) return false;
+  const int R = rope_dim_of(rp, D);
+  if (R % 2 != 0 || R > D || R < 2) return false;
+  switch (rp->scaling_type) {
+    case ATTN_ROPE_SCALING_NONE:
+      return true;
+    case ATTN_ROPE_SCALING_LINEAR:
+      return rp->factor > 0.0 && isfinite(rp->factor);
+    case ATTN_ROPE_SCALING_LLAMA3:
+      return rp->factor > 0.0 && isfinite(rp->factor) && rp->low_freq_factor > 0.0 &&
+             rp->high_freq_factor > rp->low_freq_factor && isfinite(rp->high_freq_factor) &&
+             rp->original_max_positions > 0;
+    default:
+      return false;
+  }
+}
+
+// theta_i = theta^(-2i/R), then the scaling rule of attn_rope_params.
+void inv_freq(const attn_rope_params* rp, int R, gqa::InvFreq* out) {
+  for (int i = 0; i < R / 2; ++i) {
+    double f = pow(rp->theta, -2.0 * i / (double)R);
+    if (rp->scaling_type == ATTN_ROPE_SCALING_LINEAR) {
+      f /= rp->factor;
+    } else if (rp->scaling_type == ATTN_ROPE_SCALING_LLAMA3) {
+      const double orig = (double)rp->original_max_positions;
+      const double wl = 2.0 * kPi / f;
+      if (wl > orig / rp->low_freq_factor) {
+        f /= rp->factor;
+      } else if (wl >= orig / rp->high_freq_factor) {
+        const double s = (orig / wl - rp->low_freq_factor) /
+                         (rp->high_freq_factor - rp->low_freq_factor);
+        f = (1.0 - s) * f / rp->factor + s * f;
+      }
+    }
+    out->v[i] = f;
+  }
+}
+
+bool dims_ok(int B, int Hx, int L, int D) {
+  return B >= 0 && Hx >= 1 && L >= 0 && D >= 2 && D <= gqa::kMaxHeadDim && D % 2 == 0;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* attn_version(void) { return "0.1.0"; }
+
+const char* attn_status_string(int code) {
+  switch (code) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_NULL: return "a required pointer is NULL";
+    case ATTN_ERR_SHAPE: return "sizes break the shape rules";
+    case ATTN_ERR_POSITION: return "a position reaches max_positions";
+    case ATTN_ERR_CAPACITY: return "a position has no cache slot";
+    case ATTN_ERR_WORKSPACE: return "decode workspace missing or too small";
+    case ATTN_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case ATTN_ERR_PARAM: return "invalid RoPE parameters or table";
+    case ATTN_ERR_CUDA: return "a CUDA launch failed";
+    default: return "unknown status";
+  }
+}
+
+size_t attn_rope_table_bytes(const attn_rope_params* rp, int D) {
+  if (!rope_params_ok(rp, D) || D > gqa::kMaxHeadDim) return 0;
+  return (size_t)max_pos_of(rp) * (size_t)(rope_dim_of(rp, D) / 2) * 2 * sizeof(float);
+}
+
+int attn_rope_table_init(const attn_rope_params* rp, int D, float* table, size_t table_bytes,
+                         void* stream) {
+  if (!rp || !table) return ATTN_ERR_NULL;
+  if (D < 2 || D > gqa::kMaxHeadDim || D % 2) return ATTN_ERR_SHAPE;
+  const size_t need = attn_rope_table_bytes(rp, D);
+  if (need == 0 || table_bytes < need) return ATTN_ERR_PARAM;
+  if (!aligned16(table)) return ATTN_ERR_ALIGN;
+  gqa::InvFreq inv;
+  const int R = rope_dim_of(rp, D);
+  inv_freq(rp, R, &inv);
+  return cuda_status(gqa::launch_rope_table(inv, R, max_pos_of(rp), reinterpret_cast<float2*>(table),
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int attn_rope_apply(float* x, int B, int Hx, int L, int D, const int32_t* start,
+                    int32_t max_start, const attn_rope_params* rp, const float* table,
+                    const float* norm_w, float norm_eps, int32_t* status, void* stream) {
+  if (!rp || !table) return ATTN_ERR_NULL;
+  if (!dims_ok(B, Hx, L, D)) return ATTN_ERR_SHAPE;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!x || !start) return ATTN_ERR_NULL;
+  if (!rope_params_ok(rp, D) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
+  if (!aligned16(x) || !aligned16(table) || (norm_w && !aligned16(norm_w))) return ATTN_ERR_ALIGN;
+  if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_pos_of(rp))
+    return ATTN_ERR_POSITION;
+  gqa::RopeJob j{};
+  j.x = x; j.B = B; j.NH = Hx; j.L = L; j.D = D; j.R = rope_dim_of(rp, D);
+  j.start = start; j.max_positions = max_pos_of(rp);
+  j.table = reinterpret_cast<const float2*>(table);
+  j.norm_w = norm_w; j.norm_eps = norm_eps; j.status = status;
+  return cuda_status(gqa::launch_rope_rows(j, static_cast<cudaStream_t>(stream)));
+}
+
+int kv_cache_append(float* k, const float* v, int B, int Hkv, int L, int D,
+                    const int32_t* start, int32_t max_start, const attn_rope_params* rp,
+                    const float* table, const float* k_norm_w, float norm_eps, float* k_cache,
+                    float* v_cache, int capacity, int window, int32_t* status, void* stream) {
+  if (!dims_ok(B, Hkv, L, D) || capacity < 1 || window < 0) return ATTN_ERR_SHAPE;
+  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!k || !v || !start || !k_cache || !v_cache) return ATTN_ERR_NULL;
+  if (rp ? !table : (table || k_norm_w)) return rp ? ATTN_ERR_NULL : ATTN_ERR_PARAM;
+  if (rp && !rope_params_ok(rp, D)) return ATTN_ERR_PARAM;
+  if (!(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (table && !aligned16(table)) || (k_norm_w && !aligned16(k_norm_w)))
+    return ATTN_ERR_ALIGN;
+  const int max_positions = rp ? max_pos_of(rp) : 0x7fffffff;
+  if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_positions)
+    return ATTN_ERR_POSITION;
+  if (window == 0 && (int64_t)max_start + L > (int64_t)capacity) return ATTN_ERR_CAPACITY;
+  gqa::RopeJob j{};
+  j.x = k; j.B = B; j.NH = Hkv; j.L = L; j.D = D; j.R = rp ? rope_dim_of(rp, D) : D;
+  j.start = start; j.max_positions = max_positions;
+  j.table = reinterpret_cast<const float2*>(table);
+  j.norm_w = k_norm_w; j.norm_eps = norm_eps; j.status = status;
+  j.v = v; j.k_cache = k_cache; j.v_cache = v_cache; j.capacity = capacity; j.window = window;
+  return cuda_status(gqa::launch_rope_rows(j, static_cast<cudaStream_t>(stream)));
+}
+
+int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out, int B, int H,
+                     int Hkv, int L, int D, int window, float softcap, float scale,
+                     int32_t* status, void* stream) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!q || !k || !v || !out) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return ATTN_ERR_ALIGN;
+  gqa::AttnShape a{};
+  a.q = q; a.k = k; a.v = v; a.out = out;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.L = L; a.D = D;
+  a.window = window; a.softcap = softcap > 0.f ? softcap : 0.f;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  a.status = status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (gqa::prefill_tc_supports(D)) return cuda_status(gqa::launch_prefill_tc(a, s));
+  return cuda_status(gqa::launch_prefill_simt(a, s));
+}
+
+size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cache_len,
+                                      int window) {
+  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv || D < 2 || max_cache_len < 1 || window < 0) return 0;
+  int nsplit, chunk;
+  gqa::decode_split_plan(B, Hkv, max_cache_len, window, &nsplit, &chunk);
+  if (nsplit <= 1) return 16;      // never read; a non-empty buffer keeps the rule simple
+  return (size_t)B * H * nsplit * (D + 2) * sizeof(float);
+}
+
+int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
+                    const int32_t* cache_len, int32_t max_cache_len, float* out, int B, int H,
+                    int Hkv, int D, int capacity, int window, float softcap, float scale,
+                    void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  if (!dims_ok(B, H, 1, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || capacity < 1)
+    return ATTN_ERR_SHAPE;
+  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (B == 0) return ATTN_OK;
+  if (max_cache_len < 1) return ATTN_ERR_SHAPE;
+  if (window == 0 && max_cache_len > capacity) return ATTN_ERR_CAPACITY;
+  if (!q || !k_cache || !v_cache || !cache_len || !out) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return ATTN_ERR_ALIGN;
+  gqa::DecodeJob j{};
+  j.q = q; j.k_cache = k_cache; j.v_cache = v_cache; j.cache_len = cache_len;
+  j.max_cache_len = max_cache_len; j.out = out;
+  j.B = B; j.H = H; j.Hkv = Hkv; j.D = D; j.capacity = capacity; j.window = window;
+  j.softcap = softcap > 0.f ? softcap : 0.f;
+  j.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  j.status = status;
+  gqa::decode_split_plan(B, Hkv, max_cache_len, window, &j.nsplit, &j.chunk);
+  if (j.nsplit > 1) {
+    const size_t need = gqa_attn_decode_workspace_size(B, H, Hkv, D, max_cache_len, window);
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  }
+  j.partial = static_cast<float*>(workspace);
+  return cuda_status(gqa::launch_decode(j, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,267 @@
+// Single-token decode over a caller-owned cache, split over the key axis.
+//
+// "mojolearn.transformer", TransformerBlock.step: one new token per row at
+// position cached_tokens, attending every cached position (or the last W of
+// them under a window; the cache is then a ring of W slots, TransformerState).
+// Softmax attention is invariant to the order of its keys, so the live slots
+// of a ring are read in slot order.
+//
+// Split-KV: block (split, kv-head group, b) reduces `chunk` cache slots for
+// the GT query heads that share one KV head, so every K/V byte is read once
+// for the whole group. Each block leaves (m, l, o) partial results -- row
+// maximum and sum in base 2, unnormalised output -- and the combine kernel
+// merges them with the usual log-sum-exp rescaling. A row that fits in one
+// split is finished by its split block directly.
+//
+// The work is HBM-bound: 2 * D * 4 bytes per cached position and KV head.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gqa {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kDecodeThreads = 128;
+constexpr int kDecodeWarps = kDecodeThreads / 32;
+constexpr int kUnroll = 4;          // keys per warp per step
+
+// Lane-to-dimension map. V4: lane owns dims 4*lane + 128*k .. +3 (D % 128 == 0);
+// otherwise lane owns dims lane + 32*k (any D <= 256).
+template <bool V4, int NV>
+struct Dims {
+  static __device__ __forceinline__ int dim(int lane, int e) {
+    return V4 ? (4 * lane + 128 * (e / 4) + (e % 4)) : (lane + 32 * e);
+  }
+  static __device__ __forceinline__ void load(const float* __restrict__ row, int lane, int D,
+                                              float* r) {
+    if (V4) {
+#pragma unroll
+      for (int k = 0; k < NV / 4; ++k) {
+        const float4 t = __ldg(reinterpret_cast<const float4*>(row + 4 * lane + 128 * k));
+        r[4 * k] = t.x; r[4 * k + 1] = t.y; r[4 * k + 2] = t.z; r[4 * k + 3] = t.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        const int d = lane + 32 * e;
+        r[e] = d < D ? __ldg(row + d) : 0.f;
+      }
+    }
+  }
+};
+
+}  // namespace
+
+template <int GT, int NV, bool V4>
+__global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeJob j) {
+  using DM = Dims<V4, NV>;
+  __shared__ float sm_m[kDecodeWarps][GT];
+  __shared__ float sm_l[kDecodeWarps][GT];
+  __shared__ float sm_o[kDecodeWarps][GT][kMaxHeadDim];
+
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int G = j.H / j.Hkv;
+  const int ngroups = (G + GT - 1) / GT;
+  const int hkv = blockIdx.y / ngroups;
+  const int g0 = (blockIdx.y % ngroups) * GT;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int D = j.D;
+
+  const int n = j.cache_len[b];
+  if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) {
+    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) report(j.status, ATTN_DEV_LENGTH);
+    return;
+  }
+  const int nlive = j.window > 0 ? min(n, j.window) : n;
+  const int nsplit_b = (nlive + j.chunk - 1) / j.chunk;
+  const int k0 = split * j.chunk;
+  if (k0 >= nlive) return;
+  const int k1 = min(k0 + j.chunk, nlive);
+
+  // Queries of the GT heads, pre-multiplied by the softmax scale.
+  float q[GT][NV];
+#pragma unroll
+  for (int g = 0; g < GT; ++g) {
+    const int h = hkv * G + g0 + g;
+    if (g0 + g < G) {
+      DM::load(j.q + ((long)b * j.H + h) * D, lane, D, q[g]);
+#pragma unroll
+      for (int e = 0; e < NV; ++e) q[g][e] *= j.scale;
+    } else {
+#pragma unroll
+      for (int e = 0; e < NV; ++e) q[g][e] = 0.f;
+    }
+  }
+
+  const long head_off = ((long)b * j.Hkv + hkv) * j.capacity * D;
+  const float* kbase = j.k_cache + head_off;
+  const float* vbase = j.v_cache + head_off;
+  const bool capped = j.softcap > 0.f;
+  const float cap_k = capped ? 2.0f * kLog2e / j.softcap : 0.f;
+
+  float m[GT], l[GT], o[GT][NV];
+#pragma unroll
+  for (int g = 0; g < GT; ++g) {
+    m[g] = -INFINITY;
+    l[g] = 0.f;
+#pragma unroll
+    for (int e = 0; e < NV; ++e) o[g][e] = 0.f;
+  }
+
+  for (int base = k0 + warp * kUnroll; base < k1; base += kDecodeWarps * kUnroll) {
+    float kr[kUnroll][NV], vr[kUnroll][NV];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (base + u < k1) {
+        DM::load(kbase + (long)(base + u) * D, lane, D, kr[u]);
+        DM::load(vbase + (long)(base + u) * D, lane, D, vr[u]);
+      }
+    }
+    float s[kUnroll][GT];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) acc = fmaf(q[g][e], kr[u][e], acc);
+        acc = warp_sum(acc);
+        if (capped) acc = softcap_apply(acc, j.softcap, cap_k);
+        s[u][g] = (base + u < k1) ? acc * kLog2e : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+      float mx = s[0][g];
+#pragma unroll
+      for (int u = 1; u < kUnroll; ++u) mx = fmaxf(mx, s[u][g]);
+      const float mn = fmaxf(m[g], mx);
+      const float corr = exp2f(m[g] - mn);
+      m[g] = mn;
+      float p[kUnroll];
+      float ps = 0.f;
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        p[u] = exp2f(s[u][g] - mn);
+        ps += p[u];
+      }
+      l[g] = l[g] * corr + ps;
+#pragma unroll
+      for (int e = 0; e < NV; ++e) {
+        float acc = o[g][e] * corr;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u)
+          if (base + u < k1) acc = fmaf(p[u], vr[u][e], acc);
+        o[g][e] = acc;
+      }
+    }
+  }
+
+  // Merge the warps of this block.
+#pragma unroll
+  for (int g = 0; g < GT; ++g) {
+    if (lane == 0) {
+      sm_m[warp][g] = m[g];
+      sm_l[warp][g] = l[g];
+    }
+#pragma unroll
+    for (int e = 0; e < NV; ++e) {
+      const int d = DM::dim(lane, e);
+      if (d < D) sm_o[warp][g][d] = o[g][e];
+    }
+  }
+  __syncthreads();
+
+  const bool single = nsplit_b == 1;
+  for (int t = threadIdx.x; t < GT * D; t += kDecodeThreads) {
+    const int g = t / D, d = t % D;
+    if (g0 + g >= G) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, sm_m[w][g]);
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecodeWarps; ++w) {
+      const float c = sm_m[w][g] == -INFINITY ? 0.f : exp2f(sm_m[w][g] - M);
+      num = fmaf(c, sm_o[w][g][d], num);
+      den = fmaf(c, sm_l[w][g], den);
+    }
+    const long hrow = (long)b * j.H + hkv * G + g0 + g;
+    if (single) {
+      j.out[hrow * D + d] = num / den;
+    } else {
+      const long pi = hrow * j.nsplit + split;
+      j.partial[pi * D + d] = num;
+      if (d == 0) {
+        float* ml = j.partial + (long)j.B * j.H * j.nsplit * D;
+        ml[2 * pi] = M;
+        ml[2 * pi + 1] = den;
+      }
+    }
+  }
+}
+
+// out[b, h, :] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits of row b.
+__global__ void __launch_bounds__(128) decode_combine_kernel(DecodeJob j) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int n = j.cache_len[b];
+  if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) return;
+  const int nlive = j.window > 0 ? min(n, j.window) : n;
+  const int ns = (nlive + j.chunk - 1) / j.chunk;
+  if (ns <= 1) return;                       // finished by the split block
+  const long hrow = (long)b * j.H + h;
+  const float* ml = j.partial + (long)j.B * j.H * j.nsplit * j.D + 2 * hrow * j.nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, ml[2 * s]);
+  float den = 0.f;
+  for (int s = 0; s < ns; ++s) den = fmaf(exp2f(ml[2 * s] - M), ml[2 * s + 1], den);
+  const float inv = 1.0f / den;
+  const float* op = j.partial + hrow * j.nsplit * j.D;
+  for (int d = threadIdx.x; d < j.D; d += blockDim.x) {
+    float num = 0.f;
+    for (int s = 0; s < ns; ++s) num = fmaf(exp2f(ml[2 * s] - M), op[(long)s * j.D + d], num);
+    j.out[hrow * j.D + d] = num * inv;
+  }
+}
+
+void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk) {
+  const int eff = window > 0 ? (max_cache_len < window ? max_cache_len : window) : max_cache_len;
+  const int units = B * Hkv;
+  const int per_row = (1216 + units - 1) / units;       // aim for ~8 blocks per SM
+  int c = (eff + per_row - 1) / per_row;
+  c = ((c + 63) / 64) * 64;
+  if (c < 128) c = 128;
+  if (c > 512) c = 512;
+  *chunk = c;
+  *nsplit = (eff + c - 1) / c;
+}
+
+template <int GT>
+static cudaError_t launch_gt(const DecodeJob& j, cudaStream_t stream) {
+  const int G = j.H / j.Hkv;
+  const int ngroups = (G + GT - 1) / GT;
+  dim3 grid(j.nsplit, j.Hkv * ngroups, j.B);
+  if (j.D % 128 == 0) {
+    if (j.D == 128)
+      decode_split_kernel<GT, 4, true><<<grid, kDecodeThreads, 0, stream>>>(j);
+    else
+      decode_split_kernel<GT, 8, true><<<grid, kDecodeThreads, 0, stream>>>(j);
+  } else {
+    decode_split_kernel<GT, kMaxHeadDim / 32, false><<<grid, kDecodeThreads, 0, stream>>>(j);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || j.nsplit <= 1) return e;
+  decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream) {
+  const int G = j.H / j.Hkv;
+  if (G == 1) return launch_gt<1>(j, stream);
+  if (G == 2) return launch_gt<2>(j, stream);
+  if (G <= 4) return launch_gt<4>(j, stream);
+  return launch_gt<8>(j, stream);
+}
+
+}  // namespace gqa

@@ -1,0 +1,73 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+// Host-side only; every launcher enqueues on `stream` and returns the launch
+// status. Arguments have been validated by the caller.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gqa {
+
+constexpr int kMaxHeadDim = 256;
+constexpr int kMaxRopeHalf = kMaxHeadDim / 2;
+
+struct InvFreq {
+  double v[kMaxRopeHalf];   // rotary frequencies theta_i, i < R/2
+};
+
+struct RopeJob {
+  float* x;                 // [B, NH, L, D], rotated in place
+  int B, NH, L, D, R;
+  const int32_t* start;     // [B]
+  int max_positions;
+  const float2* table;      // [max_positions][R/2] (cos, sin), or nullptr: no rotation
+  const float* norm_w;      // [D] or nullptr
+  float norm_eps;
+  int32_t* status;
+  // cache append (k rows only); k_cache == nullptr: plain rotation
+  const float* v;
+  float* k_cache;
+  float* v_cache;
+  int capacity;
+  int window;
+};
+
+cudaError_t launch_rope_table(const InvFreq& inv, int R, int max_positions, float2* table,
+                              cudaStream_t stream);
+cudaError_t launch_rope_rows(const RopeJob& job, cudaStream_t stream);
+
+struct AttnShape {
+  const float* q;           // [B, H, L, D]
+  const float* k;           // [B, Hkv, L, D]
+  const float* v;           // [B, Hkv, L, D]
+  float* out;               // [B, H, L, D]
+  int B, H, Hkv, L, D;
+  int window;               // 0: causal
+  float softcap;            // <= 0: off
+  float scale;              // > 0
+  int32_t* status;
+};
+
+cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
+// Returns cudaErrorNotSupported (nothing launched) for shapes it does not take.
+cudaError_t launch_prefill_tc(const AttnShape& a, cudaStream_t stream);
+bool prefill_tc_supports(int D);
+
+struct DecodeJob {
+  const float* q;           // [B, H, D]
+  const float* k_cache;     // [B, Hkv, capacity, D]
+  const float* v_cache;
+  const int32_t* cache_len; // [B]
+  int max_cache_len;
+  float* out;               // [B, H, D]
+  int B, H, Hkv, D, capacity, window;
+  float softcap, scale;
+  float* partial;           // workspace [B, H, nsplit, D + 2]
+  int nsplit, chunk;
+  int32_t* status;
+};
+
+void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
+cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream);
+
+}  // namespace gqa

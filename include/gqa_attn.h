@@ -1,0 +1,179 @@
+/*
+ * gqa_attn.h -- C ABI of the grouped-query causal attention library
+ * (libgqa_attn.so, CUDA kernels for sm_103a).
+ *
+ * The operation is the self-attention of one Llama-shaped decoder layer as
+ * the "mojolearn.transformer" page states it (TransformerBlock: grouped-query
+ * attention with RoPE and a KV cache; options window, rope_theta,
+ * rope_scaling, rope_dim, max_positions, qk_norm, attn_softcap, norm_eps;
+ * TransformerState: the caller-owned cache; step: one token at position
+ * cached_tokens). The formulas are those of "Core Layers -- Deep Reference"
+ * (sections "RMSNorm", "RoPE", "MHA and GQA", "Sliding window attention").
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensors are fp32, contiguous, row-major, in DEVICE memory owned by the
+ *   caller. The library never allocates, frees or keeps device memory.
+ *   Tensor pointers must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
+ * - Shapes: Q and outputs [B, H, L, D]; K and V [B, Hkv, L, D]; caches
+ *   [B, Hkv, capacity, D]. H % Hkv == 0; query head h reads key/value head
+ *   h / (H / Hkv) (contiguous groups). D is even, 2 <= D <= 256.
+ * - Positions are absolute: row b's token l sits at start[b] + l.
+ * - stream is a cudaStream_t (NULL: the legacy default stream). Every call
+ *   only enqueues work on it and returns; nothing is synchronised.
+ * - Errors: arguments are checked on the host before anything is launched,
+ *   and a negative ATTN_ERR_* is returned with nothing enqueued. Values that
+ *   live on the device (start, cache_len) are checked again by the kernels:
+ *   a row that breaks a rule is skipped (its outputs are left untouched) and
+ *   an ATTN_DEV_* bit is OR-ed into *status (a caller-owned device int32,
+ *   which may be NULL to skip the report). Kernels never trap.
+ */
+#ifndef GQA_ATTN_H
+#define GQA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Host-side return codes. */
+#define ATTN_OK             0
+#define ATTN_ERR_NULL      -1  /* a required pointer is NULL */
+#define ATTN_ERR_SHAPE     -2  /* sizes break the shape rules above */
+#define ATTN_ERR_POSITION  -3  /* a position would reach max_positions */
+#define ATTN_ERR_CAPACITY  -4  /* a position has no cache slot (no window) */
+#define ATTN_ERR_WORKSPACE -5  /* decode workspace missing or too small */
+#define ATTN_ERR_ALIGN     -6  /* a tensor pointer is not 16-byte aligned */
+#define ATTN_ERR_PARAM     -7  /* RoPE parameters or a rope table are invalid */
+#define ATTN_ERR_CUDA      -8  /* a CUDA launch or query failed */
+
+/* Device status bits, OR-ed into *status by the kernels. */
+#define ATTN_DEV_POSITION  1   /* start[b] < 0 or start[b] + L - 1 >= max_positions */
+#define ATTN_DEV_CAPACITY  2   /* start[b] + L > capacity without a window */
+#define ATTN_DEV_LENGTH    4   /* cache_len[b] outside [1, max_cache_len] or > capacity */
+#define ATTN_DEV_TIMEOUT   8   /* a pipeline wait ran past its limit; outputs invalid */
+
+/* RoPE frequency scaling ("mojolearn.transformer", rope_scaling). */
+#define ATTN_ROPE_SCALING_NONE   0
+#define ATTN_ROPE_SCALING_LINEAR 1  /* every frequency divided by factor */
+#define ATTN_ROPE_SCALING_LLAMA3 2  /* Llama 3 frequency ramp */
+
+/*
+ * Rotary position parameters ("mojolearn.transformer": rope_theta,
+ * rope_scaling, rope_dim, max_positions). Frequencies are
+ * theta_i = theta^(-2i/R) for i < R/2 ("Core Layers -- Deep Reference",
+ * "RoPE", with the rotary width R as d_h), then scaled:
+ *   LINEAR: theta_i / factor;
+ *   LLAMA3: with wavelength w = 2*pi/theta_i, kept when
+ *           w < original_max_positions / high_freq_factor, divided by factor
+ *           when w > original_max_positions / low_freq_factor, and in between
+ *           (1-s)*theta_i/factor + s*theta_i with
+ *           s = (original_max_positions / w - low) / (high - low).
+ * Pairs are rotate-half, (i, i + R/2), and dims R..D-1 pass through.
+ */
+typedef struct attn_rope_params {
+    double theta;                    /* RoPE base, > 0 */
+    int32_t rope_dim;                /* R: even, <= D; 0 means D */
+    int32_t max_positions;           /* positions must stay below; 0 means 8192 */
+    int32_t scaling_type;            /* ATTN_ROPE_SCALING_* */
+    int32_t original_max_positions;  /* LLAMA3 only */
+    double factor;                   /* LINEAR and LLAMA3, > 0 */
+    double low_freq_factor;          /* LLAMA3 only */
+    double high_freq_factor;         /* LLAMA3 only, > low_freq_factor */
+} attn_rope_params;
+
+/*
+ * Bytes of the cos/sin table for these parameters at head dimension D:
+ * max_positions * (R/2) * 2 floats. Returns 0 if the parameters are invalid.
+ */
+size_t attn_rope_table_bytes(const attn_rope_params* rp, int D);
+
+/*
+ * Fill a caller-owned device table [max_positions][R/2][2] with
+ * (cos, sin) of position * theta_i. Angles and their cosines and sines are
+ * computed in fp64 on the device and rounded once to fp32 ("Core Layers --
+ * Deep Reference", "RoPE": frequencies precomputed once into an angle table).
+ * Build it once per parameter set and pass it to the calls below.
+ */
+int attn_rope_table_init(const attn_rope_params* rp, int D, float* table, size_t table_bytes,
+                         void* stream);
+
+/*
+ * In place on x [B, Hx, L, D] (queries, or any per-head rows): optional
+ * RMSNorm over D, y = x / sqrt(mean(x^2) + norm_eps) * norm_w ("mojolearn
+ * .transformer", qk_norm: before RoPE; "Core Layers -- Deep Reference",
+ * "RMSNorm"), then RoPE at position start[b] + l using table (built by
+ * attn_rope_table_init with the same rp and D).
+ *   start      device int32 [B]
+ *   max_start  host bound on every start[b], checked against max_positions
+ *   norm_w     device [D] or NULL (no norm)
+ */
+int attn_rope_apply(float* x, int B, int Hx, int L, int D, const int32_t* start,
+                    int32_t max_start, const attn_rope_params* rp, const float* table,
+                    const float* norm_w, float norm_eps, int32_t* status, void* stream);
+
+/*
+ * Cache append ("mojolearn.transformer", TransformerState; "Core Layers --
+ * Deep Reference", "Static KV-Cache": new rows written at the cache index).
+ * For each row b, kv head, token l at position p = start[b] + l:
+ *   k[b,hkv,l,:] <- RoPE(RMSNorm(k)) in place (norm if k_norm_w, RoPE if rp);
+ *   k_cache[b,hkv,slot(p),:] <- that rotated k;  v_cache[...] <- v (exact copy).
+ * slot(p) = p without a window (capacity >= every p + 1), p mod W with one
+ * (window = W > 0: the caches are rings with capacity == W; of a chunk longer
+ * than W only its last W positions are stored). rp == NULL (then table and
+ * k_norm_w must be NULL too) stores k as given.
+ */
+int kv_cache_append(float* k, const float* v, int B, int Hkv, int L, int D,
+                    const int32_t* start, int32_t max_start, const attn_rope_params* rp,
+                    const float* table, const float* k_norm_w, float norm_eps, float* k_cache,
+                    float* v_cache, int capacity, int window, int32_t* status, void* stream);
+
+/*
+ * Multi-token prefill attention over the chunk's own keys (a prefill from an
+ * empty cache; "mojolearn.transformer", forward with a zero state):
+ *   out[b,h,l,:] = sum_m softmax_m(cap(scale * q[b,h,l,:] . k[b,h/G,m,:])) v[b,h/G,m,:]
+ * over keys m <= l with l - m < window (window = 0: all m <= l). cap(s) =
+ * softcap * tanh(s / softcap) when softcap > 0 ("mojolearn.transformer",
+ * attn_softcap). scale <= 0 means 1/sqrt(D). q and k are already rotated.
+ * Uses tcgen05 tensor cores (TF32 operands, fp32 accumulation) when D % 4 == 0.
+ */
+int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out, int B, int H,
+                     int Hkv, int L, int D, int window, float softcap, float scale,
+                     int32_t* status, void* stream);
+
+/*
+ * Bytes of scratch gqa_attn_decode needs for these sizes (split-KV partial
+ * results). max_cache_len bounds every cache_len[b].
+ */
+size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cache_len,
+                                      int window);
+
+/*
+ * Single-token decode ("mojolearn.transformer", step: forward with L = 1 at
+ * position cached_tokens). Row b's query q[b,:,0,:] (rotated) sits at
+ * p = cache_len[b] - 1 (cache_len counts the token just appended) and reads
+ * cache positions max(0, p - W + 1) .. p: slots 0 .. p without a window, or
+ * the min(cache_len[b], W) live slots of the ring with one.
+ *   q [B, H, 1, D], out [B, H, 1, D]; caches [B, Hkv, capacity, D].
+ *   cache_len       device int32 [B], each in [1, max_cache_len]
+ *   workspace       device scratch of gqa_attn_decode_workspace_size bytes
+ * Output rows are overwritten; the workspace contents are clobbered.
+ */
+int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
+                    const int32_t* cache_len, int32_t max_cache_len, float* out, int B, int H,
+                    int Hkv, int D, int capacity, int window, float softcap, float scale,
+                    void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+
+/* A static string naming a return code (ATTN_OK / ATTN_ERR_*). */
+const char* attn_status_string(int code);
+
+/* Library version, e.g. "0.1.0". */
+const char* attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_ATTN_H */

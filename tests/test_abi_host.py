@@ -1,0 +1,172 @@
+"""The C ABI on the host: the library loads without a GPU, exports every
+function the header declares, and rejects bad arguments before launching
+anything (no test here touches a GPU).
+
+Bad-argument cases pass stand-in pointers, so they run only where no CUDA
+device is visible; every case is one the host check must refuse.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gqa_causal_attention_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gqa_attn.h")
+
+no_device = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="stand-in pointers are only used without a device")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_four_entry_points():
+    fns = declared_functions()
+    for name in ("attn_rope_apply", "kv_cache_append", "gqa_attn_prefill", "gqa_attn_decode"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_function():
+    lib = g.load()
+    raw = ctypes.CDLL(g.library_path())
+    missing = [f for f in declared_functions() if not hasattr(raw, f)]
+    assert not missing, missing
+    assert lib.attn_version().decode().count(".") == 2
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
+        s = g.attn_status_string(code)
+        assert s and s != "unknown status"
+    assert g.attn_status_string(-99) == "unknown status"
+
+
+def test_rope_table_bytes():
+    rp = g.RopeParams.make(theta=1e4, max_positions=100)
+    assert g.attn_rope_table_bytes(rp, 16) == 100 * 8 * 2 * 4
+    rp = g.RopeParams.make(theta=1e4, rope_dim=64, max_positions=0)      # default 8192
+    assert g.attn_rope_table_bytes(rp, 128) == 8192 * 32 * 2 * 4
+    for bad in (g.RopeParams.make(theta=0.0), g.RopeParams.make(rope_dim=3),
+                g.RopeParams.make(rope_dim=32), g.RopeParams.make(scaling=("linear", 0.0)),
+                g.RopeParams.make(scaling=("llama3", 8.0, 4.0, 1.0, 8192))):
+        assert g.attn_rope_table_bytes(bad, 16) == 0
+
+
+def test_decode_workspace_size():
+    # one split needs no real workspace; many splits need B*H*nsplit*(D+2) floats
+    small = g.gqa_attn_decode_workspace_size(1, 4, 2, 16, 20)
+    assert 0 < small <= 16
+    big = g.gqa_attn_decode_workspace_size(64, 32, 8, 128, 8193)
+    assert big % (64 * 32 * 130 * 4) == 0 and big // (64 * 32 * 130 * 4) >= 2
+    assert g.gqa_attn_decode_workspace_size(1, 3, 2, 16, 20) == 0     # H % Hkv != 0
+
+
+P = ctypes.c_void_p(0x100000)        # stand-in, 16-byte aligned, never dereferenced
+P_ODD = ctypes.c_void_p(0x100004)    # not 16-byte aligned
+S = ctypes.c_void_p(None)
+
+
+def rp(**kw):
+    return ctypes.byref(g.RopeParams.make(**kw))
+
+
+@no_device
+@pytest.mark.parametrize("args,code", [
+    # x, B, Hx, L, D, start, max_start, rp, table, norm_w, eps
+    ((P, 1, 2, 4, 7, P, 0, rp(), P, None, 1e-6), -2),            # odd D
+    ((P, 1, 2, 4, 258, P, 0, rp(), P, None, 1e-6), -2),          # D too large
+    ((P, 1, 0, 4, 8, P, 0, rp(), P, None, 1e-6), -2),            # no heads
+    ((None, 1, 2, 4, 8, P, 0, rp(), P, None, 1e-6), -1),         # null x
+    ((P, 1, 2, 4, 8, None, 0, rp(), P, None, 1e-6), -1),         # null start
+    ((P, 1, 2, 4, 8, P, 0, rp(), None, None, 1e-6), -1),         # null table
+    ((P, 1, 2, 4, 8, P, 0, rp(rope_dim=10), P, None, 1e-6), -7),  # rope_dim > D
+    ((P, 1, 2, 4, 8, P, 0, rp(rope_dim=6, theta=-1.0), P, None, 1e-6), -7),
+    ((P_ODD, 1, 2, 4, 8, P, 0, rp(), P, None, 1e-6), -6),        # misaligned
+    ((P, 1, 2, 4, 8, P, 8189, rp(), P, None, 1e-6), -3),         # 8189 + 3 >= 8192
+    ((P, 1, 2, 4, 8, P, -1, rp(), P, None, 1e-6), -3),
+    ((P, 1, 2, 4, 8, P, 97, rp(max_positions=100), P, None, 1e-6), -3),   # 97 + 3 >= 100
+])
+def test_rope_apply_rejects(args, code):
+    lib = g.load()
+    assert lib.attn_rope_apply(*args, None, S) == code
+
+
+@no_device
+def test_rope_apply_empty_is_a_no_op():
+    lib = g.load()
+    assert lib.attn_rope_apply(None, 0, 2, 4, 8, None, 0, rp(), P, None, 1e-6, None, S) == 0
+    assert lib.attn_rope_apply(None, 3, 2, 0, 8, None, 0, rp(), P, None, 1e-6, None, S) == 0
+
+
+@no_device
+@pytest.mark.parametrize("over,code", [
+    (dict(capacity=10, max_start=7), -4),          # 7 + 4 > 10, no window
+    (dict(window=4, capacity=8), -2),               # a ring has exactly W slots
+    (dict(window=-1), -2),
+    (dict(k=None), -1),
+    (dict(v_cache=None), -1),
+    (dict(table=None), -1),                         # rp without a table
+    (dict(rp=None), -7),                            # a table without rp
+    (dict(v=P_ODD), -6),
+    (dict(max_start=8190), -3),
+    (dict(D=5), -2),
+])
+def test_append_rejects(over, code):
+    a = dict(k=P, v=P, B=1, Hkv=2, L=4, D=8, start=P, max_start=0, rp=rp(), table=P, kn=None,
+             eps=1e-6, k_cache=P, v_cache=P, capacity=16, window=0, status=None, stream=S)
+    a.update(over)
+    lib = g.load()
+    assert lib.kv_cache_append(*a.values()) == code
+
+
+@no_device
+@pytest.mark.parametrize("over,code", [
+    (dict(H=6, Hkv=4), -2),                         # H % Hkv != 0
+    (dict(Hkv=0), -2),
+    (dict(D=3), -2),
+    (dict(window=-2), -2),
+    (dict(q=None), -1),
+    (dict(out=P_ODD), -6),
+    (dict(softcap=float("inf")), -7),
+    (dict(scale=float("nan")), -7),
+])
+def test_prefill_rejects(over, code):
+    a = dict(q=P, k=P, v=P, out=P, B=1, H=4, Hkv=2, L=8, D=16, window=0, softcap=0.0,
+             scale=0.0, status=None, stream=S)
+    a.update(over)
+    assert g.load().gqa_attn_prefill(*a.values()) == code
+
+
+@no_device
+@pytest.mark.parametrize("over,code", [
+    (dict(max_cache_len=0), -2),
+    (dict(max_cache_len=5000, capacity=4096), -4),  # beyond the cache, no window
+    (dict(window=8, capacity=16), -2),
+    (dict(H=5), -2),
+    (dict(cache_len=None), -1),
+    (dict(workspace=None), -5),
+    (dict(ws_bytes=64), -5),
+    (dict(k_cache=P_ODD), -6),
+])
+def test_decode_rejects(over, code):
+    a = dict(q=P, k_cache=P, v_cache=P, cache_len=P, max_cache_len=4000, out=P, B=8, H=4, Hkv=2, D=64,
+             capacity=4096, window=0, softcap=0.0, scale=0.0, workspace=P, ws_bytes=1 << 30,
+             status=None, stream=S)
+    a.update(over)
+    assert g.load().gqa_attn_decode(*a.values()) == code
+
+
+def test_binding_refuses_other_dtypes():
+    x = torch.zeros(1, 2, 3, 4, dtype=torch.float64)
+    with pytest.raises(TypeError):
+        g.gqa_attn_prefill(x, x, x, x)
+    xb = torch.zeros(1, 2, 3, 4, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        g.gqa_attn_prefill(xb, xb, xb, xb)
