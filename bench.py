@@ -1,0 +1,426 @@
+"""Throughput of the GQA attention hot path on GB300.
+
+Default run (N=1): the Llama-3-8B-shaped prefill (B=4, L=2048, H=32, Hkv=8,
+D=128, rope_theta 5e5 with the Llama 3 ramp, causal). One step is the whole
+prefill path through the C ABI: RoPE on q, the fused K RoPE + cache append,
+and the prefill attention. value = attention FLOP per step / step time.
+
+The same line carries the decode half of the metric, measured on the
+64-row batched decode (cached lengths U{512..8192}, H=32, Hkv=8, D=128): one
+step is RoPE on q, the append of the new token and the split-KV decode;
+GB/s = K/V cache bytes read per step / step time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+For N > 1 launch under torchrun: each rank runs the same workload on its own
+GPU (the path needs no exchange between GPUs), value sums all ranks' work over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn TFLOP/s (% TC peak); decode KV-cache GB/s (% of 8 TB/s HBM)"
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25        # dense TF32 vs dense BF16 nominal rates
+NOMINAL_HBM_GBS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=200)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = {"hbm_gbs": 6669.5, "bf16_tflops": 1926.5, "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        p.update({"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                  "source": "measured"})
+    p["tf32_tflops"] = p["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
+    return p
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() in ("active", "yes", "1"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def timed(fn, steps, warmup, dist, events_for=None):
+    """Run fn() warmup + steps times; device time of the timed steps (ms, max over ranks)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    torch.cuda.synchronize()
+    return ms
+
+
+def visible_pairs(L, window):
+    """Number of (query, key) pairs the causal (or windowed) mask admits in one row."""
+    if window <= 0 or window >= L:
+        return L * (L + 1) // 2
+    return window * (window + 1) // 2 + (L - window) * window
+
+
+def prefill_flops(w, B=None, H=None):
+    B = w.B if B is None else B
+    H = w.H if H is None else H
+    return 4.0 * B * H * w.D * visible_pairs(w.L, w.window)
+
+
+def bench_prefill(w, args, dist, dev, rank):
+    import torch
+    import gqa_causal_attention_gb300 as g
+    from gqa_causal_attention_gb300 import synthetic as syn
+
+    inp = syn.prefill_inputs(w)
+    rp = g.RopeParams.make(theta=w.theta, rope_dim=w.rope_dim, max_positions=w.max_positions,
+                           scaling=w.scaling)
+    table = g.rope_table(rp, w.D, dev)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    qn = None if inp["q_norm_w"] is None else inp["q_norm_w"].to(dev)
+    kn = None if inp["k_norm_w"] is None else inp["k_norm_w"].to(dev)
+    cap = w.window if w.window else w.capacity
+    kc = torch.zeros(w.B, w.Hkv, cap, w.D, device=dev)
+    vc = torch.zeros_like(kc)
+    out = torch.empty_like(q)
+    start = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kern = []
+
+    def step(record=False):
+        g.attn_rope_apply(q, start, 0, rp, table, qn, w.norm_eps, status)
+        g.kv_cache_append(k, v, start, 0, rp, table, kn, w.norm_eps, kc, vc, w.window, status)
+        if record:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, status)
+            b.record()
+            kern.append((a, b))
+        else:
+            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, status)
+
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = timed(lambda: step(True), args.steps, args.warmup, dist)
+    kern = kern[args.warmup:]
+    kern_ms = sum(a.elapsed_time(b) for a, b in kern) / max(1, len(kern))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    res = {"ms": ms / args.steps, "kernel_ms": kern_ms, "clocks": clk.summary(),
+           "launches_per_step": 3}
+
+    if not args.no_e2e:
+        hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
+        hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+
+        def e2e_step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            step()
+            hout.copy_(out, non_blocking=True)
+
+        e_steps = max(3, min(args.steps, 50))
+        ems = timed(e2e_step, e_steps, 3, dist)
+        res["e2e_ms"] = ems / e_steps
+        res["h2d"] = sum(t.numel() * 4 for t in (hq, hk, hv))
+        res["d2h"] = hout.numel() * 4
+    return res
+
+
+def bench_decode(w, args, dist, dev):
+    import torch
+    import gqa_causal_attention_gb300 as g
+    from gqa_causal_attention_gb300 import synthetic as syn
+
+    n = syn.cache_lengths(w.seed, w.B, *w.cache_len_range)
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    kc = torch.randn(w.B, w.Hkv, w.capacity, w.D, device=dev, generator=gen)
+    vc = torch.randn(w.B, w.Hkv, w.capacity, w.D, device=dev, generator=gen)
+    tok = syn.decode_token_inputs(w, 0)
+    q, k, v = (tok[x].to(dev) for x in ("q", "k", "v"))
+    rp = g.RopeParams.make(theta=w.theta, rope_dim=w.rope_dim, max_positions=w.max_positions,
+                           scaling=w.scaling)
+    table = g.rope_table(rp, w.D, dev)
+    pos = n.to(dev)
+    cl = (n + 1).to(dev)
+    maxlen = int(n.max()) + 1
+    ws = torch.empty(max(4, g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, maxlen,
+                                                             w.window) // 4), device=dev)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kern = []
+
+    def step():
+        g.attn_rope_apply(q, pos, maxlen - 1, rp, table, None, w.norm_eps, status)
+        g.kv_cache_append(k, v, pos, maxlen - 1, rp, table, None, w.norm_eps, kc, vc, 0, status)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        g.gqa_attn_decode(q, kc, vc, cl, maxlen, out, 0, w.softcap, 0.0, ws, status)
+        b.record()
+        kern.append((a, b))
+
+    steps = args.decode_steps
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = timed(step, steps, args.warmup, dist)
+    kern = kern[args.warmup:]
+    kern_ms = sum(a.elapsed_time(b) for a, b in kern) / max(1, len(kern))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    nbytes = 2.0 * w.Hkv * w.D * 4 * float((n + 1).sum())
+    ksplit = 2 if g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, maxlen, w.window) > 16 \
+        else 1
+    return {"ms": ms / steps, "kernel_ms": kern_ms, "bytes": nbytes, "clocks": clk.summary(),
+            "launches_per_step": 2 + ksplit}
+
+
+def cpu_baseline_prefill(w, budget_s=20.0):
+    """The oracle, as it stands, on a bounded sample of the prefill workload."""
+    import oracle
+    from gqa_causal_attention_gb300 import synthetic as syn
+
+    B1 = 1
+    inp = syn.prefill_inputs(w, B=B1)
+    cfg = oracle.Cfg(B=B1, H=w.H, Hkv=w.Hkv, L=w.L, D=w.D, rope_dim=w.R, theta=w.theta,
+                     scaling=w.scaling, norm_eps=w.norm_eps, window=w.window,
+                     softcap=w.softcap)
+    # calibrate on 2 heads (one KV head when G == 2), then size the sample
+    Hs = max(w.G, 2)
+    t0 = time.perf_counter()
+    oracle.prefill(inp["q"][:, :Hs], inp["k"][:, :Hs // w.G], inp["v"][:, :Hs // w.G], [0],
+                   oracle.Cfg(**{**cfg.__dict__, "H": Hs, "Hkv": Hs // w.G}),
+                   inp["q_norm_w"], inp["k_norm_w"])
+    t1 = time.perf_counter() - t0
+    groups = max(1, min(w.Hkv, int(budget_s / max(t1, 1e-3) * (Hs // w.G))))
+    H2, Hkv2 = groups * w.G, groups
+    sub = oracle.Cfg(**{**cfg.__dict__, "H": H2, "Hkv": Hkv2})
+    t0 = time.perf_counter()
+    oracle.prefill(inp["q"][:, :H2], inp["k"][:, :Hkv2], inp["v"][:, :Hkv2], [0], sub,
+                   inp["q_norm_w"], inp["k_norm_w"])
+    dt = time.perf_counter() - t0
+    fl = prefill_flops(w, B=1, H=H2)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"batch row 0, heads 0..{H2 - 1} ({Hkv2} KV heads) of the {w.name} "
+                      f"prefill, full L={w.L}: {fl:.3e} FLOP in {dt:.2f} s"}
+
+
+def reference_arm(args, w, rank):
+    """The oracle, as it stands, timed on the host cores over a bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle
+    from gqa_causal_attention_gb300 import synthetic as syn
+
+    oracle.build()
+    per_step = max(0.2, 150.0 / max(1, args.steps + args.warmup))   # whole run within minutes
+    inp = syn.prefill_inputs(w, B=1)
+    cfg = oracle.Cfg(B=1, H=w.G, Hkv=1, L=w.L, D=w.D, rope_dim=w.R, theta=w.theta,
+                     scaling=w.scaling, norm_eps=w.norm_eps, window=w.window,
+                     softcap=w.softcap)
+    # one KV head with its query group at full length, trimmed until it fits the step budget
+    L = w.L
+    while True:
+        sub = oracle.Cfg(**{**cfg.__dict__, "L": L})
+        t0 = time.perf_counter()
+        oracle.prefill(inp["q"][:, :w.G, :L], inp["k"][:, :1, :L], inp["v"][:, :1, :L], [0], sub,
+                       inp["q_norm_w"], inp["k_norm_w"])
+        dt = time.perf_counter() - t0
+        if dt <= per_step or L <= 128:
+            break
+        L = max(128, L // 2)
+
+    def one():
+        oracle.prefill(inp["q"][:, :w.G, :L], inp["k"][:, :1, :L], inp["v"][:, :1, :L], [0], sub,
+                       inp["q_norm_w"], inp["k_norm_w"])
+
+    for _ in range(args.warmup):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one()
+    dt = (time.perf_counter() - t0) / args.steps
+    fl = 4.0 * w.G * w.D * visible_pairs(L, w.window)
+    val = fl / dt / 1e12
+    sample = (f"batch row 0, KV head 0 with its {w.G} query heads, first {L} tokens of the "
+              f"{w.name} prefill ({fl:.3e} FLOP per step)")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "Hkv": w.Hkv,
+                       "D": w.D},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from gqa_causal_attention_gb300 import synthetic as syn
+    w = syn.WORKLOADS["llama3_8b_prefill"]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, w, rank)
+        return
+
+    import torch
+    import torch.distributed as tdist
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        tdist.init_process_group("nccl", device_id=dev)
+        dist = tdist
+    import gqa_causal_attention_gb300 as g
+    g.load()
+    pk = peaks()
+
+    pre = bench_prefill(w, args, dist, dev, rank)
+    fl = prefill_flops(w)
+    value = world * fl / (pre["ms"] * 1e-3) / 1e12
+    kern_tflops = fl / (pre["kernel_ms"] * 1e-3) / 1e12
+    dec = None
+    if not args.no_decode:
+        wd = syn.WORKLOADS["batched_decode"]
+        dec = bench_decode(wd, args, dist, dev)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": pre["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "tf32" if g.load() and w.D % 4 == 0 else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "Hkv": w.Hkv, "D": w.D,
+                   "rope": "theta 5e5, llama3 (8, 1, 4, 8192)", "mask": "causal",
+                   "step": "rope(q) + rope(k)+cache append + prefill attention",
+                   "l2": "inputs larger than L2 (q, k, v, out, cache: 384 MiB per step)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": pk["tf32_tflops"],
+                     "unit": "TFLOP/s", "frac": kern_tflops / pk["tf32_tflops"],
+                     "traffic": None,
+                     "kernel": "gqa_attn_prefill", "kernel_ms": pre["kernel_ms"],
+                     "peak_note": f"dense TF32 = {pk['source']} bf16 burst "
+                                  f"{pk['bf16_tflops']} x nominal 1.1/2.25",
+                     "frac_of_bf16_peak": kern_tflops / pk["bf16_tflops"]},
+        "gpu_launches": pre["launches_per_step"] * args.steps,
+        "clocks": pre["clocks"],
+    }
+    if "e2e_ms" in pre:
+        line["e2e"] = {"value": world * fl / (pre["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                       "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"],
+                       "ms_per_step": pre["e2e_ms"]}
+    if dec is not None:
+        gbs = dec["bytes"] / (dec["ms"] * 1e-3) / 1e9
+        kgbs = dec["bytes"] / (dec["kernel_ms"] * 1e-3) / 1e9
+        line["decode"] = {
+            "workload": "batched_decode", "value": world * gbs, "unit": "GB/s",
+            "ms_per_step": dec["ms"], "bytes_per_step": dec["bytes"],
+            "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+            "roofline": {"bound": "hbm", "achieved": kgbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": kgbs / pk["hbm_gbs"], "traffic": None,
+                         "kernel": "gqa_attn_decode", "kernel_ms": dec["kernel_ms"]},
+            "gpu_launches": dec["launches_per_step"] * args.decode_steps,
+            "clocks": dec["clocks"]}
+        line["gpu_launches"] += line["decode"]["gpu_launches"]
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill(w)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
