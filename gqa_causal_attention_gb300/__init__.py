@@ -22,6 +22,7 @@ __all__ = [
     "AttnError", "RopeParams", "load", "library_path",
     "attn_rope_table_bytes", "attn_rope_table_init", "attn_rope_apply", "kv_cache_append",
     "gqa_attn_prefill", "gqa_attn_decode_workspace_size", "gqa_attn_decode",
+    "gqa_attn_decode_static",
     "attn_status_string", "attn_version", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
@@ -96,6 +97,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
+            "gqa_attn_decode_static": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32,
+                                             i32, i32, i32, f, f, vp, vp]),
             "attn_status_string": (ctypes.c_char_p, [i32]),
             "attn_version": (ctypes.c_char_p, []),
         }
@@ -241,3 +244,22 @@ def gqa_attn_decode(q, k_cache, v_cache, cache_len, max_cache_len: int, out, win
                                 float(softcap), float(scale), _ptr(workspace), wbytes,
                                 _ptr(status), _stream(stream))
     _check("gqa_attn_decode", rc)
+
+
+def gqa_attn_decode_static(q, k_cache, v_cache, cache_len, max_cache_len: int, out,
+                           window: int = 0, softcap: float = 0.0, scale: float = 0.0,
+                           status=None, stream=None) -> None:
+    """gqa_attn_decode for callers that cannot allocate: the split-KV scratch is a
+    fixed 32 MiB array inside the library (shared by all calls; calls that overlap
+    on the GPU race on it). The first call on a device sets it up."""
+    _f32("q", q, 4); _f32("out", out, 4); _f32("k_cache", k_cache, 4)
+    _f32("v_cache", v_cache, 4); _i32("cache_len", cache_len); _i32("status", status)
+    B, H, one, D = q.shape
+    Bc, Hkv, cap, Dc = k_cache.shape
+    if one != 1 or Bc != B or Dc != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("gqa_attn_decode_static: inconsistent shapes")
+    rc = load().gqa_attn_decode_static(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
+                                       int(max_cache_len), _ptr(out), B, H, Hkv, D, cap,
+                                       int(window), float(softcap), float(scale), _ptr(status),
+                                       _stream(stream))
+    _check("gqa_attn_decode_static", rc)

@@ -166,6 +166,33 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
                     int Hkv, int D, int capacity, int window, float softcap, float scale,
                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
+/*
+ * gqa_attn_decode without a caller workspace, for callers that cannot
+ * allocate device memory: code running where cudaMalloc is not allowed (a
+ * plug-in inside a host framework that owns all device memory, a serving path
+ * that must not allocate after start-up) or a plain C caller with no device
+ * allocator. The pages this library follows have no counterpart to it.
+ *
+ * The split-KV scratch comes from a fixed array in this library's device
+ * memory, GQA_ATTN_STATIC_SCRATCH_BYTES (32 MiB), which every GPU that loads
+ * the library holds until the process exits. Arguments and results are those
+ * of gqa_attn_decode. Sizes whose scratch (gqa_attn_decode_workspace_size)
+ * exceeds the array are refused with ATTN_ERR_WORKSPACE before anything runs.
+ * The call allocates nothing.
+ *
+ * - The first call on a device, with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress) and keeps it; make that
+ *   first call before any stream capture.
+ * - All calls share the one array and it keeps the last call's contents;
+ *   nothing in it has to start at zero. Calls whose work overlaps on the GPU
+ *   (other streams, other host threads) race on it: order them on one stream.
+ */
+#define GQA_ATTN_STATIC_SCRATCH_BYTES (32u << 20)
+int gqa_attn_decode_static(const float* q, const float* k_cache, const float* v_cache,
+                           const int32_t* cache_len, int32_t max_cache_len, float* out, int B,
+                           int H, int Hkv, int D, int capacity, int window, float softcap,
+                           float scale, int32_t* status, void* stream);
+
 /* A static string naming a return code (ATTN_OK / ATTN_ERR_*). */
 const char* attn_status_string(int code);
 
