@@ -171,6 +171,8 @@ def bench_prefill(w, args, dist, dev, rank):
     out = torch.empty_like(q)
     start = torch.zeros(w.B, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pws = torch.empty(max(4, g.gqa_attn_prefill_workspace_size(w.B, w.Hkv, w.L, w.D) // 4),
+                      device=dev)
     kern = []
 
     def step(record=False):
@@ -179,11 +181,13 @@ def bench_prefill(w, args, dist, dev, rank):
         if record:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, status)
+            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
+                               status=status)
             b.record()
             kern.append((a, b))
         else:
-            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, status)
+            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
+                               status=status)
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         ms = timed(lambda: step(True), args.steps, args.warmup, dist)
@@ -192,7 +196,7 @@ def bench_prefill(w, args, dist, dev, rank):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     res = {"ms": ms / args.steps, "kernel_ms": kern_ms, "clocks": clk.summary(),
-           "launches_per_step": 3}
+           "launches_per_step": 4}
 
     if not args.no_e2e:
         hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))

@@ -21,7 +21,8 @@ from . import _build
 __all__ = [
     "AttnError", "RopeParams", "load", "library_path",
     "attn_rope_table_bytes", "attn_rope_table_init", "attn_rope_apply", "kv_cache_append",
-    "gqa_attn_prefill", "gqa_attn_decode_workspace_size", "gqa_attn_decode",
+    "gqa_attn_prefill", "gqa_attn_prefill_workspace_size", "gqa_attn_decode_workspace_size",
+    "gqa_attn_decode",
     "gqa_attn_decode_static",
     "attn_status_string", "attn_version", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
@@ -92,8 +93,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                       vp, vp]),
             "kv_cache_append": (i32, [vp, vp, i32, i32, i32, i32, vp, ctypes.c_int32, rp, vp,
                                       vp, f, vp, vp, i32, i32, vp, vp]),
+            "gqa_attn_prefill_workspace_size": (sz, [i32, i32, i32, i32]),
             "gqa_attn_prefill": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f, f, vp,
-                                       vp]),
+                                       sz, vp, vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -204,9 +206,16 @@ def kv_cache_append(k, v, start, max_start: int, params, table, k_norm_w, norm_e
     _check("kv_cache_append", rc)
 
 
+def gqa_attn_prefill_workspace_size(B: int, Hkv: int, L: int, D: int) -> int:
+    return int(load().gqa_attn_prefill_workspace_size(B, Hkv, L, D))
+
+
 def gqa_attn_prefill(q, k, v, out, window: int = 0, softcap: float = 0.0, scale: float = 0.0,
-                     status=None, stream=None) -> None:
-    """out [B, H, L, D] = causal (or windowed) GQA attention of rotated q, k and v."""
+                     workspace=None, status=None, stream=None) -> None:
+    """out [B, H, L, D] = causal (or windowed) GQA attention of rotated q, k and v.
+
+    workspace: device scratch of gqa_attn_prefill_workspace_size bytes; when None a
+    torch tensor of that size is taken from the caching allocator for this call."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
         _f32(n, t, 4)
     _i32("status", status)
@@ -214,9 +223,15 @@ def gqa_attn_prefill(q, k, v, out, window: int = 0, softcap: float = 0.0, scale:
     Hkv = k.shape[1]
     if tuple(k.shape) != (B, Hkv, L, D) or v.shape != k.shape or out.shape != q.shape:
         raise ValueError("gqa_attn_prefill: inconsistent shapes")
+    if workspace is None:
+        n = gqa_attn_prefill_workspace_size(B, Hkv, L, D)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
     rc = load().gqa_attn_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, L, D,
-                                 int(window), float(softcap), float(scale), _ptr(status),
-                                 _stream(stream))
+                                 int(window), float(softcap), float(scale), _ptr(workspace),
+                                 wbytes, _ptr(status), _stream(stream))
     _check("gqa_attn_prefill", rc)
 
 

@@ -78,7 +78,7 @@ const char* attn_status_string(int code) {
     case ATTN_ERR_SHAPE: return "sizes break the shape rules";
     case ATTN_ERR_POSITION: return "a position reaches max_positions";
     case ATTN_ERR_CAPACITY: return "a position has no cache slot";
-    case ATTN_ERR_WORKSPACE: return "decode workspace missing or too small";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
     case ATTN_ERR_ALIGN: return "a tensor pointer is not 16-byte aligned";
     case ATTN_ERR_PARAM: return "invalid RoPE parameters or table";
     case ATTN_ERR_CUDA: return "a CUDA launch failed";
@@ -151,9 +151,15 @@ int kv_cache_append(float* k, const float* v, int B, int Hkv, int L, int D,
   return cuda_status(gqa::launch_rope_rows(j, static_cast<cudaStream_t>(stream)));
 }
 
+size_t gqa_attn_prefill_workspace_size(int B, int Hkv, int L, int D) {
+  if (B < 0 || Hkv < 1 || L < 0 || D < 2 || D > gqa::kMaxHeadDim || D % 2) return 0;
+  if (!gqa::prefill_tc_supports(D) || B == 0 || L == 0) return 16;
+  return (size_t)B * Hkv * D * gqa::prefill_vt_pitch(L) * sizeof(float);
+}
+
 int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out, int B, int H,
                      int Hkv, int L, int D, int window, float softcap, float scale,
-                     int32_t* status, void* stream) {
+                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
   if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
   if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
   if (B == 0 || L == 0) return ATTN_OK;
@@ -166,7 +172,14 @@ int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out,
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   a.status = status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (gqa::prefill_tc_supports(D)) return cuda_status(gqa::launch_prefill_tc(a, s));
+  if (gqa::prefill_tc_supports(D)) {
+    if (!workspace || workspace_bytes < gqa_attn_prefill_workspace_size(B, Hkv, L, D))
+      return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+    a.vt = static_cast<float*>(workspace);
+    a.vt_pitch = gqa::prefill_vt_pitch(L);
+    return cuda_status(gqa::launch_prefill_tc(a, s));
+  }
   return cuda_status(gqa::launch_prefill_simt(a, s));
 }
 

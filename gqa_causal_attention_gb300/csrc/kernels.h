@@ -41,6 +41,8 @@ struct AttnShape {
   const float* k;           // [B, Hkv, L, D]
   const float* v;           // [B, Hkv, L, D]
   float* out;               // [B, H, L, D]
+  float* vt;                // workspace: V^T [B, Hkv, D, vt_pitch] (tensor-core path)
+  int vt_pitch;
   int B, H, Hkv, L, D;
   int window;               // 0: causal
   float softcap;            // <= 0: off
@@ -52,6 +54,7 @@ cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
 // Returns cudaErrorNotSupported (nothing launched) for shapes it does not take.
 cudaError_t launch_prefill_tc(const AttnShape& a, cudaStream_t stream);
 bool prefill_tc_supports(int D);
+int prefill_vt_pitch(int L);   // row pitch (floats) of the V^T workspace
 
 struct DecodeJob {
   const float* q;           // [B, H, D]

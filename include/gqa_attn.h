@@ -44,7 +44,7 @@ extern "C" {
 #define ATTN_ERR_SHAPE     -2  /* sizes break the shape rules above */
 #define ATTN_ERR_POSITION  -3  /* a position would reach max_positions */
 #define ATTN_ERR_CAPACITY  -4  /* a position has no cache slot (no window) */
-#define ATTN_ERR_WORKSPACE -5  /* decode workspace missing or too small */
+#define ATTN_ERR_WORKSPACE -5  /* workspace missing or too small */
 #define ATTN_ERR_ALIGN     -6  /* a tensor pointer is not 16-byte aligned */
 #define ATTN_ERR_PARAM     -7  /* RoPE parameters or a rope table are invalid */
 #define ATTN_ERR_CUDA      -8  /* a CUDA launch or query failed */
@@ -137,11 +137,16 @@ int kv_cache_append(float* k, const float* v, int B, int Hkv, int L, int D,
  * over keys m <= l with l - m < window (window = 0: all m <= l). cap(s) =
  * softcap * tanh(s / softcap) when softcap > 0 ("mojolearn.transformer",
  * attn_softcap). scale <= 0 means 1/sqrt(D). q and k are already rotated.
- * Uses tcgen05 tensor cores (TF32 operands, fp32 accumulation) when D % 4 == 0.
+ * For D % 4 == 0 and D >= 32 the work runs on the tcgen05 tensor cores (TF32
+ * operands, fp32 accumulation and softmax); other even D run on the CUDA cores
+ * in fp32.
+ *   workspace  device scratch of gqa_attn_prefill_workspace_size bytes
+ *              (holds a transposed copy of v; contents clobbered)
  */
+size_t gqa_attn_prefill_workspace_size(int B, int Hkv, int L, int D);
 int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out, int B, int H,
                      int Hkv, int L, int D, int window, float softcap, float scale,
-                     int32_t* status, void* stream);
+                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
  * Bytes of scratch gqa_attn_decode needs for these sizes (split-KV partial

@@ -65,7 +65,7 @@ class Path:
         g.kv_cache_append(k, v, st, start, self.rp, self.table, self.kn, w.norm_eps, self.kc,
                           self.vc, w.window, self.status)
         out = torch.empty_like(q)
-        g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, self.status)
+        g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, status=self.status)
         return out, k
 
     def step(self, q, k, v, pos):

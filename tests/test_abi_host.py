@@ -59,6 +59,13 @@ def test_rope_table_bytes():
         assert g.attn_rope_table_bytes(bad, 16) == 0
 
 
+def test_prefill_workspace_size():
+    # tensor-core head dims need V^T with rows padded to a multiple of 4 keys
+    assert g.gqa_attn_prefill_workspace_size(2, 8, 130, 128) == 2 * 8 * 128 * 132 * 4
+    assert g.gqa_attn_prefill_workspace_size(1, 2, 16, 16) == 16     # CUDA-core path: none
+    assert g.gqa_attn_prefill_workspace_size(1, 2, 16, 7) == 0       # odd D: invalid
+
+
 def test_decode_workspace_size():
     # one split needs no real workspace; many splits need B*H*nsplit*(D+2) floats
     small = g.gqa_attn_decode_workspace_size(1, 4, 2, 16, 20)
@@ -121,6 +128,7 @@ def test_rope_apply_empty_is_a_no_op():
 def test_append_rejects(over, code):
     a = dict(k=P, v=P, B=1, Hkv=2, L=4, D=8, start=P, max_start=0, rp=rp(), table=P, kn=None,
              eps=1e-6, k_cache=P, v_cache=P, capacity=16, window=0, status=None, stream=S)
+    assert set(over) <= set(a)
     a.update(over)
     lib = g.load()
     assert lib.kv_cache_append(*a.values()) == code
@@ -136,10 +144,14 @@ def test_append_rejects(over, code):
     (dict(out=P_ODD), -6),
     (dict(softcap=float("inf")), -7),
     (dict(scale=float("nan")), -7),
+    (dict(D=64, workspace=None), -5),               # the tensor-core path needs V^T scratch
+    (dict(D=64, ws_bytes=64), -5),
+    (dict(D=64, workspace=P_ODD), -6),
 ])
 def test_prefill_rejects(over, code):
     a = dict(q=P, k=P, v=P, out=P, B=1, H=4, Hkv=2, L=8, D=16, window=0, softcap=0.0,
-             scale=0.0, status=None, stream=S)
+             scale=0.0, workspace=P, ws_bytes=1 << 30, status=None, stream=S)
+    assert set(over) <= set(a)
     a.update(over)
     assert g.load().gqa_attn_prefill(*a.values()) == code
 
@@ -159,6 +171,7 @@ def test_decode_rejects(over, code):
     a = dict(q=P, k_cache=P, v_cache=P, cache_len=P, max_cache_len=4000, out=P, B=8, H=4, Hkv=2, D=64,
              capacity=4096, window=0, softcap=0.0, scale=0.0, workspace=P, ws_bytes=1 << 30,
              status=None, stream=S)
+    assert set(over) <= set(a)
     a.update(over)
     assert g.load().gqa_attn_decode(*a.values()) == code
 

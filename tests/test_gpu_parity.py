@@ -168,7 +168,8 @@ def test_prefill_attention(B, H, Hkv, L, D, window, softcap):
     v = syn.normal(21, "v", (B, Hkv, L, D))
     out = torch.empty(B, H, L, D, device=dev())
     status = torch.zeros(1, dtype=torch.int32, device=dev())
-    g.gqa_attn_prefill(q.to(dev()), k.to(dev()), v.to(dev()), out, window, softcap, 0.0, status)
+    g.gqa_attn_prefill(q.to(dev()), k.to(dev()), v.to(dev()), out, window, softcap, 0.0,
+                       status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, rope_dim=0, window=window, softcap=softcap)
