@@ -55,6 +55,7 @@ cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const AttnShape& a, cudaStream_t stream);
 bool prefill_tc_supports(int D);
 int prefill_vt_pitch(int L);   // row pitch (floats) of the V^T workspace
+cudaError_t launch_prefill_tq(const AttnShape& a, cudaStream_t stream);  // D <= 128
 
 struct DecodeJob {
   const float* q;           // [B, H, D]

@@ -1,0 +1,113 @@
+// Pieces shared by the tensor-core prefill kernels: launch arguments, the
+// timeout-only drain wait, row-wise TMEM moves and TMA tensor maps.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc_ptx.cuh"
+
+namespace gqa {
+namespace prefill {
+
+constexpr int kBM = 128;                       // query rows per tile = MMA M = TMEM lanes
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;           // rescale O when the max grows by > 2^8
+constexpr int kSmemLimit = 232448;             // 227 KB of dynamic shared memory per block
+constexpr int kTmemCols = 512;
+
+struct TcArgs {
+  const float* q;                              // [B, H, L, D] (read directly when Q is in TMEM)
+  float* out;
+  int B, H, Hkv, L, D;
+  int G, QT, ntiles, npairs;                   // per (b, kv head): tiles and tile groups
+  int units;                                   // persistent kernel: B * H * QT query tiles
+  int window;
+  int softcap_on;
+  float c_score;                               // scale * log2(e)
+  float c_cap_in;                              // 2 * log2(e) * scale / cap
+  float c_cap_out;                             // log2(e) * cap
+  int32_t* status;
+};
+
+// Timeout-only wait used while winding down after an abort.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = tc::globaltimer();
+  while (!tc::mbar_try_wait(bar, parity)) {
+    if (tc::globaltimer() - t0 > tc::kWaitLimitNs) return;
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_ld_row(uint32_t addr, float* v) {
+  if constexpr (N % 64 == 0) {
+#pragma unroll
+    for (int c = 0; c < N; c += 64) tc::tmem_ld64(addr + c, v + c);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N; c += 32) tc::tmem_ld32(addr + c, v + c);
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void tmem_st_row(uint32_t addr, const float* v) {
+  if constexpr (N % 64 == 0) {
+#pragma unroll
+    for (int c = 0; c < N; c += 64) tc::tmem_st64(addr + c, v + c);
+  } else {
+#pragma unroll
+    for (int c = 0; c < N; c += 32) tc::tmem_st32(addr + c, v + c);
+  }
+}
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// [NH, L, D] fp32 rows as a 3-D tensor map; boxes of 32 columns x box_rows rows.
+inline bool make_map(CUtensorMap* m, const float* base, int D, int L, int NH, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(NH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
+                                 static_cast<cuuint64_t>(L) * D * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// V^T [B*Hkv, D, L] (rows of pitch Lp) for TMA: boxes of 32 keys x box_rows dims.
+inline bool make_map_vt(CUtensorMap* m, const float* base, int D, int L, int Lp, int NH, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(D),
+                              static_cast<cuuint64_t>(NH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Lp) * 4,
+                                 static_cast<cuuint64_t>(Lp) * D * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace prefill
+}  // namespace gqa

@@ -29,35 +29,13 @@
 //  * Every pipeline wait is bounded; a wait that runs out reports
 //    ATTN_DEV_TIMEOUT, the block drains its own copies and MMAs, frees its
 //    tensor memory and exits.
-#include <cudaTypedefs.h>
-
-#include <mutex>
-
-#include "common.cuh"
-#include "kernels.h"
-#include "tc_ptx.cuh"
+#include "prefill_common.cuh"
 
 namespace gqa {
 
 namespace {
 
-constexpr int kBM = 128;                       // query rows per tile = MMA M = TMEM lanes
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleLog2 = 8.0f;           // rescale O when the max grows by > 2^8
-constexpr int kSmemLimit = 232448;             // 227 KB of dynamic shared memory per block
-constexpr int kTmemCols = 512;
-
-struct TcArgs {
-  float* out;
-  int B, H, Hkv, L, D;
-  int G, QT, ntiles, npairs;                   // per (b, kv head): tiles and tile groups
-  int window;
-  int softcap_on;
-  float c_score;                               // scale * log2(e)
-  float c_cap_in;                              // 2 * log2(e) * scale / cap
-  float c_cap_out;                             // log2(e) * cap
-  int32_t* status;
-};
+using namespace prefill;
 
 struct alignas(8) Bars {
   uint64_t q_full;
@@ -72,14 +50,19 @@ struct alignas(8) Bars {
   int abort;
 };
 
+// Two shapes. DP <= 128: Q lives in tensor memory (A operand of S = Q K^T
+// from TMEM), 128-key blocks (N = 128 MMAs run at the full TF32 rate) and a
+// double-buffered S: TMEM = Q | O | S0 | S1. DP > 128: Q stays in shared
+// memory and 32-key blocks keep K/V stages within the 227 KB.
 template <int DP_>
 struct Cfg {
   static constexpr int DP = DP_;                        // head dim padded to 32
-  static constexpr int NQ = DP <= 128 ? 2 : 1;          // query tiles per block
-  static constexpr int BK = DP <= 128 ? 64 : 32;        // keys per block
+  static constexpr bool QTM = DP <= 128;                // Q in tensor memory
+  static constexpr int NQ = 1;                          // query tiles per block
+  static constexpr int BK = QTM ? 128 : 32;             // keys per block
   static constexpr int kChunks = DP / 32;               // 128-byte column chunks
   static constexpr int kQChunk = kBM * 128;
-  static constexpr int kQBytes = NQ * kChunks * kQChunk;
+  static constexpr int kQBytes = QTM ? 0 : NQ * kChunks * kQChunk;
   static constexpr int kKVChunk = BK * 128;
   static constexpr int kStage = kChunks * kKVChunk;
   static constexpr int kVtChunk = DP * 128;             // 32 keys x DP rows of V^T
@@ -91,20 +74,16 @@ struct Cfg {
   static constexpr int kSmemNeed = kQBytes + NS * kStage + 2048;
   static constexpr int kSmem = kSmemNeed > kSmemLimit / 2 + 4096 ? kSmemNeed
                                                                   : kSmemLimit / 2 + 4096;
-  static __host__ __device__ constexpr int o_col(int t) { return t * DP; }
-  static __host__ __device__ constexpr int s_col(int t, int b) { return NQ * DP + (2 * t + b) * BK; }
+  static constexpr int kQCol = 0;                       // QTM: Q columns [0, DP)
+  static constexpr int kOBase = QTM ? DP : 0;
+  static __host__ __device__ constexpr int o_col(int t) { return kOBase + t * DP; }
+  static __host__ __device__ constexpr int s_col(int t, int b) {
+    return kOBase + NQ * DP + (2 * t + b) * BK;
+  }
   static_assert(NS >= 2, "shared memory too small for two stages");
-  static_assert(NQ * (DP + 2 * BK) <= kTmemCols, "tensor memory budget");
+  static_assert(kOBase + NQ * (DP + 2 * BK) <= kTmemCols, "tensor memory budget");
   static_assert(kSmem <= kSmemLimit, "shared memory budget");
 };
-
-// Timeout-only wait used while winding down after an abort.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-  const uint64_t t0 = tc::globaltimer();
-  while (!tc::mbar_try_wait(bar, parity)) {
-    if (tc::globaltimer() - t0 > tc::kWaitLimitNs) return;
-  }
-}
 
 struct Unit {
   int b, hk;
@@ -149,17 +128,19 @@ __device__ void run_producer(const Unit& u, const TcArgs& a, const CUtensorMap* 
   tc::tma_prefetch(tq);
   tc::tma_prefetch(tk);
   tc::tma_prefetch(tv);
-  uint32_t qbytes = 0;
+  if constexpr (!C::QTM) {
+    uint32_t qbytes = 0;
 #pragma unroll
-  for (int t = 0; t < C::NQ; ++t)
-    if (u.valid[t]) qbytes += C::kChunks * C::kQChunk;
-  tc::mbar_arrive_expect_tx(&bars->q_full, qbytes);
+    for (int t = 0; t < C::NQ; ++t)
+      if (u.valid[t]) qbytes += C::kChunks * C::kQChunk;
+    tc::mbar_arrive_expect_tx(&bars->q_full, qbytes);
 #pragma unroll
-  for (int t = 0; t < C::NQ; ++t) {
-    if (!u.valid[t]) continue;
-    for (int c = 0; c < C::kChunks; ++c)
-      tc::tma_load_3d(sq + (t * C::kChunks + c) * C::kQChunk, tq, &bars->q_full, 32 * c, u.q0[t],
-                      u.b * a.H + u.head[t]);
+    for (int t = 0; t < C::NQ; ++t) {
+      if (!u.valid[t]) continue;
+      for (int c = 0; c < C::kChunks; ++c)
+        tc::tma_load_3d(sq + (t * C::kChunks + c) * C::kQChunk, tq, &bars->q_full, 32 * c,
+                        u.q0[t], u.b * a.H + u.head[t]);
+    }
   }
   int stage = 0;
   uint32_t phase = 0;
@@ -199,7 +180,7 @@ __device__ void run_producer(const Unit& u, const TcArgs& a, const CUtensorMap* 
   (void)ok;
   // Every copy this block started lands before the block may exit, whether or
   // not the consumers saw it (they may have stopped on an abort).
-  drain_wait(&bars->q_full, 0);
+  if constexpr (!C::QTM) drain_wait(&bars->q_full, 0);
   for (int s = 0; s < C::NS; ++s)
     if (filled[s]) drain_wait(&bars->kv_full[s], fill_parity[s]);
 }
@@ -221,28 +202,39 @@ __device__ void run_mma(const Unit& u, uint32_t tmem, uint8_t* sq, uint8_t* skv,
     }
     return true;
   };
+  // Descriptors are built once; an operand offset is added to the start-address
+  // field (address >> 4), which stays below 2^14 for any shared-memory address.
+  uint64_t qdesc[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t)
+    qdesc[t] = tc::sdesc_sw128(tc::smem_u32(sq + (t < C::NQ ? t : 0) * C::kChunks * C::kQChunk),
+                               16, 1024);
+  const uint64_t kvdesc = tc::sdesc_sw128(tc::smem_u32(skv), 16, 1024);
   // S_t[buf] = Q_t K^T: K-major A (Q) and B (K), 8 columns of D per instruction.
   auto issue_s = [&](int t, int buf, int st) {
     const uint32_t d = tmem + C::s_col(t, buf);
-    const uint32_t qa = tc::smem_u32(sq + t * C::kChunks * C::kQChunk);
-    const uint32_t kb = tc::smem_u32(skv + st * C::kStage);
+    const uint64_t qd = qdesc[t];
+    const uint64_t kd = kvdesc + static_cast<uint32_t>((st * C::kStage) >> 4);
 #pragma unroll
     for (int kk = 0; kk < C::DP / 8; ++kk) {
       const int c = kk / 4, off = (kk % 4) * 32;
-      tc::mma_tf32_ss(d, tc::sdesc_sw128(qa + c * C::kQChunk + off, 16, 1024),
-                      tc::sdesc_sw128(kb + c * C::kKVChunk + off, 16, 1024), id_s, kk > 0);
+      if constexpr (C::QTM)
+        tc::mma_tf32_ts(d, tmem + C::kQCol + 8 * kk, kd + ((c * C::kKVChunk + off) >> 4), id_s,
+                        kk > 0);
+      else
+        tc::mma_tf32_ss(d, qd + ((c * C::kQChunk + off) >> 4),
+                        kd + ((c * C::kKVChunk + off) >> 4), id_s, kk > 0);
     }
   };
   // O_t += P_t[buf] V: A from tensor memory, B = V^T (K-major, keys contiguous).
   auto issue_pv = [&](int t, int buf, int st, bool acc) {
     const uint32_t d = tmem + C::o_col(t);
-    const uint32_t vb = tc::smem_u32(skv + st * C::kStage);
+    const uint64_t vd = kvdesc + static_cast<uint32_t>((st * C::kStage) >> 4);
 #pragma unroll
     for (int kk = 0; kk < C::BK / 8; ++kk) {
       const int c = kk / 4, off = (kk % 4) * 32;
-      tc::mma_tf32_ts(d, tmem + C::s_col(t, buf) + 8 * kk,
-                      tc::sdesc_sw128(vb + c * C::kVtChunk + off, 16, 1024), id_pv,
-                      (acc || kk > 0) ? 1u : 0u);
+      tc::mma_tf32_ts(d, tmem + C::s_col(t, buf) + 8 * kk, vd + ((c * C::kVtChunk + off) >> 4),
+                      id_pv, (acc || kk > 0) ? 1u : 0u);
     }
   };
 
@@ -295,12 +287,35 @@ __device__ void run_mma(const Unit& u, uint32_t tmem, uint8_t* sq, uint8_t* skv,
 template <class C>
 __device__ void run_softmax(const Unit& u, const TcArgs& a, uint32_t tmem, Bars* bars, int t,
                             int quarter, int lane) {
+  constexpr int BK = C::BK;
+  constexpr int NA = 8;                       // independent partial max / sum chains
   volatile int* abort = &bars->abort;
   const int row = quarter * 32 + lane;
   const int qpos = u.q0[t] + row;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  // Running max m (log2 units, of the scaled and capped scores) and sum l.
   float m_ref = -INFINITY, l = 0.f;
   bool ok = true;
+
+  if constexpr (C::QTM) {
+    // This thread's query row goes into the Q columns of its TMEM lane (zeros
+    // past the sequence end and past D), then the MMA issuer may start.
+    const bool live = qpos < a.L;
+    const float* src = a.q + ((static_cast<long>(u.b) * a.H + u.head[t]) * a.L + qpos) * a.D;
+#pragma unroll 1
+    for (int c = 0; c < C::DP; c += 32) {
+      float qv[32];
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && c + e < a.D) x = __ldg(reinterpret_cast<const float4*>(src + c + e));
+        qv[e] = x.x; qv[e + 1] = x.y; qv[e + 2] = x.z; qv[e + 3] = x.w;
+      }
+      tc::tmem_st32(lane_base + C::kQCol + c, qv);
+    }
+    tc::fence_before_sync();
+    tc::mbar_arrive(&bars->q_full);
+  }
 
   for (int i = 0; i < u.n; ++i) {
     const int buf = i & 1;
@@ -310,34 +325,38 @@ __device__ void run_softmax(const Unit& u, const TcArgs& a, uint32_t tmem, Bars*
       break;
     }
     tc::fence_after_sync();
-    float s[C::BK];
-#pragma unroll
-    for (int c = 0; c < C::BK; c += 32) tc::tmem_ld32(lane_base + C::s_col(t, buf) + c, s + c);
+    float s[BK];
+    tmem_ld_row<BK>(lane_base + C::s_col(t, buf), s);
 
-    // scores in log2 units, optionally softcapped: cap * tanh(score / cap)
+    // Softcap turns raw scores into log2-unit capped scores:
+    // log2(e) * cap * tanh(scale * s / cap) = c_out - 2 c_out / (2^(s c_in) + 1).
     if (a.softcap_on) {
 #pragma unroll
-      for (int c = 0; c < C::BK; ++c) {
-        const float e = exp2f(s[c] * a.c_cap_in);
-        s[c] = a.c_cap_out - __fdividef(2.0f * a.c_cap_out, e + 1.0f);
-      }
-    } else {
-#pragma unroll
-      for (int c = 0; c < C::BK; ++c) s[c] *= a.c_score;
-    }
-    const int k0 = (u.jlo + i) * C::BK;
-    const bool whole = (k0 + C::BK - 1 <= qpos) && (a.window == 0 || k0 > qpos - a.window);
-    if (!whole) {
-#pragma unroll
-      for (int c = 0; c < C::BK; ++c) {
-        const int kp = k0 + c;
-        if (kp > qpos || (a.window > 0 && kp <= qpos - a.window)) s[c] = -INFINITY;
+      for (int c = 0; c < BK; ++c) {
+        const float e = tc::ex2(s[c] * a.c_cap_in);
+        s[c] = fmaf(-2.0f * a.c_cap_out, tc::rcp(e + 1.0f), a.c_cap_out);
       }
     }
-    float mb = s[0];
+    // Keys outside the causal / window band of this row (boundary blocks only).
+    const int k0 = (u.jlo + i) * BK;
+    const int hi = qpos - k0;                                    // visible: c <= hi
+    const int lo = a.window > 0 ? qpos - a.window + 1 - k0 : -1;  // visible: c >= lo
+    if (hi < BK - 1 || lo > 0) {
 #pragma unroll
-    for (int c = 1; c < C::BK; ++c) mb = fmaxf(mb, s[c]);
-    const float m_new = fmaxf(m_ref, mb);
+      for (int c = 0; c < BK; ++c) s[c] = (c > hi || c < lo) ? -INFINITY : s[c];
+    }
+    float mx[NA];
+#pragma unroll
+    for (int j = 0; j < NA; ++j) mx[j] = s[j];
+#pragma unroll
+    for (int c = NA; c < BK; ++c) mx[c % NA] = fmaxf(mx[c % NA], s[c]);
+#pragma unroll
+    for (int j = NA / 2; j > 0; j /= 2)
+#pragma unroll
+      for (int q = 0; q < j; ++q) mx[q] = fmaxf(mx[q], mx[q + j]);
+    // Scores in log2 units: capped ones already are; plain ones get scale * log2(e).
+    const float cs = a.softcap_on ? 1.0f : a.c_score;
+    const float m_new = fmaxf(m_ref, mx[0] * cs);
 
     // Rescale O only when the running maximum has grown a lot (warp-uniform).
     const bool grow = m_ref != -INFINITY && m_new - m_ref > kRescaleLog2;
@@ -348,7 +367,7 @@ __device__ void run_softmax(const Unit& u, const TcArgs& a, uint32_t tmem, Bars*
         break;
       }
       tc::fence_after_sync();
-      const float f = grow ? exp2f(m_ref - m_new) : 1.0f;
+      const float f = grow ? tc::ex2(m_ref - m_new) : 1.0f;
 #pragma unroll 1
       for (int c = 0; c < C::DP; c += 32) {
         float o[32];
@@ -362,18 +381,28 @@ __device__ void run_softmax(const Unit& u, const TcArgs& a, uint32_t tmem, Bars*
         m_ref = m_new;
       }
     }
-    if (m_ref == -INFINITY) m_ref = m_new;      // first visible keys of this row (O, l are 0)
+    if (m_ref == -INFINITY) m_ref = m_new;    // first visible keys of the row (O, l are 0)
+    // Reference for the exponent: -inf only while every key so far was masked,
+    // and then every score is -inf too, so any finite value gives p = 0.
+    const float mref = m_ref == -INFINITY ? 0.f : m_ref;
 
-    float ps = 0.f;
+    // p = 2^(score - m), truncated to the TF32 value the tensor core will use, so
+    // that l sums exactly the weights applied to V.
+    float ps[NA];
 #pragma unroll
-    for (int c = 0; c < C::BK; ++c) {
-      const float p = m_ref == -INFINITY ? 0.f : tc::round_tf32(exp2f(s[c] - m_ref));
-      ps += p;
+    for (int j = 0; j < NA; ++j) ps[j] = 0.f;
+#pragma unroll
+    for (int c = 0; c < BK; ++c) {
+      const float p = tc::trunc_tf32(tc::ex2(fmaf(s[c], cs, -mref)));
+      ps[c % NA] += p;
       s[c] = p;
     }
-    l += ps;
 #pragma unroll
-    for (int c = 0; c < C::BK; c += 32) tc::tmem_st32(lane_base + C::s_col(t, buf) + c, s + c);
+    for (int j = NA / 2; j > 0; j /= 2)
+#pragma unroll
+      for (int q = 0; q < j; ++q) ps[q] += ps[q + j];
+    l += ps[0];
+    tmem_st_row<BK>(lane_base + C::s_col(t, buf), s);
     tc::fence_before_sync();
     tc::mbar_arrive(&bars->p_ready[t][buf]);
   }
@@ -416,7 +445,7 @@ __global__ void __launch_bounds__(Cfg<DP>::kThreads, 1)
   const Unit u = decode_unit<C>(a);
 
   if (threadIdx.x == 0) {
-    tc::mbar_init(&bars->q_full, 1);
+    tc::mbar_init(&bars->q_full, C::QTM ? 128 : 1);
     for (int s = 0; s < C::NS; ++s) {
       tc::mbar_init(&bars->kv_full[s], 1);
       tc::mbar_init(&bars->kv_empty[s], 1);
@@ -464,69 +493,33 @@ __global__ void __launch_bounds__(Cfg<DP>::kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    else
-      cudaGetLastError();
-  });
-  return fn;
-}
-
-// [NH, L, D] fp32 rows as a 3-D tensor map; boxes of 32 columns x box_rows rows.
-bool make_map(CUtensorMap* m, const float* base, int D, int L, int NH, int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
-                              static_cast<cuuint64_t>(NH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
-                                 static_cast<cuuint64_t>(L) * D * 4};
-  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// V^T [B*Hkv, D, L] (rows of pitch Lp) for TMA: boxes of 32 keys x box_rows dims.
-bool make_map_vt(CUtensorMap* m, const float* base, int D, int L, int Lp, int NH, int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(D),
-                              static_cast<cuuint64_t>(NH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(Lp) * 4,
-                                 static_cast<cuuint64_t>(Lp) * D * 4};
-  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// vt[bh, d, l] = v[bh, l, d], 32 x 32 tiles through shared memory.
+// vt[bh, d, l] = v[bh, l, d] for D % 4 == 0: 32 x 32 tiles through shared
+// memory, 16-byte loads along d and 16-byte stores along l (rows of vt have a
+// pitch Lp that is a multiple of 4, so a store may run into the padding).
 __global__ void __launch_bounds__(256) transpose_v_kernel(const float* __restrict__ v,
                                                           float* __restrict__ vt, int L, int D,
                                                           int Lp) {
   __shared__ float tile[32][33];
   const long bh = blockIdx.z;
   const int l0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
+  const int r = threadIdx.x / 8, q = threadIdx.x % 8;
   const float* src = v + bh * L * D;
   float* dst = vt + bh * D * Lp;
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int l = l0 + r, d = d0 + threadIdx.x;
-    tile[r][threadIdx.x] = (l < L && d < D) ? src[static_cast<long>(l) * D + d] : 0.f;
+  {
+    const int l = l0 + r, d = d0 + 4 * q;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (l < L && d < D) x = __ldg(reinterpret_cast<const float4*>(src + static_cast<long>(l) * D + d));
+    tile[r][4 * q] = x.x;
+    tile[r][4 * q + 1] = x.y;
+    tile[r][4 * q + 2] = x.z;
+    tile[r][4 * q + 3] = x.w;
   }
   __syncthreads();
-  for (int r = threadIdx.y; r < 32; r += 8) {
-    const int d = d0 + r, l = l0 + threadIdx.x;
-    if (d < D && l < L) dst[static_cast<long>(d) * Lp + l] = tile[threadIdx.x][r];
+  {
+    const int d = d0 + r, l = l0 + 4 * q;
+    if (d < D && l < L)
+      *reinterpret_cast<float4*>(dst + static_cast<long>(d) * Lp + l) =
+          make_float4(tile[4 * q][r], tile[4 * q + 1][r], tile[4 * q + 2][r], tile[4 * q + 3][r]);
   }
 }
 
@@ -545,10 +538,11 @@ cudaError_t launch_dp(const AttnShape& s, cudaStream_t stream) {
       !make_map(&tk, s.k, s.D, s.L, s.B * s.Hkv, C::BK) ||
       !make_map_vt(&tv, s.vt, s.D, s.L, s.vt_pitch, s.B * s.Hkv, C::DP))
     return cudaErrorInvalidValue;
-  transpose_v_kernel<<<dim3((s.L + 31) / 32, (s.D + 31) / 32, s.B * s.Hkv), dim3(32, 8), 0,
+  transpose_v_kernel<<<dim3((s.L + 31) / 32, (s.D + 31) / 32, s.B * s.Hkv), 256, 0,
                        stream>>>(s.v, s.vt, s.L, s.D, s.vt_pitch);
   if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
   TcArgs a{};
+  a.q = s.q;
   a.out = s.out;
   a.B = s.B; a.H = s.H; a.Hkv = s.Hkv; a.L = s.L; a.D = s.D;
   a.G = s.H / s.Hkv;
@@ -575,11 +569,13 @@ int prefill_vt_pitch(int L) { return (L + 3) / 4 * 4; }
 
 cudaError_t launch_prefill_tc(const AttnShape& s, cudaStream_t stream) {
   if (!prefill_tc_supports(s.D)) return cudaErrorNotSupported;
+  if (s.D <= 128) {
+    transpose_v_kernel<<<dim3((s.L + 31) / 32, (s.D + 31) / 32, s.B * s.Hkv), 256, 0,
+                         stream>>>(s.v, s.vt, s.L, s.D, s.vt_pitch);
+    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
+    return launch_prefill_tq(s, stream);
+  }
   switch ((s.D + 31) / 32) {
-    case 1: return launch_dp<32>(s, stream);
-    case 2: return launch_dp<64>(s, stream);
-    case 3: return launch_dp<96>(s, stream);
-    case 4: return launch_dp<128>(s, stream);
     case 5: return launch_dp<160>(s, stream);
     case 6: return launch_dp<192>(s, stream);
     case 7: return launch_dp<224>(s, stream);

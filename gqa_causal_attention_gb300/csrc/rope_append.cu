@@ -69,151 +69,206 @@ __device__ __forceinline__ void store_vec(float* p, const float* r) {
   *reinterpret_cast<T*>(p) = t;
 }
 
-// One warp per row of x [B, NH, L, D]. Lane `lane` holds the rotary pairs
-// i = (lane + 32 k) * VEC .. + VEC - 1 (and their partners i + R/2), and the
-// float2 pairs of the pass-through part at R + 2 (lane + 32 k).
-// With k_cache set, the row is a key row: after its rotation it is stored at
-// its cache slot, and the matching value row is copied beside it.
-template <int VEC>
+// Warps own groups of RPW consecutive rows of x [B, NH, L, D] and load all of
+// a group before using any of it, so each warp keeps RPW rows of reads in
+// flight. Lane `lane` holds the rotary pairs i = (lane + 32 k) * VEC .. + VEC - 1
+// (and their partners i + R/2), and the float2 pairs of the pass-through part
+// at R + 2 (lane + 32 k). With k_cache set, the rows are key rows: after their
+// rotation they are stored at their cache slots, and the matching value rows
+// are copied beside them.
+template <int VEC, int RPW, bool APPEND, bool TAIL>
 __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
   constexpr int NP = 4 / VEC;            // R/2 <= 128  ->  <= 4/VEC vectors per lane
   const int lane = threadIdx.x & 31;
-  const int wpb = blockDim.x >> 5;
+  const long warps = (long)gridDim.x * (blockDim.x >> 5);
+  const long gwarp = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long rows = (long)j.B * j.NH * j.L;
   const int D = j.D, R = j.R, half = R / 2;
   const int ntail = (D - R) / 2;
-  const bool append = j.k_cache != nullptr;
-  const bool need_tail = append || j.norm_w != nullptr;
+  constexpr bool append = APPEND;             // key rows: also store k and v in the cache
+  constexpr bool need_tail = TAIL;            // dims past R are read (norm or cache copy)
 
-  for (long row = (long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows;
-       row += (long)gridDim.x * wpb) {
-    const int b = (int)(row / ((long)j.NH * j.L));
-    const int l = (int)(row % j.L);
-    const int s0 = j.start[b];
-    // Device-side re-check of the positions the host could not see.
-    if (s0 < 0 || (long)s0 + j.L - 1 >= (long)j.max_positions) {
-      if (lane == 0 && l == 0) report(j.status, ATTN_DEV_POSITION);
-      continue;
-    }
-    if (append && j.window == 0 && (long)s0 + j.L > (long)j.capacity) {
-      if (lane == 0 && l == 0) report(j.status, ATTN_DEV_CAPACITY);
-      continue;
-    }
-    const int p = s0 + l;
-    float* x = j.x + row * D;
-
-    float lo[NP * VEC], hi[NP * VEC];
-    float2 tl[4];
-    float ss = 0.f;
+  for (long row0 = gwarp * RPW; row0 < rows; row0 += warps * RPW) {
+    float lo[RPW][NP * VEC], hi[RPW][NP * VEC];
+    float2 cs[RPW][NP * VEC];
+    float2 tl[RPW][TAIL ? 4 : 1], vv[RPW][APPEND ? 4 : 1];
+    bool live[RPW];
+    int pos[RPW];
 #pragma unroll
-    for (int k = 0; k < NP; ++k) {
-      const int i = (lane + 32 * k) * VEC;
-      if (i < half) {
-        load_vec<VEC>(x + i, lo + k * VEC);
-        load_vec<VEC>(x + i + half, hi + k * VEC);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-          ss += lo[k * VEC + e] * lo[k * VEC + e] + hi[k * VEC + e] * hi[k * VEC + e];
+    for (int r = 0; r < RPW; ++r) {
+      const long row = row0 + r;
+      live[r] = row < rows;
+      pos[r] = 0;
+      if (!live[r]) continue;
+      const int b = (int)(row / ((long)j.NH * j.L));
+      const int l = (int)(row % j.L);
+      const int s0 = j.start[b];
+      // Device-side re-check of the positions the host could not see.
+      if (s0 < 0 || (long)s0 + j.L - 1 >= (long)j.max_positions) {
+        if (lane == 0 && l == 0) report(j.status, ATTN_DEV_POSITION);
+        live[r] = false;
+        continue;
       }
-    }
-    if (need_tail) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int t = lane + 32 * k;
-        if (t < ntail) {
-          tl[k] = *reinterpret_cast<const float2*>(x + R + 2 * t);
-          ss += tl[k].x * tl[k].x + tl[k].y * tl[k].y;
-        }
+      if (append && j.window == 0 && (long)s0 + j.L > (long)j.capacity) {
+        if (lane == 0 && l == 0) report(j.status, ATTN_DEV_CAPACITY);
+        live[r] = false;
+        continue;
       }
-    }
-
-    if (j.norm_w) {
-      ss = warp_sum(ss);
-      const float inv_rms = 1.0f / sqrtf(ss / (float)D + j.norm_eps);
+      pos[r] = s0 + l;
+      const float* x = j.x + row * D;
 #pragma unroll
       for (int k = 0; k < NP; ++k) {
         const int i = (lane + 32 * k) * VEC;
         if (i < half) {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            lo[k * VEC + e] = lo[k * VEC + e] * inv_rms * j.norm_w[i + e];
-            hi[k * VEC + e] = hi[k * VEC + e] * inv_rms * j.norm_w[i + half + e];
-          }
+          load_vec<VEC>(x + i, lo[r] + k * VEC);
+          load_vec<VEC>(x + i + half, hi[r] + k * VEC);
         }
       }
+      if (j.table) {
+        const float2* tab = j.table + (long)pos[r] * half;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int t = lane + 32 * k;
-        if (t < ntail) {
-          tl[k].x = tl[k].x * inv_rms * j.norm_w[R + 2 * t];
-          tl[k].y = tl[k].y * inv_rms * j.norm_w[R + 2 * t + 1];
+        for (int k = 0; k < NP; ++k) {
+          const int i = (lane + 32 * k) * VEC;
+          if (i < half)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) cs[r][k * VEC + e] = tab[i + e];
         }
       }
-    }
-
-    if (j.table) {
-      const float2* tab = j.table + (long)p * half;
-#pragma unroll
-      for (int k = 0; k < NP; ++k) {
-        const int i = (lane + 32 * k) * VEC;
-        if (i < half) {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float2 cs = tab[i + e];
-            const float a = lo[k * VEC + e], bb = hi[k * VEC + e];
-            lo[k * VEC + e] = fmaf(a, cs.x, -bb * cs.y);
-            hi[k * VEC + e] = fmaf(a, cs.y, bb * cs.x);
-          }
-        }
-      }
-    }
-
-    // Write back the rotated row (in place) ...
-    if (j.table || j.norm_w) {
-#pragma unroll
-      for (int k = 0; k < NP; ++k) {
-        const int i = (lane + 32 * k) * VEC;
-        if (i < half) {
-          store_vec<VEC>(x + i, lo + k * VEC);
-          store_vec<VEC>(x + i + half, hi + k * VEC);
-        }
-      }
-      if (j.norm_w) {
+      if constexpr (TAIL) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int t = lane + 32 * k;
-          if (t < ntail) *reinterpret_cast<float2*>(x + R + 2 * t) = tl[k];
+          if (t < ntail) tl[r][k] = *reinterpret_cast<const float2*>(x + R + 2 * t);
+        }
+      }
+      if constexpr (APPEND) {
+        const float2* vs = reinterpret_cast<const float2*>(j.v + row * D);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = lane + 32 * k;
+          if (t < D / 2) vv[r][k] = vs[t];
         }
       }
     }
 
-    // ... and, for key rows, into the cache next to the value row.
-    if (append) {
-      // Of a chunk longer than the ring only its last W positions survive;
-      // writing the earlier ones would race on the same slots.
-      if (j.window > 0 && l < j.L - j.window) continue;
-      const long slot = j.window > 0 ? (long)(p % j.window) : (long)p;
-      const long hrow = row / j.L;                      // b * NH + head
-      const long dst = (hrow * j.capacity + slot) * D;
-      float* kc = j.k_cache + dst;
 #pragma unroll
-      for (int k = 0; k < NP; ++k) {
-        const int i = (lane + 32 * k) * VEC;
-        if (i < half) {
-          store_vec<VEC>(kc + i, lo + k * VEC);
-          store_vec<VEC>(kc + i + half, hi + k * VEC);
+    for (int r = 0; r < RPW; ++r) {
+      if (!live[r]) continue;
+      const long row = row0 + r;
+      if (TAIL && j.norm_w) {
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < NP; ++k)
+          if ((lane + 32 * k) * VEC < half)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+              ss += lo[r][k * VEC + e] * lo[r][k * VEC + e] + hi[r][k * VEC + e] * hi[r][k * VEC + e];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (lane + 32 * k < ntail) ss += tl[r][k].x * tl[r][k].x + tl[r][k].y * tl[r][k].y;
+        ss = warp_sum(ss);
+        const float inv_rms = 1.0f / sqrtf(ss / (float)D + j.norm_eps);
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+          const int i = (lane + 32 * k) * VEC;
+          if (i < half) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+              lo[r][k * VEC + e] = lo[r][k * VEC + e] * inv_rms * j.norm_w[i + e];
+              hi[r][k * VEC + e] = hi[r][k * VEC + e] * inv_rms * j.norm_w[i + half + e];
+            }
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = lane + 32 * k;
+          if (t < ntail) {
+            tl[r][k].x = tl[r][k].x * inv_rms * j.norm_w[R + 2 * t];
+            tl[r][k].y = tl[r][k].y * inv_rms * j.norm_w[R + 2 * t + 1];
+          }
         }
       }
+      if (j.table) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int t = lane + 32 * k;
-        if (t < ntail) *reinterpret_cast<float2*>(kc + R + 2 * t) = tl[k];
+        for (int k = 0; k < NP; ++k) {
+          const int i = (lane + 32 * k) * VEC;
+          if (i < half) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+              const float2 c = cs[r][k * VEC + e];
+              const float a = lo[r][k * VEC + e], bb = hi[r][k * VEC + e];
+              lo[r][k * VEC + e] = fmaf(a, c.x, -bb * c.y);
+              hi[r][k * VEC + e] = fmaf(a, c.y, bb * c.x);
+            }
+          }
+        }
       }
-      const float2* vs = reinterpret_cast<const float2*>(j.v + row * D);
-      float2* vd = reinterpret_cast<float2*>(j.v_cache + dst);
-      for (int t = lane; t < D / 2; t += 32) vd[t] = vs[t];
+      float* x = j.x + row * D;
+      // Write back the rotated row (in place) ...
+      if (j.table || j.norm_w) {
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+          const int i = (lane + 32 * k) * VEC;
+          if (i < half) {
+            store_vec<VEC>(x + i, lo[r] + k * VEC);
+            store_vec<VEC>(x + i + half, hi[r] + k * VEC);
+          }
+        }
+        if (TAIL && j.norm_w) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int t = lane + 32 * k;
+            if (t < ntail) *reinterpret_cast<float2*>(x + R + 2 * t) = tl[r][k];
+          }
+        }
+      }
+      // ... and, for key rows, into the cache next to the value row.
+      if constexpr (APPEND) {
+        const int l = (int)(row % j.L);
+        // Of a chunk longer than the ring only its last W positions survive;
+        // writing the earlier ones would race on the same slots.
+        if (j.window > 0 && l < j.L - j.window) continue;
+        const long slot = j.window > 0 ? (long)(pos[r] % j.window) : (long)pos[r];
+        const long hrow = row / j.L;                      // b * NH + head
+        const long dst = (hrow * j.capacity + slot) * D;
+        float* kc = j.k_cache + dst;
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+          const int i = (lane + 32 * k) * VEC;
+          if (i < half) {
+            store_vec<VEC>(kc + i, lo[r] + k * VEC);
+            store_vec<VEC>(kc + i + half, hi[r] + k * VEC);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = lane + 32 * k;
+          if (t < ntail) *reinterpret_cast<float2*>(kc + R + 2 * t) = tl[r][k];
+        }
+        float2* vd = reinterpret_cast<float2*>(j.v_cache + dst);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int t = lane + 32 * k;
+          if (t < D / 2) vd[t] = vv[r][k];
+        }
+      }
     }
   }
+}
+
+// Rows per warp: 4 for plain rotations, 2 when value rows and tails ride along
+// (register budget vs. reads in flight).
+template <int VEC>
+cudaError_t launch_rows(const RopeJob& j, bool append, bool tail, long blocks,
+                        cudaStream_t stream) {
+  const unsigned g4 = (unsigned)blocks, g2 = (unsigned)(blocks * 2 < 152L * 8 ? blocks * 2 : 152L * 8);
+  if (append)
+    rope_rows_kernel<VEC, 2, true, true><<<g2, 256, 0, stream>>>(j);
+  else if (tail)
+    rope_rows_kernel<VEC, 2, false, true><<<g2, 256, 0, stream>>>(j);
+  else
+    rope_rows_kernel<VEC, 4, false, false><<<g4, 256, 0, stream>>>(j);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_rope_rows(const RopeJob& j, cudaStream_t stream) {
@@ -221,16 +276,15 @@ cudaError_t launch_rope_rows(const RopeJob& j, cudaStream_t stream) {
   const long rows = (long)j.B * j.NH * j.L;
   if (rows == 0) return cudaSuccess;
   const int threads = 256, wpb = threads / 32;
-  long blocks = (rows + wpb - 1) / wpb;
-  const long cap = 152L * 16;                   // up to 16 resident blocks per SM
+  long blocks = (rows + wpb * 4 - 1) / (wpb * 4);
+  const long cap = 152L * 8;                    // one full wave of 8 blocks per SM
   if (blocks > cap) blocks = cap;
+  const bool append = j.k_cache != nullptr;
+  const bool tail = append || j.norm_w != nullptr;
   if (half % 4 == 0 && half >= 128)
-    rope_rows_kernel<4><<<(unsigned)blocks, threads, 0, stream>>>(j);
-  else if (half % 2 == 0)
-    rope_rows_kernel<2><<<(unsigned)blocks, threads, 0, stream>>>(j);
-  else
-    rope_rows_kernel<1><<<(unsigned)blocks, threads, 0, stream>>>(j);
-  return cudaGetLastError();
+    return launch_rows<4>(j, append, tail, blocks, stream);
+  if (half % 2 == 0) return launch_rows<2>(j, append, tail, blocks, stream);
+  return launch_rows<1>(j, append, tail, blocks, stream);
 }
 
 }  // namespace gqa
