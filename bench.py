@@ -44,6 +44,12 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workload", default="llama3_8b_prefill",
+                    choices=["llama3_8b_prefill", "gemma2_window"],
+                    help="prefill workload of the timed step")
+    ap.add_argument("--decode-batch", type=int, default=0,
+                    help="rows of the batched decode (default: the workload's 64; smaller "
+                         "values are for profiling captures)")
     return ap.parse_args()
 
 
@@ -151,6 +157,13 @@ def prefill_flops(w, B=None, H=None):
     B = w.B if B is None else B
     H = w.H if H is None else H
     return 4.0 * B * H * w.D * visible_pairs(w.L, w.window)
+
+
+def prefill_bytes(w):
+    """Bytes the prefill step touches: q, k, v, out and both cache buffers."""
+    cap = w.window if w.window else w.capacity
+    return 4 * (2 * w.B * w.H * w.L * w.D + 2 * w.B * w.Hkv * w.L * w.D
+                + 2 * w.B * w.Hkv * cap * w.D)
 
 
 def bench_prefill(w, args, dist, dev, rank):
@@ -349,7 +362,7 @@ def reference_arm(args, w, rank):
 def main():
     args = parse()
     from gqa_causal_attention_gb300 import synthetic as syn
-    w = syn.WORKLOADS["llama3_8b_prefill"]
+    w = syn.WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
@@ -376,6 +389,9 @@ def main():
     dec = None
     if not args.no_decode:
         wd = syn.WORKLOADS["batched_decode"]
+        if args.decode_batch:
+            import dataclasses
+            wd = dataclasses.replace(wd, B=args.decode_batch)
         dec = bench_decode(wd, args, dist, dev)
 
     if rank != 0:
@@ -388,9 +404,12 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "tf32" if g.load() and w.D % 4 == 0 else "f32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "Hkv": w.Hkv, "D": w.D,
-                   "rope": "theta 5e5, llama3 (8, 1, 4, 8192)", "mask": "causal",
+                   "rope": f"theta {w.theta:g}" + (f", {w.scaling[0]} {tuple(w.scaling[1:])}"
+                                                   if w.scaling else ""),
+                   "mask": f"window {w.window}" if w.window else "causal",
+                   "softcap": w.softcap, "qk_norm": w.qk_norm,
                    "step": "rope(q) + rope(k)+cache append + prefill attention",
-                   "l2": "inputs larger than L2 (q, k, v, out, cache: 384 MiB per step)",
+                   "l2": f"inputs larger than L2 ({prefill_bytes(w) / 2**20:.0f} MiB per step)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": pk["tf32_tflops"],
                      "unit": "TFLOP/s", "frac": kern_tflops / pk["tf32_tflops"],
