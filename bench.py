@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b_prefill",
                     choices=["llama3_8b_prefill", "gemma2_window"],
                     help="prefill workload of the timed step")
+    ap.add_argument("--unfused-q-rope", action="store_true",
+                    help="time attn_rope_apply on q + gqa_attn_prefill instead of the fused call")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="rows of the batched decode (default: the workload's 64; smaller "
                          "values are for profiling captures)")
@@ -184,23 +186,30 @@ def bench_prefill(w, args, dist, dev, rank):
     out = torch.empty_like(q)
     start = torch.zeros(w.B, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    pws = torch.empty(max(4, g.gqa_attn_prefill_workspace_size(w.B, w.Hkv, w.L, w.D) // 4),
-                      device=dev)
+    pws = torch.empty(max(4, g.gqa_attn_prefill_rope_workspace_size(w.B, w.H, w.Hkv, w.L, w.D,
+                                                                    rp) // 4), device=dev)
     kern = []
 
+    def prefill():
+        if args.unfused_q_rope:
+            g.attn_rope_apply(q, start, 0, rp, table, qn, w.norm_eps, status)
+            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
+                               status=status)
+        else:
+            g.gqa_attn_prefill_rope(q, k, v, out, start, 0, rp, table, qn, w.norm_eps, w.window,
+                                    w.softcap, 0.0, workspace=pws, status=status)
+
     def step(record=False):
-        g.attn_rope_apply(q, start, 0, rp, table, qn, w.norm_eps, status)
+        # k: RMSNorm + RoPE in place and into the cache; q: RMSNorm + RoPE inside the prefill
         g.kv_cache_append(k, v, start, 0, rp, table, kn, w.norm_eps, kc, vc, w.window, status)
         if record:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
-                               status=status)
+            prefill()
             b.record()
             kern.append((a, b))
         else:
-            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
-                               status=status)
+            prefill()
 
     with ClockSampler(torch.cuda.current_device()) as clk:
         ms = timed(lambda: step(True), args.steps, args.warmup, dist)
@@ -209,7 +218,7 @@ def bench_prefill(w, args, dist, dev, rank):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     res = {"ms": ms / args.steps, "kernel_ms": kern_ms, "clocks": clk.summary(),
-           "launches_per_step": 4}
+           "launches_per_step": 3}
 
     if not args.no_e2e:
         hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
@@ -408,13 +417,14 @@ def main():
                                                    if w.scaling else ""),
                    "mask": f"window {w.window}" if w.window else "causal",
                    "softcap": w.softcap, "qk_norm": w.qk_norm,
-                   "step": "rope(q) + rope(k)+cache append + prefill attention",
+                   "step": "kv_cache_append (k RMSNorm/RoPE + cache) + gqa_attn_prefill_rope "
+                           "(V^T pre-pass; q RMSNorm/RoPE fused into the attention kernel)",
                    "l2": f"inputs larger than L2 ({prefill_bytes(w) / 2**20:.0f} MiB per step)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": pk["tf32_tflops"],
                      "unit": "TFLOP/s", "frac": kern_tflops / pk["tf32_tflops"],
                      "traffic": None,
-                     "kernel": "gqa_attn_prefill", "kernel_ms": pre["kernel_ms"],
+                     "kernel": "gqa_attn_prefill_rope", "kernel_ms": pre["kernel_ms"],
                      "peak_note": f"dense TF32 = {pk['source']} bf16 burst "
                                   f"{pk['bf16_tflops']} x nominal 1.1/2.25",
                      "frac_of_bf16_peak": kern_tflops / pk["bf16_tflops"]},

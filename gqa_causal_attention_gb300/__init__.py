@@ -22,7 +22,7 @@ __all__ = [
     "AttnError", "RopeParams", "load", "library_path",
     "attn_rope_table_bytes", "attn_rope_table_init", "attn_rope_apply", "kv_cache_append",
     "gqa_attn_prefill", "gqa_attn_prefill_workspace_size", "gqa_attn_decode_workspace_size",
-    "gqa_attn_decode",
+    "gqa_attn_decode", "gqa_attn_prefill_rope", "gqa_attn_prefill_rope_workspace_size",
     "gqa_attn_decode_static",
     "attn_status_string", "attn_version", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
@@ -96,6 +96,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_attn_prefill_workspace_size": (sz, [i32, i32, i32, i32]),
             "gqa_attn_prefill": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f, f, vp,
                                        sz, vp, vp]),
+            "gqa_attn_prefill_rope_workspace_size": (sz, [i32, i32, i32, i32, i32, rp]),
+            "gqa_attn_prefill_rope": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                            ctypes.c_int32, rp, vp, vp, f, i32, f, f, vp, sz, vp,
+                                            vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -233,6 +237,40 @@ def gqa_attn_prefill(q, k, v, out, window: int = 0, softcap: float = 0.0, scale:
                                  int(window), float(softcap), float(scale), _ptr(workspace),
                                  wbytes, _ptr(status), _stream(stream))
     _check("gqa_attn_prefill", rc)
+
+
+def gqa_attn_prefill_rope_workspace_size(B: int, H: int, Hkv: int, L: int, D: int,
+                                         params: RopeParams) -> int:
+    return int(load().gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D,
+                                                           ctypes.byref(params)))
+
+
+def gqa_attn_prefill_rope(q, k, v, out, start, max_start: int, params: RopeParams, table,
+                          q_norm_w=None, norm_eps: float = 1e-6, window: int = 0,
+                          softcap: float = 0.0, scale: float = 0.0, workspace=None, status=None,
+                          stream=None) -> None:
+    """Prefill attention of raw q (RMSNorm + RoPE applied inside; q is not modified) over
+    rotated k and v. workspace: gqa_attn_prefill_rope_workspace_size bytes, or None to take
+    one from torch's caching allocator for this call."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _f32(n, t, 4)
+    _f32("table", table); _f32("q_norm_w", q_norm_w); _i32("start", start); _i32("status", status)
+    B, H, L, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, L, D) or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("gqa_attn_prefill_rope: inconsistent shapes")
+    if workspace is None:
+        n = gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, params)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().gqa_attn_prefill_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, L, D,
+                                      _ptr(start), int(max_start), ctypes.byref(params),
+                                      _ptr(table), _ptr(q_norm_w), float(norm_eps), int(window),
+                                      float(softcap), float(scale), _ptr(workspace), wbytes,
+                                      _ptr(status), _stream(stream))
+    _check("gqa_attn_prefill_rope", rc)
 
 
 def gqa_attn_decode_workspace_size(B: int, H: int, Hkv: int, D: int, max_cache_len: int,

@@ -183,6 +183,80 @@ int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out,
   return cuda_status(gqa::launch_prefill_simt(a, s));
 }
 
+namespace {
+// The fused path applies q's RMSNorm + RoPE inside the tensor-core kernel.
+bool rope_fused(int D, int R) {
+  return gqa::prefill_tc_supports(D) && gqa::prefill_fuses_rope(D) && R % 64 == 0;
+}
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+}  // namespace
+
+size_t gqa_attn_prefill_rope_workspace_size(int B, int H, int Hkv, int L, int D,
+                                            const attn_rope_params* rp) {
+  const size_t base = gqa_attn_prefill_workspace_size(B, Hkv, L, D);
+  if (base == 0 || H < 1 || !rope_params_ok(rp, D)) return 0;
+  if (rope_fused(D, rope_dim_of(rp, D))) return base;
+  return round256(base) + (size_t)B * H * L * D * sizeof(float);
+}
+
+int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float* out, int B,
+                          int H, int Hkv, int L, int D, const int32_t* start, int32_t max_start,
+                          const attn_rope_params* rp, const float* table, const float* q_norm_w,
+                          float norm_eps, int window, float softcap, float scale,
+                          void* workspace, size_t workspace_bytes, int32_t* status,
+                          void* stream) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!q || !k || !v || !out || !start || !rp || !table) return ATTN_ERR_NULL;
+  if (!rope_params_ok(rp, D) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(table) ||
+      (q_norm_w && !aligned16(q_norm_w)))
+    return ATTN_ERR_ALIGN;
+  if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_pos_of(rp))
+    return ATTN_ERR_POSITION;
+  const size_t need = gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = rope_dim_of(rp, D);
+  gqa::AttnShape a{};
+  a.k = k; a.v = v; a.out = out;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.L = L; a.D = D;
+  a.window = window; a.softcap = softcap > 0.f ? softcap : 0.f;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  a.status = status;
+  if (rope_fused(D, R)) {
+    a.q = q;
+    a.rope.table = reinterpret_cast<const float2*>(table);
+    a.rope.start = start;
+    a.rope.norm_w = q_norm_w;
+    a.rope.norm_eps = norm_eps;
+    a.rope.R = R;
+    a.rope.max_positions = max_pos_of(rp);
+    a.vt = static_cast<float*>(workspace);
+    a.vt_pitch = gqa::prefill_vt_pitch(L);
+    return cuda_status(gqa::launch_prefill_tc(a, s));
+  }
+  // Other shapes: rotate q out of place into the workspace, then the plain kernels.
+  const size_t base = gqa_attn_prefill_workspace_size(B, Hkv, L, D);
+  float* qrot = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(base));
+  gqa::RopeJob j{};
+  j.x = const_cast<float*>(q); j.y = qrot;
+  j.B = B; j.NH = H; j.L = L; j.D = D; j.R = R;
+  j.start = start; j.max_positions = max_pos_of(rp);
+  j.table = reinterpret_cast<const float2*>(table);
+  j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status;
+  if (cudaError_t e = gqa::launch_rope_rows(j, s); e != cudaSuccess) return ATTN_ERR_CUDA;
+  a.q = qrot;
+  if (gqa::prefill_tc_supports(D)) {
+    a.vt = static_cast<float*>(workspace);
+    a.vt_pitch = gqa::prefill_vt_pitch(L);
+    return cuda_status(gqa::launch_prefill_tc(a, s));
+  }
+  return cuda_status(gqa::launch_prefill_simt(a, s));
+}
+
 size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cache_len,
                                       int window) {
   if (B < 1 || H < 1 || Hkv < 1 || H % Hkv || D < 2 || max_cache_len < 1 || window < 0) return 0;

@@ -16,7 +16,8 @@ struct InvFreq {
 };
 
 struct RopeJob {
-  float* x;                 // [B, NH, L, D], rotated in place
+  float* x;                 // [B, NH, L, D], rotated in place (or read only, see y)
+  float* y;                 // nullptr: in place; else rotated rows go here ([B, NH, L, D])
   int B, NH, L, D, R;
   const int32_t* start;     // [B]
   int max_positions;
@@ -36,6 +37,15 @@ cudaError_t launch_rope_table(const InvFreq& inv, int R, int max_positions, floa
                               cudaStream_t stream);
 cudaError_t launch_rope_rows(const RopeJob& job, cudaStream_t stream);
 
+// Fused q RMSNorm + RoPE inside the tensor-core prefill (q is then the raw query).
+struct QRope {
+  const float2* table;      // [max_positions][R/2] (cos, sin); nullptr: q already rotated
+  const int32_t* start;     // [B]
+  const float* norm_w;      // [D] or nullptr
+  float norm_eps;
+  int R, max_positions;
+};
+
 struct AttnShape {
   const float* q;           // [B, H, L, D]
   const float* k;           // [B, Hkv, L, D]
@@ -48,6 +58,7 @@ struct AttnShape {
   float softcap;            // <= 0: off
   float scale;              // > 0
   int32_t* status;
+  QRope rope;               // rope.table == nullptr: q already rotated
 };
 
 cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
@@ -56,6 +67,7 @@ cudaError_t launch_prefill_tc(const AttnShape& a, cudaStream_t stream);
 bool prefill_tc_supports(int D);
 int prefill_vt_pitch(int L);   // row pitch (floats) of the V^T workspace
 cudaError_t launch_prefill_tq(const AttnShape& a, cudaStream_t stream);  // D <= 128
+bool prefill_fuses_rope(int D);  // the kernel taking D applies a.rope itself
 
 struct DecodeJob {
   const float* q;           // [B, H, D]

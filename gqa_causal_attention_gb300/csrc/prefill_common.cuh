@@ -25,6 +25,12 @@ struct TcArgs {
   int B, H, Hkv, L, D;
   int G, QT, ntiles, npairs;                   // per (b, kv head): tiles and tile groups
   int units;                                   // persistent kernel: B * H * QT query tiles
+  // Fused q RMSNorm + RoPE (persistent kernel): rope_table == nullptr means q is rotated.
+  const float2* rope_table;                    // [max_positions][R/2] (cos, sin)
+  const int32_t* rope_start;                   // [B]
+  const float* qnorm_w;                        // [D] or nullptr
+  float qnorm_eps;
+  int rope_R, rope_max_positions;
   int window;
   int softcap_on;
   float c_score;                               // scale * log2(e)

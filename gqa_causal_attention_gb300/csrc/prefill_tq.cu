@@ -40,7 +40,7 @@ struct PCfg {
   static constexpr int kEpi = 4 * 4096;                 // per-warp 32 x 32 output staging
   static constexpr int kNSraw = (kSmemLimit - 2048 - kEpi) / kStage;
   static constexpr int NS = kNSraw > 8 ? 8 : kNSraw;
-  static constexpr int kThreads = 64 + 128;
+  static constexpr int kThreads = 64 + 128 + 32;     // producer, MMA, 4 softmax, Q prep
   static constexpr int kSmemNeed = NS * kStage + kEpi + 2048;
   static constexpr int kSmem =
       kSmemNeed > kSmemLimit / 2 + 4096 ? kSmemNeed : kSmemLimit / 2 + 4096;
@@ -58,6 +58,9 @@ struct PBars {
   uint64_t o_done;
   uint64_t o_final;
   uint64_t o_free;
+  uint64_t q_full;                             // fused RoPE: a Q tile has landed (one phase per unit)
+  uint64_t q_ready;                            // fused RoPE: Q tile rotated in its stage
+  uint64_t q_taken;                            // the MMA issuer has seen that q_ready
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -102,10 +105,20 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
   bool filled[8];
 #pragma unroll
   for (int s = 0; s < 8; ++s) filled[s] = false;
+  uint32_t q_fills = 0;
   // kind: 0 = Q tile, 1 = K block, 2 = V^T block
   auto load = [&](int kind, const PUnit& u, int j) -> bool {
     if (!tc::mbar_wait(&bars->kv_empty[stage], phase ^ 1u, abort)) return false;
     uint64_t* full = &bars->kv_full[stage];
+    if (kind == 0 && a.rope_table) {
+      // Fused RoPE: the Q warp must wait for exactly this tile, so it lands on
+      // q_full (one phase per unit); the stage's own barrier gets a plain
+      // arrival to keep the ring's phase count (the MMA issuer also waits for
+      // the Q warp before touching this stage).
+      tc::mbar_arrive(full);
+      full = &bars->q_full;
+      ++q_fills;
+    }
     tc::mbar_arrive_expect_tx(full, C::kStage);
     uint8_t* dst = skv + stage * C::kStage;
     if (kind == 0) {
@@ -134,6 +147,14 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
     ok = load(0, u, 0) && load(1, u, u.jlo);
+    // The next unit's Q tile enters the ring only after this unit's last K
+    // block is consumed; warm it into L2 now so that load is short.
+    const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
+    if (ok && xn < a.units) {
+      const PUnit un = get_unit<C>(a, xn);
+      for (int c = 0; c < C::kChunks; ++c)
+        tc::tma_prefetch_l2_3d(tq, 32 * c, un.q0, un.b * a.H + un.h);
+    }
     for (int i = 0; ok && i < u.n; ++i) {
       if (i + 1 < u.n) ok = load(1, u, u.jlo + i + 1);
       if (ok) ok = load(2, u, u.jlo + i);
@@ -142,6 +163,7 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
   // Every copy this block started lands before the block may exit.
   for (int s = 0; s < C::NS; ++s)
     if (filled[s]) drain_wait(&bars->kv_full[s], fill_parity[s]);
+  if (q_fills > 0) drain_wait(&bars->q_full, (q_fills - 1) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
@@ -195,8 +217,13 @@ __device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
     int st = 0;
-    // Q tile: shared -> tensor memory, behind every earlier MMA that read Q.
+    // Q tile: shared -> tensor memory, behind every earlier MMA that read Q. With
+    // fused RoPE the softmax warps first rotate the tile in place (q_ready).
     if (!(ok = next(st))) break;
+    if (a.rope_table) {
+      if (!(ok = tc::mbar_wait(&bars->q_ready, uc & 1, abort))) break;
+      tc::mbar_arrive(&bars->q_taken);        // keeps the Q warp at most one unit ahead
+    }
     tc::fence_after_sync();
     {
       const uint64_t qd = stage_desc(st);
@@ -237,11 +264,144 @@ __device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars
   drain_wait(&bars->drain, 0);
 }
 
+// ---------------------------------------------------------------- fused q RoPE (Q-prep warp)
+// The unit's Q tile is rotated in place in its ring stage before the MMA issuer
+// copies it to tensor memory with tcgen05.cp. A row is handled by LPR lanes, each
+// holding two 16-byte units of it: a rotating lane t holds columns 4t .. 4t+3
+// and their rotate-half partners 4t+R/2 .. (units t and t + R/8); the remaining
+// lanes hold the pass-through columns past R in pairs of units. So every access
+// is one 16-byte shared-memory load or store (the 128-byte swizzle keeps a row's
+// eight units of a chunk in distinct bank groups), and 32 / LPR rows go per warp
+// access. RMSNorm (if q_norm_w) first, over the row's lanes, then RoPE at the
+// row's absolute position. Requires D % 32 == 0, D <= 128 and R % 64 == 0.
+template <class C>
+__device__ bool tq_qprep(const TcArgs& a, uint8_t* skv, PBars* bars, const PUnit& u,
+                         uint32_t ring_pos, uint32_t uc, int lane) {
+  volatile int* abort = &bars->abort;
+  constexpr int LPR = C::DP > 64 ? 16 : 8;    // lanes per row
+  constexpr int RPI = 32 / LPR;               // rows per warp-wide access
+  constexpr int NJ = 4;                       // independent rows per lane and iteration
+  constexpr int ROWS = NJ * RPI;              // rows per iteration (kBM is a multiple)
+  static_assert(kBM % ROWS == 0, "tile rows");
+  const int t = lane % LPR, grp = lane / LPR;
+  const int half = a.rope_R / 2;
+  const int nrot = a.rope_R / 8;              // rotating lanes, 4 pairs each
+  const bool active = t < a.D / 8;
+  const bool rot = t < nrot;
+  const int ua = rot ? t : a.rope_R / 4 + (t - nrot);
+  const int ub = rot ? t + nrot : ua + (a.D - a.rope_R) / 8;
+  uint8_t* base = skv + (ring_pos % C::NS) * C::kStage;
+  // 16-byte unit U (columns 4U .. 4U+3) of row r: line r of chunk U / 8, swizzled by r % 8
+  auto unit = [&](int r, int U) -> float4* {
+    return reinterpret_cast<float4*>(base + (U >> 3) * C::kKChunk + r * 128 +
+                                     (((U & 7) ^ (r & 7)) << 4));
+  };
+  // Rows past L are zeros and stay zeros. Angles advance by recurrence: the row
+  // ROWS further on uses (cos, sin)((p + ROWS) theta_i), the current pair turned
+  // by (cos, sin)(ROWS theta_i) from table row ROWS; at most kBM / ROWS - 1 = 15
+  // turns per tile keep the drift near 1e-6 relative.
+  const int nrows = max(0, min(kBM, a.L - u.q0));
+  const long p0 = static_cast<long>(a.rope_start[u.b]) + u.q0;
+  const bool inrange = p0 >= 0 && p0 + nrows <= a.rope_max_positions;
+  if (!inrange && nrows > 0 && lane == 0) report(a.status, ATTN_DEV_POSITION);
+  auto row_cs = [&](long p, bool use, float2 (&c)[4]) {
+    const float4* tr = reinterpret_cast<const float4*>(a.rope_table + (use ? p : 0) * half + 4 * t);
+    const float4 c01 = use ? __ldg(tr) : make_float4(1.f, 0.f, 1.f, 0.f);
+    const float4 c23 = use ? __ldg(tr + 1) : make_float4(1.f, 0.f, 1.f, 0.f);
+    c[0] = make_float2(c01.x, c01.y); c[1] = make_float2(c01.z, c01.w);
+    c[2] = make_float2(c23.x, c23.y); c[3] = make_float2(c23.z, c23.w);
+  };
+  float2 cs[NJ][4], st[4];
+#pragma unroll
+  for (int j = 0; j < NJ; ++j) row_cs(p0 + RPI * j + grp, rot && inrange && RPI * j + grp < nrows, cs[j]);
+  // a table of at most ROWS rows means at most ROWS rows here: the step is never used
+  row_cs(ROWS, rot && inrange && a.rope_max_positions > ROWS, st);
+  float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
+  if (a.qnorm_w && active) {
+    wa = __ldg(reinterpret_cast<const float4*>(a.qnorm_w) + ua);
+    wb = __ldg(reinterpret_cast<const float4*>(a.qnorm_w) + ub);
+  }
+  const bool ok = tc::mbar_wait(&bars->q_full, uc & 1, abort);
+  if (__any_sync(0xffffffffu, !ok)) return false;
+  auto turn = [](float& x0, float& x1, float2 c) {
+    const float a0 = x0, a1 = x1;
+    x0 = fmaf(a0, c.x, -a1 * c.y);
+    x1 = fmaf(a0, c.y, a1 * c.x);
+  };
+  const float inv_d = 1.0f / static_cast<float>(a.D);
+#pragma unroll 1
+  for (int r0 = 0; r0 < nrows; r0 += ROWS) {
+    float4 xa[NJ], xb[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      xa[j] = xb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (active) {
+        xa[j] = *unit(r0 + RPI * j + grp, ua);
+        xb[j] = *unit(r0 + RPI * j + grp, ub);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      if (a.qnorm_w) {
+        float ss = xa[j].x * xa[j].x + xa[j].y * xa[j].y + xa[j].z * xa[j].z + xa[j].w * xa[j].w +
+                   xb[j].x * xb[j].x + xb[j].y * xb[j].y + xb[j].z * xb[j].z + xb[j].w * xb[j].w;
+#pragma unroll
+        for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.0f / sqrtf(ss * inv_d + a.qnorm_eps);
+        xa[j].x *= inv * wa.x; xa[j].y *= inv * wa.y; xa[j].z *= inv * wa.z; xa[j].w *= inv * wa.w;
+        xb[j].x *= inv * wb.x; xb[j].y *= inv * wb.y; xb[j].z *= inv * wb.z; xb[j].w *= inv * wb.w;
+      }
+      if (rot) {
+        turn(xa[j].x, xb[j].x, cs[j][0]);
+        turn(xa[j].y, xb[j].y, cs[j][1]);
+        turn(xa[j].z, xb[j].z, cs[j][2]);
+        turn(xa[j].w, xb[j].w, cs[j][3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) turn(cs[j][e].x, cs[j][e].y, st[e]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const int r = r0 + RPI * j + grp;
+      if (active && r < nrows) {
+        *unit(r, ua) = xa[j];
+        *unit(r, ub) = xb[j];
+      }
+    }
+  }
+  tc::fence_proxy_async();                    // generic writes -> visible to tcgen05.cp
+  __syncwarp();
+  // Signal unit uc only after the issuer has taken unit uc - 1's signal: parity
+  // waits must never see a barrier two phases ahead.
+  if (uc > 0) {
+    const bool seen = lane == 0 ? tc::mbar_wait(&bars->q_taken, (uc - 1) & 1, abort) : true;
+    if (!__shfl_sync(0xffffffffu, seen, 0)) return false;
+  }
+  if (lane == 0) tc::mbar_arrive(&bars->q_ready);
+  return true;
+}
+
+// The Q-prep warp: rotates every unit's Q tile in its ring stage, in unit order,
+// as soon as the tile lands (ring position of a unit's Q: one Q and 2 n blocks
+// per earlier unit).
+template <class C>
+__device__ void tq_qwarp(const TcArgs& a, uint8_t* skv, PBars* bars, int lane) {
+  uint32_t g = 0, uc = 0;
+  for (int r = 0;; ++r) {
+    const int x = unit_of(blockIdx.x, r, gridDim.x);
+    if (x >= a.units) break;
+    const PUnit u = get_unit<C>(a, x);
+    if (!tq_qprep<C>(a, skv, bars, u, uc + 2 * g, uc, lane)) break;
+    g += u.n;
+    ++uc;
+  }
+}
+
 // ---------------------------------------------------------------- softmax (4 warps)
 // Thread = one query row of the current unit; tcgen05.ld/st run on full warps.
 template <class C>
 __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quarter, int lane,
-                           const CUtensorMap* tout, uint8_t* stage_out) {
+                           const CUtensorMap* tout, uint8_t* stage_out, uint8_t* skv) {
   constexpr int BK = C::BK;
   constexpr int NA = 8;                       // independent partial max / sum chains
   volatile int* abort = &bars->abort;
@@ -250,7 +410,6 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
   const float cs = a.softcap_on ? 1.0f : a.c_score;   // raw score -> log2 units
   uint32_t g = 0, uc = 0;
   bool ok = true;
-
   for (int r = 0; ok; ++r) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
@@ -409,6 +568,9 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     tc::mbar_init(&bars->o_done, 1);
     tc::mbar_init(&bars->o_final, 1);
     tc::mbar_init(&bars->o_free, 128);
+    tc::mbar_init(&bars->q_full, 1);
+    tc::mbar_init(&bars->q_ready, 1);
+    tc::mbar_init(&bars->q_taken, 1);
     tc::mbar_init(&bars->drain, 1);
     bars->abort = 0;
     tc::fence_mbar_init();
@@ -429,7 +591,10 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     if (lane == 0) tq_mma<C>(a, tmem, skv, bars);
     __syncwarp();
   } else {
-    tq_softmax<C>(a, tmem, bars, warp % 4, lane, &tm_o, sepi + (warp % 4) * 4096);
+    if (warp < 6)
+      tq_softmax<C>(a, tmem, bars, warp % 4, lane, &tm_o, sepi + (warp % 4) * 4096, skv);
+    else if (a.rope_table)
+      tq_qwarp<C>(a, skv, bars, lane);
   }
 
   tc::fence_before_sync();
@@ -480,12 +645,20 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   a.c_cap_in = s.softcap > 0.f ? 2.0f * kLog2e * s.scale / s.softcap : 0.f;
   a.c_cap_out = kLog2e * s.softcap;
   a.status = s.status;
+  a.rope_table = s.rope.table;
+  a.rope_start = s.rope.start;
+  a.qnorm_w = s.rope.norm_w;
+  a.qnorm_eps = s.rope.norm_eps;
+  a.rope_R = s.rope.R;
+  a.rope_max_positions = s.rope.max_positions;
   const int grid = a.units < sm_count() ? a.units : sm_count();
   prefill_tq_kernel<DP><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+bool prefill_fuses_rope(int D) { return D % 32 == 0 && D <= 128; }
 
 // D <= 128; V^T must already be in s.vt (launch_prefill_tc runs the transpose first).
 cudaError_t launch_prefill_tq(const AttnShape& s, cudaStream_t stream) {

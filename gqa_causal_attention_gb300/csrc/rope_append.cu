@@ -203,9 +203,9 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
           }
         }
       }
-      float* x = j.x + row * D;
-      // Write back the rotated row (in place) ...
-      if (j.table || j.norm_w) {
+      float* x = (j.y ? j.y : j.x) + row * D;
+      // Write back the rotated row (in place or to y) ...
+      if (j.table || j.norm_w || j.y) {
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
           const int i = (lane + 32 * k) * VEC;
@@ -214,7 +214,7 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
             store_vec<VEC>(x + i + half, hi[r] + k * VEC);
           }
         }
-        if (TAIL && j.norm_w) {
+        if (TAIL && (j.norm_w || j.y)) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int t = lane + 32 * k;
@@ -280,7 +280,7 @@ cudaError_t launch_rope_rows(const RopeJob& j, cudaStream_t stream) {
   const long cap = 152L * 8;                    // one full wave of 8 blocks per SM
   if (blocks > cap) blocks = cap;
   const bool append = j.k_cache != nullptr;
-  const bool tail = append || j.norm_w != nullptr;
+  const bool tail = append || j.norm_w != nullptr || (j.y != nullptr && j.R < j.D);
   if (half % 4 == 0 && half >= 128)
     return launch_rows<4>(j, append, tail, blocks, stream);
   if (half % 2 == 0) return launch_rows<2>(j, append, tail, blocks, stream);

@@ -149,6 +149,24 @@ int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out,
                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * Prefill attention with the queries' RMSNorm and RoPE fused in: the same
+ * result as attn_rope_apply(q, start, rp, table, q_norm_w) followed by
+ * gqa_attn_prefill, but q is the raw query and is left unmodified. k must
+ * already be rotated (kv_cache_append does that). For D % 32 == 0, D <= 128 and
+ * rope_dim % 64 == 0 the rotation happens inside the tensor-core kernel, on the
+ * way from shared to tensor memory; other shapes rotate q into the workspace
+ * first. Positions are start[b] + l; max_start bounds every start[b].
+ */
+size_t gqa_attn_prefill_rope_workspace_size(int B, int H, int Hkv, int L, int D,
+                                            const attn_rope_params* rp);
+int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float* out, int B,
+                          int H, int Hkv, int L, int D, const int32_t* start, int32_t max_start,
+                          const attn_rope_params* rp, const float* table, const float* q_norm_w,
+                          float norm_eps, int window, float softcap, float scale,
+                          void* workspace, size_t workspace_bytes, int32_t* status,
+                          void* stream);
+
+/*
  * Bytes of scratch gqa_attn_decode needs for these sizes (split-KV partial
  * results). max_cache_len bounds every cache_len[b].
  */
