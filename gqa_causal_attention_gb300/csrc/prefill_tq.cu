@@ -15,6 +15,10 @@
 //    tensor memory with tcgen05.cp, in order with its MMAs, so the next
 //    unit's first S products overlap the previous unit's last softmax and its
 //    epilogue; only the first P V of a unit waits for O to be read out.
+//  * With q RoPE fused (gqa_attn_prefill_rope), the softmax warps rotate each
+//    Q tile in tensor memory after tcgen05.cp and before its first S MMA (the
+//    tile enters the ring right after the previous unit's last K block, so
+//    this overlaps that unit's last P V products).
 //  * Softmax, masking, softcap, rescaling and the epilogue are those of the
 //    non-persistent kernel (one query row per thread, base-2 online softmax,
 //    P truncated to TF32 in place of S).
@@ -40,7 +44,7 @@ struct PCfg {
   static constexpr int kEpi = 4 * 4096;                 // per-warp 32 x 32 output staging
   static constexpr int kNSraw = (kSmemLimit - 2048 - kEpi) / kStage;
   static constexpr int NS = kNSraw > 8 ? 8 : kNSraw;
-  static constexpr int kThreads = 64 + 128 + 32;     // producer, MMA, 4 softmax, Q prep
+  static constexpr int kThreads = 64 + 128;          // producer, MMA, 4 softmax
   static constexpr int kSmemNeed = NS * kStage + kEpi + 2048;
   static constexpr int kSmem =
       kSmemNeed > kSmemLimit / 2 + 4096 ? kSmemNeed : kSmemLimit / 2 + 4096;
@@ -58,9 +62,8 @@ struct PBars {
   uint64_t o_done;
   uint64_t o_final;
   uint64_t o_free;
-  uint64_t q_full;                             // fused RoPE: a Q tile has landed (one phase per unit)
-  uint64_t q_ready;                            // fused RoPE: Q tile rotated in its stage
-  uint64_t q_taken;                            // the MMA issuer has seen that q_ready
+  uint64_t q_copied;                           // a Q tile is in tensor memory (one phase per unit)
+  uint64_t q_ready;                            // fused RoPE: that Q tile is rotated
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -91,7 +94,12 @@ __device__ __forceinline__ PUnit get_unit(const TcArgs& a, int x) {
 }
 
 // ---------------------------------------------------------------- producer (one thread)
-// Ring order per unit: Q tile, K_0, then (K_{i+1}, V^T_i) for each key block i.
+// Ring order: the first unit's Q tile; then per unit K_0 .. K_{n-1} interleaved
+// with V^T_0 .. V^T_{n-1} as K_0, (K_{i+1}, V^T_i)..., and the next unit's Q
+// tile. With fused RoPE that Q tile comes right after this unit's last K block,
+// so it lands while this unit's last P V products are pending and the softmax
+// warps can rotate it in tensor memory before the next unit's first S = Q K^T;
+// otherwise it comes after the last V^T block.
 template <class C>
 __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                             const CUtensorMap* tv, uint8_t* skv, PBars* bars) {
@@ -105,20 +113,10 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
   bool filled[8];
 #pragma unroll
   for (int s = 0; s < 8; ++s) filled[s] = false;
-  uint32_t q_fills = 0;
   // kind: 0 = Q tile, 1 = K block, 2 = V^T block
   auto load = [&](int kind, const PUnit& u, int j) -> bool {
     if (!tc::mbar_wait(&bars->kv_empty[stage], phase ^ 1u, abort)) return false;
     uint64_t* full = &bars->kv_full[stage];
-    if (kind == 0 && a.rope_table) {
-      // Fused RoPE: the Q warp must wait for exactly this tile, so it lands on
-      // q_full (one phase per unit); the stage's own barrier gets a plain
-      // arrival to keep the ring's phase count (the MMA issuer also waits for
-      // the Q warp before touching this stage).
-      tc::mbar_arrive(full);
-      full = &bars->q_full;
-      ++q_fills;
-    }
     tc::mbar_arrive_expect_tx(full, C::kStage);
     uint8_t* dst = skv + stage * C::kStage;
     if (kind == 0) {
@@ -146,24 +144,29 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
-    ok = load(0, u, 0) && load(1, u, u.jlo);
-    // The next unit's Q tile enters the ring only after this unit's last K
-    // block is consumed; warm it into L2 now so that load is short.
     const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
-    if (ok && xn < a.units) {
-      const PUnit un = get_unit<C>(a, xn);
+    const bool has_next = xn < a.units;
+    const PUnit un = get_unit<C>(a, has_next ? xn : x);
+    // Warm the next Q tile into L2 now: its load comes within a few blocks.
+    if (has_next)
       for (int c = 0; c < C::kChunks; ++c)
         tc::tma_prefetch_l2_3d(tq, 32 * c, un.q0, un.b * a.H + un.h);
-    }
+    const bool early = a.rope_table && has_next;  // next Q after the last K, else after the last V
+    if (r == 0) ok = load(0, u, 0);
+    if (ok) ok = load(1, u, u.jlo);
+    if (ok && u.n == 1 && early) ok = load(0, un, 0);
     for (int i = 0; ok && i < u.n; ++i) {
-      if (i + 1 < u.n) ok = load(1, u, u.jlo + i + 1);
+      if (i + 1 < u.n) {
+        ok = load(1, u, u.jlo + i + 1);
+        if (ok && i + 2 == u.n && early) ok = load(0, un, 0);
+      }
       if (ok) ok = load(2, u, u.jlo + i);
     }
+    if (ok && has_next && !early) ok = load(0, un, 0);
   }
   // Every copy this block started lands before the block may exit.
   for (int s = 0; s < C::NS; ++s)
     if (filled[s]) drain_wait(&bars->kv_full[s], fill_parity[s]);
-  if (q_fills > 0) drain_wait(&bars->q_full, (q_fills - 1) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuer (one thread)
@@ -210,34 +213,40 @@ __device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars
     }
   };
 
+  // Q tile: shared -> tensor memory, in order behind every earlier MMA that
+  // read the previous Q; q_copied tells the softmax warps it is there.
+  auto copy_q = [&]() -> bool {
+    int st = 0;
+    if (!next(st)) return false;
+    const uint64_t qd = stage_desc(st);
+#pragma unroll
+    for (int kk = 0; kk < C::DP / 8; ++kk) {
+      const int c = kk / 4, j = kk % 4;
+      tc::tmem_cp_128x256b(tmem + C::kQCol + 8 * kk, qd + ((c * C::kKChunk + 32 * j) >> 4));
+    }
+    tc::mma_commit(&bars->q_copied);
+    tc::mma_commit(&bars->kv_empty[st]);
+    return true;
+  };
+
   uint32_t g = 0, uc = 0;       // key blocks and units done so far by this block
   bool ok = true;
   for (int r = 0; ok; ++r) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
+    const bool has_next = unit_of(blockIdx.x, r + 1, gridDim.x) < a.units;
+    const bool early = a.rope_table && has_next;    // ring order as in the producer
     int st = 0;
-    // Q tile: shared -> tensor memory, behind every earlier MMA that read Q. With
-    // fused RoPE the softmax warps first rotate the tile in place (q_ready).
-    if (!(ok = next(st))) break;
-    if (a.rope_table) {
-      if (!(ok = tc::mbar_wait(&bars->q_ready, uc & 1, abort))) break;
-      tc::mbar_arrive(&bars->q_taken);        // keeps the Q warp at most one unit ahead
-    }
+    if (r == 0 && !(ok = copy_q())) break;
+    // With fused RoPE the softmax warps rotate Q in tensor memory first.
+    if (a.rope_table && !(ok = tc::mbar_wait(&bars->q_ready, uc & 1, abort))) break;
     tc::fence_after_sync();
-    {
-      const uint64_t qd = stage_desc(st);
-#pragma unroll
-      for (int kk = 0; kk < C::DP / 8; ++kk) {
-        const int c = kk / 4, j = kk % 4;
-        tc::tmem_cp_128x256b(tmem + C::kQCol + 8 * kk, qd + ((c * C::kKChunk + 32 * j) >> 4));
-      }
-    }
-    tc::mma_commit(&bars->kv_empty[st]);
     if (!(ok = next(st))) break;
     issue_s(g & 1, st);
     tc::mma_commit(&bars->s_full[g & 1]);
     tc::mma_commit(&bars->kv_empty[st]);
+    if (u.n == 1 && early && !(ok = copy_q())) break;
     for (int i = 0; i < u.n; ++i) {
       const uint32_t G = g + i;
       if (i + 1 < u.n) {
@@ -245,6 +254,7 @@ __device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars
         issue_s((G + 1) & 1, st);
         tc::mma_commit(&bars->s_full[(G + 1) & 1]);
         tc::mma_commit(&bars->kv_empty[st]);
+        if (i + 2 == u.n && early && !(ok = copy_q())) break;
       }
       if (!(ok = next(st))) break;
       if (!(ok = tc::mbar_wait(&bars->p_ready[G & 1], (G >> 1) & 1, abort))) break;
@@ -256,6 +266,7 @@ __device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars
     }
     if (!ok) break;
     tc::mma_commit(&bars->o_final);
+    if (has_next && !early && !(ok = copy_q())) break;
     g += u.n;
     ++uc;
   }
@@ -264,144 +275,101 @@ __device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars
   drain_wait(&bars->drain, 0);
 }
 
-// ---------------------------------------------------------------- fused q RoPE (Q-prep warp)
-// The unit's Q tile is rotated in place in its ring stage before the MMA issuer
-// copies it to tensor memory with tcgen05.cp. A row is handled by LPR lanes, each
-// holding two 16-byte units of it: a rotating lane t holds columns 4t .. 4t+3
-// and their rotate-half partners 4t+R/2 .. (units t and t + R/8); the remaining
-// lanes hold the pass-through columns past R in pairs of units. So every access
-// is one 16-byte shared-memory load or store (the 128-byte swizzle keeps a row's
-// eight units of a chunk in distinct bank groups), and 32 / LPR rows go per warp
-// access. RMSNorm (if q_norm_w) first, over the row's lanes, then RoPE at the
-// row's absolute position. Requires D % 32 == 0, D <= 128 and R % 64 == 0.
+// ---------------------------------------------------------------- fused q RoPE (softmax warps)
+// Rotates the unit's Q tile where the MMA reads it, in tensor memory: thread =
+// query row, as in the softmax. RMSNorm (if q_norm_w) over the row first, then
+// RoPE at the row's absolute position start[b] + q0 + row, pairs (i, i + R/2)
+// taken 32 at a time with tcgen05.ld / tcgen05.st, (cos, sin) from the row's
+// table line. Rows past L hold zeros (TMA fill) and are left alone. Requires
+// D % 32 == 0, D <= 128 and R % 64 == 0.
 template <class C>
-__device__ bool tq_qprep(const TcArgs& a, uint8_t* skv, PBars* bars, const PUnit& u,
-                         uint32_t ring_pos, uint32_t uc, int lane) {
+__device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars, const PUnit& u,
+                            int row, uint32_t ucx) {
   volatile int* abort = &bars->abort;
-  constexpr int LPR = C::DP > 64 ? 16 : 8;    // lanes per row
-  constexpr int RPI = 32 / LPR;               // rows per warp-wide access
-  constexpr int NJ = 4;                       // independent rows per lane and iteration
-  constexpr int ROWS = NJ * RPI;              // rows per iteration (kBM is a multiple)
-  static_assert(kBM % ROWS == 0, "tile rows");
-  const int t = lane % LPR, grp = lane / LPR;
+  const int qpos = u.q0 + row;
+  const bool live = qpos < a.L;
+  const long p = static_cast<long>(a.rope_start[u.b]) + qpos;
+  const bool inrange = p >= 0 && p < a.rope_max_positions;
+  if (live && !inrange) report(a.status, ATTN_DEV_POSITION);
+  const bool rot = live && inrange;
   const int half = a.rope_R / 2;
-  const int nrot = a.rope_R / 8;              // rotating lanes, 4 pairs each
-  const bool active = t < a.D / 8;
-  const bool rot = t < nrot;
-  const int ua = rot ? t : a.rope_R / 4 + (t - nrot);
-  const int ub = rot ? t + nrot : ua + (a.D - a.rope_R) / 8;
-  uint8_t* base = skv + (ring_pos % C::NS) * C::kStage;
-  // 16-byte unit U (columns 4U .. 4U+3) of row r: line r of chunk U / 8, swizzled by r % 8
-  auto unit = [&](int r, int U) -> float4* {
-    return reinterpret_cast<float4*>(base + (U >> 3) * C::kKChunk + r * 128 +
-                                     (((U & 7) ^ (r & 7)) << 4));
-  };
-  // Rows past L are zeros and stay zeros. Angles advance by recurrence: the row
-  // ROWS further on uses (cos, sin)((p + ROWS) theta_i), the current pair turned
-  // by (cos, sin)(ROWS theta_i) from table row ROWS; at most kBM / ROWS - 1 = 15
-  // turns per tile keep the drift near 1e-6 relative.
-  const int nrows = max(0, min(kBM, a.L - u.q0));
-  const long p0 = static_cast<long>(a.rope_start[u.b]) + u.q0;
-  const bool inrange = p0 >= 0 && p0 + nrows <= a.rope_max_positions;
-  if (!inrange && nrows > 0 && lane == 0) report(a.status, ATTN_DEV_POSITION);
-  auto row_cs = [&](long p, bool use, float2 (&c)[4]) {
-    const float4* tr = reinterpret_cast<const float4*>(a.rope_table + (use ? p : 0) * half + 4 * t);
-    const float4 c01 = use ? __ldg(tr) : make_float4(1.f, 0.f, 1.f, 0.f);
-    const float4 c23 = use ? __ldg(tr + 1) : make_float4(1.f, 0.f, 1.f, 0.f);
-    c[0] = make_float2(c01.x, c01.y); c[1] = make_float2(c01.z, c01.w);
-    c[2] = make_float2(c23.x, c23.y); c[3] = make_float2(c23.z, c23.w);
-  };
-  float2 cs[NJ][4], st[4];
+  const float4* trow = reinterpret_cast<const float4*>(a.rope_table + (rot ? p : 0) * half);
+  // The row's whole table line (R/2 <= 64 pairs, two per 16-byte load) is
+  // requested before the wait, so its latency overlaps it.
+  float4 t0[16], t1[16];
 #pragma unroll
-  for (int j = 0; j < NJ; ++j) row_cs(p0 + RPI * j + grp, rot && inrange && RPI * j + grp < nrows, cs[j]);
-  // a table of at most ROWS rows means at most ROWS rows here: the step is never used
-  row_cs(ROWS, rot && inrange && a.rope_max_positions > ROWS, st);
-  float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
-  if (a.qnorm_w && active) {
-    wa = __ldg(reinterpret_cast<const float4*>(a.qnorm_w) + ua);
-    wb = __ldg(reinterpret_cast<const float4*>(a.qnorm_w) + ub);
+  for (int e = 0; e < 16; ++e) {
+    t0[e] = rot ? __ldg(trow + e) : make_float4(1.f, 0.f, 1.f, 0.f);
+    t1[e] = rot && half > 32 ? __ldg(trow + 16 + e) : make_float4(1.f, 0.f, 1.f, 0.f);
   }
-  const bool ok = tc::mbar_wait(&bars->q_full, uc & 1, abort);
-  if (__any_sync(0xffffffffu, !ok)) return false;
-  auto turn = [](float& x0, float& x1, float2 c) {
-    const float a0 = x0, a1 = x1;
-    x0 = fmaf(a0, c.x, -a1 * c.y);
-    x1 = fmaf(a0, c.y, a1 * c.x);
-  };
-  const float inv_d = 1.0f / static_cast<float>(a.D);
+  const bool ok = tc::mbar_wait(&bars->q_copied, ucx & 1, abort);
+  if (__any_sync(0xffffffffu, !ok)) return false;   // tcgen05.ld is warp-wide
+  tc::fence_after_sync();
+  const uint32_t qa = lane_base + C::kQCol;
+  float inv = 1.0f;
+  if (a.qnorm_w) {
+    float ss = 0.f;
 #pragma unroll 1
-  for (int r0 = 0; r0 < nrows; r0 += ROWS) {
-    float4 xa[NJ], xb[NJ];
+    for (int c = 0; c < a.D; c += 32) {
+      float x[32];
+      tc::tmem_ld32(qa + c, x);
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      xa[j] = xb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (active) {
-        xa[j] = *unit(r0 + RPI * j + grp, ua);
-        xb[j] = *unit(r0 + RPI * j + grp, ub);
-      }
+      for (int e = 0; e < 32; ++e) ss = fmaf(x[e], x[e], ss);
+    }
+    // rows past L stay zero (with eps = 0 their 1/rms would be infinite)
+    inv = live ? 1.0f / sqrtf(ss / static_cast<float>(a.D) + a.qnorm_eps) : 1.0f;
+  }
+  auto scale = [&](float* x, int c) {
+    const float4* w = reinterpret_cast<const float4*>(a.qnorm_w + c);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float4 we = __ldg(w + e);
+      x[4 * e] *= inv * we.x; x[4 * e + 1] *= inv * we.y;
+      x[4 * e + 2] *= inv * we.z; x[4 * e + 3] *= inv * we.w;
+    }
+  };
+  // pairs c0 .. c0 + 31 with (cos, sin) in t
+  auto rotate32 = [&](int c0, const float4* t) {
+    float x0[32], x1[32];
+    tc::tmem_ld32(qa + c0, x0);
+    tc::tmem_ld32(qa + c0 + half, x1);
+    if (a.qnorm_w) {
+      scale(x0, c0);
+      scale(x1, c0 + half);
     }
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      if (a.qnorm_w) {
-        float ss = xa[j].x * xa[j].x + xa[j].y * xa[j].y + xa[j].z * xa[j].z + xa[j].w * xa[j].w +
-                   xb[j].x * xb[j].x + xb[j].y * xb[j].y + xb[j].z * xb[j].z + xb[j].w * xb[j].w;
-#pragma unroll
-        for (int o = LPR / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        const float inv = 1.0f / sqrtf(ss * inv_d + a.qnorm_eps);
-        xa[j].x *= inv * wa.x; xa[j].y *= inv * wa.y; xa[j].z *= inv * wa.z; xa[j].w *= inv * wa.w;
-        xb[j].x *= inv * wb.x; xb[j].y *= inv * wb.y; xb[j].z *= inv * wb.z; xb[j].w *= inv * wb.w;
-      }
-      if (rot) {
-        turn(xa[j].x, xb[j].x, cs[j][0]);
-        turn(xa[j].y, xb[j].y, cs[j][1]);
-        turn(xa[j].z, xb[j].z, cs[j][2]);
-        turn(xa[j].w, xb[j].w, cs[j][3]);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) turn(cs[j][e].x, cs[j][e].y, st[e]);
-      }
+    for (int e = 0; e < 16; ++e) {
+      const float4 cs = t[e];
+      const float a0 = x0[2 * e], b0 = x1[2 * e], a1 = x0[2 * e + 1], b1 = x1[2 * e + 1];
+      x0[2 * e] = fmaf(a0, cs.x, -b0 * cs.y);
+      x1[2 * e] = fmaf(a0, cs.y, b0 * cs.x);
+      x0[2 * e + 1] = fmaf(a1, cs.z, -b1 * cs.w);
+      x1[2 * e + 1] = fmaf(a1, cs.w, b1 * cs.z);
     }
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const int r = r0 + RPI * j + grp;
-      if (active && r < nrows) {
-        *unit(r, ua) = xa[j];
-        *unit(r, ub) = xb[j];
-      }
+    tc::tmem_st32(qa + c0, x0);
+    tc::tmem_st32(qa + c0 + half, x1);
+  };
+  rotate32(0, t0);
+  if (half > 32) rotate32(32, t1);
+  if (a.qnorm_w) {                            // columns past R: normalised, not rotated
+#pragma unroll 1
+    for (int c = a.rope_R; c < a.D; c += 32) {
+      float x[32];
+      tc::tmem_ld32(qa + c, x);
+      scale(x, c);
+      tc::tmem_st32(qa + c, x);
     }
   }
-  tc::fence_proxy_async();                    // generic writes -> visible to tcgen05.cp
-  __syncwarp();
-  // Signal unit uc only after the issuer has taken unit uc - 1's signal: parity
-  // waits must never see a barrier two phases ahead.
-  if (uc > 0) {
-    const bool seen = lane == 0 ? tc::mbar_wait(&bars->q_taken, (uc - 1) & 1, abort) : true;
-    if (!__shfl_sync(0xffffffffu, seen, 0)) return false;
-  }
-  if (lane == 0) tc::mbar_arrive(&bars->q_ready);
+  tc::fence_before_sync();
+  tc::mbar_arrive(&bars->q_ready);
   return true;
-}
-
-// The Q-prep warp: rotates every unit's Q tile in its ring stage, in unit order,
-// as soon as the tile lands (ring position of a unit's Q: one Q and 2 n blocks
-// per earlier unit).
-template <class C>
-__device__ void tq_qwarp(const TcArgs& a, uint8_t* skv, PBars* bars, int lane) {
-  uint32_t g = 0, uc = 0;
-  for (int r = 0;; ++r) {
-    const int x = unit_of(blockIdx.x, r, gridDim.x);
-    if (x >= a.units) break;
-    const PUnit u = get_unit<C>(a, x);
-    if (!tq_qprep<C>(a, skv, bars, u, uc + 2 * g, uc, lane)) break;
-    g += u.n;
-    ++uc;
-  }
 }
 
 // ---------------------------------------------------------------- softmax (4 warps)
 // Thread = one query row of the current unit; tcgen05.ld/st run on full warps.
-template <class C>
+template <class C, bool ROPE>
 __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quarter, int lane,
-                           const CUtensorMap* tout, uint8_t* stage_out, uint8_t* skv) {
+                           const CUtensorMap* tout, uint8_t* stage_out) {
   constexpr int BK = C::BK;
   constexpr int NA = 8;                       // independent partial max / sum chains
   volatile int* abort = &bars->abort;
@@ -410,6 +378,12 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
   const float cs = a.softcap_on ? 1.0f : a.c_score;   // raw score -> log2 units
   uint32_t g = 0, uc = 0;
   bool ok = true;
+  // Fused RoPE: the first unit's Q is rotated up front, every later one right
+  // after the previous unit's last P (before its epilogue), while the tensor
+  // core still runs that unit's last P V products.
+  if (ROPE && blockIdx.x < a.units)
+    ok = tq_rotate_q<C>(a, lane_base, bars, get_unit<C>(a, unit_of(blockIdx.x, 0, gridDim.x)),
+                        row, 0);
   for (int r = 0; ok; ++r) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
@@ -504,6 +478,10 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       tc::mbar_arrive(&bars->p_ready[buf]);
     }
     if (!ok) break;
+    const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
+    if (ROPE && xn < a.units &&
+        !(ok = tq_rotate_q<C>(a, lane_base, bars, get_unit<C>(a, xn), row, uc + 1)))
+      break;
 
     // Epilogue: read O out of TMEM (then O is free for the next unit), scale by
     // 1/l, and write it with TMA: each warp stages 32 rows x 32 columns in a
@@ -542,7 +520,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
   __syncwarp();
 }
 
-template <int DP>
+template <int DP, bool ROPE>
 __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     prefill_tq_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -568,9 +546,8 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     tc::mbar_init(&bars->o_done, 1);
     tc::mbar_init(&bars->o_final, 1);
     tc::mbar_init(&bars->o_free, 128);
-    tc::mbar_init(&bars->q_full, 1);
-    tc::mbar_init(&bars->q_ready, 1);
-    tc::mbar_init(&bars->q_taken, 1);
+    tc::mbar_init(&bars->q_copied, 1);
+    tc::mbar_init(&bars->q_ready, 128);
     tc::mbar_init(&bars->drain, 1);
     bars->abort = 0;
     tc::fence_mbar_init();
@@ -591,10 +568,7 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     if (lane == 0) tq_mma<C>(a, tmem, skv, bars);
     __syncwarp();
   } else {
-    if (warp < 6)
-      tq_softmax<C>(a, tmem, bars, warp % 4, lane, &tm_o, sepi + (warp % 4) * 4096, skv);
-    else if (a.rope_table)
-      tq_qwarp<C>(a, skv, bars, lane);
+    tq_softmax<C, ROPE>(a, tmem, bars, warp % 4, lane, &tm_o, sepi + (warp % 4) * 4096);
   }
 
   tc::fence_before_sync();
@@ -616,13 +590,13 @@ int sm_count() {
   return n;
 }
 
-template <int DP>
+template <int DP, bool ROPE>
 cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   using C = PCfg<DP>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tq_kernel<DP>,
+    attr_err = cudaFuncSetAttribute(prefill_tq_kernel<DP, ROPE>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -645,14 +619,14 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   a.c_cap_in = s.softcap > 0.f ? 2.0f * kLog2e * s.scale / s.softcap : 0.f;
   a.c_cap_out = kLog2e * s.softcap;
   a.status = s.status;
-  a.rope_table = s.rope.table;
+  a.rope_table = ROPE ? s.rope.table : nullptr;
   a.rope_start = s.rope.start;
   a.qnorm_w = s.rope.norm_w;
   a.qnorm_eps = s.rope.norm_eps;
   a.rope_R = s.rope.R;
   a.rope_max_positions = s.rope.max_positions;
   const int grid = a.units < sm_count() ? a.units : sm_count();
-  prefill_tq_kernel<DP><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
+  prefill_tq_kernel<DP, ROPE><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
@@ -663,10 +637,11 @@ bool prefill_fuses_rope(int D) { return D % 32 == 0 && D <= 128; }
 // D <= 128; V^T must already be in s.vt (launch_prefill_tc runs the transpose first).
 cudaError_t launch_prefill_tq(const AttnShape& s, cudaStream_t stream) {
   switch ((s.D + 31) / 32) {
-    case 1: return launch_tq<32>(s, stream);
-    case 2: return launch_tq<64>(s, stream);
-    case 3: return launch_tq<96>(s, stream);
-    case 4: return launch_tq<128>(s, stream);
+    // with q RoPE fused (R % 64 == 0, so D >= 64) or without
+    case 1: return s.rope.table ? cudaErrorNotSupported : launch_tq<32, false>(s, stream);
+    case 2: return s.rope.table ? launch_tq<64, true>(s, stream) : launch_tq<64, false>(s, stream);
+    case 3: return s.rope.table ? launch_tq<96, true>(s, stream) : launch_tq<96, false>(s, stream);
+    case 4: return s.rope.table ? launch_tq<128, true>(s, stream) : launch_tq<128, false>(s, stream);
     default: return cudaErrorNotSupported;
   }
 }
