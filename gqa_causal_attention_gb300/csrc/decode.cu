@@ -16,6 +16,9 @@
 // The work is HBM-bound: 2 * D * 4 bytes per cached position and KV head.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
+
+#include <mutex>
 
 namespace gqa {
 
@@ -202,6 +205,232 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeJob 
   }
 }
 
+// ---------------------------------------------------------------- bulk-copy split kernel
+// D % 4 == 0: the same split-KV reduction with the cache rows streamed by the
+// copy engine. One warp per block; a ring of `nst` stages, each holding KW
+// consecutive cache slots of K and of V (each one contiguous run of bytes,
+// fetched by cp.async.bulk onto the stage's mbarrier), so the bytes in flight
+// are bounded by shared memory rather than registers. Lane l owns dimensions
+// 4l + 128c .. +3 of every row.
+//
+// Scores of a batch: each lane forms its partial dot products for the KW keys
+// x GT heads (KW * GT = 32 values), and a butterfly reduce-scatter over the
+// warp (5 shuffle steps, 31 shuffles) leaves lane l holding the full score of
+// key l / GT and head l % GT. Running maximum and sum then reduce over the
+// lanes of one head; P V needs each p broadcast once.
+constexpr int kBulkMaxStages = 4;
+
+template <int GT, int NC, int KW>
+__global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
+  constexpr int NVAL = KW * GT;               // scores per batch
+  constexpr int RL = 32 / NVAL;               // lanes holding each reduced score
+  static_assert(NVAL <= 32 && 32 % NVAL == 0, "batch shape");
+  constexpr int NV = 4 * NC;                  // dims per lane
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kBulkMaxStages];
+  __shared__ int abort_flag;
+
+  const int lane = threadIdx.x;
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int G = j.H / j.Hkv;
+  const int ngroups = (G + GT - 1) / GT;
+  const int hkv = blockIdx.y / ngroups;
+  const int g0 = (blockIdx.y % ngroups) * GT;
+  const int D = j.D;
+
+  const int n = j.cache_len[b];
+  if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) {
+    if (lane == 0 && split == 0 && blockIdx.y == 0) report(j.status, ATTN_DEV_LENGTH);
+    return;
+  }
+  const int nlive = j.window > 0 ? min(n, j.window) : n;
+  const int nsplit_b = (nlive + j.chunk - 1) / j.chunk;
+  const int k0 = split * j.chunk;
+  if (k0 >= nlive) return;
+  const int k1 = min(k0 + j.chunk, nlive);
+  const int nb = (k1 - k0 + KW - 1) / KW;    // batches of this block
+
+  const long head_off = ((long)b * j.Hkv + hkv) * j.capacity * D;
+  const float* kbase = j.k_cache + head_off;
+  const float* vbase = j.v_cache + head_off;
+  const uint32_t part_bytes = KW * D * 4;     // K (then V) rows of one stage
+  auto stage_k = [&](int s) { return reinterpret_cast<const float*>(ring + 2 * s * part_bytes); };
+  auto stage_v = [&](int s) {
+    return reinterpret_cast<const float*>(ring + (2 * s + 1) * part_bytes);
+  };
+  auto issue = [&](int t) {                   // lane 0: batch t into stage t % nst
+    const int s = t % nst;
+    const int kb = k0 + t * KW;
+    const uint32_t bytes = static_cast<uint32_t>(min(KW, k1 - kb)) * D * 4;
+    tc::mbar_arrive_expect_tx(&full[s], 2 * bytes);
+    tc::bulk_load(ring + 2 * s * part_bytes, kbase + (long)kb * D, bytes, &full[s]);
+    tc::bulk_load(ring + (2 * s + 1) * part_bytes, vbase + (long)kb * D, bytes, &full[s]);
+  };
+  if (lane == 0) {
+    for (int s = 0; s < nst; ++s) tc::mbar_init(&full[s], 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  __syncwarp();
+  const int first = min(nst, nb);
+  if (lane == 0)
+    for (int t = 0; t < first; ++t) issue(t);
+
+  // Queries of the GT heads (scaled), this lane's dimensions.
+  float q[GT][NV];
+#pragma unroll
+  for (int g = 0; g < GT; ++g)
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int d = 4 * lane + 128 * c;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g0 + g < G && d < D)
+        t = __ldg(reinterpret_cast<const float4*>(j.q + ((long)b * j.H + hkv * G + g0 + g) * D + d));
+      q[g][4 * c] = t.x * j.scale; q[g][4 * c + 1] = t.y * j.scale;
+      q[g][4 * c + 2] = t.z * j.scale; q[g][4 * c + 3] = t.w * j.scale;
+    }
+  const bool capped = j.softcap > 0.f;
+  const float cap_k = capped ? 2.0f * kLog2e / j.softcap : 0.f;
+  auto load_row = [&](const float* row, float* r) {
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int d = 4 * lane + 128 * c;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (d < D) t = *reinterpret_cast<const float4*>(row + d);
+      r[4 * c] = t.x; r[4 * c + 1] = t.y; r[4 * c + 2] = t.z; r[4 * c + 3] = t.w;
+    }
+  };
+
+  const int my_u = lane / RL / GT;            // key (within the batch) and head of this
+  float m_run = -INFINITY, l_run = 0.f;       // lane's score; running max / sum of that head
+  float o[GT][NV];
+#pragma unroll
+  for (int g = 0; g < GT; ++g)
+#pragma unroll
+    for (int e = 0; e < NV; ++e) o[g][e] = 0.f;
+
+  int t = 0;
+  for (; t < nb; ++t) {
+    const int s = t % nst;
+    const bool ok = tc::mbar_wait(&full[s], (t / nst) & 1, &abort_flag);
+    if (__any_sync(0xffffffffu, !ok)) break;
+    const int valid = min(KW, k1 - (k0 + t * KW));
+    const float* sk = stage_k(s);
+    const float* sv = stage_v(s);
+
+    // partial dot products, index u * GT + g
+    float v[NVAL];
+#pragma unroll
+    for (int u = 0; u < KW; ++u) {
+      float kr[NV];
+      load_row(sk + u * D, kr);
+#pragma unroll
+      for (int g = 0; g < GT; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < NV; ++e) acc = fmaf(q[g][e], kr[e], acc);
+        v[u * GT + g] = acc;
+      }
+    }
+    // reduce-scatter: the step over lane bit `off` halves the values a lane
+    // keeps (upper half where that bit is set); once one value is left the
+    // remaining bits are summed outright. Lane l ends with the full score of
+    // index l / RL.
+#pragma unroll
+    for (int half = NVAL / 2, off = 16; half >= 1; half >>= 1, off >>= 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float send = upper ? v[i] : v[i + half];
+        const float keep = upper ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    }
+#pragma unroll
+    for (int off = RL / 2; off >= 1; off >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    float sc = v[0];
+    if (capped) sc = softcap_apply(sc, j.softcap, cap_k);
+    sc = my_u < valid ? sc * kLog2e : -INFINITY;
+    // over the keys of one head: lanes that differ above bit log2(RL * GT)
+    float mx = sc;
+#pragma unroll
+    for (int off = RL * GT; off < 32; off <<= 1)
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float m_new = fmaxf(m_run, mx);
+    const float corr = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+    const float p = m_new == -INFINITY ? 0.f : exp2f(sc - m_new);
+    float ps = p;
+#pragma unroll
+    for (int off = RL * GT; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+    l_run = l_run * corr + ps;
+    m_run = m_new;
+
+#pragma unroll
+    for (int g = 0; g < GT; ++g) {
+      const float cg = __shfl_sync(0xffffffffu, corr, g * RL);
+#pragma unroll
+      for (int e = 0; e < NV; ++e) o[g][e] *= cg;
+    }
+#pragma unroll
+    for (int u = 0; u < KW; ++u) {
+      if (u < valid) {                        // slots past the copied rows hold stale bytes
+        float vr[NV];
+        load_row(sv + u * D, vr);
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+          const float pg = __shfl_sync(0xffffffffu, p, (u * GT + g) * RL);
+#pragma unroll
+          for (int e = 0; e < NV; ++e) o[g][e] = fmaf(pg, vr[e], o[g][e]);
+        }
+      }
+    }
+    __syncwarp();                             // every lane is done reading stage s
+    if (lane == 0 && t + nst < nb) issue(t + nst);
+  }
+  if (t < nb) {
+    // A wait ran out: let the copies already issued land, then report.
+    if (lane == 0) {
+      for (int u = t; u < min(nb, t + nst); ++u) {
+        const uint64_t t0 = tc::globaltimer();
+        while (!tc::mbar_try_wait(&full[u % nst], (u / nst) & 1))
+          if (tc::globaltimer() - t0 > tc::kWaitLimitNs) break;
+      }
+      report(j.status, ATTN_DEV_TIMEOUT);
+    }
+    return;
+  }
+
+  const bool single = nsplit_b == 1;
+#pragma unroll
+  for (int g = 0; g < GT; ++g) {
+    const float M = __shfl_sync(0xffffffffu, m_run, g * RL);
+    const float L = __shfl_sync(0xffffffffu, l_run, g * RL);
+    if (g0 + g >= G) continue;
+    const long hrow = (long)b * j.H + hkv * G + g0 + g;
+    const float inv = 1.0f / L;
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      const int d = 4 * lane + 128 * c;
+      if (d >= D) continue;
+      if (single) {
+        *reinterpret_cast<float4*>(j.out + hrow * D + d) =
+            make_float4(o[g][4 * c] * inv, o[g][4 * c + 1] * inv, o[g][4 * c + 2] * inv,
+                        o[g][4 * c + 3] * inv);
+      } else {
+        const long pi = hrow * j.nsplit + split;
+        *reinterpret_cast<float4*>(j.partial + pi * D + d) =
+            make_float4(o[g][4 * c], o[g][4 * c + 1], o[g][4 * c + 2], o[g][4 * c + 3]);
+      }
+    }
+    if (!single && lane == 0) {
+      const long pi = hrow * j.nsplit + split;
+      float* ml = j.partial + (long)j.B * j.H * j.nsplit * D;
+      ml[2 * pi] = M;
+      ml[2 * pi + 1] = L;
+    }
+  }
+}
+
 // out[b, h, :] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits of row b.
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeJob j) {
   const int h = blockIdx.x, b = blockIdx.y;
@@ -237,11 +466,36 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
   *nsplit = (eff + c - 1) / c;
 }
 
+// Batches of KW = 8 keys (32 / GT when that is smaller) and about 16 KB of
+// ring per block: 13 one-warp blocks per SM at D = 128. Measured on the
+// batched-decode workload, wider rings (fewer blocks) and narrower batches
+// (more per-batch overhead) were both slower.
+constexpr int kBulkKeys = 8;
+constexpr int kBulkStageBudget = 16 * 1024;   // ring bytes per block (at least 2 stages)
+
+template <int GT, int NC>
+static cudaError_t launch_bulk(const DecodeJob& j, dim3 grid, cudaStream_t stream) {
+  constexpr int KW = GT * kBulkKeys > 32 ? 32 / GT : kBulkKeys;
+  const int stage = 2 * KW * j.D * 4;
+  int nst = kBulkStageBudget / stage;
+  nst = nst < 2 ? 2 : (nst > kBulkMaxStages ? kBulkMaxStages : nst);
+  decode_bulk_kernel<GT, NC, KW><<<grid, 32, nst * stage, stream>>>(j, nst);
+  return cudaSuccess;
+}
+
 template <int GT>
 static cudaError_t launch_gt(const DecodeJob& j, cudaStream_t stream) {
   const int G = j.H / j.Hkv;
   const int ngroups = (G + GT - 1) / GT;
   dim3 grid(j.nsplit, j.Hkv * ngroups, j.B);
+  if (j.D % 4 == 0) {
+    cudaError_t e = j.D <= 128 ? launch_bulk<GT, 1>(j, grid, stream)
+                               : launch_bulk<GT, 2>(j, grid, stream);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess || j.nsplit <= 1) return e;
+    decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);
+    return cudaGetLastError();
+  }
   if (j.D % 128 == 0) {
     if (j.D == 128)
       decode_split_kernel<GT, 4, true><<<grid, kDecodeThreads, 0, stream>>>(j);

@@ -96,6 +96,16 @@ __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
 // 3-D tiled load of one box into shared memory; completion is signalled on
 // `bar` as transaction bytes. c0 (innermost, in elements) must keep the
 // start 16-byte aligned.
+// Plain bulk copy global -> shared of `bytes` contiguous bytes, completing on
+// `bar` (complete_tx). Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2) {
   asm volatile(

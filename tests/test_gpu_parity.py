@@ -198,6 +198,10 @@ DECODE_CASES = [
     (2, 8, 2, 6, 50, 0, 3.0, (50, 2)),
     (5, 8, 8, 64, 1500, 0, 0.0, (1500, 1, 200, 1024, 1025)),
     (2, 12, 1, 96, 300, 0, 0.0, (300, 129)),
+    (2, 6, 2, 192, 400, 0, 0.0, (400, 33)),
+    (2, 16, 2, 256, 300, 0, 20.0, (300, 100)),
+    (1, 4, 4, 128, 5000, 0, 0.0, (4097,)),
+    (2, 8, 4, 128, 96, 96, 0.0, (3000, 17)),
 ]
 
 
