@@ -63,7 +63,7 @@ def test_static_scratch_decode_matches_workspace_decode(B, H, Hkv, D, cap, windo
 
 
 def test_static_scratch_refuses_sizes_beyond_the_array():
-    # 64 rows x 256 heads x 17 splits x 258 floats needs more than 32 MiB
+    # 64 rows x 256 heads x (tens of splits) x 258 floats: far more than 32 MiB
     B, H, Hkv, D, maxlen = 64, 256, 8, 256, 8193
     assert g.gqa_attn_decode_workspace_size(B, H, Hkv, D, maxlen, 0) > (32 << 20)
     lib = g.load()
