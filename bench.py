@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b_prefill",
                     choices=["llama3_8b_prefill", "gemma2_window"],
                     help="prefill workload of the timed step")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the steps as eager launches instead of CUDA graph replays")
     ap.add_argument("--unfused-q-rope", action="store_true",
                     help="time attn_rope_apply on q + gqa_attn_prefill instead of the fused call")
     ap.add_argument("--decode-batch", type=int, default=0,
@@ -65,6 +67,14 @@ def peaks():
                   "source": "measured"})
     p["tf32_tflops"] = p["bf16_tflops"] * NOMINAL_TF32_OVER_BF16
     return p
+
+
+# DRAM bytes (read + write) per launch from the committed ncu captures of the
+# current kernels (profiles/); None where no capture of the timed kernel exists.
+# The decode capture ran on 16 of the 64 rows; its traffic scales with the
+# algorithmic bytes processed (ratio below).
+NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 345.743616e6 + 94.777088e6}
+NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903360e6 + 4.927232e6) / 585572352.0
 
 
 def measure_tf32_peak(dev):
@@ -177,6 +187,23 @@ def timed(fn, steps, warmup, dist, events_for=None):
     return ms
 
 
+def graph_of(fn, warm=3):
+    """fn's launches captured once into a CUDA graph (warmed up on a side stream
+    first); replaying it takes the per-call host work out of the step."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warm):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        fn()
+    torch.cuda.synchronize()
+    return gr
+
+
 def visible_pairs(L, window):
     """Number of (query, key) pairs the causal (or windowed) mask admits in one row."""
     if window <= 0 or window >= L:
@@ -240,14 +267,21 @@ def bench_prefill(w, args, dist, dev, rank):
         else:
             prefill()
 
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        ms = timed(lambda: step(True), args.steps, args.warmup, dist)
+    # Eager launches, with CUDA events around the prefill call (kernel time).
+    ms_eager = timed(lambda: step(True), args.steps, args.warmup, dist)
     kern = kern[args.warmup:]
     kern_ms = sum(a.elapsed_time(b) for a, b in kern) / max(1, len(kern))
+    # The step as a CUDA graph: the whole-step time.
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if args.no_graph:
+            ms = timed(lambda: step(False), args.steps, args.warmup, dist)
+        else:
+            gr = graph_of(lambda: step(False))
+            ms = timed(gr.replay, args.steps, args.warmup, dist)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-    res = {"ms": ms / args.steps, "kernel_ms": kern_ms, "clocks": clk.summary(),
-           "launches_per_step": 3}
+    res = {"ms": ms / args.steps, "ms_eager": ms_eager / args.steps, "kernel_ms": kern_ms,
+           "clocks": clk.summary(), "launches_per_step": 3}
 
     if not args.no_e2e:
         hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
@@ -291,26 +325,34 @@ def bench_decode(w, args, dist, dev):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     kern = []
 
-    def step():
+    def step(record=True):
         g.attn_rope_apply(q, pos, maxlen - 1, rp, table, None, w.norm_eps, status)
         g.kv_cache_append(k, v, pos, maxlen - 1, rp, table, None, w.norm_eps, kc, vc, 0, status)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
+        if record:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
         g.gqa_attn_decode(q, kc, vc, cl, maxlen, out, 0, w.softcap, 0.0, ws, status)
-        b.record()
-        kern.append((a, b))
+        if record:
+            b.record()
+            kern.append((a, b))
 
     steps = args.decode_steps
-    with ClockSampler(torch.cuda.current_device()) as clk:
-        ms = timed(step, steps, args.warmup, dist)
+    ms_eager = timed(step, steps, args.warmup, dist)
     kern = kern[args.warmup:]
     kern_ms = sum(a.elapsed_time(b) for a, b in kern) / max(1, len(kern))
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        if args.no_graph:
+            ms = timed(lambda: step(False), steps, args.warmup, dist)
+        else:
+            gr = graph_of(lambda: step(False))
+            ms = timed(gr.replay, steps, args.warmup, dist)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     nbytes = 2.0 * w.Hkv * w.D * 4 * float((n + 1).sum())
     ksplit = 2 if g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, maxlen, w.window) > 16 \
         else 1
-    return {"ms": ms / steps, "kernel_ms": kern_ms, "bytes": nbytes, "clocks": clk.summary(),
+    return {"ms": ms / steps, "ms_eager": ms_eager / steps, "kernel_ms": kern_ms, "bytes": nbytes,
+            "clocks": clk.summary(),
             "launches_per_step": 2 + ksplit}
 
 
@@ -448,13 +490,20 @@ def main():
                                                    if w.scaling else ""),
                    "mask": f"window {w.window}" if w.window else "causal",
                    "softcap": w.softcap, "qk_norm": w.qk_norm,
-                   "step": "kv_cache_append (k RMSNorm/RoPE + cache) + gqa_attn_prefill_rope "
-                           "(V^T pre-pass; q RMSNorm/RoPE fused into the attention kernel)",
+                   "step": ("kv_cache_append (k RMSNorm/RoPE + cache) + "
+                            + ("attn_rope_apply (q) + gqa_attn_prefill" if args.unfused_q_rope
+                               else "gqa_attn_prefill_rope (V^T pre-pass; q RMSNorm/RoPE fused "
+                                    "into the attention kernel)")
+                            + ("" if args.no_graph else "; timed as CUDA graph replays")),
+                   "ms_per_step_eager": pre["ms_eager"],
                    "l2": f"inputs larger than L2 ({prefill_bytes(w) / 2**20:.0f} MiB per step)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": kern_tflops, "peak": pk["tf32_tflops"],
                      "unit": "TFLOP/s", "frac": kern_tflops / pk["tf32_tflops"],
-                     "traffic": None,
+                     "traffic": NCU_PREFILL_TRAFFIC.get(
+                         (w.name, "unfused" if args.unfused_q_rope else "fused")),
+                     "traffic_note": "ncu dram bytes of prefill_tq_kernel (one launch); the "
+                                     "achieved rate covers the whole call (V^T pre-pass too)",
                      "kernel": "gqa_attn_prefill_rope", "kernel_ms": pre["kernel_ms"],
                      "peak_note": "dense TF32 measured in this run: cuBLAS fp32 8192^3 "
                                   "with TF32 allowed, best of 10",
@@ -472,10 +521,12 @@ def main():
         kgbs = dec["bytes"] / (dec["kernel_ms"] * 1e-3) / 1e9
         line["decode"] = {
             "workload": "batched_decode", "value": world * gbs, "unit": "GB/s",
-            "ms_per_step": dec["ms"], "bytes_per_step": dec["bytes"],
+            "ms_per_step": dec["ms"], "ms_per_step_eager": dec["ms_eager"],
+            "bytes_per_step": dec["bytes"],
             "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
             "roofline": {"bound": "hbm", "achieved": kgbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                         "frac": kgbs / pk["hbm_gbs"], "traffic": None,
+                         "frac": kgbs / pk["hbm_gbs"],
+                         "traffic": NCU_DECODE_TRAFFIC_PER_ALG_BYTE * dec["bytes"],
                          "kernel": "gqa_attn_decode", "kernel_ms": dec["kernel_ms"]},
             "gpu_launches": dec["launches_per_step"] * args.decode_steps,
             "clocks": dec["clocks"]}
