@@ -24,7 +24,7 @@ __all__ = [
     "gqa_attn_prefill", "gqa_attn_prefill_workspace_size", "gqa_attn_decode_workspace_size",
     "gqa_attn_decode", "gqa_attn_prefill_rope", "gqa_attn_prefill_rope_workspace_size",
     "gqa_attn_decode_static",
-    "attn_status_string", "attn_version", "rope_table", "ROPE_SCALING",
+    "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
 
@@ -34,7 +34,10 @@ ROPE_SCALING = {None: 0, "none": 0, "linear": 1, "llama3": 2}
 
 class AttnError(RuntimeError):
     def __init__(self, fn: str, code: int):
-        super().__init__(f"{fn}: {attn_status_string(code)} (code {code})")
+        msg = f"{fn}: {attn_status_string(code)} (code {code})"
+        if code == -8:
+            msg += f": {attn_last_cuda_error()}"
+        super().__init__(msg)
         self.code = code
 
 
@@ -107,6 +110,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                              i32, i32, i32, f, f, vp, vp]),
             "attn_status_string": (ctypes.c_char_p, [i32]),
             "attn_version": (ctypes.c_char_p, []),
+            "attn_last_cuda_error": (ctypes.c_char_p, []),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -157,6 +161,11 @@ def attn_status_string(code: int) -> str:
 
 def attn_version() -> str:
     return load().attn_version().decode()
+
+
+def attn_last_cuda_error() -> str:
+    """The CUDA error behind the last ATTN_ERR_CUDA on this thread."""
+    return load().attn_last_cuda_error().decode()
 
 
 def attn_rope_table_bytes(params: RopeParams, D: int) -> int:

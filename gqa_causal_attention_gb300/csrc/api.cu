@@ -63,13 +63,24 @@ bool dims_ok(int B, int Hx, int L, int D) {
   return B >= 0 && Hx >= 1 && L >= 0 && D >= 2 && D <= gqa::kMaxHeadDim && D % 2 == 0;
 }
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+// The CUDA error behind the last ATTN_ERR_CUDA returned on this host thread.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return ATTN_OK;
+  g_last_cuda_error = e;
+  return ATTN_ERR_CUDA;
+}
 
 }  // namespace
 
 extern "C" {
 
 const char* attn_version(void) { return "0.1.0"; }
+
+const char* attn_last_cuda_error(void) {
+  return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
+}
 
 const char* attn_status_string(int code) {
   switch (code) {
@@ -247,7 +258,7 @@ int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float*
   j.start = start; j.max_positions = max_pos_of(rp);
   j.table = reinterpret_cast<const float2*>(table);
   j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status;
-  if (cudaError_t e = gqa::launch_rope_rows(j, s); e != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaError_t e = gqa::launch_rope_rows(j, s); e != cudaSuccess) return cuda_status(e);
   a.q = qrot;
   if (gqa::prefill_tc_supports(D)) {
     a.vt = static_cast<float*>(workspace);

@@ -222,6 +222,11 @@ const char* attn_status_string(int code);
 /* Library version, e.g. "0.1.0". */
 const char* attn_version(void);
 
+/* The CUDA runtime's description of the error behind the last ATTN_ERR_CUDA
+ * returned to this host thread ("no CUDA error" if there was none). A static
+ * string; not cleared by later successful calls. */
+const char* attn_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -39,6 +39,8 @@ def test_library_exports_every_declared_function():
     missing = [f for f in declared_functions() if not hasattr(raw, f)]
     assert not missing, missing
     assert lib.attn_version().decode().count(".") == 2
+    assert "attn_last_cuda_error" in declared_functions()
+    assert g.attn_last_cuda_error() == "no CUDA error"     # nothing failed on this thread
 
 
 def test_status_strings():
