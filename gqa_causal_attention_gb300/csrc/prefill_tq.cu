@@ -365,13 +365,60 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars, co
   return true;
 }
 
+// ---------------------------------------------------------------- softmax helpers
+// The block's P is accepted against the running reference while its sum stays
+// at most 2^kRescaleLog2 (no single weight can then exceed it).
+constexpr float kRescaleLimit = 256.0f;
+static_assert(kRescaleLog2 == 8.0f, "limit is 2^kRescaleLog2");
+
+// Row maximum of N scores (three-input maxima, 8 chains).
+template <int N>
+__device__ __forceinline__ float tq_max(const float* s) {
+  float mx[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) mx[j] = s[j];
+  int c = 8;
+#pragma unroll
+  for (; c + 16 <= N; c += 16)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx[j] = tc::max3(mx[j], s[c + j], s[c + 8 + j]);
+#pragma unroll
+  for (; c < N; c += 8)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], s[c + j]);
+  return fmaxf(tc::max3(mx[0], mx[1], mx[2]),
+               fmaxf(tc::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+}
+
+// p = 2^(score * cs - m) in place, truncated to the TF32 value the tensor core
+// uses (so the row sum adds exactly the weights applied to V); returns the sum.
+// Pairs of columns go through the paired fp32 FMA / add.
+template <int N>
+__device__ __forceinline__ float tq_exp_sum(float* s, float cs, float m) {
+  const uint64_t c2 = tc::pack2(cs, cs), m2 = tc::pack2(-m, -m);
+  uint64_t acc[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = tc::pack2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < N; c += 2) {
+    float x0, x1;
+    tc::unpack2(tc::fma2(tc::pack2(s[c], s[c + 1]), c2, m2), x0, x1);
+    const float p0 = tc::trunc_tf32(tc::ex2(x0)), p1 = tc::trunc_tf32(tc::ex2(x1));
+    s[c] = p0;
+    s[c + 1] = p1;
+    acc[(c / 2) % 4] = tc::add2(acc[(c / 2) % 4], tc::pack2(p0, p1));
+  }
+  float a0, a1;
+  tc::unpack2(tc::add2(tc::add2(acc[0], acc[1]), tc::add2(acc[2], acc[3])), a0, a1);
+  return a0 + a1;
+}
+
 // ---------------------------------------------------------------- softmax (4 warps)
 // Thread = one query row of the current unit; tcgen05.ld/st run on full warps.
 template <class C, bool ROPE>
 __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quarter, int lane,
                            const CUtensorMap* tout, uint8_t* stage_out) {
   constexpr int BK = C::BK;
-  constexpr int NA = 8;                       // independent partial max / sum chains
   volatile int* abort = &bars->abort;
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -400,80 +447,71 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
         break;
       }
       tc::fence_after_sync();
+      const uint32_t scol = lane_base + C::kSCol + buf * BK;
       float s[BK];
-      tmem_ld_row<BK>(lane_base + C::kSCol + buf * BK, s);
-
-      // Softcap: log2(e) * cap * tanh(scale * s / cap) = c_out - 2 c_out / (2^(s c_in) + 1).
-      if (a.softcap_on) {
-#pragma unroll
-        for (int c = 0; c < BK; ++c) {
-          const float e = tc::ex2(s[c] * a.c_cap_in);
-          s[c] = fmaf(-2.0f * a.c_cap_out, tc::rcp(e + 1.0f), a.c_cap_out);
-        }
-      }
-      // Keys outside this row's causal / window band (boundary blocks only).
+      // Softcap: log2(e) * cap * tanh(scale * s / cap) = c_out - 2 c_out / (2^(s c_in) + 1);
+      // then the keys outside this row's causal / window band (boundary blocks only).
       const int k0 = (u.jlo + i) * BK;
       const int hi = qpos - k0;                                     // visible: c <= hi
       const int lo = a.window > 0 ? qpos - a.window + 1 - k0 : -1;  // visible: c >= lo
-      if (hi < BK - 1 || lo > 0) {
+      auto load_scores = [&]() {
+        tmem_ld_row<BK>(scol, s);
+        if (a.softcap_on) {
 #pragma unroll
-        for (int c = 0; c < BK; ++c) s[c] = (c > hi || c < lo) ? -INFINITY : s[c];
-      }
-      float mx[NA];
-#pragma unroll
-      for (int j = 0; j < NA; ++j) mx[j] = s[j];
-#pragma unroll
-      for (int c = NA; c < BK; ++c) mx[c % NA] = fmaxf(mx[c % NA], s[c]);
-#pragma unroll
-      for (int j = NA / 2; j > 0; j /= 2)
-#pragma unroll
-        for (int q = 0; q < j; ++q) mx[q] = fmaxf(mx[q], mx[q + j]);
-      const float m_new = fmaxf(m_ref, mx[0] * cs);
-
-      // Rescale O only when the running maximum has grown a lot (warp-uniform).
-      const bool grow = m_ref != -INFINITY && m_new - m_ref > kRescaleLog2;
-      if (__any_sync(0xffffffffu, grow)) {
-        ok = tc::mbar_wait(&bars->o_done, (G - 1) & 1, abort);
-        if (__any_sync(0xffffffffu, !ok)) {
-          ok = false;
-          break;
+          for (int c = 0; c < BK; ++c) {
+            const float e = tc::ex2(s[c] * a.c_cap_in);
+            s[c] = fmaf(-2.0f * a.c_cap_out, tc::rcp(e + 1.0f), a.c_cap_out);
+          }
         }
-        tc::fence_after_sync();
-        const float f = grow ? tc::ex2(m_ref - m_new) : 1.0f;
+        if (hi < BK - 1 || lo > 0) {
+#pragma unroll
+          for (int c = 0; c < BK; ++c) s[c] = (c > hi || c < lo) ? -INFINITY : s[c];
+        }
+      };
+      load_scores();
+
+      // Common case: P against the running reference m_ref. It stands unless a
+      // score exceeds m_ref by more than 2^8 (where the reference is moved);
+      // then the block's sum of P exceeds 2^8 as well, and the block is done
+      // again below with its maximum (S is still in tensor memory).
+      bool slow = m_ref == -INFINITY;
+      float lsum = 0.f;
+      if (!__any_sync(0xffffffffu, slow)) {
+        lsum = tq_exp_sum<BK>(s, cs, m_ref);
+        slow = !(lsum <= kRescaleLimit);
+        if (__any_sync(0xffffffffu, slow)) load_scores();
+      }
+      if (__any_sync(0xffffffffu, slow)) {
+        const float m_new = fmaxf(m_ref, tq_max<BK>(s) * cs);
+        // Rescale O only when the running maximum has grown a lot (warp-uniform).
+        const bool grow = m_ref != -INFINITY && m_new - m_ref > kRescaleLog2;
+        if (__any_sync(0xffffffffu, grow)) {
+          ok = tc::mbar_wait(&bars->o_done, (G - 1) & 1, abort);
+          if (__any_sync(0xffffffffu, !ok)) {
+            ok = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const float f = grow ? tc::ex2(m_ref - m_new) : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < C::DP; c += 32) {
-          float o[32];
-          tc::tmem_ld32(lane_base + C::kOCol + c, o);
+          for (int c = 0; c < C::DP; c += 32) {
+            float o[32];
+            tc::tmem_ld32(lane_base + C::kOCol + c, o);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] *= f;
-          tc::tmem_st32(lane_base + C::kOCol + c, o);
+            for (int e = 0; e < 32; ++e) o[e] *= f;
+            tc::tmem_st32(lane_base + C::kOCol + c, o);
+          }
+          if (grow) {
+            l *= f;
+            m_ref = m_new;
+          }
         }
-        if (grow) {
-          l *= f;
-          m_ref = m_new;
-        }
+        if (m_ref == -INFINITY) m_ref = m_new;  // first visible keys of the row (O, l are 0)
+        // -inf only while every key so far was masked; then every score is -inf.
+        lsum = tq_exp_sum<BK>(s, cs, m_ref == -INFINITY ? 0.f : m_ref);
       }
-      if (m_ref == -INFINITY) m_ref = m_new;  // first visible keys of the row (O, l are 0)
-      // -inf only while every key so far was masked; then every score is -inf.
-      const float mref = m_ref == -INFINITY ? 0.f : m_ref;
-
-      // p = 2^(score - m), truncated to the TF32 value the tensor core uses, so
-      // that l sums exactly the weights applied to V.
-      float ps[NA];
-#pragma unroll
-      for (int j = 0; j < NA; ++j) ps[j] = 0.f;
-#pragma unroll
-      for (int c = 0; c < BK; ++c) {
-        const float p = tc::trunc_tf32(tc::ex2(fmaf(s[c], cs, -mref)));
-        ps[c % NA] += p;
-        s[c] = p;
-      }
-#pragma unroll
-      for (int j = NA / 2; j > 0; j /= 2)
-#pragma unroll
-        for (int q = 0; q < j; ++q) ps[q] += ps[q + j];
-      l += ps[0];
-      tmem_st_row<BK>(lane_base + C::kSCol + buf * BK, s);
+      l += lsum;
+      tmem_st_row<BK>(scol, s);
       tc::fence_before_sync();
       tc::mbar_arrive(&bars->p_ready[buf]);
     }

@@ -93,9 +93,6 @@ __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 3-D tiled load of one box into shared memory; completion is signalled on
-// `bar` as transaction bytes. c0 (innermost, in elements) must keep the
-// start 16-byte aligned.
 // Plain bulk copy global -> shared of `bytes` contiguous bytes, completing on
 // `bar` (complete_tx). Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
@@ -106,6 +103,9 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// 3-D tiled load of one box into shared memory; completion is signalled on
+// `bar` as transaction bytes. c0 (innermost, in elements) must keep the
+// start 16-byte aligned.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
                                             int c0, int c1, int c2) {
   asm volatile(
@@ -324,6 +324,38 @@ __device__ __forceinline__ float2 ldg_pinned(const float2* p) {
 // Keep the 19 bits a TF32 operand uses (the tensor core ignores the rest).
 __device__ __forceinline__ float trunc_tf32(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// Packed pairs of fp32 (two registers as one 64-bit operand) for the paired
+// FMA / add / multiply of sm_100+; each lane of a pair rounds as the scalar op.
+__device__ __forceinline__ uint64_t pack2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 }  // namespace tc
