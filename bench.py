@@ -73,7 +73,7 @@ def peaks():
 # current kernels (profiles/); None where no capture of the timed kernel exists.
 # The decode capture ran on 16 of the 64 rows; its traffic scales with the
 # algorithmic bytes processed (ratio below).
-NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 345.743616e6 + 94.777088e6}
+NCU_PREFILL_TRAFFIC = {}
 NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903360e6 + 4.927232e6) / 585572352.0
 
 
@@ -244,28 +244,36 @@ def bench_prefill(w, args, dist, dev, rank):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     pws = torch.empty(max(4, g.gqa_attn_prefill_rope_workspace_size(w.B, w.H, w.Hkv, w.L, w.D,
                                                                     rp) // 4), device=dev)
+    vt = torch.empty(w.B * w.Hkv * w.D * g.gqa_attn_vt_pitch(w.L), device=dev)
+    vws = torch.empty(max(4, g.gqa_attn_prefill_rope_vt_workspace_size(w.B, w.H, w.L, w.D, rp)
+                          // 4), device=dev)
     kern = []
 
-    def prefill():
+    def attention():
+        # the attention kernel alone (timed for the roofline): v arrives transposed
         if args.unfused_q_rope:
-            g.attn_rope_apply(q, start, 0, rp, table, qn, w.norm_eps, status)
             g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
                                status=status)
         else:
-            g.gqa_attn_prefill_rope(q, k, v, out, start, 0, rp, table, qn, w.norm_eps, w.window,
-                                    w.softcap, 0.0, workspace=pws, status=status)
+            g.gqa_attn_prefill_rope_vt(q, k, vt, out, start, 0, rp, table, qn, w.norm_eps,
+                                       w.window, w.softcap, 0.0, workspace=vws, status=status)
 
     def step(record=False):
-        # k: RMSNorm + RoPE in place and into the cache; q: RMSNorm + RoPE inside the prefill
+        # k: RMSNorm + RoPE in place and into the cache; v transposed for the tensor cores;
+        # q: RMSNorm + RoPE inside the attention kernel
         g.kv_cache_append(k, v, start, 0, rp, table, kn, w.norm_eps, kc, vc, w.window, status)
+        if args.unfused_q_rope:
+            g.attn_rope_apply(q, start, 0, rp, table, qn, w.norm_eps, status)
+        else:
+            g.gqa_attn_v_transpose(v, vt)
         if record:
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
-            prefill()
+            attention()
             b.record()
             kern.append((a, b))
         else:
-            prefill()
+            attention()
 
     # Eager launches, with CUDA events around the prefill call (kernel time).
     ms_eager = timed(lambda: step(True), args.steps, args.warmup, dist)
@@ -281,7 +289,7 @@ def bench_prefill(w, args, dist, dev, rank):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     res = {"ms": ms / args.steps, "ms_eager": ms_eager / args.steps, "kernel_ms": kern_ms,
-           "clocks": clk.summary(), "launches_per_step": 3}
+           "clocks": clk.summary(), "launches_per_step": 4 if args.unfused_q_rope else 3}
 
     if not args.no_e2e:
         hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
@@ -491,9 +499,10 @@ def main():
                    "mask": f"window {w.window}" if w.window else "causal",
                    "softcap": w.softcap, "qk_norm": w.qk_norm,
                    "step": ("kv_cache_append (k RMSNorm/RoPE + cache) + "
-                            + ("attn_rope_apply (q) + gqa_attn_prefill" if args.unfused_q_rope
-                               else "gqa_attn_prefill_rope (V^T pre-pass; q RMSNorm/RoPE fused "
-                                    "into the attention kernel)")
+                            + ("attn_rope_apply (q) + gqa_attn_prefill (V^T pre-pass inside)"
+                               if args.unfused_q_rope
+                               else "gqa_attn_v_transpose + gqa_attn_prefill_rope_vt (q "
+                                    "RMSNorm/RoPE fused into the attention kernel)")
                             + ("" if args.no_graph else "; timed as CUDA graph replays")),
                    "ms_per_step_eager": pre["ms_eager"],
                    "l2": f"inputs larger than L2 ({prefill_bytes(w) / 2**20:.0f} MiB per step)",
@@ -502,9 +511,11 @@ def main():
                      "unit": "TFLOP/s", "frac": kern_tflops / pk["tf32_tflops"],
                      "traffic": NCU_PREFILL_TRAFFIC.get(
                          (w.name, "unfused" if args.unfused_q_rope else "fused")),
-                     "traffic_note": "ncu dram bytes of prefill_tq_kernel (one launch); the "
-                                     "achieved rate covers the whole call (V^T pre-pass too)",
-                     "kernel": "gqa_attn_prefill_rope", "kernel_ms": pre["kernel_ms"],
+                     "traffic_note": "ncu dram bytes of prefill_tq_kernel (one launch)",
+                     "kernel": ("gqa_attn_prefill (V^T pre-pass + attention)"
+                                if args.unfused_q_rope else
+                                "gqa_attn_prefill_rope_vt (the attention kernel alone)"),
+                     "kernel_ms": pre["kernel_ms"],
                      "peak_note": "dense TF32 measured in this run: cuBLAS fp32 8192^3 "
                                   "with TF32 allowed, best of 10",
                      "frac_of_tf32_nominal_ratio_peak": kern_tflops / pk["tf32_derived"],

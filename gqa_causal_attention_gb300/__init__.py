@@ -23,7 +23,8 @@ __all__ = [
     "attn_rope_table_bytes", "attn_rope_table_init", "attn_rope_apply", "kv_cache_append",
     "gqa_attn_prefill", "gqa_attn_prefill_workspace_size", "gqa_attn_decode_workspace_size",
     "gqa_attn_decode", "gqa_attn_prefill_rope", "gqa_attn_prefill_rope_workspace_size",
-    "gqa_attn_decode_static",
+    "gqa_attn_decode_static", "gqa_attn_vt_pitch", "gqa_attn_v_transpose",
+    "gqa_attn_prefill_rope_vt", "gqa_attn_prefill_rope_vt_workspace_size",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
@@ -103,6 +104,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_attn_prefill_rope": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                             ctypes.c_int32, rp, vp, vp, f, i32, f, f, vp, sz, vp,
                                             vp]),
+            "gqa_attn_vt_pitch": (i32, [i32]),
+            "gqa_attn_v_transpose": (i32, [vp, vp, i32, i32, i32, i32, vp]),
+            "gqa_attn_prefill_rope_vt_workspace_size": (sz, [i32, i32, i32, i32, rp]),
+            "gqa_attn_prefill_rope_vt": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
+                                               ctypes.c_int32, rp, vp, vp, f, i32, f, f, vp, sz,
+                                               vp, vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -280,6 +287,58 @@ def gqa_attn_prefill_rope(q, k, v, out, start, max_start: int, params: RopeParam
                                       float(softcap), float(scale), _ptr(workspace), wbytes,
                                       _ptr(status), _stream(stream))
     _check("gqa_attn_prefill_rope", rc)
+
+
+def gqa_attn_vt_pitch(L: int) -> int:
+    """Row pitch (floats) of the transposed v that the tensor-core prefill reads."""
+    return int(load().gqa_attn_vt_pitch(int(L)))
+
+
+def gqa_attn_v_transpose(v, vt, stream=None) -> None:
+    """vt[b, hkv, d, m] = v[b, hkv, m, d]; vt holds B * Hkv * D * gqa_attn_vt_pitch(L) floats."""
+    _f32("v", v, 4)
+    B, Hkv, L, D = v.shape
+    if not vt.is_cuda or vt.dtype != torch.float32 or not vt.is_contiguous() or \
+            vt.numel() < B * Hkv * D * gqa_attn_vt_pitch(L):
+        raise ValueError("vt must be a contiguous float32 CUDA tensor of "
+                         "B * Hkv * D * gqa_attn_vt_pitch(L) elements")
+    _check("gqa_attn_v_transpose",
+           load().gqa_attn_v_transpose(_ptr(v), _ptr(vt), B, Hkv, L, D, _stream(stream)))
+
+
+def gqa_attn_prefill_rope_vt_workspace_size(B: int, H: int, L: int, D: int,
+                                            params: RopeParams) -> int:
+    return int(load().gqa_attn_prefill_rope_vt_workspace_size(B, H, L, D, ctypes.byref(params)))
+
+
+def gqa_attn_prefill_rope_vt(q, k, vt, out, start, max_start: int, params: RopeParams, table,
+                             q_norm_w=None, norm_eps: float = 1e-6, window: int = 0,
+                             softcap: float = 0.0, scale: float = 0.0, workspace=None,
+                             status=None, stream=None) -> None:
+    """gqa_attn_prefill_rope with v given transposed (from gqa_attn_v_transpose)."""
+    for n, t in (("q", q), ("k", k), ("out", out)):
+        _f32(n, t, 4)
+    _f32("table", table); _f32("q_norm_w", q_norm_w); _i32("start", start); _i32("status", status)
+    B, H, L, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, L, D) or out.shape != q.shape:
+        raise ValueError("gqa_attn_prefill_rope_vt: inconsistent shapes")
+    if not vt.is_cuda or vt.dtype != torch.float32 or not vt.is_contiguous() or \
+            vt.numel() < B * Hkv * D * gqa_attn_vt_pitch(L):
+        raise ValueError("vt must be a contiguous float32 CUDA tensor of "
+                         "B * Hkv * D * gqa_attn_vt_pitch(L) elements")
+    if workspace is None:
+        n = gqa_attn_prefill_rope_vt_workspace_size(B, H, L, D, params)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().gqa_attn_prefill_rope_vt(_ptr(q), _ptr(k), _ptr(vt), _ptr(out), B, H, Hkv, L, D,
+                                         _ptr(start), int(max_start), ctypes.byref(params),
+                                         _ptr(table), _ptr(q_norm_w), float(norm_eps),
+                                         int(window), float(softcap), float(scale),
+                                         _ptr(workspace), wbytes, _ptr(status), _stream(stream))
+    _check("gqa_attn_prefill_rope_vt", rc)
 
 
 def gqa_attn_decode_workspace_size(B: int, H: int, Hkv: int, D: int, max_cache_len: int,

@@ -210,34 +210,71 @@ size_t gqa_attn_prefill_rope_workspace_size(int B, int H, int Hkv, int L, int D,
   return round256(base) + (size_t)B * H * L * D * sizeof(float);
 }
 
-int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float* out, int B,
-                          int H, int Hkv, int L, int D, const int32_t* start, int32_t max_start,
-                          const attn_rope_params* rp, const float* table, const float* q_norm_w,
-                          float norm_eps, int window, float softcap, float scale,
-                          void* workspace, size_t workspace_bytes, int32_t* status,
-                          void* stream) {
+int gqa_attn_vt_pitch(int L) { return L < 0 ? 0 : gqa::prefill_vt_pitch(L); }
+
+int gqa_attn_v_transpose(const float* v, float* vt, int B, int Hkv, int L, int D, void* stream) {
+  if (B < 0 || Hkv < 1 || L < 0 || !gqa::prefill_tc_supports(D)) return ATTN_ERR_SHAPE;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!v || !vt) return ATTN_ERR_NULL;
+  if (!aligned16(v) || !aligned16(vt)) return ATTN_ERR_ALIGN;
+  return cuda_status(gqa::launch_transpose_v(v, vt, B * Hkv, L, D, gqa::prefill_vt_pitch(L),
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+size_t gqa_attn_prefill_rope_vt_workspace_size(int B, int H, int L, int D,
+                                               const attn_rope_params* rp) {
+  if (B < 0 || H < 1 || L < 0 || !gqa::prefill_tc_supports(D) || !rope_params_ok(rp, D))
+    return 0;
+  if (rope_fused(D, rope_dim_of(rp, D)) || B == 0 || L == 0) return 16;
+  return (size_t)B * H * L * D * sizeof(float);
+}
+
+namespace {
+// Shared by gqa_attn_prefill_rope (vt == NULL: V^T is built in the workspace)
+// and gqa_attn_prefill_rope_vt (vt given; the workspace holds only rotated q).
+int prefill_rope_impl(const float* q, const float* k, const float* v, const float* vt, float* out,
+                      int B, int H, int Hkv, int L, int D, const int32_t* start,
+                      int32_t max_start, const attn_rope_params* rp, const float* table,
+                      const float* q_norm_w, float norm_eps, int window, float softcap,
+                      float scale, void* workspace, size_t workspace_bytes, int32_t* status,
+                      void* stream) {
   if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
+  if (vt && !gqa::prefill_tc_supports(D)) return ATTN_ERR_SHAPE;
   if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
   if (B == 0 || L == 0) return ATTN_OK;
-  if (!q || !k || !v || !out || !start || !rp || !table) return ATTN_ERR_NULL;
+  if (!q || !k || !(v || vt) || !out || !start || !rp || !table) return ATTN_ERR_NULL;
   if (!rope_params_ok(rp, D) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(table) ||
-      (q_norm_w && !aligned16(q_norm_w)))
+  if (!aligned16(q) || !aligned16(k) || (v && !aligned16(v)) || (vt && !aligned16(vt)) ||
+      !aligned16(out) || !aligned16(table) || (q_norm_w && !aligned16(q_norm_w)))
     return ATTN_ERR_ALIGN;
   if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_pos_of(rp))
     return ATTN_ERR_POSITION;
-  const size_t need = gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp);
-  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t need = vt ? gqa_attn_prefill_rope_vt_workspace_size(B, H, L, D, rp)
+                         : gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp);
   const int R = rope_dim_of(rp, D);
+  const bool fused = rope_fused(D, R);
+  const bool needs_ws = !vt || !fused;
+  if (needs_ws) {
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   gqa::AttnShape a{};
   a.k = k; a.v = v; a.out = out;
   a.B = B; a.H = H; a.Hkv = Hkv; a.L = L; a.D = D;
   a.window = window; a.softcap = softcap > 0.f ? softcap : 0.f;
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   a.status = status;
-  if (rope_fused(D, R)) {
+  if (gqa::prefill_tc_supports(D)) {
+    a.vt = vt ? const_cast<float*>(vt) : static_cast<float*>(workspace);
+    a.vt_pitch = gqa::prefill_vt_pitch(L);
+  }
+  // The kernels that launch after the V^T pre-pass (when this call builds V^T).
+  auto attend = [&]() -> int {
+    if (!gqa::prefill_tc_supports(D)) return cuda_status(gqa::launch_prefill_simt(a, s));
+    return cuda_status(vt ? gqa::launch_prefill_tc_vt(a, s) : gqa::launch_prefill_tc(a, s));
+  };
+  if (fused) {
     a.q = q;
     a.rope.table = reinterpret_cast<const float2*>(table);
     a.rope.start = start;
@@ -245,13 +282,13 @@ int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float*
     a.rope.norm_eps = norm_eps;
     a.rope.R = R;
     a.rope.max_positions = max_pos_of(rp);
-    a.vt = static_cast<float*>(workspace);
-    a.vt_pitch = gqa::prefill_vt_pitch(L);
-    return cuda_status(gqa::launch_prefill_tc(a, s));
+    return attend();
   }
   // Other shapes: rotate q out of place into the workspace, then the plain kernels.
-  const size_t base = gqa_attn_prefill_workspace_size(B, Hkv, L, D);
-  float* qrot = reinterpret_cast<float*>(static_cast<char*>(workspace) + round256(base));
+  float* qrot = vt ? static_cast<float*>(workspace)
+                   : reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              round256(gqa_attn_prefill_workspace_size(B, Hkv, L,
+                                                                                       D)));
   gqa::RopeJob j{};
   j.x = const_cast<float*>(q); j.y = qrot;
   j.B = B; j.NH = H; j.L = L; j.D = D; j.R = R;
@@ -260,12 +297,30 @@ int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float*
   j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status;
   if (cudaError_t e = gqa::launch_rope_rows(j, s); e != cudaSuccess) return cuda_status(e);
   a.q = qrot;
-  if (gqa::prefill_tc_supports(D)) {
-    a.vt = static_cast<float*>(workspace);
-    a.vt_pitch = gqa::prefill_vt_pitch(L);
-    return cuda_status(gqa::launch_prefill_tc(a, s));
-  }
-  return cuda_status(gqa::launch_prefill_simt(a, s));
+  return attend();
+}
+}  // namespace
+
+int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float* out, int B,
+                          int H, int Hkv, int L, int D, const int32_t* start, int32_t max_start,
+                          const attn_rope_params* rp, const float* table, const float* q_norm_w,
+                          float norm_eps, int window, float softcap, float scale,
+                          void* workspace, size_t workspace_bytes, int32_t* status,
+                          void* stream) {
+  return prefill_rope_impl(q, k, v, nullptr, out, B, H, Hkv, L, D, start, max_start, rp, table,
+                           q_norm_w, norm_eps, window, softcap, scale, workspace, workspace_bytes,
+                           status, stream);
+}
+
+int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, float* out, int B,
+                             int H, int Hkv, int L, int D, const int32_t* start,
+                             int32_t max_start, const attn_rope_params* rp, const float* table,
+                             const float* q_norm_w, float norm_eps, int window, float softcap,
+                             float scale, void* workspace, size_t workspace_bytes,
+                             int32_t* status, void* stream) {
+  return prefill_rope_impl(q, k, nullptr, vt, out, B, H, Hkv, L, D, start, max_start, rp, table,
+                           q_norm_w, norm_eps, window, softcap, scale, workspace, workspace_bytes,
+                           status, stream);
 }
 
 size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cache_len,

@@ -63,7 +63,10 @@ struct AttnShape {
 
 cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
 // Returns cudaErrorNotSupported (nothing launched) for shapes it does not take.
-cudaError_t launch_prefill_tc(const AttnShape& a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const AttnShape& a, cudaStream_t stream);      // V^T pre-pass + kernel
+cudaError_t launch_prefill_tc_vt(const AttnShape& a, cudaStream_t stream);   // a.vt already written
+cudaError_t launch_transpose_v(const float* v, float* vt, int BHkv, int L, int D, int vt_pitch,
+                               cudaStream_t stream);
 bool prefill_tc_supports(int D);
 int prefill_vt_pitch(int L);   // row pitch (floats) of the V^T workspace
 cudaError_t launch_prefill_tq(const AttnShape& a, cudaStream_t stream);  // D <= 128

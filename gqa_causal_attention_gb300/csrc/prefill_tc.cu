@@ -538,9 +538,6 @@ cudaError_t launch_dp(const AttnShape& s, cudaStream_t stream) {
       !make_map(&tk, s.k, s.D, s.L, s.B * s.Hkv, C::BK) ||
       !make_map_vt(&tv, s.vt, s.D, s.L, s.vt_pitch, s.B * s.Hkv, C::DP))
     return cudaErrorInvalidValue;
-  transpose_v_kernel<<<dim3((s.L + 31) / 32, (s.D + 31) / 32, s.B * s.Hkv), 256, 0,
-                       stream>>>(s.v, s.vt, s.L, s.D, s.vt_pitch);
-  if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
   TcArgs a{};
   a.q = s.q;
   a.out = s.out;
@@ -567,14 +564,24 @@ bool prefill_tc_supports(int D) { return D % 4 == 0 && D >= 32 && D <= kMaxHeadD
 
 int prefill_vt_pitch(int L) { return (L + 3) / 4 * 4; }
 
+cudaError_t launch_transpose_v(const float* v, float* vt, int BHkv, int L, int D, int vt_pitch,
+                               cudaStream_t stream) {
+  transpose_v_kernel<<<dim3((L + 31) / 32, (D + 31) / 32, BHkv), 256, 0, stream>>>(v, vt, L, D,
+                                                                                  vt_pitch);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prefill_tc(const AttnShape& s, cudaStream_t stream) {
   if (!prefill_tc_supports(s.D)) return cudaErrorNotSupported;
-  if (s.D <= 128) {
-    transpose_v_kernel<<<dim3((s.L + 31) / 32, (s.D + 31) / 32, s.B * s.Hkv), 256, 0,
-                         stream>>>(s.v, s.vt, s.L, s.D, s.vt_pitch);
-    if (cudaError_t e = cudaGetLastError(); e != cudaSuccess) return e;
-    return launch_prefill_tq(s, stream);
-  }
+  if (cudaError_t e = launch_transpose_v(s.v, s.vt, s.B * s.Hkv, s.L, s.D, s.vt_pitch, stream);
+      e != cudaSuccess)
+    return e;
+  return launch_prefill_tc_vt(s, stream);
+}
+
+cudaError_t launch_prefill_tc_vt(const AttnShape& s, cudaStream_t stream) {
+  if (!prefill_tc_supports(s.D)) return cudaErrorNotSupported;
+  if (s.D <= 128) return launch_prefill_tq(s, stream);
   switch ((s.D + 31) / 32) {
     case 5: return launch_dp<160>(s, stream);
     case 6: return launch_dp<192>(s, stream);

@@ -153,9 +153,9 @@ int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out,
  * result as attn_rope_apply(q, start, rp, table, q_norm_w) followed by
  * gqa_attn_prefill, but q is the raw query and is left unmodified. k must
  * already be rotated (kv_cache_append does that). For D % 32 == 0, D <= 128 and
- * rope_dim % 64 == 0 the rotation happens inside the tensor-core kernel, on the
- * way from shared to tensor memory; other shapes rotate q into the workspace
- * first. Positions are start[b] + l; max_start bounds every start[b].
+ * rope_dim % 64 == 0 the rotation happens inside the tensor-core kernel, in
+ * tensor memory after the Q tile's copy there; other shapes rotate q into the
+ * workspace first. Positions are start[b] + l; max_start bounds every start[b].
  */
 size_t gqa_attn_prefill_rope_workspace_size(int B, int H, int Hkv, int L, int D,
                                             const attn_rope_params* rp);
@@ -165,6 +165,35 @@ int gqa_attn_prefill_rope(const float* q, const float* k, const float* v, float*
                           float norm_eps, int window, float softcap, float scale,
                           void* workspace, size_t workspace_bytes, int32_t* status,
                           void* stream);
+
+/*
+ * v transposed for the tensor-core prefill: vt[b, hkv, d, m] = v[b, hkv, m, d],
+ * each (b, hkv, d) row holding gqa_attn_vt_pitch(L) floats (the first L used).
+ * gqa_attn_prefill and gqa_attn_prefill_rope build it in their workspace on
+ * every call; a caller can build it once with gqa_attn_v_transpose and hand it
+ * to gqa_attn_prefill_rope_vt. Tensor-core head dims only (D % 4 == 0,
+ * 32 <= D <= 256; ATTN_ERR_SHAPE otherwise).
+ *   v   [B, Hkv, L, D]                          fp32, 16-byte aligned, read
+ *   vt  B * Hkv * D * gqa_attn_vt_pitch(L) floats, 16-byte aligned, written
+ */
+int gqa_attn_vt_pitch(int L);
+int gqa_attn_v_transpose(const float* v, float* vt, int B, int Hkv, int L, int D, void* stream);
+
+/*
+ * gqa_attn_prefill_rope with v given transposed (vt as gqa_attn_v_transpose
+ * writes it, read only): the attention kernel alone, no pre-pass. Same
+ * arguments and results otherwise; tensor-core head dims only. The workspace
+ * (gqa_attn_prefill_rope_vt_workspace_size bytes) holds rotated q for the
+ * shapes that do not rotate inside the kernel; for the others it may be NULL.
+ */
+size_t gqa_attn_prefill_rope_vt_workspace_size(int B, int H, int L, int D,
+                                               const attn_rope_params* rp);
+int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, float* out, int B,
+                             int H, int Hkv, int L, int D, const int32_t* start,
+                             int32_t max_start, const attn_rope_params* rp, const float* table,
+                             const float* q_norm_w, float norm_eps, int window, float softcap,
+                             float scale, void* workspace, size_t workspace_bytes,
+                             int32_t* status, void* stream);
 
 /*
  * Bytes of scratch gqa_attn_decode needs for these sizes (split-KV partial

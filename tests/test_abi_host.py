@@ -185,3 +185,28 @@ def test_binding_refuses_other_dtypes():
     xb = torch.zeros(1, 2, 3, 4, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         g.gqa_attn_prefill(xb, xb, xb, xb)
+
+
+@no_device
+def test_vt_entry_points_refuse_before_launch():
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+    assert lib.gqa_attn_vt_pitch(10) == 12 and lib.gqa_attn_vt_pitch(16) == 16
+    # head dims the tensor-core kernels do not take
+    assert lib.gqa_attn_v_transpose(P, P, 1, 2, 16, 6, None) == -2       # ATTN_ERR_SHAPE
+    assert lib.gqa_attn_v_transpose(P, P, 1, 2, 16, 20, None) == -2
+    assert lib.gqa_attn_v_transpose(P, None, 1, 2, 16, 64, None) == -1    # ATTN_ERR_NULL
+    assert lib.gqa_attn_v_transpose(P, ctypes.c_void_p(0x100004), 1, 2, 16, 64, None) == -6
+    rp = g.RopeParams.make(theta=1e4, max_positions=64)
+    st = P
+    args = (P, P, P, P, 1, 4, 2, 16, 20, st, 0, ctypes.byref(rp), P, None, 1e-6, 0, 0.0, 0.0,
+            None, 0, None, None)
+    assert lib.gqa_attn_prefill_rope_vt(*args) == -2                       # D = 20
+    # fused shape: no workspace needed; unfused (rope_dim 32): workspace refused
+    assert lib.gqa_attn_prefill_rope_vt_workspace_size(1, 4, 16, 64, ctypes.byref(rp)) == 16
+    rp32 = g.RopeParams.make(theta=1e4, rope_dim=32, max_positions=64)
+    assert lib.gqa_attn_prefill_rope_vt_workspace_size(1, 4, 16, 64, ctypes.byref(rp32)) == \
+        4 * 16 * 64 * 4
+    args32 = (P, P, P, P, 1, 4, 2, 16, 64, st, 0, ctypes.byref(rp32), P, None, 1e-6, 0, 0.0, 0.0,
+              None, 0, None, None)
+    assert lib.gqa_attn_prefill_rope_vt(*args32) == -5                     # ATTN_ERR_WORKSPACE

@@ -152,3 +152,36 @@ def test_prefill_rope_positions_up_to_the_table_end(L, start, max_positions):
     cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, theta=1e4)
     want, _, _ = oracle.prefill(q, k, v, torch.tensor([start], dtype=torch.int32), cfg)
     assert_close(out, want, "fused prefill at the table end")
+
+
+@pytest.mark.parametrize("B,H,Hkv,L,D,R,norm,window,softcap", [
+    (2, 8, 2, 300, 128, 128, False, 0, 0.0),      # q RoPE inside the kernel
+    (1, 4, 2, 130, 96, 32, True, 0, 0.0),         # q rotated into the workspace first
+    (1, 4, 2, 260, 256, 256, True, 100, 50.0),    # D = 256 kernel
+])
+def test_prefill_rope_vt_matches_prefill_rope(B, H, Hkv, L, D, R, norm, window, softcap):
+    """gqa_attn_v_transpose + gqa_attn_prefill_rope_vt: vt is v transposed exactly,
+    and the attention equals gqa_attn_prefill_rope bit for bit (same kernels)."""
+    q = syn.normal(81, "q", (B, H, L, D)).to(dev())
+    k = syn.normal(81, "k", (B, Hkv, L, D)).to(dev())
+    v = syn.normal(81, "v", (B, Hkv, L, D)).to(dev())
+    qn = syn.norm_weight(81, "qn", D).to(dev()) if norm else None
+    rp = g.RopeParams.make(theta=1e4, rope_dim=R, max_positions=4096)
+    table = g.rope_table(rp, D, dev())
+    st = torch.tensor([3] * B, dtype=torch.int32, device=dev())
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    pitch = g.gqa_attn_vt_pitch(L)
+    assert pitch >= L and pitch % 4 == 0
+    vt = torch.full((B, Hkv, D, pitch), float("nan"), device=dev())
+    g.gqa_attn_v_transpose(v, vt)
+    torch.cuda.synchronize()
+    assert torch.equal(vt[..., :L], v.transpose(2, 3))
+    out_vt = torch.empty_like(q)
+    g.gqa_attn_prefill_rope_vt(q, k, vt, out_vt, st, 3, rp, table, qn, 1e-6, window, softcap,
+                               status=status)
+    out = torch.empty_like(q)
+    g.gqa_attn_prefill_rope(q, k, v, out, st, 3, rp, table, qn, 1e-6, window, softcap,
+                            status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out_vt, out)
