@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b_prefill",
                     choices=["llama3_8b_prefill", "gemma2_window"],
                     help="prefill workload of the timed step")
+    ap.add_argument("--no-long-decode", action="store_true",
+                    help="skip the carried-cache decode (1024 steps after a 1024-token prefill)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the steps as eager launches instead of CUDA graph replays")
     ap.add_argument("--unfused-q-rope", action="store_true",
@@ -364,6 +366,55 @@ def bench_decode(w, args, dist, dev):
             "launches_per_step": 2 + ksplit}
 
 
+def bench_long_decode(w, args, dist, dev):
+    """The carried-cache decode workload: a cache filled by a 1024-token prefill's
+    append, then 1024 single-token steps (q RoPE, k RoPE + append, decode over the
+    growing cache), all 1024 captured in one CUDA graph and replayed."""
+    import torch
+    import gqa_causal_attention_gb300 as g
+
+    gen = torch.Generator(device=dev).manual_seed(w.seed)
+    rp = g.RopeParams.make(theta=w.theta, rope_dim=w.rope_dim, max_positions=w.max_positions,
+                           scaling=w.scaling)
+    table = g.rope_table(rp, w.D, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kc = torch.zeros(w.B, w.Hkv, w.capacity, w.D, device=dev)
+    vc = torch.zeros_like(kc)
+    k0 = torch.randn(w.B, w.Hkv, w.L, w.D, device=dev, generator=gen)
+    v0 = torch.randn(w.B, w.Hkv, w.L, w.D, device=dev, generator=gen)
+    zero = torch.zeros(w.B, dtype=torch.int32, device=dev)
+    g.kv_cache_append(k0, v0, zero, 0, rp, table, None, w.norm_eps, kc, vc, 0, status)
+    n = w.decode_steps
+    qs = torch.randn(n, w.B, w.H, 1, w.D, device=dev, generator=gen)
+    ks = torch.randn(n, w.B, w.Hkv, 1, w.D, device=dev, generator=gen)
+    vs = torch.randn(n, w.B, w.Hkv, 1, w.D, device=dev, generator=gen)
+    out = torch.empty(w.B, w.H, 1, w.D, device=dev)
+    pos = torch.arange(w.L, w.L + n, dtype=torch.int32, device=dev).repeat(w.B, 1).t().contiguous()
+    cl = (pos + 1).contiguous()
+    ws = torch.empty(max(4, g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, w.L + n, 0)
+                         // 4), device=dev)
+
+    def steps():
+        for t in range(n):
+            p = w.L + t
+            g.attn_rope_apply(qs[t], pos[t], p, rp, table, None, w.norm_eps, status)
+            g.kv_cache_append(ks[t], vs[t], pos[t], p, rp, table, None, w.norm_eps, kc, vc, 0,
+                              status)
+            g.gqa_attn_decode(qs[t], kc, vc, cl[t], p + 1, out, 0, 0.0, 0.0, ws, status)
+
+    gr = graph_of(steps, warm=1)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms = timed(gr.replay, 1, 2, dist)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    nbytes = 2.0 * w.Hkv * w.D * 4 * w.B * sum(w.L + t + 1 for t in range(n))
+    launches = sum(3 if g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, w.L + t + 1, 0)
+                   <= 16 else 4 for t in range(n))
+    return {"steps": n, "ms_per_step": ms / n, "us_per_token_step": 1e3 * ms / n,
+            "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "launches": launches,
+            "clocks": clk.summary()}
+
+
 def cpu_baseline_prefill(w, budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the prefill workload."""
     import oracle
@@ -483,6 +534,9 @@ def main():
             import dataclasses
             wd = dataclasses.replace(wd, B=args.decode_batch)
         dec = bench_decode(wd, args, dist, dev)
+    lng = None
+    if not args.no_decode and not args.no_long_decode:
+        lng = bench_long_decode(syn.WORKLOADS["long_decode"], args, dist, dev)
 
     if rank != 0:
         if dist:
@@ -542,6 +596,19 @@ def main():
             "gpu_launches": dec["launches_per_step"] * args.decode_steps,
             "clocks": dec["clocks"]}
         line["gpu_launches"] += line["decode"]["gpu_launches"]
+    if lng is not None:
+        wl = syn.WORKLOADS["long_decode"]
+        line["long_decode"] = {
+            "workload": "long_decode", "config": {"B": wl.B, "H": wl.H, "Hkv": wl.Hkv,
+                                                   "D": wl.D, "rope_dim": wl.rope_dim,
+                                                   "prefill": wl.L, "steps": wl.decode_steps},
+            "value": world * lng["gbs"], "unit": "GB/s",
+            "us_per_step": lng["us_per_token_step"], "bytes_total": lng["bytes"],
+            "step": "attn_rope_apply (q) + kv_cache_append + gqa_attn_decode, 1024 steps in one "
+                    "CUDA graph",
+            "note": "the cache (134 MB) is about L2-sized; part of each step's reads hit L2",
+            "gpu_launches": lng["launches"], "clocks": lng["clocks"]}
+        line["gpu_launches"] += lng["launches"]
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(w)
     print(json.dumps(line), flush=True)

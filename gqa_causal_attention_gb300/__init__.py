@@ -25,6 +25,7 @@ __all__ = [
     "gqa_attn_decode", "gqa_attn_prefill_rope", "gqa_attn_prefill_rope_workspace_size",
     "gqa_attn_decode_static", "gqa_attn_vt_pitch", "gqa_attn_v_transpose",
     "gqa_attn_prefill_rope_vt", "gqa_attn_prefill_rope_vt_workspace_size",
+    "gqa_attn_prefill_cached", "gqa_attn_prefill_cached_workspace_size",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
@@ -110,6 +111,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_attn_prefill_rope_vt": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                                ctypes.c_int32, rp, vp, vp, f, i32, f, f, vp, sz,
                                                vp, vp]),
+            "gqa_attn_prefill_cached_workspace_size": (sz, [i32, i32, i32, i32, i32,
+                                                            ctypes.c_int32, i32, rp]),
+            "gqa_attn_prefill_cached": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                              i32, vp, ctypes.c_int32, rp, vp, vp, f, i32, f, f,
+                                              vp, sz, vp, vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -339,6 +345,44 @@ def gqa_attn_prefill_rope_vt(q, k, vt, out, start, max_start: int, params: RopeP
                                          int(window), float(softcap), float(scale),
                                          _ptr(workspace), wbytes, _ptr(status), _stream(stream))
     _check("gqa_attn_prefill_rope_vt", rc)
+
+
+def gqa_attn_prefill_cached_workspace_size(B: int, H: int, Hkv: int, L: int, D: int,
+                                           max_start: int, window: int = 0,
+                                           params: RopeParams = None) -> int:
+    return int(load().gqa_attn_prefill_cached_workspace_size(
+        B, H, Hkv, L, D, int(max_start), int(window),
+        None if params is None else ctypes.byref(params)))
+
+
+def gqa_attn_prefill_cached(q, k, v, k_cache, v_cache, out, start, max_start: int,
+                            params: RopeParams = None, table=None, q_norm_w=None,
+                            norm_eps: float = 1e-6, window: int = 0, softcap: float = 0.0,
+                            scale: float = 0.0, workspace=None, status=None, stream=None) -> None:
+    """Prefill of a chunk (q [B,H,L,D], rotated k and v [B,Hkv,L,D]) continuing the cache
+    (k_cache, v_cache [B,Hkv,capacity,D]) after start[b] positions. params/table: q's RoPE
+    applied inside (q raw), or None (q already rotated)."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("out", out)):
+        _f32(n, t, 4)
+    _f32("table", table); _f32("q_norm_w", q_norm_w); _i32("start", start); _i32("status", status)
+    B, H, L, D = q.shape
+    Hkv, cap = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k.shape) != (B, Hkv, L, D) or v.shape != k.shape or out.shape != q.shape or \
+            tuple(k_cache.shape) != (B, Hkv, cap, D) or v_cache.shape != k_cache.shape:
+        raise ValueError("gqa_attn_prefill_cached: inconsistent shapes")
+    if workspace is None:
+        n = gqa_attn_prefill_cached_workspace_size(B, H, Hkv, L, D, max_start, window, params)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().gqa_attn_prefill_cached(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), cap, _ptr(out), B, H, Hkv, L, D,
+        _ptr(start), int(max_start), None if params is None else ctypes.byref(params),
+        _ptr(table), _ptr(q_norm_w), float(norm_eps), int(window), float(softcap), float(scale),
+        _ptr(workspace), wbytes, _ptr(status), _stream(stream))
+    _check("gqa_attn_prefill_cached", rc)
 
 
 def gqa_attn_decode_workspace_size(B: int, H: int, Hkv: int, D: int, max_cache_len: int,

@@ -323,6 +323,116 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
                            status, stream);
 }
 
+namespace {
+// Key rows per head of the continued prefill's key buffer.
+int64_t cached_lk(int32_t max_start, int window, int L) {
+  const int64_t pre = window > 0 ? (max_start < window - 1 ? max_start : window - 1) : max_start;
+  return pre + L;
+}
+struct CachedLayout {
+  size_t pre, kg, vtg, qrot, total;
+};
+CachedLayout cached_layout(int B, int H, int Hkv, int L, int D, int32_t max_start, int window,
+                           bool rotate_q_first) {
+  const int64_t Lk = cached_lk(max_start, window, L);
+  CachedLayout c{};
+  c.pre = 0;
+  c.kg = round256((size_t)B * sizeof(int32_t));
+  c.vtg = c.kg + round256((size_t)B * Hkv * Lk * D * sizeof(float));
+  c.qrot = c.vtg + round256((size_t)B * Hkv * D * gqa::prefill_vt_pitch((int)Lk) * sizeof(float));
+  c.total = c.qrot + (rotate_q_first ? (size_t)B * H * L * D * sizeof(float) : 0);
+  return c;
+}
+}  // namespace
+
+size_t gqa_attn_prefill_cached_workspace_size(int B, int H, int Hkv, int L, int D,
+                                              int32_t max_start, int window,
+                                              const attn_rope_params* rp) {
+  if (B < 0 || H < 1 || Hkv < 1 || L < 0 || max_start < 0 || window < 0 ||
+      !gqa::prefill_tq_supports_kv_off(D))
+    return 0;
+  if (rp && !rope_params_ok(rp, D)) return 0;
+  if (cached_lk(max_start, window, L) > (int64_t)1 << 30) return 0;
+  const bool rotate_first = rp && !rope_fused(D, rope_dim_of(rp, D));
+  return cached_layout(B, H, Hkv, L, D, max_start, window, rotate_first).total;
+}
+
+int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, const float* k_cache,
+                            const float* v_cache, int capacity, float* out, int B, int H,
+                            int Hkv, int L, int D, const int32_t* start, int32_t max_start,
+                            const attn_rope_params* rp, const float* table,
+                            const float* q_norm_w, float norm_eps, int window, float softcap,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || capacity < 1)
+    return ATTN_ERR_SHAPE;
+  if (!gqa::prefill_tq_supports_kv_off(D)) return ATTN_ERR_SHAPE;
+  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!q || !k || !v || !k_cache || !v_cache || !out || !start) return ATTN_ERR_NULL;
+  if (rp && (!table || !rope_params_ok(rp, D) || !(norm_eps >= 0.f))) return ATTN_ERR_PARAM;
+  if (!rp && (table || q_norm_w)) return ATTN_ERR_PARAM;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || (table && !aligned16(table)) ||
+      (q_norm_w && !aligned16(q_norm_w)))
+    return ATTN_ERR_ALIGN;
+  if (max_start < 0) return ATTN_ERR_POSITION;
+  if (rp && (int64_t)max_start + L - 1 >= (int64_t)max_pos_of(rp)) return ATTN_ERR_POSITION;
+  if (window == 0 && max_start > capacity) return ATTN_ERR_CAPACITY;
+  const size_t need =
+      gqa_attn_prefill_cached_workspace_size(B, H, Hkv, L, D, max_start, window, rp);
+  if (need == 0) return ATTN_ERR_SHAPE;
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int R = rp ? rope_dim_of(rp, D) : 0;
+  const bool fused = rp && rope_fused(D, R);
+  const CachedLayout lay = cached_layout(B, H, Hkv, L, D, max_start, window, rp && !fused);
+  char* ws = static_cast<char*>(workspace);
+  const int Lk = (int)cached_lk(max_start, window, L);
+
+  gqa::GatherJob gj{};
+  gj.k = k; gj.v = v; gj.k_cache = k_cache; gj.v_cache = v_cache; gj.start = start;
+  gj.pre = reinterpret_cast<int32_t*>(ws + lay.pre);
+  gj.kg = reinterpret_cast<float*>(ws + lay.kg);
+  gj.vtg = reinterpret_cast<float*>(ws + lay.vtg);
+  gj.B = B; gj.Hkv = Hkv; gj.L = L; gj.D = D; gj.capacity = capacity; gj.window = window;
+  gj.Lk = Lk; gj.vt_pitch = gqa::prefill_vt_pitch(Lk); gj.max_start = max_start;
+  gj.status = status;
+  if (cudaError_t e = gqa::launch_gather_kv(gj, s); e != cudaSuccess) return cuda_status(e);
+
+  gqa::AttnShape a{};
+  a.k = gj.kg; a.v = nullptr; a.out = out;
+  a.vt = gj.vtg; a.vt_pitch = gj.vt_pitch;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.L = L; a.D = D;
+  a.window = window; a.softcap = softcap > 0.f ? softcap : 0.f;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  a.status = status;
+  a.kv_off = gj.pre;
+  a.Lk = Lk;
+  a.q = q;
+  if (fused) {
+    a.rope.table = reinterpret_cast<const float2*>(table);
+    a.rope.start = start;
+    a.rope.norm_w = q_norm_w;
+    a.rope.norm_eps = norm_eps;
+    a.rope.R = R;
+    a.rope.max_positions = max_pos_of(rp);
+  } else if (rp) {
+    float* qrot = reinterpret_cast<float*>(ws + lay.qrot);
+    gqa::RopeJob j{};
+    j.x = const_cast<float*>(q); j.y = qrot;
+    j.B = B; j.NH = H; j.L = L; j.D = D; j.R = R;
+    j.start = start; j.max_positions = max_pos_of(rp);
+    j.table = reinterpret_cast<const float2*>(table);
+    j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status;
+    if (cudaError_t e = gqa::launch_rope_rows(j, s); e != cudaSuccess) return cuda_status(e);
+    a.q = qrot;
+  }
+  return cuda_status(gqa::launch_prefill_tq(a, s));
+}
+
 size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cache_len,
                                       int window) {
   if (B < 1 || H < 1 || Hkv < 1 || H % Hkv || D < 2 || max_cache_len < 1 || window < 0) return 0;

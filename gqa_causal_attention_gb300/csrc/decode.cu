@@ -463,7 +463,7 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
   const int per_row = (4096 + units - 1) / units;
   int c = (eff + per_row - 1) / per_row;
   c = ((c + 63) / 64) * 64;
-  if (c < 128) c = 128;
+  if (c < 64) c = 64;                            // few rows: more, shorter splits fill the GPU
   if (c > 256) c = 256;
   *chunk = c;
   *nsplit = (eff + c - 1) / c;

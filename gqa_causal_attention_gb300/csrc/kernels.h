@@ -59,6 +59,10 @@ struct AttnShape {
   float scale;              // > 0
   int32_t* status;
   QRope rope;               // rope.table == nullptr: q already rotated
+  // Continuing a cached prefix (D <= 128 kernel only): k and vt then hold Lk
+  // key rows per head, kv_off[b] of them before query row 0 of row b.
+  const int32_t* kv_off = nullptr;
+  int Lk = 0;               // 0: the chunk's own keys (Lk = L)
 };
 
 cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
@@ -68,6 +72,25 @@ cudaError_t launch_prefill_tc_vt(const AttnShape& a, cudaStream_t stream);   // 
 cudaError_t launch_transpose_v(const float* v, float* vt, int BHkv, int L, int D, int vt_pitch,
                                cudaStream_t stream);
 bool prefill_tc_supports(int D);
+// Keys for continuing a cached prefix: per (b, kv head), rows [0, pre_b) from the
+// cache (positions start[b] - pre_b .. start[b] - 1; slot = position, or position
+// mod window for a ring), then the chunk's L rows of k / v, then zeros up to Lk.
+// K goes to kg [B, Hkv, Lk, D], V transposed to vtg [B, Hkv, D, vt_pitch].
+// pre_b = start[b] (window 0) or min(start[b], window - 1); written to pre[b].
+struct GatherJob {
+  const float* k;           // [B, Hkv, L, D] rotated chunk keys
+  const float* v;
+  const float* k_cache;     // [B, Hkv, capacity, D]
+  const float* v_cache;
+  const int32_t* start;     // [B]
+  int32_t* pre;             // [B] out: prefix keys per row
+  float* kg;
+  float* vtg;
+  int B, Hkv, L, D, capacity, window, Lk, vt_pitch, max_start;
+  int32_t* status;
+};
+cudaError_t launch_gather_kv(const GatherJob& j, cudaStream_t stream);
+bool prefill_tq_supports_kv_off(int D);
 int prefill_vt_pitch(int L);   // row pitch (floats) of the V^T workspace
 cudaError_t launch_prefill_tq(const AttnShape& a, cudaStream_t stream);  // D <= 128
 bool prefill_fuses_rope(int D);  // the kernel taking D applies a.rope itself

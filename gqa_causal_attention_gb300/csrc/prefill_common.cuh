@@ -37,6 +37,11 @@ struct TcArgs {
   float c_cap_in;                              // 2 * log2(e) * scale / cap
   float c_cap_out;                             // log2(e) * cap
   int32_t* status;
+  // Keys continuing a cached prefix (persistent kernel): kv_off[b] keys precede
+  // query row 0 of batch row b in the key buffer, which has Lk rows per head.
+  // kv_off == nullptr: keys are the chunk's own (offset 0, Lk = L).
+  const int32_t* kv_off;
+  int Lk;
 };
 
 // Timeout-only wait used while winding down after an abort.

@@ -71,6 +71,7 @@ struct PBars {
 
 struct PUnit {
   int b, h, q0, jlo, n;
+  int qk0;                                    // key index of query row q0 (q0 + kv_off[b])
 };
 
 // Unit x of round r for block c: snake order evens out the heavy-first list.
@@ -86,8 +87,10 @@ __device__ __forceinline__ PUnit get_unit(const TcArgs& a, int x) {
   u.b = bh / a.H;
   u.h = bh % a.H;
   u.q0 = (a.QT - 1 - rank) * kBM;
-  const int lo = a.window > 0 ? max(0, u.q0 - a.window + 1) / C::BK : 0;
-  const int hi = min(u.q0 + kBM - 1, a.L - 1) / C::BK;
+  const int off = a.kv_off ? a.kv_off[u.b] : 0;
+  u.qk0 = u.q0 + off;
+  const int lo = a.window > 0 ? max(0, u.qk0 - a.window + 1) / C::BK : 0;
+  const int hi = min(u.qk0 + kBM - 1, off + a.L - 1) / C::BK;
   u.jlo = lo;
   u.n = hi - lo + 1;
   return u;
@@ -435,7 +438,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
-    const int qpos = u.q0 + row;
+    const int qpos = u.qk0 + row;               // the query's own key index
     float m_ref = -INFINITY, l = 0.f;         // running max (log2 units) and sum
 
     for (int i = 0; i < u.n; ++i) {
@@ -638,10 +641,11 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
+  const int Lk = s.Lk > 0 ? s.Lk : s.L;
   CUtensorMap tq, tk, tv, to;
   if (!make_map(&tq, s.q, s.D, s.L, s.B * s.H, kBM) ||
-      !make_map(&tk, s.k, s.D, s.L, s.B * s.Hkv, C::BK) ||
-      !make_map_vt(&tv, s.vt, s.D, s.L, s.vt_pitch, s.B * s.Hkv, C::DP) ||
+      !make_map(&tk, s.k, s.D, Lk, s.B * s.Hkv, C::BK) ||
+      !make_map_vt(&tv, s.vt, s.D, Lk, s.vt_pitch, s.B * s.Hkv, C::DP) ||
       !make_map(&to, s.out, s.D, s.L, s.B * s.H, 32))
     return cudaErrorInvalidValue;
   TcArgs a{};
@@ -663,6 +667,8 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   a.qnorm_eps = s.rope.norm_eps;
   a.rope_R = s.rope.R;
   a.rope_max_positions = s.rope.max_positions;
+  a.kv_off = s.kv_off;
+  a.Lk = Lk;
   const int grid = a.units < sm_count() ? a.units : sm_count();
   prefill_tq_kernel<DP, ROPE><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
@@ -671,6 +677,8 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
 }  // namespace
 
 bool prefill_fuses_rope(int D) { return D % 32 == 0 && D <= 128; }
+
+bool prefill_tq_supports_kv_off(int D) { return D % 4 == 0 && D >= 32 && D <= 128; }
 
 // D <= 128; V^T must already be in s.vt (launch_prefill_tc runs the transpose first).
 cudaError_t launch_prefill_tq(const AttnShape& s, cudaStream_t stream) {

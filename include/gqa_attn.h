@@ -196,6 +196,45 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
                              int32_t* status, void* stream);
 
 /*
+ * Prefill of a chunk that continues a carried cache ("mojolearn.transformer",
+ * TransformerBlock.forward with a TransformerState): the chunk's L queries at
+ * positions start[b] + l attend, causally, to the positions kept in the cache
+ * before the chunk and to the chunk itself:
+ *   out[b,h,l,:] = sum over positions m <= p = start[b] + l (and p - m < window
+ *   when window > 0) of softmax_m(cap(scale * q . key_m)) value_m,
+ * with key_m, value_m read from the cache for m < start[b] and from k, v (the
+ * chunk, row m - start[b]) for m >= start[b].
+ *   q        [B, H, L, D]   raw if rp != NULL (RMSNorm + RoPE applied here, at
+ *                           positions start[b] + l, as in gqa_attn_prefill_rope;
+ *                           q is not modified), else already rotated
+ *   k, v     [B, Hkv, L, D] the chunk's keys (rotated, e.g. by attn_rope_apply
+ *                           or kv_cache_append) and values
+ *   k_cache, v_cache [B, Hkv, capacity, D] the carried cache, rotated keys, as
+ *                           kv_cache_append fills it: slot = position (window 0,
+ *                           capacity >= every start[b]) or position mod window
+ *                           (a ring, capacity == window). With a ring, call this
+ *                           before appending the chunk, whose rows may overwrite
+ *                           the prefix the chunk's first queries need.
+ *   start    [B] device int32, positions already cached; max_start bounds them
+ *   workspace gqa_attn_prefill_cached_workspace_size bytes (the gathered keys,
+ *            transposed values and, for some rope shapes, rotated q)
+ * Head dims D % 4 == 0, 32 <= D <= 128 (ATTN_ERR_SHAPE otherwise). A start[b]
+ * outside [0, max_start] (or above capacity without a window) sets
+ * ATTN_DEV_POSITION (ATTN_DEV_CAPACITY) and that row attends only to the chunk.
+ * Cost: the gather reads the kept prefix of every (b, kv head) once per call.
+ */
+size_t gqa_attn_prefill_cached_workspace_size(int B, int H, int Hkv, int L, int D,
+                                              int32_t max_start, int window,
+                                              const attn_rope_params* rp);
+int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, const float* k_cache,
+                            const float* v_cache, int capacity, float* out, int B, int H,
+                            int Hkv, int L, int D, const int32_t* start, int32_t max_start,
+                            const attn_rope_params* rp, const float* table,
+                            const float* q_norm_w, float norm_eps, int window, float softcap,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream);
+
+/*
  * Bytes of scratch gqa_attn_decode needs for these sizes (split-KV partial
  * results). max_cache_len bounds every cache_len[b].
  */

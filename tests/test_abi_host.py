@@ -210,3 +210,25 @@ def test_vt_entry_points_refuse_before_launch():
     args32 = (P, P, P, P, 1, 4, 2, 16, 64, st, 0, ctypes.byref(rp32), P, None, 1e-6, 0, 0.0, 0.0,
               None, 0, None, None)
     assert lib.gqa_attn_prefill_rope_vt(*args32) == -5                     # ATTN_ERR_WORKSPACE
+
+
+@no_device
+def test_cached_prefill_refuses_before_launch():
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+
+    def call(D=64, capacity=128, max_start=32, window=0, ws=None, wbytes=0, L=16):
+        return lib.gqa_attn_prefill_cached(P, P, P, P, P, capacity, P, 1, 4, 2, L, D, P,
+                                           max_start, None, None, None, 1e-6, window, 0.0, 0.0,
+                                           ws, wbytes, None, None)
+
+    assert call(D=256) == -2                      # head dims past the persistent kernel
+    assert call(D=20) == -2
+    assert call(window=64, capacity=128) == -2    # a ring holds exactly window slots
+    assert call(max_start=200) == -4              # prefix positions without cache slots
+    assert call() == -5                           # no workspace
+    need = lib.gqa_attn_prefill_cached_workspace_size(1, 4, 2, 16, 64, 32, 0, None)
+    # pre [B] + K rows (32 prefix + 16 chunk) + V^T rows of the same keys
+    assert need >= 2 * 2 * 48 * 64 * 4
+    assert lib.gqa_attn_prefill_cached_workspace_size(1, 4, 2, 16, 64, 1000, 64, None) < need * 3
+    assert call(ws=ctypes.c_void_p(0x100004), wbytes=need) == -6
