@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b_prefill",
                     choices=["llama3_8b_prefill", "gemma2_window"],
                     help="prefill workload of the timed step")
+    ap.add_argument("--no-chunked", action="store_true",
+                    help="skip the chunked prefill continuing a cached prefix")
     ap.add_argument("--no-long-decode", action="store_true",
                     help="skip the carried-cache decode (1024 steps after a 1024-token prefill)")
     ap.add_argument("--no-graph", action="store_true",
@@ -415,6 +417,45 @@ def bench_long_decode(w, args, dist, dev):
             "clocks": clk.summary()}
 
 
+CHUNKED = {"B": 1, "H": 32, "Hkv": 8, "D": 128, "prefix": 6144, "L": 2048, "theta": 5e5}
+
+
+def bench_chunked_prefill(args, dist, dev):
+    """A 2048-token chunk continuing a 6144-token cache (Llama-3-8B attention shape):
+    gqa_attn_prefill_cached with q's RoPE fused; the call gathers the kept prefix and
+    the chunk, then runs the persistent tensor-core kernel."""
+    import torch
+    import gqa_causal_attention_gb300 as g
+
+    c = CHUNKED
+    B, H, Hkv, D, P, L = c["B"], c["H"], c["Hkv"], c["D"], c["prefix"], c["L"]
+    gen = torch.Generator(device=dev).manual_seed(5)
+    rp = g.RopeParams.make(theta=c["theta"], max_positions=P + L)
+    table = g.rope_table(rp, D, dev)
+    kc = torch.randn(B, Hkv, P + L, D, device=dev, generator=gen)
+    vc = torch.randn(B, Hkv, P + L, D, device=dev, generator=gen)
+    q = torch.randn(B, H, L, D, device=dev, generator=gen)
+    k = torch.randn(B, Hkv, L, D, device=dev, generator=gen)
+    v = torch.randn(B, Hkv, L, D, device=dev, generator=gen)
+    out = torch.empty_like(q)
+    st = torch.full((B,), P, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(g.gqa_attn_prefill_cached_workspace_size(B, H, Hkv, L, D, P, 0, rp) // 4 + 4,
+                     device=dev)
+
+    def call():
+        g.gqa_attn_prefill_cached(q, k, v, kc, vc, out, st, P, rp, table, workspace=ws,
+                                  status=status)
+
+    steps = max(3, min(args.steps, 100))
+    ms = timed(call, steps, max(3, args.warmup), dist) / steps
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    flops = 4.0 * B * H * D * sum(P + l + 1 for l in range(L))
+    return {"config": dict(c), "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "flops": flops,
+            "launches": 2}
+
+
 def cpu_baseline_prefill(w, budget_s=20.0):
     """The oracle, as it stands, on a bounded sample of the prefill workload."""
     import oracle
@@ -534,6 +575,7 @@ def main():
             import dataclasses
             wd = dataclasses.replace(wd, B=args.decode_batch)
         dec = bench_decode(wd, args, dist, dev)
+    chk = None if args.no_chunked else bench_chunked_prefill(args, dist, dev)
     lng = None
     if not args.no_decode and not args.no_long_decode:
         lng = bench_long_decode(syn.WORKLOADS["long_decode"], args, dist, dev)
@@ -596,6 +638,15 @@ def main():
             "gpu_launches": dec["launches_per_step"] * args.decode_steps,
             "clocks": dec["clocks"]}
         line["gpu_launches"] += line["decode"]["gpu_launches"]
+    if chk is not None:
+        line["chunked_prefill"] = {
+            "workload": "chunked_prefill", "config": chk["config"], "value": world * chk["tflops"],
+            "unit": "TFLOP/s", "ms_per_step": chk["ms"], "flops_per_step": chk["flops"],
+            "frac_of_tf32_peak": chk["tflops"] / pk["tf32_tflops"],
+            "step": "gqa_attn_prefill_cached (gather of the cached prefix + chunk, then the "
+                    "persistent kernel with q RoPE fused)",
+            "gpu_launches": chk["launches"] * max(3, min(args.steps, 100))}
+        line["gpu_launches"] += line["chunked_prefill"]["gpu_launches"]
     if lng is not None:
         wl = syn.WORKLOADS["long_decode"]
         line["long_decode"] = {
