@@ -368,54 +368,6 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars, co
   return true;
 }
 
-// ---------------------------------------------------------------- softmax helpers
-// The block's P is accepted against the running reference while its sum stays
-// at most 2^kRescaleLog2 (no single weight can then exceed it).
-constexpr float kRescaleLimit = 256.0f;
-static_assert(kRescaleLog2 == 8.0f, "limit is 2^kRescaleLog2");
-
-// Row maximum of N scores (three-input maxima, 8 chains).
-template <int N>
-__device__ __forceinline__ float tq_max(const float* s) {
-  float mx[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) mx[j] = s[j];
-  int c = 8;
-#pragma unroll
-  for (; c + 16 <= N; c += 16)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) mx[j] = tc::max3(mx[j], s[c + j], s[c + 8 + j]);
-#pragma unroll
-  for (; c < N; c += 8)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) mx[j] = fmaxf(mx[j], s[c + j]);
-  return fmaxf(tc::max3(mx[0], mx[1], mx[2]),
-               fmaxf(tc::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-}
-
-// p = 2^(score * cs - m) in place, truncated to the TF32 value the tensor core
-// uses (so the row sum adds exactly the weights applied to V); returns the sum.
-// Pairs of columns go through the paired fp32 FMA / add.
-template <int N>
-__device__ __forceinline__ float tq_exp_sum(float* s, float cs, float m) {
-  const uint64_t c2 = tc::pack2(cs, cs), m2 = tc::pack2(-m, -m);
-  uint64_t acc[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = tc::pack2(0.f, 0.f);
-#pragma unroll
-  for (int c = 0; c < N; c += 2) {
-    float x0, x1;
-    tc::unpack2(tc::fma2(tc::pack2(s[c], s[c + 1]), c2, m2), x0, x1);
-    const float p0 = tc::trunc_tf32(tc::ex2(x0)), p1 = tc::trunc_tf32(tc::ex2(x1));
-    s[c] = p0;
-    s[c + 1] = p1;
-    acc[(c / 2) % 4] = tc::add2(acc[(c / 2) % 4], tc::pack2(p0, p1));
-  }
-  float a0, a1;
-  tc::unpack2(tc::add2(tc::add2(acc[0], acc[1]), tc::add2(acc[2], acc[3])), a0, a1);
-  return a0 + a1;
-}
-
 // ---------------------------------------------------------------- softmax (4 warps)
 // Thread = one query row of the current unit; tcgen05.ld/st run on full warps.
 template <class C, bool ROPE>
