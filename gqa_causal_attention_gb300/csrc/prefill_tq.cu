@@ -11,14 +11,15 @@
 //    TMEM = Q | O | S0 | S1 (S double-buffered: S of the next key block is
 //    computed while softmax turns this one into P).
 //  * TMA streams Q tiles, K blocks and V^T blocks of successive units through
-//    one ring of stages. The MMA issuer moves each Q tile from shared to
-//    tensor memory with tcgen05.cp, in order with its MMAs, so the next
-//    unit's first S products overlap the previous unit's last softmax and its
-//    epilogue; only the first P V of a unit waits for O to be read out.
-//  * With q RoPE fused (gqa_attn_prefill_rope), the softmax warps rotate each
-//    Q tile in tensor memory after tcgen05.cp and before its first S MMA (the
-//    tile enters the ring right after the previous unit's last K block, so
-//    this overlaps that unit's last P V products).
+//    one ring of stages; a unit's Q tile enters right after the previous
+//    unit's last K block. The S issuer moves it to tensor memory with
+//    tcgen05.cp, in pipe order right after that unit's last S, which frees its
+//    stage early; the next unit's first S products then overlap the previous
+//    unit's last softmax and its epilogue. With q RoPE fused
+//    (gqa_attn_prefill_rope) the softmax warps normalise and rotate the tile in
+//    tensor memory after the previous unit's last P.
+//  * S = Q K^T and O += P V^T come from two issuing threads on different SM
+//    sub-partitions, each sharing its sub-partition with one softmax warp.
 //  * Softmax, masking, softcap, rescaling and the epilogue are those of the
 //    non-persistent kernel (one query row per thread, base-2 online softmax,
 //    P truncated to TF32 in place of S).
@@ -42,10 +43,11 @@ struct PCfg {
   static constexpr int kVtChunk = DP * 128;             // DP rows x 128 B (32 keys of V^T)
   static constexpr int kStage = kChunks * kKChunk;      // one K block, V^T block or Q tile
   static constexpr int kEpi = 4 * 4096;                 // per-warp 32 x 32 output staging
-  static constexpr int kNSraw = (kSmemLimit - 2048 - kEpi) / kStage;
+  static constexpr int kTab = 32 * 64 * 8;              // RoPE table rows 0..31, up to 64 pairs
+  static constexpr int kNSraw = (kSmemLimit - 2048 - kEpi - kTab) / kStage;
   static constexpr int NS = kNSraw > 8 ? 8 : kNSraw;
-  static constexpr int kThreads = 64 + 128;          // producer, MMA, 4 softmax
-  static constexpr int kSmemNeed = NS * kStage + kEpi + 2048;
+  static constexpr int kThreads = 64 + 128 + 32;     // producer, S issuer, 4 softmax, P V issuer
+  static constexpr int kSmemNeed = NS * kStage + kEpi + kTab + 2048;
   static constexpr int kSmem =
       kSmemNeed > kSmemLimit / 2 + 4096 ? kSmemNeed : kSmemLimit / 2 + 4096;
   static constexpr int kQCol = 0, kOCol = DP, kSCol = 2 * DP;
@@ -59,12 +61,12 @@ struct PBars {
   uint64_t kv_empty[8];
   uint64_t s_full[2];
   uint64_t p_ready[2];
-  uint64_t o_done;
+  uint64_t o_done[2];                          // P V of block X done (X % 2)
   uint64_t o_final;
   uint64_t o_free;
   uint64_t q_copied;                           // a Q tile is in tensor memory (one phase per unit)
   uint64_t q_ready;                            // fused RoPE: that Q tile is rotated
-  uint64_t drain;
+  uint64_t drain[2];                           // each issuer's MMAs and copies done
   uint32_t tmem_base;
   int abort;
 };
@@ -98,11 +100,10 @@ __device__ __forceinline__ PUnit get_unit(const TcArgs& a, int x) {
 
 // ---------------------------------------------------------------- producer (one thread)
 // Ring order: the first unit's Q tile; then per unit K_0 .. K_{n-1} interleaved
-// with V^T_0 .. V^T_{n-1} as K_0, (K_{i+1}, V^T_i)..., and the next unit's Q
-// tile. With fused RoPE that Q tile comes right after this unit's last K block,
-// so it lands while this unit's last P V products are pending and the softmax
-// warps can rotate it in tensor memory before the next unit's first S = Q K^T;
-// otherwise it comes after the last V^T block.
+// with V^T_0 .. V^T_{n-1} as K_0, (K_{i+1}, V^T_i)..., with the next unit's Q
+// tile right after the last K block, so it lands while this unit's last P V
+// products are pending and the softmax warps can move it to tensor memory
+// before the next unit's first S = Q K^T.
 template <class C>
 __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
                             const CUtensorMap* tv, uint8_t* skv, PBars* bars) {
@@ -150,84 +151,110 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
     const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
     const bool has_next = xn < a.units;
     const PUnit un = get_unit<C>(a, has_next ? xn : x);
-    // Warm the next Q tile into L2 now: its load comes within a few blocks.
-    if (has_next)
+    // Warm the next Q tile (and its RoPE table lines) into L2 now: they are
+    // read within a few blocks.
+    if (has_next) {
       for (int c = 0; c < C::kChunks; ++c)
         tc::tma_prefetch_l2_3d(tq, 32 * c, un.q0, un.b * a.H + un.h);
-    const bool early = a.rope_table && has_next;  // next Q after the last K, else after the last V
+      if (a.rope_table) {
+        const long half = a.rope_R / 2;
+        const long p0 = min(max(static_cast<long>(a.rope_start[un.b]) + un.q0, 0L),
+                            static_cast<long>(a.rope_max_positions - 1));
+        const long p1 = min(p0 + kBM, static_cast<long>(a.rope_max_positions));
+        tc::bulk_prefetch_l2(a.rope_table + p0 * half, static_cast<uint32_t>((p1 - p0) * half * 8));
+      }
+    }
     if (r == 0) ok = load(0, u, 0);
     if (ok) ok = load(1, u, u.jlo);
-    if (ok && u.n == 1 && early) ok = load(0, un, 0);
+    if (ok && u.n == 1 && has_next) ok = load(0, un, 0);
     for (int i = 0; ok && i < u.n; ++i) {
       if (i + 1 < u.n) {
         ok = load(1, u, u.jlo + i + 1);
-        if (ok && i + 2 == u.n && early) ok = load(0, un, 0);
+        if (ok && i + 2 == u.n && has_next) ok = load(0, un, 0);
       }
       if (ok) ok = load(2, u, u.jlo + i);
     }
-    if (ok && has_next && !early) ok = load(0, un, 0);
   }
   // Every copy this block started lands before the block may exit.
   for (int s = 0; s < C::NS; ++s)
     if (filled[s]) drain_wait(&bars->kv_full[s], fill_parity[s]);
 }
 
-// ---------------------------------------------------------------- MMA issuer (one thread)
+// ---------------------------------------------------------------- MMA issuers (two threads)
+// S = Q K^T and O += P V^T are issued by two threads on different SM
+// sub-partitions (warps 1 and 6). Each sub-partition also runs a softmax warp,
+// and a busy neighbour slows one issuer's M128 N128 instructions to ~110
+// cycles; two issuers in parallel keep the tensor pipe at its 64-cycle rate.
+// Both walk the producer's ring order, each taking its own items and stepping
+// over the other's; P V of block X signals o_done[X % 2], so every wait on it
+// (S of block X + 2 overwrites X's P; a rescale of O in block X + 1) names a
+// phase that cannot be two behind.
 template <class C>
-__device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars) {
-  volatile int* abort = &bars->abort;
-  constexpr uint32_t id_s = tc::idesc_tf32(kBM, C::BK, false);
-  constexpr uint32_t id_pv = tc::idesc_tf32(kBM, C::DP, false);
-  // Descriptors are built once; an operand offset is added to the start-address
-  // field (address >> 4), which stays below 2^14 for any shared-memory address.
-  const uint64_t base_desc = tc::sdesc_sw128(tc::smem_u32(skv), 16, 1024);
+struct RingCursor {
   int stage = 0;
   uint32_t phase = 0;
-  auto next = [&](int& st) -> bool {
-    if (!tc::mbar_wait(&bars->kv_full[stage], phase, abort)) return false;
-    st = stage;
+  __device__ __forceinline__ void skip() {
     if (++stage == C::NS) {
       stage = 0;
       phase ^= 1u;
     }
+  }
+  __device__ __forceinline__ bool take(PBars* bars, volatile int* abort, int& st) {
+    if (!tc::mbar_wait(&bars->kv_full[stage], phase, abort)) return false;
+    st = stage;
+    skip();
     return true;
-  };
-  auto stage_desc = [&](int st) { return base_desc + static_cast<uint32_t>((st * C::kStage) >> 4); };
-  // S[buf] = Q K^T: A = Q from TMEM, B = K block (K-major).
-  auto issue_s = [&](int buf, int st) {
-    const uint32_t d = tmem + C::kSCol + buf * C::BK;
-    const uint64_t kd = stage_desc(st);
-#pragma unroll
-    for (int kk = 0; kk < C::DP / 8; ++kk) {
-      const int c = kk / 4, off = (kk % 4) * 32;
-      tc::mma_tf32_ts(d, tmem + C::kQCol + 8 * kk, kd + ((c * C::kKChunk + off) >> 4), id_s,
-                      kk > 0);
-    }
-  };
-  // O += P V: A = P from TMEM (in place of S), B = V^T block (K-major).
-  auto issue_pv = [&](int buf, int st, bool acc) {
-    const uint32_t d = tmem + C::kOCol;
-    const uint64_t vd = stage_desc(st);
-#pragma unroll
-    for (int kk = 0; kk < C::BK / 8; ++kk) {
-      const int c = kk / 4, off = (kk % 4) * 32;
-      tc::mma_tf32_ts(d, tmem + C::kSCol + buf * C::BK + 8 * kk,
-                      vd + ((c * C::kVtChunk + off) >> 4), id_pv, (acc || kk > 0) ? 1u : 0u);
-    }
-  };
+  }
+};
 
-  // Q tile: shared -> tensor memory, in order behind every earlier MMA that
-  // read the previous Q; q_copied tells the softmax warps it is there.
+template <class C>
+__device__ __forceinline__ uint64_t stage_desc(uint64_t base_desc, int st) {
+  return base_desc + static_cast<uint32_t>((st * C::kStage) >> 4);
+}
+
+// The S issuer: Q tiles to tensor memory (tcgen05.cp) and S = Q K^T.
+template <class C>
+__device__ void tq_mma_s(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars) {
+  volatile int* abort = &bars->abort;
+  constexpr uint32_t id_s = tc::idesc_tf32(kBM, C::BK, false);
+  // Descriptors are built once; an operand offset is added to the start-address
+  // field (address >> 4), which stays below 2^14 for any shared-memory address.
+  const uint64_t base_desc = tc::sdesc_sw128(tc::smem_u32(skv), 16, 1024);
+  RingCursor<C> ring;
+  // Q tile: shared -> tensor memory, in pipe order behind the last S that read
+  // the previous Q (so the next unit's S products follow without a wait); its
+  // stage is free once the copy is done.
   auto copy_q = [&]() -> bool {
     int st = 0;
-    if (!next(st)) return false;
-    const uint64_t qd = stage_desc(st);
+    if (!ring.take(bars, abort, st)) return false;
+    const uint64_t qd = stage_desc<C>(base_desc, st);
 #pragma unroll
     for (int kk = 0; kk < C::DP / 8; ++kk) {
       const int c = kk / 4, j = kk % 4;
       tc::tmem_cp_128x256b(tmem + C::kQCol + 8 * kk, qd + ((c * C::kKChunk + 32 * j) >> 4));
     }
     tc::mma_commit(&bars->q_copied);
+    tc::mma_commit(&bars->kv_empty[st]);
+    return true;
+  };
+  // S[G % 2] = Q K^T for global block G, once P V of block G - 2 has read that buffer.
+  // The o_done wait comes before the ring wait: it also shows that the stage's
+  // previous item (possibly a V^T this thread skipped) has landed, so the
+  // parity of the ring wait cannot alias an older fill.
+  auto issue_s = [&](uint32_t G) -> bool {
+    if (G >= 2 && !tc::mbar_wait(&bars->o_done[G & 1], ((G - 2) >> 1) & 1, abort)) return false;
+    int st = 0;
+    if (!ring.take(bars, abort, st)) return false;
+    tc::fence_after_sync();
+    const uint32_t d = tmem + C::kSCol + (G & 1) * C::BK;
+    const uint64_t kd = stage_desc<C>(base_desc, st);
+#pragma unroll
+    for (int kk = 0; kk < C::DP / 8; ++kk) {
+      const int c = kk / 4, off = (kk % 4) * 32;
+      tc::mma_tf32_ts(d, tmem + C::kQCol + 8 * kk, kd + ((c * C::kKChunk + off) >> 4), id_s,
+                      kk > 0);
+    }
+    tc::mma_commit(&bars->s_full[G & 1]);
     tc::mma_commit(&bars->kv_empty[st]);
     return true;
   };
@@ -239,72 +266,110 @@ __device__ void tq_mma(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
     const bool has_next = unit_of(blockIdx.x, r + 1, gridDim.x) < a.units;
-    const bool early = a.rope_table && has_next;    // ring order as in the producer
-    int st = 0;
     if (r == 0 && !(ok = copy_q())) break;
     // With fused RoPE the softmax warps rotate Q in tensor memory first.
-    if (a.rope_table && !(ok = tc::mbar_wait(&bars->q_ready, uc & 1, abort))) break;
-    tc::fence_after_sync();
-    if (!(ok = next(st))) break;
-    issue_s(g & 1, st);
-    tc::mma_commit(&bars->s_full[g & 1]);
-    tc::mma_commit(&bars->kv_empty[st]);
-    if (u.n == 1 && early && !(ok = copy_q())) break;
+    if (a.rope_table) {
+      if (!(ok = tc::mbar_wait(&bars->q_ready, uc & 1, abort))) break;
+      tc::fence_after_sync();
+    }
+    if (!(ok = issue_s(g))) break;
+    if (u.n == 1 && has_next && !(ok = copy_q())) break;
+    for (int i = 0; i < u.n; ++i) {
+      if (i + 1 < u.n) {
+        if (!(ok = issue_s(g + i + 1))) break;
+        if (i + 2 == u.n && has_next && !(ok = copy_q())) break;
+      }
+      ring.skip();                                  // V^T_i: the P V issuer's
+    }
+    if (!ok) break;
+    g += u.n;
+    ++uc;
+  }
+  // No MMA or copy of this thread may still run when the block frees its TMEM.
+  tc::mma_commit(&bars->drain[0]);
+  drain_wait(&bars->drain[0], 0);
+}
+
+// The P V issuer: O += P V^T once the softmax has written P of the block.
+template <class C>
+__device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars) {
+  volatile int* abort = &bars->abort;
+  constexpr uint32_t id_pv = tc::idesc_tf32(kBM, C::DP, false);
+  const uint64_t base_desc = tc::sdesc_sw128(tc::smem_u32(skv), 16, 1024);
+  RingCursor<C> ring;
+  uint32_t g = 0, uc = 0;
+  bool ok = true;
+  for (int r = 0; ok; ++r) {
+    const int x = unit_of(blockIdx.x, r, gridDim.x);
+    if (x >= a.units) break;
+    const PUnit u = get_unit<C>(a, x);
+    const bool has_next = unit_of(blockIdx.x, r + 1, gridDim.x) < a.units;
+    if (r == 0) ring.skip();                        // the first Q tile
+    ring.skip();                                    // K_0
+    if (u.n == 1 && has_next) ring.skip();          // next Q
     for (int i = 0; i < u.n; ++i) {
       const uint32_t G = g + i;
       if (i + 1 < u.n) {
-        if (!(ok = next(st))) break;
-        issue_s((G + 1) & 1, st);
-        tc::mma_commit(&bars->s_full[(G + 1) & 1]);
-        tc::mma_commit(&bars->kv_empty[st]);
-        if (i + 2 == u.n && early && !(ok = copy_q())) break;
+        ring.skip();                                // K_{i+1}
+        if (i + 2 == u.n && has_next) ring.skip();  // next Q
       }
-      if (!(ok = next(st))) break;
+      // P of block G first: S of block G has then read K_G, the stage's previous
+      // item when no Q tile sits between, so the ring wait below cannot alias.
       if (!(ok = tc::mbar_wait(&bars->p_ready[G & 1], (G >> 1) & 1, abort))) break;
+      int st = 0;
+      if (!(ok = ring.take(bars, abort, st))) break;
       if (i == 0 && uc > 0 && !(ok = tc::mbar_wait(&bars->o_free, (uc - 1) & 1, abort))) break;
       tc::fence_after_sync();
-      issue_pv(G & 1, st, i > 0);
-      tc::mma_commit(&bars->o_done);
+      const uint32_t d = tmem + C::kOCol;
+      const uint64_t vd = stage_desc<C>(base_desc, st);
+#pragma unroll
+      for (int kk = 0; kk < C::BK / 8; ++kk) {
+        const int c = kk / 4, off = (kk % 4) * 32;
+        tc::mma_tf32_ts(d, tmem + C::kSCol + (G & 1) * C::BK + 8 * kk,
+                        vd + ((c * C::kVtChunk + off) >> 4), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+      }
+      tc::mma_commit(&bars->o_done[G & 1]);
       tc::mma_commit(&bars->kv_empty[st]);
     }
     if (!ok) break;
     tc::mma_commit(&bars->o_final);
-    if (has_next && !early && !(ok = copy_q())) break;
     g += u.n;
     ++uc;
   }
-  // No MMA or copy may still run when the block frees its tensor memory.
-  tc::mma_commit(&bars->drain);
-  drain_wait(&bars->drain, 0);
+  tc::mma_commit(&bars->drain[1]);
+  drain_wait(&bars->drain[1], 0);
 }
 
 // ---------------------------------------------------------------- fused q RoPE (softmax warps)
-// Rotates the unit's Q tile where the MMA reads it, in tensor memory: thread =
-// query row, as in the softmax. RMSNorm (if q_norm_w) over the row first, then
-// RoPE at the row's absolute position start[b] + q0 + row, pairs (i, i + R/2)
-// taken 32 at a time with tcgen05.ld / tcgen05.st, (cos, sin) from the row's
-// table line. Rows past L hold zeros (TMA fill) and are left alone. Requires
-// D % 32 == 0, D <= 128 and R % 64 == 0.
+// Rotates the next unit's Q tile where the MMA reads it, in tensor memory:
+// thread = query row, as in the softmax. RMSNorm (if q_norm_w) over the row
+// first, then RoPE at the row's absolute position p = start[b] + q0 + row,
+// pairs (i, i + R/2) taken 16 at a time with tcgen05.ld / tcgen05.st; requires
+// D % 32 == 0, D <= 128 and R % 64 == 0. Rows past L hold zeros (TMA fill).
+// The angle of row 32 w + l of warp w is split as (B + l) theta_i with
+// B = start[b] + q0 + 32 w, and its cosine and sine are formed by the
+// angle-addition identities from table row B (one line per warp, lane l holding
+// its 16-byte granule l, taken by shuffle) and table row l < 32, which stays in
+// shared memory for the whole kernel; the fp32 products differ from table row
+// p by a few ulp. (Reading table row p per thread would scatter each load
+// instruction over 32 cache lines and stall the SM's load/store path, mbarrier
+// operations included, for thousands of cycles.)
 template <class C>
-__device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars, const PUnit& u,
-                            int row, uint32_t ucx) {
+__device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars,
+                            const uint8_t* stage_tab, const PUnit& u, int start_b, int quarter,
+                            int lane, uint32_t ucx) {
   volatile int* abort = &bars->abort;
-  const int qpos = u.q0 + row;
-  const bool live = qpos < a.L;
-  const long p = static_cast<long>(a.rope_start[u.b]) + qpos;
-  const bool inrange = p >= 0 && p < a.rope_max_positions;
-  if (live && !inrange) report(a.status, ATTN_DEV_POSITION);
-  const bool rot = live && inrange;
-  const int half = a.rope_R / 2;
-  const float4* trow = reinterpret_cast<const float4*>(a.rope_table + (rot ? p : 0) * half);
-  // The row's whole table line (R/2 <= 64 pairs, two per 16-byte load) is
-  // requested before the wait, so its latency overlaps it.
-  float4 t0[16], t1[16];
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    t0[e] = rot ? __ldg(trow + e) : make_float4(1.f, 0.f, 1.f, 0.f);
-    t1[e] = rot && half > 32 ? __ldg(trow + 16 + e) : make_float4(1.f, 0.f, 1.f, 0.f);
-  }
+  const int row = quarter * 32 + lane;
+  const bool live = u.q0 + row < a.L;
+  const int half = a.rope_R / 2;                 // 32 or 64 pairs
+  // Row B; a position outside the table is reported (the host bounds start[b]
+  // too) and clamped, so the loads stay in bounds.
+  const long p0 = static_cast<long>(start_b) + u.q0 + quarter * 32;
+  if (live && !(p0 + lane >= 0 && p0 + lane < a.rope_max_positions))
+    report(a.status, ATTN_DEV_POSITION);
+  const long pb = min(max(p0, 0L), static_cast<long>(a.rope_max_positions - 1));
+  float4 bg = make_float4(1.f, 0.f, 1.f, 0.f);
+  if (2 * lane < half) bg = __ldg(reinterpret_cast<const float4*>(a.rope_table + pb * half) + lane);
   const bool ok = tc::mbar_wait(&bars->q_copied, ucx & 1, abort);
   if (__any_sync(0xffffffffu, !ok)) return false;   // tcgen05.ld is warp-wide
   tc::fence_after_sync();
@@ -322,26 +387,50 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars, co
     // rows past L stay zero (with eps = 0 their 1/rms would be infinite)
     inv = live ? 1.0f / sqrtf(ss / static_cast<float>(a.D) + a.qnorm_eps) : 1.0f;
   }
-  auto scale = [&](float* x, int c) {
+  auto scale = [&](float* x, int c, int n) {
     const float4* w = reinterpret_cast<const float4*>(a.qnorm_w + c);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
+      if (4 * e >= n) break;
       const float4 we = __ldg(w + e);
       x[4 * e] *= inv * we.x; x[4 * e + 1] *= inv * we.y;
       x[4 * e + 2] *= inv * we.z; x[4 * e + 3] *= inv * we.w;
     }
   };
-  // pairs c0 .. c0 + 31 with (cos, sin) in t
-  auto rotate32 = [&](int c0, const float4* t) {
-    float x0[32], x1[32];
-    tc::tmem_ld32(qa + c0, x0);
-    tc::tmem_ld32(qa + c0 + half, x1);
+  if (a.qnorm_w) {                               // columns past R: normalised, not rotated
+#pragma unroll 1
+    for (int c = a.rope_R; c < C::DP; c += 32) {
+      float x[32];
+      tc::tmem_ld32(qa + c, x);
+      scale(x, c, 32);
+      tc::tmem_st32(qa + c, x);
+    }
+  }
+  const float4* lrow = reinterpret_cast<const float4*>(stage_tab) + lane * 32;
+#pragma unroll 1
+  for (int j = 0; j < half / 16; ++j) {
+    // (cos, sin) of (B + l) theta for pairs 16 j + 2 g, + 1 (in t[g])
+    float4 t[8];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const int src = 8 * j + g;
+      const float4 cb = make_float4(__shfl_sync(0xffffffffu, bg.x, src),     // row B
+                                    __shfl_sync(0xffffffffu, bg.y, src),
+                                    __shfl_sync(0xffffffffu, bg.z, src),
+                                    __shfl_sync(0xffffffffu, bg.w, src));
+      const float4 cl = lrow[src ^ lane];                  // row l (swizzled granules)
+      t[g] = make_float4(fmaf(cb.x, cl.x, -cb.y * cl.y), fmaf(cb.y, cl.x, cb.x * cl.y),
+                         fmaf(cb.z, cl.z, -cb.w * cl.w), fmaf(cb.w, cl.z, cb.z * cl.w));
+    }
+    float x0[16], x1[16];
+    tc::tmem_ld16(qa + 16 * j, x0);
+    tc::tmem_ld16(qa + 16 * j + half, x1);
     if (a.qnorm_w) {
-      scale(x0, c0);
-      scale(x1, c0 + half);
+      scale(x0, 16 * j, 16);
+      scale(x1, 16 * j + half, 16);
     }
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
+    for (int e = 0; e < 8; ++e) {
       const float4 cs = t[e];
       const float a0 = x0[2 * e], b0 = x1[2 * e], a1 = x0[2 * e + 1], b1 = x1[2 * e + 1];
       x0[2 * e] = fmaf(a0, cs.x, -b0 * cs.y);
@@ -349,19 +438,8 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars, co
       x0[2 * e + 1] = fmaf(a1, cs.z, -b1 * cs.w);
       x1[2 * e + 1] = fmaf(a1, cs.w, b1 * cs.z);
     }
-    tc::tmem_st32(qa + c0, x0);
-    tc::tmem_st32(qa + c0 + half, x1);
-  };
-  rotate32(0, t0);
-  if (half > 32) rotate32(32, t1);
-  if (a.qnorm_w) {                            // columns past R: normalised, not rotated
-#pragma unroll 1
-    for (int c = a.rope_R; c < a.D; c += 32) {
-      float x[32];
-      tc::tmem_ld32(qa + c, x);
-      scale(x, c);
-      tc::tmem_st32(qa + c, x);
-    }
+    tc::tmem_st16(qa + 16 * j, x0);
+    tc::tmem_st16(qa + 16 * j + half, x1);
   }
   tc::fence_before_sync();
   tc::mbar_arrive(&bars->q_ready);
@@ -372,7 +450,7 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars, co
 // Thread = one query row of the current unit; tcgen05.ld/st run on full warps.
 template <class C, bool ROPE>
 __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quarter, int lane,
-                           const CUtensorMap* tout, uint8_t* stage_out) {
+                           const CUtensorMap* tout, uint8_t* stage_out, const uint8_t* stage_tab) {
   constexpr int BK = C::BK;
   volatile int* abort = &bars->abort;
   const int row = quarter * 32 + lane;
@@ -382,14 +460,19 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
   bool ok = true;
   // Fused RoPE: the first unit's Q is rotated up front, every later one right
   // after the previous unit's last P (before its epilogue), while the tensor
-  // core still runs that unit's last P V products.
-  if (ROPE && blockIdx.x < a.units)
-    ok = tq_rotate_q<C>(a, lane_base, bars, get_unit<C>(a, unit_of(blockIdx.x, 0, gridDim.x)),
-                        row, 0);
+  // core runs that unit's last P V products.
+  if (ROPE && blockIdx.x < a.units) {
+    const PUnit u0 = get_unit<C>(a, unit_of(blockIdx.x, 0, gridDim.x));
+    ok = tq_rotate_q<C>(a, lane_base, bars, stage_tab, u0, a.rope_start[u0.b], quarter, lane, 0);
+  }
   for (int r = 0; ok; ++r) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
+    const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
+    // start[b] of the next unit, read now so that its latency is not on the
+    // path of that unit's rotation.
+    const int next_start = ROPE && xn < a.units ? a.rope_start[get_unit<C>(a, xn).b] : 0;
     const int qpos = u.qk0 + row;               // the query's own key index
     float m_ref = -INFINITY, l = 0.f;         // running max (log2 units) and sum
 
@@ -403,77 +486,96 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       }
       tc::fence_after_sync();
       const uint32_t scol = lane_base + C::kSCol + buf * BK;
-      float s[BK];
-      // Softcap: log2(e) * cap * tanh(scale * s / cap) = c_out - 2 c_out / (2^(s c_in) + 1);
-      // then the keys outside this row's causal / window band (boundary blocks only).
       const int k0 = (u.jlo + i) * BK;
       const int hi = qpos - k0;                                     // visible: c <= hi
       const int lo = a.window > 0 ? qpos - a.window + 1 - k0 : -1;  // visible: c >= lo
-      auto load_scores = [&]() {
+      // Boundary blocks (the causal diagonal, a window's edge): softcap and the
+      // band mask are applied in tensor memory first, 32 columns at a time in a
+      // rolled loop, so the unrolled 128-column code below stays lean.
+      const bool edge = __any_sync(0xffffffffu, hi < BK - 1 || lo > 0);
+      if (edge) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BK; c0 += 32) {
+          float x[32];
+          tc::tmem_ld32(scol + c0, x);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            if (a.softcap_on) {
+              const float t = tc::ex2(x[e] * a.c_cap_in);
+              x[e] = fmaf(-2.0f * a.c_cap_out, tc::rcp(t + 1.0f), a.c_cap_out);
+            }
+            const int c = c0 + e;
+            x[e] = c > hi ? -INFINITY : x[e];
+            x[e] = c < lo ? -INFINITY : x[e];
+          }
+          tc::tmem_st32(scol + c0, x);
+        }
+      }
+      float s[BK];
+      float lsum = 0.f;
+      // Pass 0, the common case: P against the running reference m_ref. It
+      // stands unless a score exceeds m_ref by more than 2^8 (where the
+      // reference is moved); then the block's sum of P exceeds 2^8 as well.
+      // Pass 1 (a row's first block, or pass 0 rejected): S read again, P
+      // against the block maximum. One copy of the code serves both passes:
+      // this kernel's code far exceeds the instruction caches, so every copy
+      // of an unrolled 128-column loop costs fetch stalls.
+      const bool fast = !__any_sync(0xffffffffu, m_ref == -INFINITY);
+#pragma unroll 1
+      for (int pass = fast ? 0 : 1; pass < 2; ++pass) {
         tmem_ld_row<BK>(scol, s);
-        if (a.softcap_on) {
+        // Softcap: log2(e) * cap * tanh(scale * s / cap) = c_out - 2 c_out / (2^(s c_in) + 1)
+        // (boundary blocks have it already).
+        if (a.softcap_on && !edge) {
 #pragma unroll
           for (int c = 0; c < BK; ++c) {
             const float e = tc::ex2(s[c] * a.c_cap_in);
             s[c] = fmaf(-2.0f * a.c_cap_out, tc::rcp(e + 1.0f), a.c_cap_out);
           }
         }
-        if (hi < BK - 1 || lo > 0) {
-#pragma unroll
-          for (int c = 0; c < BK; ++c) s[c] = (c > hi || c < lo) ? -INFINITY : s[c];
-        }
-      };
-      load_scores();
-
-      // Common case: P against the running reference m_ref. It stands unless a
-      // score exceeds m_ref by more than 2^8 (where the reference is moved);
-      // then the block's sum of P exceeds 2^8 as well, and the block is done
-      // again below with its maximum (S is still in tensor memory).
-      bool slow = m_ref == -INFINITY;
-      float lsum = 0.f;
-      if (!__any_sync(0xffffffffu, slow)) {
-        lsum = tq_exp_sum<BK>(s, cs, m_ref);
-        slow = !(lsum <= kRescaleLimit);
-        if (__any_sync(0xffffffffu, slow)) load_scores();
-      }
-      if (__any_sync(0xffffffffu, slow)) {
-        const float m_new = fmaxf(m_ref, tq_max<BK>(s) * cs);
-        // Rescale O only when the running maximum has grown a lot (warp-uniform).
-        const bool grow = m_ref != -INFINITY && m_new - m_ref > kRescaleLog2;
-        if (__any_sync(0xffffffffu, grow)) {
-          ok = tc::mbar_wait(&bars->o_done, (G - 1) & 1, abort);
-          if (__any_sync(0xffffffffu, !ok)) {
-            ok = false;
-            break;
-          }
-          tc::fence_after_sync();
-          const float f = grow ? tc::ex2(m_ref - m_new) : 1.0f;
+        float m_use = m_ref;
+        if (pass == 1) {
+          const float m_new = fmaxf(m_ref, tq_max<BK>(s) * cs);
+          // Rescale O only when the running maximum has grown a lot (warp-uniform).
+          const bool grow = m_ref != -INFINITY && m_new - m_ref > kRescaleLog2;
+          if (__any_sync(0xffffffffu, grow)) {
+            ok = tc::mbar_wait(&bars->o_done[(G - 1) & 1], ((G - 1) >> 1) & 1, abort);
+            if (__any_sync(0xffffffffu, !ok)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            const float f = grow ? tc::ex2(m_ref - m_new) : 1.0f;
 #pragma unroll 1
-          for (int c = 0; c < C::DP; c += 32) {
-            float o[32];
-            tc::tmem_ld32(lane_base + C::kOCol + c, o);
+            for (int c = 0; c < C::DP; c += 32) {
+              float o[32];
+              tc::tmem_ld32(lane_base + C::kOCol + c, o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= f;
-            tc::tmem_st32(lane_base + C::kOCol + c, o);
+              for (int e = 0; e < 32; ++e) o[e] *= f;
+              tc::tmem_st32(lane_base + C::kOCol + c, o);
+            }
+            if (grow) {
+              l *= f;
+              m_ref = m_new;
+            }
           }
-          if (grow) {
-            l *= f;
-            m_ref = m_new;
-          }
+          if (m_ref == -INFINITY) m_ref = m_new;  // first visible keys of the row (O, l are 0)
+          // -inf only while every key so far was masked; then every score is -inf.
+          m_use = m_ref == -INFINITY ? 0.f : m_ref;
         }
-        if (m_ref == -INFINITY) m_ref = m_new;  // first visible keys of the row (O, l are 0)
-        // -inf only while every key so far was masked; then every score is -inf.
-        lsum = tq_exp_sum<BK>(s, cs, m_ref == -INFINITY ? 0.f : m_ref);
+        lsum = tq_exp_sum<BK>(s, cs, m_use);
+        if (pass == 1 || !__any_sync(0xffffffffu, !(lsum <= kRescaleLimit))) break;
       }
+      if (!ok) break;
       l += lsum;
       tmem_st_row<BK>(scol, s);
       tc::fence_before_sync();
       tc::mbar_arrive(&bars->p_ready[buf]);
     }
     if (!ok) break;
-    const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
     if (ROPE && xn < a.units &&
-        !(ok = tq_rotate_q<C>(a, lane_base, bars, get_unit<C>(a, xn), row, uc + 1)))
+        !(ok = tq_rotate_q<C>(a, lane_base, bars, stage_tab, get_unit<C>(a, xn), next_start,
+                              quarter, lane, uc + 1)))
       break;
 
     // Epilogue: read O out of TMEM (then O is free for the next unit), scale by
@@ -524,7 +626,8 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
   uint8_t* skv = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sepi = skv + C::NS * C::kStage;      // 4 x 4 KB output staging tiles
-  PBars* bars = reinterpret_cast<PBars*>(sepi + C::kEpi);
+  uint8_t* stab = sepi + C::kEpi;               // RoPE table rows 0..31 (ROPE)
+  PBars* bars = reinterpret_cast<PBars*>(stab + C::kTab);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -536,18 +639,34 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
       tc::mbar_init(&bars->s_full[b], 1);
       tc::mbar_init(&bars->p_ready[b], 128);
     }
-    tc::mbar_init(&bars->o_done, 1);
+    tc::mbar_init(&bars->o_done[0], 1);
+    tc::mbar_init(&bars->o_done[1], 1);
     tc::mbar_init(&bars->o_final, 1);
     tc::mbar_init(&bars->o_free, 128);
     tc::mbar_init(&bars->q_copied, 1);
     tc::mbar_init(&bars->q_ready, 128);
-    tc::mbar_init(&bars->drain, 1);
+    tc::mbar_init(&bars->drain[0], 1);
+    tc::mbar_init(&bars->drain[1], 1);
     bars->abort = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
     tc::tmem_alloc(&bars->tmem_base, kTmemCols);
     tc::tmem_relinquish();
+  }
+  if (ROPE) {
+    // Table rows l < 32 ((cos, sin) of l theta_i, pairs i < R/2) stay here; row
+    // l's 16-byte granule g (pairs 2 g, 2 g + 1) sits at g ^ l, so that a warp
+    // whose lane l reads granule g of row l hits distinct banks. Rows past the
+    // table (max_positions < 32) are never used for a valid position.
+    const int half = a.rope_R / 2, gran = half / 2;
+    float4* t = reinterpret_cast<float4*>(stab);
+    for (int e = threadIdx.x; e < 32 * gran; e += C::kThreads) {
+      const int l = e / gran, gidx = e % gran;
+      const float4* src = reinterpret_cast<const float4*>(a.rope_table + static_cast<long>(l) * half);
+      t[l * 32 + (gidx ^ l)] = l < a.rope_max_positions ? __ldg(src + gidx)
+                                                          : make_float4(1.f, 0.f, 1.f, 0.f);
+    }
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -558,10 +677,13 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     if (lane == 0) tq_producer<C>(a, &tm_q, &tm_k, &tm_v, skv, bars);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) tq_mma<C>(a, tmem, skv, bars);
+    if (lane == 0) tq_mma_s<C>(a, tmem, skv, bars);
+    __syncwarp();
+  } else if (warp == 6) {
+    if (lane == 0) tq_mma_pv<C>(a, tmem, skv, bars);
     __syncwarp();
   } else {
-    tq_softmax<C, ROPE>(a, tmem, bars, warp % 4, lane, &tm_o, sepi + (warp % 4) * 4096);
+    tq_softmax<C, ROPE>(a, tmem, bars, warp % 4, lane, &tm_o, sepi + (warp % 4) * 4096, stab);
   }
 
   tc::fence_before_sync();
