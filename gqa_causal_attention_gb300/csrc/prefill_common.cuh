@@ -153,6 +153,21 @@ inline bool make_map(CUtensorMap* m, const float* base, int D, int L, int NH, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Output [NH, L, D] for TMA stores of 16 columns x 32 rows (64-byte swizzle).
+inline bool make_map_out16(CUtensorMap* m, const float* base, int D, int L, int NH) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
+                              static_cast<cuuint64_t>(NH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
+                                 static_cast<cuuint64_t>(L) * D * 4};
+  const cuuint32_t box[3] = {16, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // V^T [B*Hkv, D, L] (rows of pitch Lp) for TMA: boxes of 32 keys x box_rows dims.
 inline bool make_map_vt(CUtensorMap* m, const float* base, int D, int L, int Lp, int NH, int box_rows) {
   auto enc = encode_fn();

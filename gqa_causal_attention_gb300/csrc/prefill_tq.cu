@@ -52,6 +52,7 @@ struct PCfg {
       kSmemNeed > kSmemLimit / 2 + 4096 ? kSmemNeed : kSmemLimit / 2 + 4096;
   static constexpr int kQCol = 0, kOCol = DP, kSCol = 2 * DP;
   static_assert(NS >= 3, "ring too short");
+  static_assert(DP % 32 == 0, "epilogue tiles alternate across units: DP / 16 must be even");
   static_assert(kSCol + 2 * BK <= kTmemCols, "tensor memory budget");
   static_assert(kSmem <= kSmemLimit, "shared memory budget");
 };
@@ -348,8 +349,8 @@ __device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* b
 // D % 32 == 0, D <= 128 and R % 64 == 0. Rows past L hold zeros (TMA fill).
 // The angle of row 32 w + l of warp w is split as (B + l) theta_i with
 // B = start[b] + q0 + 32 w, and its cosine and sine are formed by the
-// angle-addition identities from table row B (one line per warp, lane l holding
-// its 16-byte granule l, taken by shuffle) and table row l < 32, which stays in
+// angle-addition identities from table row B (one line per warp, prefetched
+// into L1 and read with broadcast loads) and table row l < 32, which stays in
 // shared memory for the whole kernel; the fp32 products differ from table row
 // p by a few ulp. (Reading table row p per thread would scatter each load
 // instruction over 32 cache lines and stall the SM's load/store path, mbarrier
@@ -368,8 +369,8 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars,
   if (live && !(p0 + lane >= 0 && p0 + lane < a.rope_max_positions))
     report(a.status, ATTN_DEV_POSITION);
   const long pb = min(max(p0, 0L), static_cast<long>(a.rope_max_positions - 1));
-  float4 bg = make_float4(1.f, 0.f, 1.f, 0.f);
-  if (2 * lane < half) bg = __ldg(reinterpret_cast<const float4*>(a.rope_table + pb * half) + lane);
+  const float4* brow = reinterpret_cast<const float4*>(a.rope_table + pb * half);
+  if (lane < half / 16) tc::prefetch_l1(brow + 8 * lane);   // its 128-byte lines
   const bool ok = tc::mbar_wait(&bars->q_copied, ucx & 1, abort);
   if (__any_sync(0xffffffffu, !ok)) return false;   // tcgen05.ld is warp-wide
   tc::fence_after_sync();
@@ -414,17 +415,13 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars,
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
       const int src = 8 * j + g;
-      const float4 cb = make_float4(__shfl_sync(0xffffffffu, bg.x, src),     // row B
-                                    __shfl_sync(0xffffffffu, bg.y, src),
-                                    __shfl_sync(0xffffffffu, bg.z, src),
-                                    __shfl_sync(0xffffffffu, bg.w, src));
+      const float4 cb = __ldg(brow + src);                 // row B (the same for every lane)
       const float4 cl = lrow[src ^ lane];                  // row l (swizzled granules)
       t[g] = make_float4(fmaf(cb.x, cl.x, -cb.y * cl.y), fmaf(cb.y, cl.x, cb.x * cl.y),
                          fmaf(cb.z, cl.z, -cb.w * cl.w), fmaf(cb.w, cl.z, cb.z * cl.w));
     }
     float x0[16], x1[16];
-    tc::tmem_ld16(qa + 16 * j, x0);
-    tc::tmem_ld16(qa + 16 * j + half, x1);
+    tc::tmem_ld16x2(qa + 16 * j, qa + 16 * j + half, x0, x1);
     if (a.qnorm_w) {
       scale(x0, 16 * j, 16);
       scale(x1, 16 * j + half, 16);
@@ -438,8 +435,7 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars,
       x0[2 * e + 1] = fmaf(a1, cs.z, -b1 * cs.w);
       x1[2 * e + 1] = fmaf(a1, cs.w, b1 * cs.z);
     }
-    tc::tmem_st16(qa + 16 * j, x0);
-    tc::tmem_st16(qa + 16 * j + half, x1);
+    tc::tmem_st16x2(qa + 16 * j, qa + 16 * j + half, x0, x1);
   }
   tc::fence_before_sync();
   tc::mbar_arrive(&bars->q_ready);
@@ -491,22 +487,32 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       const int lo = a.window > 0 ? qpos - a.window + 1 - k0 : -1;  // visible: c >= lo
       // Boundary blocks (the causal diagonal, a window's edge): softcap and the
       // band mask are applied in tensor memory first, 32 columns at a time in a
-      // rolled loop, so the unrolled 128-column code below stays lean.
+      // rolled loop, so the unrolled 128-column code below stays lean. Chunks
+      // that no row of the warp sees are written as -inf without a load;
+      // chunks every row sees are left alone unless softcap needs applying.
       const bool edge = __any_sync(0xffffffffu, hi < BK - 1 || lo > 0);
       if (edge) {
 #pragma unroll 1
         for (int c0 = 0; c0 < BK; c0 += 32) {
           float x[32];
-          tc::tmem_ld32(scol + c0, x);
+          const bool none = __all_sync(0xffffffffu, hi < c0 || lo > c0 + 31);
+          const bool all = __all_sync(0xffffffffu, hi >= c0 + 31 && lo <= c0);
+          if (none) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            if (a.softcap_on) {
-              const float t = tc::ex2(x[e] * a.c_cap_in);
-              x[e] = fmaf(-2.0f * a.c_cap_out, tc::rcp(t + 1.0f), a.c_cap_out);
+            for (int e = 0; e < 32; ++e) x[e] = -INFINITY;
+          } else {
+            if (all && !a.softcap_on) continue;
+            tc::tmem_ld32(scol + c0, x);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (a.softcap_on) {
+                const float t = tc::ex2(x[e] * a.c_cap_in);
+                x[e] = fmaf(-2.0f * a.c_cap_out, tc::rcp(t + 1.0f), a.c_cap_out);
+              }
+              const int c = c0 + e;
+              x[e] = c > hi ? -INFINITY : x[e];
+              x[e] = c < lo ? -INFINITY : x[e];
             }
-            const int c = c0 + e;
-            x[e] = c > hi ? -INFINITY : x[e];
-            x[e] = c < lo ? -INFINITY : x[e];
           }
           tc::tmem_st32(scol + c0, x);
         }
@@ -579,8 +585,10 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       break;
 
     // Epilogue: read O out of TMEM (then O is free for the next unit), scale by
-    // 1/l, and write it with TMA: each warp stages 32 rows x 32 columns in a
-    // 128-byte-swizzled tile and stores that box (rows past L are clipped).
+    // 1/l, and write it with TMA: each warp stages its 32 rows 16 columns at a
+    // time in two alternating 2 KB tiles (64-byte swizzle: 16-byte granule g of
+    // row r at g ^ ((r / 2) % 4)), so a tile is rewritten once the store issued
+    // two steps earlier has read it; rows past L are clipped.
     ok = tc::mbar_wait(&bars->o_final, uc & 1, abort);
     if (__any_sync(0xffffffffu, !ok || *abort)) {
       ok = false;
@@ -593,18 +601,19 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
     tc::mbar_arrive(&bars->o_free);
     const float inv = 1.0f / l;
 #pragma unroll
-    for (int c = 0; c < C::DP; c += 32) {
-      if (lane == 0) tc::bulk_wait_read();      // the previous box has left the staging tile
+    for (int c = 0; c < C::DP; c += 16) {
+      uint8_t* tile = stage_out + ((c / 16) & 1) * 2048;
+      if (lane == 0) tc::bulk_wait_read_all_but_one();
       __syncwarp();
-      float4* row_out = reinterpret_cast<float4*>(stage_out + lane * 128);
+      float4* row_out = reinterpret_cast<float4*>(tile + lane * 64);
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        row_out[q ^ (lane & 7)] = make_float4(o[c + 4 * q] * inv, o[c + 4 * q + 1] * inv,
-                                              o[c + 4 * q + 2] * inv, o[c + 4 * q + 3] * inv);
+      for (int q = 0; q < 4; ++q)
+        row_out[q ^ ((lane >> 1) & 3)] = make_float4(o[c + 4 * q] * inv, o[c + 4 * q + 1] * inv,
+                                                     o[c + 4 * q + 2] * inv, o[c + 4 * q + 3] * inv);
       tc::fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
-        tc::tma_store_3d(tout, stage_out, c, u.q0 + quarter * 32, u.b * a.H + u.h);
+        tc::tma_store_3d(tout, tile, c, u.q0 + quarter * 32, u.b * a.H + u.h);
         tc::bulk_commit();
       }
     }
@@ -720,7 +729,7 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   if (!make_map(&tq, s.q, s.D, s.L, s.B * s.H, kBM) ||
       !make_map(&tk, s.k, s.D, Lk, s.B * s.Hkv, C::BK) ||
       !make_map_vt(&tv, s.vt, s.D, Lk, s.vt_pitch, s.B * s.Hkv, C::DP) ||
-      !make_map(&to, s.out, s.D, s.L, s.B * s.H, 32))
+      !make_map_out16(&to, s.out, s.D, s.L, s.B * s.H))
     return cudaErrorInvalidValue;
   TcArgs a{};
   a.q = s.q;
