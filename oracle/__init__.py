@@ -198,6 +198,22 @@ def prefill(q, k, v, start, cfg: Cfg, q_norm_w=None, k_norm_w=None):
     return attention(qr, kr, v, start, cfg), qr, kr
 
 
+def prefill_ragged(q, k, v, lengths, cfg: Cfg, q_norm_w=None, k_norm_w=None) -> np.ndarray:
+    """A ragged batch ("mojolearn.transformer", TransformerBlock.forward, lengths): row b is
+    real at positions [0, lengths[b]) and padding after. Each real output is row b run alone
+    at its own length (a fresh sequence, start 0), and every padding output is exactly +0.0.
+    Raw q, k, v (normalised and rotated here) -> out [B, H, L, D] float64."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    out = np.zeros(q.shape, dtype=np.float64)
+    for b, n in enumerate(int(x) for x in lengths):
+        assert 1 <= n <= cfg.L
+        alone = Cfg(**{**cfg.__dict__, "B": 1, "L": n})
+        o, _, _ = prefill(q[b:b + 1, :, :n], k[b:b + 1, :, :n], v[b:b + 1, :, :n], [0], alone,
+                          q_norm_w, k_norm_w)
+        out[b, :, :n] = o[0]
+    return out
+
+
 def append(kr, v, start, cfg: Cfg, capacity: int, k_cache=None, v_cache=None, written=None):
     """Store rotated k and raw v at their cache slots. Returns (k_cache, v_cache, written).
 

@@ -357,3 +357,56 @@ def test_append_full_cache_positions():
     assert list(wr[0, 0]) == [0, 1, 2, 3, 4, -1, -1, -1, -1]
     assert list(wr[1, 0]) == [-1, -1, -1, 3, 4, 5, 6, 7, -1]
     np.testing.assert_array_equal(kc[1, 0, 3:8], kr[1, 0])
+
+
+# ----------------------------------------------------------------------------- ragged batch
+
+
+def _ragged_inputs(B, H, Hkv, L, D):
+    return (RNG.standard_normal((B, H, L, D)), RNG.standard_normal((B, Hkv, L, D)),
+            RNG.standard_normal((B, Hkv, L, D)))
+
+
+def test_ragged_full_lengths_is_the_plain_prefill():
+    """lengths == L everywhere: no padding, the ordinary prefill."""
+    B, H, Hkv, L, D = 3, 4, 2, 9, 8
+    q, k, v = _ragged_inputs(B, H, Hkv, L, D)
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=4, softcap=5.0)
+    want, _, _ = oracle.prefill(q, k, v, [0] * B, cfg)
+    got = oracle.prefill_ragged(q, k, v, [L] * B, cfg)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_ragged_length_one_row_is_its_first_value():
+    """A row of length 1 has one real query, which sees only itself: its output is v at
+    position 0 (weight 1), and the rest of the row is +0.0."""
+    B, H, Hkv, L, D = 2, 4, 2, 6, 8
+    q, k, v = _ragged_inputs(B, H, Hkv, L, D)
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D)
+    got = oracle.prefill_ragged(q, k, v, [1, L], cfg)
+    for h in range(H):
+        np.testing.assert_array_equal(got[0, h, 0], v[0, h // 2, 0])
+    assert (got[0, :, 1:] == 0).all() and not np.signbit(got[0, :, 1:]).any()
+
+
+def test_ragged_real_rows_are_the_causal_prefix_and_ignore_padding():
+    """Causal attention at position l reads positions <= l only, so a row of length n equals
+    the first n positions of the full-length prefill of that row; padding holds NaN here and
+    must not reach any output, and padding outputs are exactly +0.0."""
+    B, H, Hkv, L, D = 3, 6, 2, 12, 8
+    q, k, v = _ragged_inputs(B, H, Hkv, L, D)
+    lengths = [5, 12, 1]
+    for window, softcap in ((0, 0.0), (3, 0.0), (0, 2.0)):
+        cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=window, softcap=softcap,
+                         rope_dim=4)
+        full, _, _ = oracle.prefill(q, k, v, [0] * B, cfg)
+        qn, kn, vn = q.copy(), k.copy(), v.copy()
+        for b, n in enumerate(lengths):
+            qn[b, :, n:] = np.nan
+            kn[b, :, n:] = np.nan
+            vn[b, :, n:] = np.nan
+        got = oracle.prefill_ragged(qn, kn, vn, lengths, cfg)
+        for b, n in enumerate(lengths):
+            np.testing.assert_allclose(got[b, :, :n], full[b, :, :n], rtol=1e-12, atol=1e-13)
+            pad = got[b, :, n:]
+            assert (pad == 0).all() and not np.signbit(pad).any()
