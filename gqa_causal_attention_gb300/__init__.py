@@ -26,6 +26,7 @@ __all__ = [
     "gqa_attn_decode_static", "gqa_attn_vt_pitch", "gqa_attn_v_transpose",
     "gqa_attn_prefill_rope_vt", "gqa_attn_prefill_rope_vt_workspace_size",
     "gqa_attn_prefill_cached", "gqa_attn_prefill_cached_workspace_size",
+    "gqa_attn_prefill_ragged", "gqa_attn_prefill_ragged_workspace_size",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
@@ -116,6 +117,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_attn_prefill_cached": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                               i32, vp, ctypes.c_int32, rp, vp, vp, f, i32, f, f,
                                               vp, sz, vp, vp]),
+            "gqa_attn_prefill_ragged_workspace_size": (sz, [i32, i32, i32, i32, i32, rp]),
+            "gqa_attn_prefill_ragged": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, rp,
+                                              vp, vp, f, i32, f, f, vp, sz, vp, vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -293,6 +297,46 @@ def gqa_attn_prefill_rope(q, k, v, out, start, max_start: int, params: RopeParam
                                       float(softcap), float(scale), _ptr(workspace), wbytes,
                                       _ptr(status), _stream(stream))
     _check("gqa_attn_prefill_rope", rc)
+
+
+def gqa_attn_prefill_ragged_workspace_size(B: int, H: int, Hkv: int, L: int, D: int,
+                                           params: RopeParams = None) -> int:
+    return int(load().gqa_attn_prefill_ragged_workspace_size(
+        B, H, Hkv, L, D, None if params is None else ctypes.byref(params)))
+
+
+def gqa_attn_prefill_ragged(q, k, v, out, lengths, params: RopeParams = None, table=None,
+                            q_norm_w=None, norm_eps: float = 1e-6, window: int = 0,
+                            softcap: float = 0.0, scale: float = 0.0, workspace=None,
+                            status=None, stream=None) -> None:
+    """Prefill of a ragged batch: row b is real at positions [0, lengths[b]) (lengths: int32
+    CUDA tensor [B]) and its padding outputs are +0.0. With params, q is raw (RMSNorm + RoPE
+    at position l applied inside); without, q is already rotated. workspace:
+    gqa_attn_prefill_ragged_workspace_size bytes, or None to take one from torch's caching
+    allocator for this call."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        _f32(n, t, 4)
+    _f32("table", table); _f32("q_norm_w", q_norm_w); _i32("lengths", lengths)
+    _i32("status", status)
+    B, H, L, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, L, D) or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("gqa_attn_prefill_ragged: inconsistent shapes")
+    if lengths is None or lengths.numel() != B:
+        raise ValueError("gqa_attn_prefill_ragged: lengths must hold B values")
+    if workspace is None:
+        n = gqa_attn_prefill_ragged_workspace_size(B, H, Hkv, L, D, params)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().gqa_attn_prefill_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, L, D,
+                                        _ptr(lengths),
+                                        None if params is None else ctypes.byref(params),
+                                        _ptr(table), _ptr(q_norm_w), float(norm_eps),
+                                        int(window), float(softcap), float(scale),
+                                        _ptr(workspace), wbytes, _ptr(status), _stream(stream))
+    _check("gqa_attn_prefill_ragged", rc)
 
 
 def gqa_attn_vt_pitch(L: int) -> int:

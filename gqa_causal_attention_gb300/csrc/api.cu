@@ -168,9 +168,12 @@ size_t gqa_attn_prefill_workspace_size(int B, int Hkv, int L, int D) {
   return (size_t)B * Hkv * D * gqa::prefill_vt_pitch(L) * sizeof(float);
 }
 
-int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out, int B, int H,
-                     int Hkv, int L, int D, int window, float softcap, float scale,
-                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+namespace {
+// gqa_attn_prefill, and gqa_attn_prefill_ragged without RoPE (lengths != NULL).
+int prefill_impl(const float* q, const float* k, const float* v, float* out, int B, int H,
+                 int Hkv, int L, int D, int window, float softcap, float scale, void* workspace,
+                 size_t workspace_bytes, int32_t* status, void* stream,
+                 const int32_t* lengths) {
   if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
   if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
   if (B == 0 || L == 0) return ATTN_OK;
@@ -182,6 +185,7 @@ int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out,
   a.window = window; a.softcap = softcap > 0.f ? softcap : 0.f;
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   a.status = status;
+  a.lengths = lengths;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (gqa::prefill_tc_supports(D)) {
     if (!workspace || workspace_bytes < gqa_attn_prefill_workspace_size(B, Hkv, L, D))
@@ -192,6 +196,14 @@ int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out,
     return cuda_status(gqa::launch_prefill_tc(a, s));
   }
   return cuda_status(gqa::launch_prefill_simt(a, s));
+}
+}  // namespace
+
+int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out, int B, int H,
+                     int Hkv, int L, int D, int window, float softcap, float scale,
+                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+  return prefill_impl(q, k, v, out, B, H, Hkv, L, D, window, softcap, scale, workspace,
+                      workspace_bytes, status, stream, nullptr);
 }
 
 namespace {
@@ -237,7 +249,7 @@ int prefill_rope_impl(const float* q, const float* k, const float* v, const floa
                       int32_t max_start, const attn_rope_params* rp, const float* table,
                       const float* q_norm_w, float norm_eps, int window, float softcap,
                       float scale, void* workspace, size_t workspace_bytes, int32_t* status,
-                      void* stream) {
+                      void* stream, const int32_t* lengths = nullptr) {
   if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
   if (vt && !gqa::prefill_tc_supports(D)) return ATTN_ERR_SHAPE;
   if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
@@ -265,6 +277,7 @@ int prefill_rope_impl(const float* q, const float* k, const float* v, const floa
   a.window = window; a.softcap = softcap > 0.f ? softcap : 0.f;
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   a.status = status;
+  a.lengths = lengths;
   if (gqa::prefill_tc_supports(D)) {
     a.vt = vt ? const_cast<float*>(vt) : static_cast<float*>(workspace);
     a.vt_pitch = gqa::prefill_vt_pitch(L);
@@ -321,6 +334,44 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
   return prefill_rope_impl(q, k, nullptr, vt, out, B, H, Hkv, L, D, start, max_start, rp, table,
                            q_norm_w, norm_eps, window, softcap, scale, workspace, workspace_bytes,
                            status, stream);
+}
+
+size_t gqa_attn_prefill_ragged_workspace_size(int B, int H, int Hkv, int L, int D,
+                                              const attn_rope_params* rp) {
+  const size_t base = rp ? gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp)
+                         : gqa_attn_prefill_workspace_size(B, Hkv, L, D);
+  if (base == 0 || H < 1) return 0;
+  return round256((size_t)B * sizeof(int32_t)) + round256(base);
+}
+
+int gqa_attn_prefill_ragged(const float* q, const float* k, const float* v, float* out, int B,
+                            int H, int Hkv, int L, int D, const int32_t* lengths,
+                            const attn_rope_params* rp, const float* table,
+                            const float* q_norm_w, float norm_eps, int window, float softcap,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
+  if (rp && !rope_params_ok(rp, D)) return ATTN_ERR_PARAM;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!lengths) return ATTN_ERR_NULL;
+  const size_t need = gqa_attn_prefill_ragged_workspace_size(B, H, Hkv, L, D, rp);
+  if (need == 0) return ATTN_ERR_SHAPE;
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  // [start = 0 per row (B int32) | the plain or RoPE prefill's workspace]
+  const size_t zb = round256((size_t)B * sizeof(int32_t));
+  char* rest = static_cast<char*>(workspace) + zb;
+  if (!rp)
+    return prefill_impl(q, k, v, out, B, H, Hkv, L, D, window, softcap, scale, rest,
+                        workspace_bytes - zb, status, stream, lengths);
+  int32_t* zero_start = static_cast<int32_t*>(workspace);
+  if (cudaError_t e = cudaMemsetAsync(zero_start, 0, (size_t)B * sizeof(int32_t),
+                                      static_cast<cudaStream_t>(stream));
+      e != cudaSuccess)
+    return cuda_status(e);
+  return prefill_rope_impl(q, k, v, nullptr, out, B, H, Hkv, L, D, zero_start, 0, rp, table,
+                           q_norm_w, norm_eps, window, softcap, scale, rest,
+                           workspace_bytes - zb, status, stream, lengths);
 }
 
 namespace {

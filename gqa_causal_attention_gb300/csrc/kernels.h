@@ -63,14 +63,22 @@ struct AttnShape {
   // key rows per head, kv_off[b] of them before query row 0 of row b.
   const int32_t* kv_off = nullptr;
   int Lk = 0;               // 0: the chunk's own keys (Lk = L)
+  // Ragged batch: row b is real at query (and key) positions [0, lengths[b]);
+  // padding rows of out are written as +0.0 and padding keys are never seen.
+  // nullptr: every row has length L. Not combined with kv_off.
+  const int32_t* lengths = nullptr;
 };
 
 cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
 // Returns cudaErrorNotSupported (nothing launched) for shapes it does not take.
 cudaError_t launch_prefill_tc(const AttnShape& a, cudaStream_t stream);      // V^T pre-pass + kernel
 cudaError_t launch_prefill_tc_vt(const AttnShape& a, cudaStream_t stream);   // a.vt already written
+// lengths (optional, [BHkv / Hkv]): columns m >= lengths[bh / Hkv] of vt are
+// written as 0, so padding values (even inf or NaN) never meet a zero weight
+// in P V.
 cudaError_t launch_transpose_v(const float* v, float* vt, int BHkv, int L, int D, int vt_pitch,
-                               cudaStream_t stream);
+                               cudaStream_t stream, const int32_t* lengths = nullptr,
+                               int Hkv = 1, int32_t* status = nullptr);
 bool prefill_tc_supports(int D);
 // Keys for continuing a cached prefix: per (b, kv head), rows [0, pre_b) from the
 // cache (positions start[b] - pre_b .. start[b] - 1; slot = position, or position

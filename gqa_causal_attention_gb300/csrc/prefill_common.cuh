@@ -42,7 +42,17 @@ struct TcArgs {
   // kv_off == nullptr: keys are the chunk's own (offset 0, Lk = L).
   const int32_t* kv_off;
   int Lk;
+  // Ragged batch (nullptr: every row has length L): see AttnShape::lengths.
+  const int32_t* lengths;
 };
+
+// Real length of batch row b (lengths outside [0, L] are clamped; the V^T
+// pre-pass or the SIMT kernel reports them).
+__device__ __forceinline__ int row_len(const TcArgs& a, int b) {
+  if (!a.lengths) return a.L;
+  const int v = a.lengths[b];
+  return v < 0 ? 0 : (v > a.L ? a.L : v);
+}
 
 // Timeout-only wait used while winding down after an abort.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {

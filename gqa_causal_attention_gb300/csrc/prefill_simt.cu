@@ -31,7 +31,16 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(AttnShape a) {
   const int q0 = blockIdx.x * kBQ;
   const int r = threadIdx.x / kTPR, t4 = threadIdx.x % kTPR;
   const int qi = q0 + r;
-  const bool row_ok = qi < L;
+  // Ragged batch: keys and queries at or past the row's length are padding;
+  // padding queries are written as +0.0.
+  int Lb = L;
+  if (a.lengths) {
+    const int n = a.lengths[b];
+    if ((n < 1 || n > L) && threadIdx.x == 0 && blockIdx.x == 0 && h == 0)
+      report(a.status, ATTN_DEV_LENGTH);
+    Lb = n < 0 ? 0 : (n > L ? L : n);
+  }
+  const bool row_ok = qi < Lb;
 
   float q[NE], o[NE];
 #pragma unroll
@@ -67,7 +76,7 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(AttnShape a) {
       }
       s += __shfl_xor_sync(0xffffffffu, s, 1);
       s += __shfl_xor_sync(0xffffffffu, s, 2);
-      const bool vis = row_ok && key < L && key <= qi && (a.window == 0 || key > qi - a.window);
+      const bool vis = row_ok && key < Lb && key <= qi && (a.window == 0 || key > qi - a.window);
       if (!vis) continue;
       if (capped) s = softcap_apply(s, a.softcap, cap_k);
       s *= kLog2e;
@@ -83,8 +92,12 @@ __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(AttnShape a) {
       }
     }
   }
-  if (!row_ok) return;
-  const float inv = 1.0f / l;
+  if (qi >= L) return;
+  const float inv = row_ok ? 1.0f / l : 0.f;
+  if (!row_ok) {
+#pragma unroll
+    for (int e = 0; e < NE; ++e) o[e] = 0.f;
+  }
 #pragma unroll
   for (int e = 0; e < NE; ++e) {
     const int d = t4 + kTPR * e;

@@ -292,6 +292,7 @@ __device__ void run_softmax(const Unit& u, const TcArgs& a, uint32_t tmem, Bars*
   volatile int* abort = &bars->abort;
   const int row = quarter * 32 + lane;
   const int qpos = u.q0[t] + row;
+  const int Lb = row_len(a, u.b);             // keys at or past the row's length: masked
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   // Running max m (log2 units, of the scaled and capped scores) and sum l.
   float m_ref = -INFINITY, l = 0.f;
@@ -339,11 +340,17 @@ __device__ void run_softmax(const Unit& u, const TcArgs& a, uint32_t tmem, Bars*
     }
     // Keys outside the causal / window band of this row (boundary blocks only).
     const int k0 = (u.jlo + i) * BK;
-    const int hi = qpos - k0;                                    // visible: c <= hi
+    const int hi = min(qpos, Lb - 1) - k0;                        // visible: c <= hi
     const int lo = a.window > 0 ? qpos - a.window + 1 - k0 : -1;  // visible: c >= lo
-    if (hi < BK - 1 || lo > 0) {
+    // One compare and select per column (a combined condition compiles to
+    // per-column branches that diverge across the rows of a warp).
+    if (hi < BK - 1) {
 #pragma unroll
-      for (int c = 0; c < BK; ++c) s[c] = (c > hi || c < lo) ? -INFINITY : s[c];
+      for (int c = 0; c < BK; ++c) s[c] = c > hi ? -INFINITY : s[c];
+    }
+    if (lo > 0) {
+#pragma unroll
+      for (int c = 0; c < BK; ++c) s[c] = c < lo ? -INFINITY : s[c];
     }
     float mx[NA];
 #pragma unroll
@@ -411,13 +418,18 @@ __device__ void run_softmax(const Unit& u, const TcArgs& a, uint32_t tmem, Bars*
   if (ok) ok = tc::mbar_wait(&bars->o_final[t], 0, abort);
   if (__any_sync(0xffffffffu, !ok || *abort)) return;
   tc::fence_after_sync();
-  const float inv = 1.0f / l;
+  // Padding rows of a ragged batch (qpos >= Lb) are written as +0.0.
+  const float inv = qpos < Lb ? 1.0f / l : 0.f;
   const bool live = qpos < a.L;
   float* dst = a.out + ((static_cast<long>(u.b) * a.H + u.head[t]) * a.L + qpos) * a.D;
 #pragma unroll 1
   for (int c = 0; c < C::DP; c += 32) {
     float o[32];
     tc::tmem_ld32(lane_base + C::o_col(t) + c, o);
+    if (qpos >= Lb) {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    }
     if (live) {
 #pragma unroll
       for (int e = 0; e < 32; e += 4) {
@@ -498,17 +510,26 @@ __global__ void __launch_bounds__(Cfg<DP>::kThreads, 1)
 // pitch Lp that is a multiple of 4, so a store may run into the padding).
 __global__ void __launch_bounds__(256) transpose_v_kernel(const float* __restrict__ v,
                                                           float* __restrict__ vt, int L, int D,
-                                                          int Lp) {
+                                                          int Lp, const int32_t* lengths,
+                                                          int Hkv, int32_t* status) {
   __shared__ float tile[32][33];
   const long bh = blockIdx.z;
   const int l0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
   const int r = threadIdx.x / 8, q = threadIdx.x % 8;
   const float* src = v + bh * L * D;
   float* dst = vt + bh * D * Lp;
+  int Lb = L;                                   // keys past the row's length read as 0
+  if (lengths) {
+    const int n = lengths[bh / Hkv];
+    if ((n < 1 || n > L) && threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0 &&
+        bh % Hkv == 0)
+      report(status, ATTN_DEV_LENGTH);
+    Lb = n < 0 ? 0 : (n > L ? L : n);
+  }
   {
     const int l = l0 + r, d = d0 + 4 * q;
     float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (l < L && d < D) x = __ldg(reinterpret_cast<const float4*>(src + static_cast<long>(l) * D + d));
+    if (l < Lb && d < D) x = __ldg(reinterpret_cast<const float4*>(src + static_cast<long>(l) * D + d));
     tile[r][4 * q] = x.x;
     tile[r][4 * q + 1] = x.y;
     tile[r][4 * q + 2] = x.z;
@@ -552,6 +573,7 @@ cudaError_t launch_dp(const AttnShape& s, cudaStream_t stream) {
   a.c_cap_in = s.softcap > 0.f ? 2.0f * kLog2e * s.scale / s.softcap : 0.f;
   a.c_cap_out = kLog2e * s.softcap;
   a.status = s.status;
+  a.lengths = s.lengths;
   const long grid = static_cast<long>(s.B) * s.Hkv * a.npairs;
   prefill_tc_kernel<DP><<<static_cast<unsigned>(grid), C::kThreads, C::kSmem, stream>>>(tq, tk, tv,
                                                                                         a);
@@ -565,15 +587,17 @@ bool prefill_tc_supports(int D) { return D % 4 == 0 && D >= 32 && D <= kMaxHeadD
 int prefill_vt_pitch(int L) { return (L + 3) / 4 * 4; }
 
 cudaError_t launch_transpose_v(const float* v, float* vt, int BHkv, int L, int D, int vt_pitch,
-                               cudaStream_t stream) {
-  transpose_v_kernel<<<dim3((L + 31) / 32, (D + 31) / 32, BHkv), 256, 0, stream>>>(v, vt, L, D,
-                                                                                  vt_pitch);
+                               cudaStream_t stream, const int32_t* lengths, int Hkv,
+                               int32_t* status) {
+  transpose_v_kernel<<<dim3((L + 31) / 32, (D + 31) / 32, BHkv), 256, 0, stream>>>(
+      v, vt, L, D, vt_pitch, lengths, Hkv, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_tc(const AttnShape& s, cudaStream_t stream) {
   if (!prefill_tc_supports(s.D)) return cudaErrorNotSupported;
-  if (cudaError_t e = launch_transpose_v(s.v, s.vt, s.B * s.Hkv, s.L, s.D, s.vt_pitch, stream);
+  if (cudaError_t e = launch_transpose_v(s.v, s.vt, s.B * s.Hkv, s.L, s.D, s.vt_pitch, stream,
+                                         s.lengths, s.Hkv, s.status);
       e != cudaSuccess)
     return e;
   return launch_prefill_tc_vt(s, stream);

@@ -73,8 +73,9 @@ struct PBars {
 };
 
 struct PUnit {
-  int b, h, q0, jlo, n;
+  int b, h, q0, jlo, n;                       // n = 0: every row is padding (ragged batch)
   int qk0;                                    // key index of query row q0 (q0 + kv_off[b])
+  int klast;                                  // the row's last real key index
 };
 
 // Unit x of round r for block c: snake order evens out the heavy-first list.
@@ -91,12 +92,25 @@ __device__ __forceinline__ PUnit get_unit(const TcArgs& a, int x) {
   u.h = bh % a.H;
   u.q0 = (a.QT - 1 - rank) * kBM;
   const int off = a.kv_off ? a.kv_off[u.b] : 0;
+  const int Lb = row_len(a, u.b);
   u.qk0 = u.q0 + off;
+  u.klast = off + Lb - 1;
   const int lo = a.window > 0 ? max(0, u.qk0 - a.window + 1) / C::BK : 0;
-  const int hi = min(u.qk0 + kBM - 1, off + a.L - 1) / C::BK;
+  const int hi = min(u.qk0 + kBM - 1, u.klast) / C::BK;
   u.jlo = lo;
-  u.n = hi - lo + 1;
+  u.n = u.q0 < Lb ? hi - lo + 1 : 0;
   return u;
+}
+
+// The first round at or after r whose unit has key blocks (or the first round
+// past the end); every role walks the same sequence.
+template <class C>
+__device__ __forceinline__ int next_live(const TcArgs& a, int r) {
+  if (!a.lengths) return r;                     // without lengths no unit is empty
+  for (;; ++r) {
+    const int x = unit_of(blockIdx.x, r, gridDim.x);
+    if (x >= a.units || get_unit<C>(a, x).n > 0) return r;
+  }
 }
 
 // ---------------------------------------------------------------- producer (one thread)
@@ -145,11 +159,12 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
     return true;
   };
   bool ok = true;
-  for (int r = 0; ok; ++r) {
+  for (int r = next_live<C>(a, 0), first = 1; ok; first = 0) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
-    const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
+    const int rn = next_live<C>(a, r + 1);
+    const int xn = unit_of(blockIdx.x, rn, gridDim.x);
     const bool has_next = xn < a.units;
     const PUnit un = get_unit<C>(a, has_next ? xn : x);
     // Warm the next Q tile (and its RoPE table lines) into L2 now: they are
@@ -165,7 +180,7 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
         tc::bulk_prefetch_l2(a.rope_table + p0 * half, static_cast<uint32_t>((p1 - p0) * half * 8));
       }
     }
-    if (r == 0) ok = load(0, u, 0);
+    if (first) ok = load(0, u, 0);
     if (ok) ok = load(1, u, u.jlo);
     if (ok && u.n == 1 && has_next) ok = load(0, un, 0);
     for (int i = 0; ok && i < u.n; ++i) {
@@ -175,6 +190,7 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
       }
       if (ok) ok = load(2, u, u.jlo + i);
     }
+    r = rn;
   }
   // Every copy this block started lands before the block may exit.
   for (int s = 0; s < C::NS; ++s)
@@ -260,14 +276,15 @@ __device__ void tq_mma_s(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* ba
     return true;
   };
 
-  uint32_t g = 0, uc = 0;       // key blocks and units done so far by this block
+  uint32_t g = 0, uc = 0;       // key blocks and live units done so far by this block
   bool ok = true;
-  for (int r = 0; ok; ++r) {
+  for (int r = next_live<C>(a, 0); ok;) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
-    const bool has_next = unit_of(blockIdx.x, r + 1, gridDim.x) < a.units;
-    if (r == 0 && !(ok = copy_q())) break;
+    const int rn = next_live<C>(a, r + 1);
+    const bool has_next = unit_of(blockIdx.x, rn, gridDim.x) < a.units;
+    if (uc == 0 && !(ok = copy_q())) break;
     // With fused RoPE the softmax warps rotate Q in tensor memory first.
     if (a.rope_table) {
       if (!(ok = tc::mbar_wait(&bars->q_ready, uc & 1, abort))) break;
@@ -285,6 +302,7 @@ __device__ void tq_mma_s(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* ba
     if (!ok) break;
     g += u.n;
     ++uc;
+    r = rn;
   }
   // No MMA or copy of this thread may still run when the block frees its TMEM.
   tc::mma_commit(&bars->drain[0]);
@@ -300,12 +318,13 @@ __device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* b
   RingCursor<C> ring;
   uint32_t g = 0, uc = 0;
   bool ok = true;
-  for (int r = 0; ok; ++r) {
+  for (int r = next_live<C>(a, 0); ok;) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
-    const bool has_next = unit_of(blockIdx.x, r + 1, gridDim.x) < a.units;
-    if (r == 0) ring.skip();                        // the first Q tile
+    const int rn = next_live<C>(a, r + 1);
+    const bool has_next = unit_of(blockIdx.x, rn, gridDim.x) < a.units;
+    if (uc == 0) ring.skip();                       // the first Q tile
     ring.skip();                                    // K_0
     if (u.n == 1 && has_next) ring.skip();          // next Q
     for (int i = 0; i < u.n; ++i) {
@@ -336,6 +355,7 @@ __device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* b
     tc::mma_commit(&bars->o_final);
     g += u.n;
     ++uc;
+    r = rn;
   }
   tc::mma_commit(&bars->drain[1]);
   drain_wait(&bars->drain[1], 0);
@@ -457,15 +477,39 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
   // Fused RoPE: the first unit's Q is rotated up front, every later one right
   // after the previous unit's last P (before its epilogue), while the tensor
   // core runs that unit's last P V products.
-  if (ROPE && blockIdx.x < a.units) {
-    const PUnit u0 = get_unit<C>(a, unit_of(blockIdx.x, 0, gridDim.x));
+  const int r0 = next_live<C>(a, 0);
+  if (ROPE && unit_of(blockIdx.x, r0, gridDim.x) < a.units) {
+    const PUnit u0 = get_unit<C>(a, unit_of(blockIdx.x, r0, gridDim.x));
     ok = tq_rotate_q<C>(a, lane_base, bars, stage_tab, u0, a.rope_start[u0.b], quarter, lane, 0);
   }
-  for (int r = 0; ok; ++r) {
+  // One 32-row x DP-column box of this warp to the output: 16 columns at a
+  // time through two alternating 2 KB staging tiles (64-byte swizzle: 16-byte
+  // granule g of row r at g ^ ((r / 2) % 4)); a tile is rewritten once the
+  // store issued two steps earlier has read it. value(c) gives columns
+  // c .. c + 3 of this thread's row; rows past L are clipped.
+  auto store_rows = [&](const PUnit& uu, auto value) {
+#pragma unroll
+    for (int c = 0; c < C::DP; c += 16) {
+      uint8_t* tile = stage_out + ((c / 16) & 1) * 2048;
+      if (lane == 0) tc::bulk_wait_read_all_but_one();
+      __syncwarp();
+      float4* row_out = reinterpret_cast<float4*>(tile + lane * 64);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) row_out[q ^ ((lane >> 1) & 3)] = value(c + 4 * q);
+      tc::fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        tc::tma_store_3d(tout, tile, c, uu.q0 + quarter * 32, uu.b * a.H + uu.h);
+        tc::bulk_commit();
+      }
+    }
+  };
+  for (int r = r0; ok;) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units) break;
     const PUnit u = get_unit<C>(a, x);
-    const int xn = unit_of(blockIdx.x, r + 1, gridDim.x);
+    const int rn = next_live<C>(a, r + 1);
+    const int xn = unit_of(blockIdx.x, rn, gridDim.x);
     // start[b] of the next unit, read now so that its latency is not on the
     // path of that unit's rotation.
     const int next_start = ROPE && xn < a.units ? a.rope_start[get_unit<C>(a, xn).b] : 0;
@@ -483,7 +527,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       tc::fence_after_sync();
       const uint32_t scol = lane_base + C::kSCol + buf * BK;
       const int k0 = (u.jlo + i) * BK;
-      const int hi = qpos - k0;                                     // visible: c <= hi
+      const int hi = min(qpos, u.klast) - k0;                       // visible: c <= hi
       const int lo = a.window > 0 ? qpos - a.window + 1 - k0 : -1;  // visible: c >= lo
       // Boundary blocks (the causal diagonal, a window's edge): softcap and the
       // band mask are applied in tensor memory first, 32 columns at a time in a
@@ -585,10 +629,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       break;
 
     // Epilogue: read O out of TMEM (then O is free for the next unit), scale by
-    // 1/l, and write it with TMA: each warp stages its 32 rows 16 columns at a
-    // time in two alternating 2 KB tiles (64-byte swizzle: 16-byte granule g of
-    // row r at g ^ ((r / 2) % 4)), so a tile is rewritten once the store issued
-    // two steps earlier has read it; rows past L are clipped.
+    // 1/l and store it; padding rows of a ragged batch are written as +0.0.
     ok = tc::mbar_wait(&bars->o_final, uc & 1, abort);
     if (__any_sync(0xffffffffu, !ok || *abort)) {
       ok = false;
@@ -599,26 +640,24 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
     tmem_ld_row<C::DP>(lane_base + C::kOCol, o);
     tc::fence_before_sync();
     tc::mbar_arrive(&bars->o_free);
-    const float inv = 1.0f / l;
-#pragma unroll
-    for (int c = 0; c < C::DP; c += 16) {
-      uint8_t* tile = stage_out + ((c / 16) & 1) * 2048;
-      if (lane == 0) tc::bulk_wait_read_all_but_one();
-      __syncwarp();
-      float4* row_out = reinterpret_cast<float4*>(tile + lane * 64);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        row_out[q ^ ((lane >> 1) & 3)] = make_float4(o[c + 4 * q] * inv, o[c + 4 * q + 1] * inv,
-                                                     o[c + 4 * q + 2] * inv, o[c + 4 * q + 3] * inv);
-      tc::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        tc::tma_store_3d(tout, tile, c, u.q0 + quarter * 32, u.b * a.H + u.h);
-        tc::bulk_commit();
-      }
-    }
+    const bool real = qpos <= u.klast;
+    const float inv = real ? 1.0f / l : 0.f;
+    store_rows(u, [&](int c) {
+      return real ? make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv)
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+    });
     g += u.n;
     ++uc;
+    r = rn;
+  }
+  // Units with no real row (ragged batch): zeros.
+  if (ok && a.lengths) {
+    for (int r = 0;; ++r) {
+      const int x = unit_of(blockIdx.x, r, gridDim.x);
+      if (x >= a.units) break;
+      const PUnit u = get_unit<C>(a, x);
+      if (u.n == 0) store_rows(u, [](int) { return make_float4(0.f, 0.f, 0.f, 0.f); });
+    }
   }
   if (lane == 0) tc::bulk_wait_all();           // output boxes written before the block exits
   __syncwarp();
@@ -752,6 +791,7 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   a.rope_max_positions = s.rope.max_positions;
   a.kv_off = s.kv_off;
   a.Lk = Lk;
+  a.lengths = s.lengths;
   const int grid = a.units < sm_count() ? a.units : sm_count();
   prefill_tq_kernel<DP, ROPE><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();

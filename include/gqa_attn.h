@@ -52,7 +52,8 @@ extern "C" {
 /* Device status bits, OR-ed into *status by the kernels. */
 #define ATTN_DEV_POSITION  1   /* start[b] < 0 or start[b] + L - 1 >= max_positions */
 #define ATTN_DEV_CAPACITY  2   /* start[b] + L > capacity without a window */
-#define ATTN_DEV_LENGTH    4   /* cache_len[b] outside [1, max_cache_len] or > capacity */
+#define ATTN_DEV_LENGTH    4   /* cache_len[b] outside [1, max_cache_len] or > capacity,
+                                  or a ragged prefill's lengths[b] outside [1, L] */
 #define ATTN_DEV_TIMEOUT   8   /* a pipeline wait ran past its limit; outputs invalid */
 
 /* RoPE frequency scaling ("mojolearn.transformer", rope_scaling). */
@@ -229,6 +230,36 @@ size_t gqa_attn_prefill_cached_workspace_size(int B, int H, int Hkv, int L, int 
 int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, const float* k_cache,
                             const float* v_cache, int capacity, float* out, int B, int H,
                             int Hkv, int L, int D, const int32_t* start, int32_t max_start,
+                            const attn_rope_params* rp, const float* table,
+                            const float* q_norm_w, float norm_eps, int window, float softcap,
+                            float scale, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream);
+
+/*
+ * Prefill of a ragged batch ("mojolearn.transformer", TransformerBlock.forward
+ * with lengths, a fresh sequence per row: start 0): row b is real at positions
+ * [0, lengths[b]) and padding after. Every real query's output equals that row
+ * run alone at its own length,
+ *   out[b,h,l,:] = sum over m <= l (and l - m < window when window > 0) of
+ *                  softmax_m(cap(scale * q . k_m)) v_m        for l < lengths[b],
+ * and padding outputs are exactly +0.0 (l >= lengths[b]). Padding rows of q, k
+ * and v are never read into a real output, whatever they hold (inf and NaN
+ * included): padding values meet no zero weight in P V.
+ *   q        [B, H, L, D]   raw if rp != NULL (RMSNorm + RoPE at position l, as
+ *                           in gqa_attn_prefill_rope with start 0; q is not
+ *                           modified), else already rotated
+ *   k, v     [B, Hkv, L, D] rotated keys and values
+ *   lengths  [B] device int32 in [1, L]; a value outside sets ATTN_DEV_LENGTH
+ *            and is clamped to [0, L]
+ *   workspace gqa_attn_prefill_ragged_workspace_size bytes
+ * Other arguments as for gqa_attn_prefill_rope (rp, table, q_norm_w may be NULL
+ * when rp is NULL). In the persistent kernel (D <= 128) query tiles with no
+ * real row cost no attention work.
+ */
+size_t gqa_attn_prefill_ragged_workspace_size(int B, int H, int Hkv, int L, int D,
+                                              const attn_rope_params* rp);
+int gqa_attn_prefill_ragged(const float* q, const float* k, const float* v, float* out, int B,
+                            int H, int Hkv, int L, int D, const int32_t* lengths,
                             const attn_rope_params* rp, const float* table,
                             const float* q_norm_w, float norm_eps, int window, float softcap,
                             float scale, void* workspace, size_t workspace_bytes,

@@ -232,3 +232,28 @@ def test_cached_prefill_refuses_before_launch():
     assert need >= 2 * 2 * 48 * 64 * 4
     assert lib.gqa_attn_prefill_cached_workspace_size(1, 4, 2, 16, 64, 1000, 64, None) < need * 3
     assert call(ws=ctypes.c_void_p(0x100004), wbytes=need) == -6
+
+
+def test_ragged_prefill_refuses_before_launch():
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+
+    def call(lengths=P, H=4, Hkv=2, D=64, window=0, ws=None, wbytes=0, rp=None, table=None):
+        return lib.gqa_attn_prefill_ragged(P, P, P, P, 2, H, Hkv, 16, D, lengths, rp, table,
+                                           None, 1e-6, window, 0.0, 0.0, ws, wbytes, None, None)
+
+    assert call(H=6, Hkv=4) == -2                 # H % Hkv != 0
+    assert call(D=7) == -2                        # odd head dim
+    assert call(window=-1) == -2
+    assert call(lengths=None) == -1               # lengths are required
+    assert call() == -5                           # no workspace
+    rp = g.RopeParams.make(theta=1e4, max_positions=64)
+    plain = lib.gqa_attn_prefill_ragged_workspace_size(2, 4, 2, 16, 64, None)
+    roped = lib.gqa_attn_prefill_ragged_workspace_size(2, 4, 2, 16, 64, ctypes.byref(rp))
+    # start = 0 per row, then V^T (2 rows x 2 kv heads x 64 dims x 16 keys)
+    assert plain >= 256 + 2 * 2 * 64 * 16 * 4 and roped >= plain
+    assert call(ws=ctypes.c_void_p(0x100004), wbytes=plain) == -6
+    bad = g.RopeParams.make(theta=1e4, rope_dim=66, max_positions=64)   # R > D
+    assert call(rp=ctypes.byref(bad)) == -7
+    assert lib.gqa_attn_prefill_ragged(P, P, P, P, 0, 4, 2, 16, 64, None, None, None, None,
+                                       1e-6, 0, 0.0, 0.0, None, 0, None, None) == 0   # empty
