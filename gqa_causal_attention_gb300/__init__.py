@@ -27,6 +27,7 @@ __all__ = [
     "gqa_attn_prefill_rope_vt", "gqa_attn_prefill_rope_vt_workspace_size",
     "gqa_attn_prefill_cached", "gqa_attn_prefill_cached_workspace_size",
     "gqa_attn_prefill_ragged", "gqa_attn_prefill_ragged_workspace_size",
+    "gqa_attn_prefill_identical", "gqa_attn_decode_identical",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
@@ -120,6 +121,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_attn_prefill_ragged_workspace_size": (sz, [i32, i32, i32, i32, i32, rp]),
             "gqa_attn_prefill_ragged": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, rp,
                                               vp, vp, f, i32, f, f, vp, sz, vp, vp]),
+            "gqa_attn_prefill_identical": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                                 i32, i32, vp, ctypes.c_int32, i32, f, f, vp,
+                                                 vp]),
+            "gqa_attn_decode_identical": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32,
+                                                i32, i32, i32, i32, f, f, vp, vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -453,6 +459,51 @@ def gqa_attn_decode(q, k_cache, v_cache, cache_len, max_cache_len: int, out, win
                                 float(softcap), float(scale), _ptr(workspace), wbytes,
                                 _ptr(status), _stream(stream))
     _check("gqa_attn_decode", rc)
+
+
+def gqa_attn_prefill_identical(q, k, v, out, start=None, max_start: int = 0, k_cache=None,
+                               v_cache=None, window: int = 0, softcap: float = 0.0,
+                               scale: float = 0.0, status=None, stream=None) -> None:
+    """Prefill attention in the identical numeric mode (bit-for-bit equal to token-by-token
+    gqa_attn_decode_identical and to chunked continuations). q, k, v rotated; with k_cache /
+    v_cache the positions before start[b] are read from the cache."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("k_cache", k_cache),
+                 ("v_cache", v_cache)):
+        _f32(n, t, 4)
+    _i32("start", start); _i32("status", status)
+    B, H, L, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, L, D) or v.shape != k.shape or out.shape != q.shape:
+        raise ValueError("gqa_attn_prefill_identical: inconsistent shapes")
+    cap = 0
+    if k_cache is not None:
+        if v_cache is None or v_cache.shape != k_cache.shape or k_cache.shape[0] != B or \
+                k_cache.shape[1] != Hkv or k_cache.shape[3] != D:
+            raise ValueError("gqa_attn_prefill_identical: inconsistent cache shapes")
+        cap = k_cache.shape[2]
+    rc = load().gqa_attn_prefill_identical(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache),
+                                           _ptr(v_cache), cap, _ptr(out), B, H, Hkv, L, D,
+                                           _ptr(start), int(max_start), int(window),
+                                           float(softcap), float(scale), _ptr(status),
+                                           _stream(stream))
+    _check("gqa_attn_prefill_identical", rc)
+
+
+def gqa_attn_decode_identical(q, k_cache, v_cache, cache_len, max_cache_len: int, out,
+                              window: int = 0, softcap: float = 0.0, scale: float = 0.0,
+                              status=None, stream=None) -> None:
+    """gqa_attn_decode in the identical numeric mode (no workspace)."""
+    _f32("q", q, 4); _f32("out", out, 4); _f32("k_cache", k_cache, 4)
+    _f32("v_cache", v_cache, 4); _i32("cache_len", cache_len); _i32("status", status)
+    B, H, one, D = q.shape
+    Bc, Hkv, cap, Dc = k_cache.shape
+    if one != 1 or Bc != B or Dc != D or v_cache.shape != k_cache.shape or out.shape != q.shape:
+        raise ValueError("gqa_attn_decode_identical: inconsistent shapes")
+    rc = load().gqa_attn_decode_identical(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(cache_len),
+                                          int(max_cache_len), _ptr(out), B, H, Hkv, D, cap,
+                                          int(window), float(softcap), float(scale),
+                                          _ptr(status), _stream(stream))
+    _check("gqa_attn_decode_identical", rc)
 
 
 def gqa_attn_decode_static(q, k_cache, v_cache, cache_len, max_cache_len: int, out,

@@ -493,6 +493,51 @@ size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cach
   return (size_t)B * H * nsplit * (D + 2) * sizeof(float);
 }
 
+int gqa_attn_prefill_identical(const float* q, const float* k, const float* v,
+                               const float* k_cache, const float* v_cache, int capacity,
+                               float* out, int B, int H, int Hkv, int L, int D,
+                               const int32_t* start, int32_t max_start, int window,
+                               float softcap, float scale, int32_t* status, void* stream) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0) return ATTN_ERR_SHAPE;
+  const bool cached = k_cache || v_cache;
+  if (cached && (capacity < 1 || (window > 0 && capacity != window))) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!q || !k || !v || !out || (cached && !(k_cache && v_cache && start))) return ATTN_ERR_NULL;
+  if (max_start < 0 || (!start && max_start != 0)) return ATTN_ERR_POSITION;
+  if (cached && window == 0 && max_start > capacity) return ATTN_ERR_CAPACITY;
+  gqa::IdentJob j{};
+  j.q = q; j.k = k; j.v = v; j.k_cache = k_cache; j.v_cache = v_cache;
+  j.start = start; j.max_start = max_start; j.out = out;
+  j.B = B; j.H = H; j.Hkv = Hkv; j.L = L; j.D = D; j.capacity = capacity; j.window = window;
+  j.softcap = softcap > 0.f ? softcap : 0.f;
+  j.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  j.status = status;
+  return cuda_status(gqa::launch_identical(j, static_cast<cudaStream_t>(stream)));
+}
+
+int gqa_attn_decode_identical(const float* q, const float* k_cache, const float* v_cache,
+                              const int32_t* cache_len, int32_t max_cache_len, float* out, int B,
+                              int H, int Hkv, int D, int capacity, int window, float softcap,
+                              float scale, int32_t* status, void* stream) {
+  if (!dims_ok(B, H, 1, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || capacity < 1)
+    return ATTN_ERR_SHAPE;
+  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (B == 0) return ATTN_OK;
+  if (max_cache_len < 1) return ATTN_ERR_SHAPE;
+  if (window == 0 && max_cache_len > capacity) return ATTN_ERR_CAPACITY;
+  if (!q || !k_cache || !v_cache || !cache_len || !out) return ATTN_ERR_NULL;
+  gqa::IdentJob j{};
+  j.q = q; j.k_cache = k_cache; j.v_cache = v_cache; j.cache_len = cache_len;
+  j.max_len = max_cache_len; j.out = out;
+  j.B = B; j.H = H; j.Hkv = Hkv; j.L = 1; j.D = D; j.capacity = capacity; j.window = window;
+  j.softcap = softcap > 0.f ? softcap : 0.f;
+  j.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  j.status = status;
+  return cuda_status(gqa::launch_identical(j, static_cast<cudaStream_t>(stream)));
+}
+
 int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
                     const int32_t* cache_len, int32_t max_cache_len, float* out, int B, int H,
                     int Hkv, int D, int capacity, int window, float softcap, float scale,

@@ -117,6 +117,27 @@ struct DecodeJob {
   int32_t* status;
 };
 
+// The identical numeric mode: one warp per query row, fixed arithmetic order
+// (identical.cu). Keys at positions >= s0 come from k / v (the chunk), below
+// s0 from the cache. Prefill: s0 = start[b] (nullptr: 0), query row l at
+// position s0 + l. Decode (cache_len != nullptr): L = 1, position
+// cache_len[b] - 1, every key from the cache.
+struct IdentJob {
+  const float* q;           // [B, H, L, D] rotated
+  const float* k;           // [B, Hkv, L, D] rotated chunk keys, or nullptr (decode)
+  const float* v;
+  const float* k_cache;     // [B, Hkv, capacity, D] or nullptr (no cached prefix)
+  const float* v_cache;
+  const int32_t* start;     // [B] or nullptr
+  const int32_t* cache_len; // [B], decode only
+  int max_start, max_len;
+  float* out;               // [B, H, L, D]
+  int B, H, Hkv, L, D, capacity, window;
+  float softcap, scale;
+  int32_t* status;
+};
+cudaError_t launch_identical(const IdentJob& j, cudaStream_t stream);
+
 void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream);
 

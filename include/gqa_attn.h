@@ -266,6 +266,44 @@ int gqa_attn_prefill_ragged(const float* q, const float* k, const float* v, floa
                             int32_t* status, void* stream);
 
 /*
+ * The identical numeric mode ("mojolearn.transformer", TransformerBlock
+ * numeric_mode 'identical': decoding token by token, or a prefill continued
+ * from a carried cache, gives the same bits as one prefill over the whole
+ * sequence). Both calls below run one kernel whose per-query arithmetic
+ * depends only on the query's position and the visible key positions: the
+ * score of key m is a fixed-order dot product, the maximum is exact, and the
+ * softmax sum and P V run over keys in ascending position order. So, with
+ * keys and values appended by kv_cache_append (the cache holds the same bits
+ * as the appended rows) and queries rotated by attn_rope_apply:
+ *   gqa_attn_decode_identical at cache_len[b] = p + 1 ==
+ *   gqa_attn_prefill_identical row p (start 0)  ==
+ *   gqa_attn_prefill_identical of any chunk holding position p, continued
+ *   from the cache of the positions before it,
+ * bit for bit. Results equal the other prefill/decode calls within the usual
+ * tolerance, not bitwise. CUDA cores, scores computed twice: for
+ * reproducibility, not speed.
+ *
+ * Prefill: q [B, H, L, D] rotated, k, v [B, Hkv, L, D] rotated keys / values of
+ * the chunk at positions start[b] + l (start NULL: 0, then max_start must be
+ * 0). With k_cache, v_cache ([B, Hkv, capacity, D], slot = position, or
+ * position mod window with capacity == window) positions below start[b] are
+ * read from the cache; without, only the chunk's own keys are seen (as in
+ * gqa_attn_prefill). A start[b] outside [0, max_start] (or above capacity
+ * without a window) sets ATTN_DEV_POSITION (ATTN_DEV_CAPACITY) and the row's
+ * outputs are left untouched.
+ * Decode: as gqa_attn_decode, without a workspace.
+ */
+int gqa_attn_prefill_identical(const float* q, const float* k, const float* v,
+                               const float* k_cache, const float* v_cache, int capacity,
+                               float* out, int B, int H, int Hkv, int L, int D,
+                               const int32_t* start, int32_t max_start, int window,
+                               float softcap, float scale, int32_t* status, void* stream);
+int gqa_attn_decode_identical(const float* q, const float* k_cache, const float* v_cache,
+                              const int32_t* cache_len, int32_t max_cache_len, float* out, int B,
+                              int H, int Hkv, int D, int capacity, int window, float softcap,
+                              float scale, int32_t* status, void* stream);
+
+/*
  * Bytes of scratch gqa_attn_decode needs for these sizes (split-KV partial
  * results). max_cache_len bounds every cache_len[b].
  */

@@ -257,3 +257,30 @@ def test_ragged_prefill_refuses_before_launch():
     assert call(rp=ctypes.byref(bad)) == -7
     assert lib.gqa_attn_prefill_ragged(P, P, P, P, 0, 4, 2, 16, 64, None, None, None, None,
                                        1e-6, 0, 0.0, 0.0, None, 0, None, None) == 0   # empty
+
+
+def test_identical_mode_refuses_before_launch():
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+
+    def pre(kc=None, vc=None, cap=0, start=None, max_start=0, window=0, H=4, Hkv=2, D=64):
+        return lib.gqa_attn_prefill_identical(P, P, P, kc, vc, cap, P, 1, H, Hkv, 16, D, start,
+                                              max_start, window, 0.0, 0.0, None, None)
+
+    assert pre(H=6, Hkv=4) == -2
+    assert pre(D=9) == -2
+    assert pre(kc=P, vc=P, cap=0, start=P) == -2          # a cache needs capacity
+    assert pre(kc=P, vc=P, cap=64, start=P, window=32) == -2   # a ring holds window slots
+    assert pre(kc=P, vc=None, cap=64, start=P) == -1      # both caches or neither
+    assert pre(kc=P, vc=P, cap=64) == -1                  # a cached prefix needs start
+    assert pre(max_start=3) == -3                         # start NULL means position 0
+    assert pre(kc=P, vc=P, cap=64, start=P, max_start=65) == -4
+
+    def dec(cap=64, max_len=10, window=0, cl=P):
+        return lib.gqa_attn_decode_identical(P, P, P, cl, max_len, P, 1, 4, 2, 64, cap, window,
+                                             0.0, 0.0, None, None)
+
+    assert dec(max_len=0) == -2
+    assert dec(max_len=65) == -4
+    assert dec(window=32) == -2
+    assert dec(cl=None) == -1
