@@ -214,6 +214,46 @@ def prefill_ragged(q, k, v, lengths, cfg: Cfg, q_norm_w=None, k_norm_w=None) -> 
     return out
 
 
+def rmsnorm(x, w, eps: float, offset: bool = False) -> np.ndarray:
+    """RMSNorm over the last axis ("Core Layers -- Deep Reference", RMSNorm): x / sqrt(mean x^2
+    + eps) times w, or times 1 + w ("mojolearn.transformer", norm='rmsnorm_offset', Gemma)."""
+    x = _f64(x)
+    scale = (1.0 + _f64(w)) if offset else _f64(w)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * scale
+
+
+def block_forward(x, weights: dict, cfg: Cfg, norm_offset: bool = False) -> np.ndarray:
+    """One decoder block ("mojolearn.transformer", TransformerBlock.forward with state None,
+    computing Hugging Face's LlamaDecoderLayer.forward): input RMSNorm, q/k/v projections,
+    (q/k norm,) RoPE and causal grouped-query attention over positions 0 .. L-1, output
+    projection, residual; post-attention RMSNorm, SiLU-gated MLP, residual.
+
+    x [B, L, d_model]; weights keyed by the Hugging Face names in torch's [out, in] layout
+    (q_norm.weight / k_norm.weight optional). Matrix products are numpy's; returns float64.
+    """
+    x = _f64(x)
+    B, L, dm = x.shape
+    H, Hkv, D = cfg.H, cfg.Hkv, cfg.D
+    W = {n: _f64(t) for n, t in weights.items()}
+    eps = cfg.norm_eps
+    n1 = rmsnorm(x, W["input_layernorm.weight"], eps, norm_offset)
+
+    def heads(y, nh):                      # [B, L, nh * D] -> [B, nh, L, D]
+        return y.reshape(B, L, nh, D).transpose(0, 2, 1, 3)
+
+    q = heads(n1 @ W["q_proj.weight"].T, H)
+    k = heads(n1 @ W["k_proj.weight"].T, Hkv)
+    v = heads(n1 @ W["v_proj.weight"].T, Hkv)
+    attn, _, _ = prefill(q, k, v, [0] * B, Cfg(**{**cfg.__dict__, "B": B, "L": L}),
+                         W.get("q_norm.weight"), W.get("k_norm.weight"))
+    h = x + attn.transpose(0, 2, 1, 3).reshape(B, L, H * D) @ W["o_proj.weight"].T
+    n2 = rmsnorm(h, W["post_attention_layernorm.weight"], eps, norm_offset)
+    gate = n2 @ W["gate_proj.weight"].T
+    up = n2 @ W["up_proj.weight"].T
+    act = gate / (1.0 + np.exp(-gate)) * up          # SiLU(gate) * up
+    return h + act @ W["down_proj.weight"].T
+
+
 def append(kr, v, start, cfg: Cfg, capacity: int, k_cache=None, v_cache=None, written=None):
     """Store rotated k and raw v at their cache slots. Returns (k_cache, v_cache, written).
 

@@ -410,3 +410,106 @@ def test_ragged_real_rows_are_the_causal_prefix_and_ignore_padding():
             np.testing.assert_allclose(got[b, :, :n], full[b, :, :n], rtol=1e-12, atol=1e-13)
             pad = got[b, :, n:]
             assert (pad == 0).all() and not np.signbit(pad).any()
+
+
+# ----------------------------------------------------------------------------- decoder block
+
+
+def _block_weights(dm, H, Hkv, D, IT, qk_norm=False, scale=0.3):
+    w = {
+        "input_layernorm.weight": 1.0 + 0.1 * RNG.standard_normal(dm),
+        "post_attention_layernorm.weight": 1.0 + 0.1 * RNG.standard_normal(dm),
+        "q_proj.weight": scale * RNG.standard_normal((H * D, dm)) / np.sqrt(dm),
+        "k_proj.weight": scale * RNG.standard_normal((Hkv * D, dm)) / np.sqrt(dm),
+        "v_proj.weight": scale * RNG.standard_normal((Hkv * D, dm)) / np.sqrt(dm),
+        "o_proj.weight": scale * RNG.standard_normal((dm, H * D)) / np.sqrt(H * D),
+        "gate_proj.weight": scale * RNG.standard_normal((IT, dm)) / np.sqrt(dm),
+        "up_proj.weight": scale * RNG.standard_normal((IT, dm)) / np.sqrt(dm),
+        "down_proj.weight": scale * RNG.standard_normal((dm, IT)) / np.sqrt(IT),
+    }
+    if qk_norm:
+        w["q_norm.weight"] = 1.0 + 0.1 * RNG.standard_normal(D)
+        w["k_norm.weight"] = 1.0 + 0.1 * RNG.standard_normal(D)
+    return w
+
+
+def test_block_with_zero_output_projections_is_the_identity():
+    B, L, H, Hkv, D, IT = 2, 7, 4, 2, 8, 24
+    dm = H * D
+    w = _block_weights(dm, H, Hkv, D, IT)
+    w["o_proj.weight"][:] = 0.0
+    w["down_proj.weight"][:] = 0.0
+    x = RNG.standard_normal((B, L, dm))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D)
+    np.testing.assert_array_equal(oracle.block_forward(x, w, cfg), x)
+
+
+def test_block_single_token_closed_form():
+    """One token attends to itself only (weight 1), so attention returns its value row: the
+    block is x + Wo . repeat_kv(Wv . n1(x)) followed by the MLP. Checks the head layout of
+    the projections and the grouping of query heads onto kv heads."""
+    B, L, H, Hkv, D, IT = 3, 1, 6, 2, 4, 10
+    dm = H * D
+    w = _block_weights(dm, H, Hkv, D, IT, qk_norm=True)
+    x = RNG.standard_normal((B, L, dm))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, softcap=3.0, window=5)
+    got = oracle.block_forward(x, w, cfg)
+    eps = cfg.norm_eps
+    for b in range(B):
+        xt = x[b, 0]
+        n1 = xt / np.sqrt(np.mean(xt * xt) + eps) * w["input_layernorm.weight"]
+        vh = (w["v_proj.weight"] @ n1).reshape(Hkv, D)
+        attn = np.concatenate([vh[h // (H // Hkv)] for h in range(H)])
+        hmid = xt + w["o_proj.weight"] @ attn
+        n2 = hmid / np.sqrt(np.mean(hmid * hmid) + eps) * w["post_attention_layernorm.weight"]
+        gt, up = w["gate_proj.weight"] @ n2, w["up_proj.weight"] @ n2
+        want = hmid + w["down_proj.weight"] @ (gt / (1 + np.exp(-gt)) * up)
+        np.testing.assert_allclose(got[b, 0], want, rtol=1e-12, atol=1e-12)
+
+
+def test_block_is_causal():
+    """Changing the tokens from position t on leaves every earlier output unchanged."""
+    B, L, H, Hkv, D, IT = 1, 9, 4, 1, 8, 16
+    dm = H * D
+    w = _block_weights(dm, H, Hkv, D, IT)
+    x = RNG.standard_normal((B, L, dm))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D)
+    base = oracle.block_forward(x, w, cfg)
+    x2 = x.copy()
+    x2[:, 5:] = RNG.standard_normal((B, L - 5, dm))
+    other = oracle.block_forward(x2, w, cfg)
+    np.testing.assert_array_equal(other[:, :5], base[:, :5])
+    assert np.abs(other[:, 5:] - base[:, 5:]).max() > 1e-3
+
+
+def test_block_mlp_is_per_token_and_linear_in_up():
+    """With W_v = 0 attention adds nothing, so the block maps each token alone: permuting the
+    tokens permutes the outputs, and scaling W_up scales the MLP's contribution (SiLU acts on
+    the gate branch only)."""
+    B, L, H, Hkv, D, IT = 1, 6, 2, 2, 8, 20
+    dm = H * D
+    w = _block_weights(dm, H, Hkv, D, IT)
+    w["v_proj.weight"][:] = 0.0
+    x = RNG.standard_normal((B, L, dm))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D)
+    base = oracle.block_forward(x, w, cfg)
+    perm = RNG.permutation(L)
+    np.testing.assert_allclose(oracle.block_forward(x[:, perm], w, cfg), base[:, perm],
+                               rtol=1e-13, atol=1e-13)
+    w3 = dict(w, **{"up_proj.weight": 3.0 * w["up_proj.weight"]})
+    np.testing.assert_allclose(oracle.block_forward(x, w3, cfg) - x, 3.0 * (base - x),
+                               rtol=1e-12, atol=1e-12)
+
+
+def test_block_offset_norm_with_zero_weight_is_plain_unit_norm():
+    B, L, H, Hkv, D, IT = 1, 4, 2, 1, 8, 12
+    dm = H * D
+    w = _block_weights(dm, H, Hkv, D, IT)
+    x = RNG.standard_normal((B, L, dm))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D)
+    w0 = dict(w, **{"input_layernorm.weight": np.zeros(dm),
+                    "post_attention_layernorm.weight": np.zeros(dm)})
+    w1 = dict(w, **{"input_layernorm.weight": np.ones(dm),
+                    "post_attention_layernorm.weight": np.ones(dm)})
+    np.testing.assert_array_equal(oracle.block_forward(x, w0, cfg, norm_offset=True),
+                                  oracle.block_forward(x, w1, cfg))
