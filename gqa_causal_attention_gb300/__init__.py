@@ -28,6 +28,7 @@ __all__ = [
     "gqa_attn_prefill_cached", "gqa_attn_prefill_cached_workspace_size",
     "gqa_attn_prefill_ragged", "gqa_attn_prefill_ragged_workspace_size",
     "gqa_attn_prefill_identical", "gqa_attn_decode_identical",
+    "gqa_block_forward", "gqa_block_forward_workspace_size", "BLOCK_WEIGHT_NAMES",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
@@ -126,6 +127,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                                  vp]),
             "gqa_attn_decode_identical": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32,
                                                 i32, i32, i32, i32, f, f, vp, vp]),
+            "gqa_block_forward_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, rp]),
+            "gqa_block_forward": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, f, rp,
+                                        vp, i32, f, f, vp, sz, vp, vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -504,6 +508,68 @@ def gqa_attn_decode_identical(q, k_cache, v_cache, cache_len, max_cache_len: int
                                           int(window), float(softcap), float(scale),
                                           _ptr(status), _stream(stream))
     _check("gqa_attn_decode_identical", rc)
+
+
+# attn_block_weights field -> Hugging Face parameter name
+BLOCK_WEIGHT_NAMES = (
+    ("input_norm", "input_layernorm.weight"), ("post_norm", "post_attention_layernorm.weight"),
+    ("wq", "q_proj.weight"), ("wk", "k_proj.weight"), ("wv", "v_proj.weight"),
+    ("wo", "o_proj.weight"), ("w_gate", "gate_proj.weight"), ("w_up", "up_proj.weight"),
+    ("w_down", "down_proj.weight"), ("q_norm", "q_norm.weight"), ("k_norm", "k_norm.weight"),
+)
+
+
+class _BlockWeights(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f, _ in BLOCK_WEIGHT_NAMES]
+
+
+def gqa_block_forward_workspace_size(B: int, L: int, H: int, Hkv: int, D: int, IT: int,
+                                     params: RopeParams) -> int:
+    return int(load().gqa_block_forward_workspace_size(B, L, H, Hkv, D, IT,
+                                                       ctypes.byref(params)))
+
+
+def gqa_block_forward(x, out, weights: dict, n_heads: int, n_kv_heads: int,
+                      params: RopeParams, table, norm_offset: bool = False,
+                      norm_eps: float = 1e-6, window: int = 0, softcap: float = 0.0,
+                      scale: float = 0.0, workspace=None, status=None, stream=None) -> None:
+    """One decoder block (TransformerBlock.forward, state None): x, out [B, L, d_model];
+    weights: float32 CUDA tensors keyed by the Hugging Face names (q_norm / k_norm
+    optional)."""
+    _f32("x", x, 3); _f32("out", out, 3); _f32("table", table); _i32("status", status)
+    B, L, dm = x.shape
+    H, Hkv = int(n_heads), int(n_kv_heads)
+    if dm % H or out.shape != x.shape:
+        raise ValueError("gqa_block_forward: d_model must be n_heads * head_dim")
+    D = dm // H
+    IT = weights["gate_proj.weight"].shape[0]
+    shapes = {"input_layernorm.weight": (dm,), "post_attention_layernorm.weight": (dm,),
+              "q_proj.weight": (H * D, dm), "k_proj.weight": (Hkv * D, dm),
+              "v_proj.weight": (Hkv * D, dm), "o_proj.weight": (dm, H * D),
+              "gate_proj.weight": (IT, dm), "up_proj.weight": (IT, dm),
+              "down_proj.weight": (dm, IT), "q_norm.weight": (D,), "k_norm.weight": (D,)}
+    w = _BlockWeights()
+    for field, name in BLOCK_WEIGHT_NAMES:
+        t = weights.get(name)
+        if t is None:
+            if name in ("q_norm.weight", "k_norm.weight"):
+                continue
+            raise ValueError(f"gqa_block_forward: missing {name}")
+        _f32(name, t)
+        if tuple(t.shape) != shapes[name] or not t.is_contiguous():
+            raise ValueError(f"gqa_block_forward: {name} must be contiguous {shapes[name]}")
+        setattr(w, field, t.data_ptr())
+    if workspace is None:
+        n = gqa_block_forward_workspace_size(B, L, H, Hkv, D, IT, params)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=x.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().gqa_block_forward(_ptr(x), _ptr(out), B, L, H, Hkv, D, IT, ctypes.byref(w),
+                                  int(bool(norm_offset)), float(norm_eps), ctypes.byref(params),
+                                  _ptr(table), int(window), float(softcap), float(scale),
+                                  _ptr(workspace), wbytes, _ptr(status), _stream(stream))
+    _check("gqa_block_forward", rc)
 
 
 def gqa_attn_decode_static(q, k_cache, v_cache, cache_len, max_cache_len: int, out,

@@ -493,6 +493,96 @@ size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cach
   return (size_t)B * H * nsplit * (D + 2) * sizeof(float);
 }
 
+size_t gqa_block_forward_workspace_size(int B, int L, int H, int Hkv, int D, int IT,
+                                        const attn_rope_params* rp) {
+  if (B < 0 || L < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || IT < 1 || !rope_params_ok(rp, D))
+    return 0;
+  const size_t T = (size_t)B * L, QW = (size_t)H * D, KW = (size_t)Hkv * D;
+  const size_t attn = gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp);
+  if (attn == 0) return 0;
+  // zero start [B] | normed rows [T, QW] | q, attention out [T, QW] x 2 | k, v token- and
+  // head-major [T, KW] x 4 | gate, up [T, IT] x 2 | the attention's own workspace
+  return round256((size_t)B * 4) + round256(T * QW * 4) * 3 + round256(T * KW * 4) * 4 +
+         round256(T * (size_t)IT * 4) * 2 + round256(attn);
+}
+
+int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, int D, int IT,
+                      const attn_block_weights* w, int norm_offset, float norm_eps,
+                      const attn_rope_params* rp, const float* table, int window, float softcap,
+                      float scale, void* workspace, size_t workspace_bytes, int32_t* status,
+                      void* stream) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || IT < 1 || window < 0)
+    return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
+  if (!rp || !rope_params_ok(rp, D)) return rp ? ATTN_ERR_PARAM : ATTN_ERR_NULL;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!x || !out || !w || !table || !w->input_norm || !w->post_norm || !w->wq || !w->wk ||
+      !w->wv || !w->wo || !w->w_gate || !w->w_up || !w->w_down)
+    return ATTN_ERR_NULL;
+  if ((int64_t)L - 1 >= (int64_t)max_pos_of(rp)) return ATTN_ERR_POSITION;
+  const size_t need = gqa_block_forward_workspace_size(B, L, H, Hkv, D, IT, rp);
+  if (need == 0) return ATTN_ERR_SHAPE;
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace) || !aligned16(x) || !aligned16(out) || !aligned16(table))
+    return ATTN_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long T = (long)B * L;
+  const int QW = H * D, KW = Hkv * D;
+  char* p = static_cast<char*>(workspace);
+  auto take = [&](size_t bytes) { char* r = p; p += round256(bytes); return r; };
+  int32_t* zero_start = reinterpret_cast<int32_t*>(take((size_t)B * 4));
+  float* nrm = reinterpret_cast<float*>(take((size_t)T * QW * 4));
+  float* qt = reinterpret_cast<float*>(take((size_t)T * QW * 4));   // token-major q, attn out
+  float* qh = reinterpret_cast<float*>(take((size_t)T * QW * 4));   // head-major q, attn out
+  float* kt = reinterpret_cast<float*>(take((size_t)T * KW * 4));
+  float* vt = reinterpret_cast<float*>(take((size_t)T * KW * 4));
+  float* kh = reinterpret_cast<float*>(take((size_t)T * KW * 4));
+  float* vh = reinterpret_cast<float*>(take((size_t)T * KW * 4));
+  float* gate = reinterpret_cast<float*>(take((size_t)T * IT * 4));
+  float* up = reinterpret_cast<float*>(take((size_t)T * IT * 4));
+  void* attn_ws = p;
+  const size_t attn_bytes = workspace_bytes - (size_t)(p - static_cast<char*>(workspace));
+  const bool offset = norm_offset != 0;
+  auto chk = [&](cudaError_t e) { return e == cudaSuccess ? ATTN_OK : cuda_status(e); };
+  int rc;
+  if ((rc = chk(cudaMemsetAsync(zero_start, 0, (size_t)B * 4, s)))) return rc;
+  // attention half: n1 = RMSNorm(x); q, k, v = n1 W^T; heads; k RoPE; attention; o_proj
+  if ((rc = chk(gqa::launch_rmsnorm_rows(x, w->input_norm, nrm, T, QW, norm_eps, offset, s))))
+    return rc;
+  if (gqa::gemm_xwt(nrm, w->wq, qt, T, QW, QW, 0.f, s) ||
+      gqa::gemm_xwt(nrm, w->wk, kt, T, KW, QW, 0.f, s) ||
+      gqa::gemm_xwt(nrm, w->wv, vt, T, KW, QW, 0.f, s))
+    return ATTN_ERR_CUDA;
+  if ((rc = chk(gqa::launch_swap_mid(qt, qh, B, L, H, D, s))) ||
+      (rc = chk(gqa::launch_swap_mid(kt, kh, B, L, Hkv, D, s))) ||
+      (rc = chk(gqa::launch_swap_mid(vt, vh, B, L, Hkv, D, s))))
+    return rc;
+  gqa::RopeJob j{};
+  j.x = kh; j.B = B; j.NH = Hkv; j.L = L; j.D = D; j.R = rope_dim_of(rp, D);
+  j.start = zero_start; j.max_positions = max_pos_of(rp);
+  j.table = reinterpret_cast<const float2*>(table);
+  j.norm_w = w->k_norm; j.norm_eps = norm_eps; j.status = status;
+  if ((rc = chk(gqa::launch_rope_rows(j, s)))) return rc;
+  rc = gqa_attn_prefill_rope(qh, kh, vh, qt, B, H, Hkv, L, D,
+                             zero_start, 0, rp, table, w->q_norm, norm_eps, window, softcap,
+                             scale, attn_ws, attn_bytes, status, stream);
+  if (rc != ATTN_OK) return rc;
+  // qt now holds the attention output, head-major; back to token-major in qh
+  if ((rc = chk(gqa::launch_swap_mid(qt, qh, B, H, L, D, s)))) return rc;
+  if ((rc = chk(cudaMemcpyAsync(out, x, (size_t)T * QW * 4, cudaMemcpyDeviceToDevice, s))))
+    return rc;
+  if (gqa::gemm_xwt(qh, w->wo, out, T, QW, QW, 1.f, s)) return ATTN_ERR_CUDA;   // h = x + o
+  // MLP half: n2 = RMSNorm(h); out = h + (SiLU(n2 Wg^T) * n2 Wu^T) Wd^T
+  if ((rc = chk(gqa::launch_rmsnorm_rows(out, w->post_norm, nrm, T, QW, norm_eps, offset, s))))
+    return rc;
+  if (gqa::gemm_xwt(nrm, w->w_gate, gate, T, IT, QW, 0.f, s) ||
+      gqa::gemm_xwt(nrm, w->w_up, up, T, IT, QW, 0.f, s))
+    return ATTN_ERR_CUDA;
+  if ((rc = chk(gqa::launch_swiglu(gate, up, T * IT, s)))) return rc;
+  if (gqa::gemm_xwt(gate, w->w_down, out, T, QW, IT, 1.f, s)) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
 int gqa_attn_prefill_identical(const float* q, const float* k, const float* v,
                                const float* k_cache, const float* v_cache, int capacity,
                                float* out, int B, int H, int Hkv, int L, int D,

@@ -138,6 +138,16 @@ struct IdentJob {
 };
 cudaError_t launch_identical(const IdentJob& j, cudaStream_t stream);
 
+// The decoder block around the attention (block.cu).
+cudaError_t launch_rmsnorm_rows(const float* x, const float* w, float* y, long T, int n,
+                                float eps, bool offset, cudaStream_t stream);
+cudaError_t launch_swap_mid(const float* in, float* out, int B, int P, int Q, int D,
+                            cudaStream_t stream);   // [B, P, Q, D] -> [B, Q, P, D]
+cudaError_t launch_swiglu(float* gate, const float* up, long n, cudaStream_t stream);
+// Y [T, N] = X [T, K] . W^T + beta * Y in fp32 (W in torch's [out, in] layout); 0 or -1.
+int gemm_xwt(const float* X, const float* W, float* Y, long T, int N, int K, float beta,
+             cudaStream_t stream);
+
 void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream);
 

@@ -266,6 +266,46 @@ int gqa_attn_prefill_ragged(const float* q, const float* k, const float* v, floa
                             int32_t* status, void* stream);
 
 /*
+ * One decoder block around the attention ("mojolearn.transformer",
+ * TransformerBlock.forward with state None, i.e. a fresh sequence at positions
+ * 0 .. L-1, computing Hugging Face's LlamaDecoderLayer.forward):
+ *   h   = x + o_proj(attention(RMSNorm_in(x)))
+ *   out = h + down_proj(SiLU(gate_proj(n)) * up_proj(n)),  n = RMSNorm_post(h)
+ * with the attention of gqa_attn_prefill_rope (q/k RMSNorm when q_norm / k_norm
+ * are given, RoPE per rp, causal or window, softcap). RMSNorm scales by w, or by
+ * 1 + w when norm_offset != 0 (Gemma). No biases.
+ *   x, out   [B, L, d_model] with d_model = H * D (distinct buffers)
+ *   weights  torch's [out, in] layout: q_proj [H*D, d_model], k_proj and v_proj
+ *            [Hkv*D, d_model], o_proj [d_model, H*D], gate_proj and up_proj
+ *            [IT, d_model], down_proj [d_model, IT]; norms [d_model]; q_norm,
+ *            k_norm [D] or NULL
+ *   workspace gqa_block_forward_workspace_size bytes
+ * The projections are fp32 GEMMs (cuBLAS, no TF32; the library creates one
+ * cuBLAS handle on first use). Returns ATTN_ERR_CUDA if a GEMM fails.
+ */
+typedef struct attn_block_weights {
+    const float* input_norm;         /* input_layernorm.weight [d_model] */
+    const float* post_norm;          /* post_attention_layernorm.weight [d_model] */
+    const float* wq;                 /* q_proj.weight */
+    const float* wk;                 /* k_proj.weight */
+    const float* wv;                 /* v_proj.weight */
+    const float* wo;                 /* o_proj.weight */
+    const float* w_gate;             /* gate_proj.weight */
+    const float* w_up;               /* up_proj.weight */
+    const float* w_down;             /* down_proj.weight */
+    const float* q_norm;             /* q_norm.weight [D] or NULL */
+    const float* k_norm;             /* k_norm.weight [D] or NULL */
+} attn_block_weights;
+
+size_t gqa_block_forward_workspace_size(int B, int L, int H, int Hkv, int D, int IT,
+                                        const attn_rope_params* rp);
+int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, int D, int IT,
+                      const attn_block_weights* w, int norm_offset, float norm_eps,
+                      const attn_rope_params* rp, const float* table, int window, float softcap,
+                      float scale, void* workspace, size_t workspace_bytes, int32_t* status,
+                      void* stream);
+
+/*
  * The identical numeric mode ("mojolearn.transformer", TransformerBlock
  * numeric_mode 'identical': decoding token by token, or a prefill continued
  * from a carried cache, gives the same bits as one prefill over the whole

@@ -284,3 +284,27 @@ def test_identical_mode_refuses_before_launch():
     assert dec(max_len=65) == -4
     assert dec(window=32) == -2
     assert dec(cl=None) == -1
+
+
+def test_block_forward_refuses_before_launch():
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+    rp = g.RopeParams.make(theta=1e4, max_positions=64)
+    w = g._BlockWeights(*([0x100000] * 9 + [0, 0]))
+
+    def call(H=4, Hkv=2, D=16, IT=32, L=8, weights=w, params=rp, ws=None, wbytes=0):
+        return lib.gqa_block_forward(P, P, 2, L, H, Hkv, D, IT,
+                                     None if weights is None else ctypes.byref(weights), 0, 1e-6,
+                                     None if params is None else ctypes.byref(params), P, 0, 0.0,
+                                     0.0, ws, wbytes, None, None)
+
+    assert call(H=6, Hkv=4) == -2
+    assert call(IT=0) == -2
+    assert call(weights=None) == -1
+    assert call(params=None) == -1
+    assert call(L=65) == -3                        # positions reach max_positions
+    assert call() == -5                            # no workspace
+    need = lib.gqa_block_forward_workspace_size(2, 8, 4, 2, 16, 32, ctypes.byref(rp))
+    assert need >= 2 * 8 * (3 * 64 + 4 * 32 + 2 * 32) * 4
+    w2 = g._BlockWeights(*([0x100000] * 8 + [0, 0, 0]))          # no down_proj
+    assert call(weights=w2, ws=P, wbytes=need) == -1
