@@ -469,6 +469,192 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
   *nsplit = (eff + c - 1) / c;
 }
 
+// ---------------------------------------------------------------- head-pair split kernel
+// Groups of 8 query heads per key/value head (G % 8 == 0), D % 4 == 0, D <= 128:
+// the same split-KV reduction and the same bulk-copy ring, with a lane map that
+// spends fewer instructions per key. The bulk kernel above holds 4 dims of all
+// 8 heads per lane, so each score needs a 32-lane reduction and P V a shuffle
+// per weight; here lane l = (pair l / 8, group l % 8) holds heads 2 pair,
+// 2 pair + 1 and dims 32 c + 4 group .. + 3 (c < 4; 16-byte shared loads of one
+// row by the 8 groups fall on distinct banks). A score is summed over the 8
+// lanes of its pair (3 shuffles), which then all hold it, so the running
+// maximum, the sum and P V need no further exchange.
+constexpr int kPairKeys = 8;                  // keys per stage
+
+__global__ void __launch_bounds__(32) decode_pair_kernel(DecodeJob j, int nst) {
+  extern __shared__ __align__(128) uint8_t ring[];
+  __shared__ uint64_t full[kBulkMaxStages];
+  __shared__ int abort_flag;
+  constexpr int KP = kPairKeys;
+
+  const int lane = threadIdx.x;
+  const int pair = lane >> 3, grp = lane & 7;
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int G = j.H / j.Hkv;
+  const int ngroups = G / 8;
+  const int hkv = blockIdx.y / ngroups;
+  const int g0 = (blockIdx.y % ngroups) * 8;
+  const int D = j.D;
+
+  const int n = j.cache_len[b];
+  if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) {
+    if (lane == 0 && split == 0 && blockIdx.y == 0) report(j.status, ATTN_DEV_LENGTH);
+    return;
+  }
+  const int nlive = j.window > 0 ? min(n, j.window) : n;
+  const int nsplit_b = (nlive + j.chunk - 1) / j.chunk;
+  const int k0 = split * j.chunk;
+  if (k0 >= nlive) return;
+  const int k1 = min(k0 + j.chunk, nlive);
+  const int nb = (k1 - k0 + KP - 1) / KP;
+
+  const long head_off = ((long)b * j.Hkv + hkv) * j.capacity * D;
+  const float* kbase = j.k_cache + head_off;
+  const float* vbase = j.v_cache + head_off;
+  const uint32_t part_bytes = KP * D * 4;
+  auto issue = [&](int t) {                   // lane 0: batch t into stage t % nst
+    const int s = t % nst;
+    const int kb = k0 + t * KP;
+    const uint32_t bytes = static_cast<uint32_t>(min(KP, k1 - kb)) * D * 4;
+    tc::mbar_arrive_expect_tx(&full[s], 2 * bytes);
+    tc::bulk_load(ring + 2 * s * part_bytes, kbase + (long)kb * D, bytes, &full[s]);
+    tc::bulk_load(ring + (2 * s + 1) * part_bytes, vbase + (long)kb * D, bytes, &full[s]);
+  };
+  if (lane == 0) {
+    for (int s = 0; s < nst; ++s) tc::mbar_init(&full[s], 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  __syncwarp();
+  if (lane == 0)
+    for (int t = 0; t < min(nst, nb); ++t) issue(t);
+
+  // this lane's 16 dims of a row (zeros past D)
+  auto load16 = [&](const float* row, float* r) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int d = 32 * c + 4 * grp;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (d < D) t = *reinterpret_cast<const float4*>(row + d);
+      r[4 * c] = t.x; r[4 * c + 1] = t.y; r[4 * c + 2] = t.z; r[4 * c + 3] = t.w;
+    }
+  };
+  float q[2][16], o[2][16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float* qr = j.q + ((long)b * j.H + hkv * G + g0 + 2 * pair + h) * D;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int d = 32 * c + 4 * grp;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (d < D) t = __ldg(reinterpret_cast<const float4*>(qr + d));
+      q[h][4 * c] = t.x * j.scale; q[h][4 * c + 1] = t.y * j.scale;
+      q[h][4 * c + 2] = t.z * j.scale; q[h][4 * c + 3] = t.w * j.scale;
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e) o[h][e] = 0.f;
+  }
+  const bool capped = j.softcap > 0.f;
+  const float cap_k = capped ? 2.0f * kLog2e / j.softcap : 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+  int t = 0;
+  for (; t < nb; ++t) {
+    const int s = t % nst;
+    const bool ok = tc::mbar_wait(&full[s], (t / nst) & 1, &abort_flag);
+    if (__any_sync(0xffffffffu, !ok)) break;
+    const int valid = min(KP, k1 - (k0 + t * KP));
+    const float* sk = reinterpret_cast<const float*>(ring + 2 * s * part_bytes);
+    const float* sv = reinterpret_cast<const float*>(ring + (2 * s + 1) * part_bytes);
+    float sc[2][KP];
+#pragma unroll
+    for (int u = 0; u < KP; ++u) {
+      float kr[16];
+      load16(sk + u * D, kr);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc = fmaf(q[h][e], kr[e], acc);
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (capped) acc = softcap_apply(acc, j.softcap, cap_k);
+        sc[h][u] = u < valid ? acc * kLog2e : -INFINITY;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float mx = sc[h][0];
+#pragma unroll
+      for (int u = 1; u < KP; ++u) mx = fmaxf(mx, sc[h][u]);
+      const float m_new = fmaxf(m_run[h], mx);
+      const float corr = m_new == -INFINITY ? 1.f : exp2f(m_run[h] - m_new);
+      float ls = 0.f;
+#pragma unroll
+      for (int u = 0; u < KP; ++u) {
+        sc[h][u] = m_new == -INFINITY ? 0.f : exp2f(sc[h][u] - m_new);
+        ls += sc[h][u];
+      }
+      l_run[h] = l_run[h] * corr + ls;
+      m_run[h] = m_new;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) o[h][e] *= corr;
+    }
+#pragma unroll
+    for (int u = 0; u < KP; ++u) {
+      if (u < valid) {                        // slots past the copied rows hold stale bytes
+        float vr[16];
+        load16(sv + u * D, vr);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int e = 0; e < 16; ++e) o[h][e] = fmaf(sc[h][u], vr[e], o[h][e]);
+      }
+    }
+    __syncwarp();                             // every lane is done reading stage s
+    if (lane == 0 && t + nst < nb) issue(t + nst);
+  }
+  if (t < nb) {
+    // A wait ran out: let the copies already issued land, then report.
+    if (lane == 0) {
+      for (int u = t; u < min(nb, t + nst); ++u) {
+        const uint64_t t0 = tc::globaltimer();
+        while (!tc::mbar_try_wait(&full[u % nst], (u / nst) & 1))
+          if (tc::globaltimer() - t0 > tc::kWaitLimitNs) break;
+      }
+      report(j.status, ATTN_DEV_TIMEOUT);
+    }
+    return;
+  }
+
+  const bool single = nsplit_b == 1;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const long hrow = (long)b * j.H + hkv * G + g0 + 2 * pair + h;
+    const float inv = 1.0f / l_run[h];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int d = 32 * c + 4 * grp;
+      if (d >= D) continue;
+      if (single) {
+        *reinterpret_cast<float4*>(j.out + hrow * D + d) =
+            make_float4(o[h][4 * c] * inv, o[h][4 * c + 1] * inv, o[h][4 * c + 2] * inv,
+                        o[h][4 * c + 3] * inv);
+      } else {
+        const long pi = hrow * j.nsplit + split;
+        *reinterpret_cast<float4*>(j.partial + pi * D + d) =
+            make_float4(o[h][4 * c], o[h][4 * c + 1], o[h][4 * c + 2], o[h][4 * c + 3]);
+      }
+    }
+    if (!single && grp == 0) {
+      const long pi = hrow * j.nsplit + split;
+      float* ml = j.partial + (long)j.B * j.H * j.nsplit * D;
+      ml[2 * pi] = m_run[h];
+      ml[2 * pi + 1] = l_run[h];
+    }
+  }
+}
+
 // Batches of KW = 8 keys (32 / GT when that is smaller) and about 16 KB of
 // ring per block: 13 one-warp blocks per SM at D = 128. Measured on the
 // batched-decode workload, wider rings (fewer blocks) and narrower batches
@@ -515,6 +701,16 @@ static cudaError_t launch_gt(const DecodeJob& j, cudaStream_t stream) {
 
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream) {
   const int G = j.H / j.Hkv;
+  if (G % 8 == 0 && j.D % 4 == 0 && j.D <= 128) {
+    const int stage = 2 * kPairKeys * j.D * 4;
+    int nst = kBulkStageBudget / stage;
+    nst = nst < 2 ? 2 : (nst > kBulkMaxStages ? kBulkMaxStages : nst);
+    decode_pair_kernel<<<dim3(j.nsplit, j.Hkv * (G / 8), j.B), 32, nst * stage, stream>>>(j, nst);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || j.nsplit <= 1) return e;
+    decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);
+    return cudaGetLastError();
+  }
   if (G == 1) return launch_gt<1>(j, stream);
   if (G == 2) return launch_gt<2>(j, stream);
   if (G <= 4) return launch_gt<4>(j, stream);

@@ -202,6 +202,10 @@ DECODE_CASES = [
     (2, 16, 2, 256, 300, 0, 20.0, (300, 100)),
     (1, 4, 4, 128, 5000, 0, 0.0, (4097,)),
     (2, 8, 4, 128, 96, 96, 0.0, (3000, 17)),
+    # groups of 8 or more query heads (the head-pair kernel)
+    (2, 16, 2, 64, 256, 256, 30.0, (1000, 3)),
+    (3, 32, 2, 128, 600, 0, 0.0, (600, 1, 65)),
+    (2, 8, 1, 40, 90, 0, 0.0, (90, 9)),
 ]
 
 
