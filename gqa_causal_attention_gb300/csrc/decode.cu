@@ -479,15 +479,23 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
 // row by the 8 groups fall on distinct banks). A score is summed over the 8
 // lanes of its pair (3 shuffles), which then all hold it, so the running
 // maximum, the sum and P V need no further exchange.
-constexpr int kPairKeys = 8;                  // keys per stage
+// Shared memory per warp: its ring, at least the 36 floats per lane it hands to
+// warp 0 at the end.
+__host__ __device__ inline uint32_t pair_ring_stride(int nst, uint32_t part_bytes) {
+  const uint32_t ring = static_cast<uint32_t>(nst) * 2 * part_bytes, merge = 36u * 32 * 4;
+  return ((ring > merge ? ring : merge) + 127) / 128 * 128;
+}
 
-__global__ void __launch_bounds__(32) decode_pair_kernel(DecodeJob j, int nst) {
-  extern __shared__ __align__(128) uint8_t ring[];
-  __shared__ uint64_t full[kBulkMaxStages];
+// NW warps per block share one split: warp w takes batches w, w + NW, ... of
+// it through its own ring, and the warps' running (max, sum, O) are merged in
+// shared memory at the end, so a split costs one partial result whatever NW is.
+template <int NW, int KP>
+__global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int nst) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t full_all[NW][kBulkMaxStages];
   __shared__ int abort_flag;
-  constexpr int KP = kPairKeys;
 
-  const int lane = threadIdx.x;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int pair = lane >> 3, grp = lane & 7;
   const int split = blockIdx.x, b = blockIdx.z;
   const int G = j.H / j.Hkv;
@@ -498,36 +506,40 @@ __global__ void __launch_bounds__(32) decode_pair_kernel(DecodeJob j, int nst) {
 
   const int n = j.cache_len[b];
   if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) {
-    if (lane == 0 && split == 0 && blockIdx.y == 0) report(j.status, ATTN_DEV_LENGTH);
-    return;
+    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) report(j.status, ATTN_DEV_LENGTH);
+    return;                                   // the whole block leaves together
   }
   const int nlive = j.window > 0 ? min(n, j.window) : n;
   const int nsplit_b = (nlive + j.chunk - 1) / j.chunk;
   const int k0 = split * j.chunk;
   if (k0 >= nlive) return;
   const int k1 = min(k0 + j.chunk, nlive);
-  const int nb = (k1 - k0 + KP - 1) / KP;
+  const int nb = (k1 - k0 + KP - 1) / KP;                 // batches of the split
+  const int nbw = nb > warp ? (nb - warp + NW - 1) / NW : 0;   // this warp's: warp + NW i
 
   const long head_off = ((long)b * j.Hkv + hkv) * j.capacity * D;
   const float* kbase = j.k_cache + head_off;
   const float* vbase = j.v_cache + head_off;
   const uint32_t part_bytes = KP * D * 4;
-  auto issue = [&](int t) {                   // lane 0: batch t into stage t % nst
-    const int s = t % nst;
-    const int kb = k0 + t * KP;
+  const uint32_t stride = pair_ring_stride(nst, part_bytes);
+  uint8_t* ring = smem + warp * stride;
+  uint64_t* full = full_all[warp];
+  auto issue = [&](int i) {                   // lane 0: this warp's batch i into stage i % nst
+    const int s = i % nst;
+    const int kb = k0 + (warp + NW * i) * KP;
     const uint32_t bytes = static_cast<uint32_t>(min(KP, k1 - kb)) * D * 4;
     tc::mbar_arrive_expect_tx(&full[s], 2 * bytes);
     tc::bulk_load(ring + 2 * s * part_bytes, kbase + (long)kb * D, bytes, &full[s]);
     tc::bulk_load(ring + (2 * s + 1) * part_bytes, vbase + (long)kb * D, bytes, &full[s]);
   };
+  if (threadIdx.x == 0) abort_flag = 0;
   if (lane == 0) {
     for (int s = 0; s < nst; ++s) tc::mbar_init(&full[s], 1);
-    abort_flag = 0;
     tc::fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
   if (lane == 0)
-    for (int t = 0; t < min(nst, nb); ++t) issue(t);
+    for (int i = 0; i < min(nst, nbw); ++i) issue(i);
 
   // this lane's 16 dims of a row (zeros past D)
   auto load16 = [&](const float* row, float* r) {
@@ -558,12 +570,12 @@ __global__ void __launch_bounds__(32) decode_pair_kernel(DecodeJob j, int nst) {
   const float cap_k = capped ? 2.0f * kLog2e / j.softcap : 0.f;
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
-  int t = 0;
-  for (; t < nb; ++t) {
-    const int s = t % nst;
-    const bool ok = tc::mbar_wait(&full[s], (t / nst) & 1, &abort_flag);
+  int i = 0;
+  for (; i < nbw; ++i) {
+    const int s = i % nst;
+    const bool ok = tc::mbar_wait(&full[s], (i / nst) & 1, &abort_flag);
     if (__any_sync(0xffffffffu, !ok)) break;
-    const int valid = min(KP, k1 - (k0 + t * KP));
+    const int valid = min(KP, k1 - (k0 + (warp + NW * i) * KP));
     const float* sk = reinterpret_cast<const float*>(ring + 2 * s * part_bytes);
     const float* sv = reinterpret_cast<const float*>(ring + (2 * s + 1) * part_bytes);
     float sc[2][KP];
@@ -573,9 +585,13 @@ __global__ void __launch_bounds__(32) decode_pair_kernel(DecodeJob j, int nst) {
       load16(sk + u * D, kr);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;             // two chains: half the dependent FMA depth
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc = fmaf(q[h][e], kr[e], acc);
+        for (int e = 0; e < 16; e += 2) {
+          a0 = fmaf(q[h][e], kr[e], a0);
+          a1 = fmaf(q[h][e + 1], kr[e + 1], a1);
+        }
+        float acc = a0 + a1;
 #pragma unroll
         for (int off = 1; off < 8; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (capped) acc = softcap_apply(acc, j.softcap, cap_k);
@@ -612,20 +628,51 @@ __global__ void __launch_bounds__(32) decode_pair_kernel(DecodeJob j, int nst) {
       }
     }
     __syncwarp();                             // every lane is done reading stage s
-    if (lane == 0 && t + nst < nb) issue(t + nst);
+    if (lane == 0 && i + nst < nbw) issue(i + nst);
   }
-  if (t < nb) {
+  const bool timed_out = i < nbw;
+  if (timed_out && lane == 0) {
     // A wait ran out: let the copies already issued land, then report.
-    if (lane == 0) {
-      for (int u = t; u < min(nb, t + nst); ++u) {
-        const uint64_t t0 = tc::globaltimer();
-        while (!tc::mbar_try_wait(&full[u % nst], (u / nst) & 1))
-          if (tc::globaltimer() - t0 > tc::kWaitLimitNs) break;
-      }
-      report(j.status, ATTN_DEV_TIMEOUT);
+    for (int u = i; u < min(nbw, i + nst); ++u) {
+      const uint64_t t0 = tc::globaltimer();
+      while (!tc::mbar_try_wait(&full[u % nst], (u / nst) & 1))
+        if (tc::globaltimer() - t0 > tc::kWaitLimitNs) break;
     }
-    return;
+    report(j.status, ATTN_DEV_TIMEOUT);
   }
+
+  if (NW > 1) {
+    // Merge: warps 1.. leave (m, l, O) in their (now idle) ring, warp 0 folds them in.
+    // Every warp reaches the barrier, also after a timeout.
+    __syncthreads();                          // all rings idle
+    float* xs = reinterpret_cast<float*>(ring) + lane * 36;
+    if (warp > 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        xs[h] = m_run[h];
+        xs[2 + h] = l_run[h];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) xs[4 + 16 * h + e] = o[h][e];
+      }
+    }
+    __syncthreads();
+    if (warp > 0) return;
+    for (int w = 1; w < NW; ++w) {
+      const float* ys = reinterpret_cast<const float*>(smem + w * stride) + lane * 36;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float m2 = ys[h];
+        const float M = fmaxf(m_run[h], m2);
+        if (M == -INFINITY) continue;         // neither warp saw a key
+        const float f1 = exp2f(m_run[h] - M), f2 = exp2f(m2 - M);
+        l_run[h] = l_run[h] * f1 + ys[2 + h] * f2;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) o[h][e] = o[h][e] * f1 + ys[4 + 16 * h + e] * f2;
+        m_run[h] = M;
+      }
+    }
+  }
+  if (__any_sync(0xffffffffu, timed_out) || abort_flag) return;
 
   const bool single = nsplit_b == 1;
 #pragma unroll
@@ -661,6 +708,7 @@ __global__ void __launch_bounds__(32) decode_pair_kernel(DecodeJob j, int nst) {
 // (more per-batch overhead) were both slower.
 constexpr int kBulkKeys = 8;
 constexpr int kBulkStageBudget = 16 * 1024;   // ring bytes per block (at least 2 stages)
+constexpr int kPairWarps = 1, kPairKeys = 8;   // head-pair kernel: warps per split, keys per batch
 
 template <int GT, int NC>
 static cudaError_t launch_bulk(const DecodeJob& j, dim3 grid, cudaStream_t stream) {
@@ -702,10 +750,15 @@ static cudaError_t launch_gt(const DecodeJob& j, cudaStream_t stream) {
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream) {
   const int G = j.H / j.Hkv;
   if (G % 8 == 0 && j.D % 4 == 0 && j.D <= 128) {
-    const int stage = 2 * kPairKeys * j.D * 4;
-    int nst = kBulkStageBudget / stage;
-    nst = nst < 2 ? 2 : (nst > kBulkMaxStages ? kBulkMaxStages : nst);
-    decode_pair_kernel<<<dim3(j.nsplit, j.Hkv * (G / 8), j.B), 32, nst * stage, stream>>>(j, nst);
+    // One warp per split with a 2-stage ring of 8-key batches (16 KB at D = 128).
+    // Measured on the long carried decode (B = 8, 64 query heads over 8 KV heads,
+    // 1-2 k cached positions): 2 or 4 warps per split and 4-key batches were no
+    // faster; every setting stays near 3 TB/s there.
+    constexpr int NW = kPairWarps, KP = kPairKeys;
+    const int nst = 2;
+    const uint32_t smem = NW * pair_ring_stride(nst, KP * j.D * 4);
+    decode_pair_kernel<NW, KP>
+        <<<dim3(j.nsplit, j.Hkv * (G / 8), j.B), 32 * NW, smem, stream>>>(j, nst);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || j.nsplit <= 1) return e;
     decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);
