@@ -34,9 +34,12 @@ namespace {
 
 using namespace prefill;
 
-template <int DP_>
+// RAGGED_: per-row lengths (gqa_attn_prefill_ragged); a separate instantiation,
+// so the other calls keep the code (and instruction-cache footprint) without it.
+template <int DP_, bool RAGGED_ = false>
 struct PCfg {
   static constexpr int DP = DP_;
+  static constexpr bool RAGGED = RAGGED_;
   static constexpr int BK = 128;                        // keys per block
   static constexpr int kChunks = DP / 32;
   static constexpr int kKChunk = BK * 128;              // 128 rows x 128 B (K block or Q tile)
@@ -92,7 +95,7 @@ __device__ __forceinline__ PUnit get_unit(const TcArgs& a, int x) {
   u.h = bh % a.H;
   u.q0 = (a.QT - 1 - rank) * kBM;
   const int off = a.kv_off ? a.kv_off[u.b] : 0;
-  const int Lb = row_len(a, u.b);
+  const int Lb = C::RAGGED ? row_len(a, u.b) : a.L;
   u.qk0 = u.q0 + off;
   u.klast = off + Lb - 1;
   const int lo = a.window > 0 ? max(0, u.qk0 - a.window + 1) / C::BK : 0;
@@ -106,7 +109,7 @@ __device__ __forceinline__ PUnit get_unit(const TcArgs& a, int x) {
 // past the end); every role walks the same sequence.
 template <class C>
 __device__ __forceinline__ int next_live(const TcArgs& a, int r) {
-  if (!a.lengths) return r;                     // without lengths no unit is empty
+  if (!C::RAGGED) return r;                     // without lengths no unit is empty
   for (;; ++r) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
     if (x >= a.units || get_unit<C>(a, x).n > 0) return r;
@@ -527,7 +530,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       tc::fence_after_sync();
       const uint32_t scol = lane_base + C::kSCol + buf * BK;
       const int k0 = (u.jlo + i) * BK;
-      const int hi = min(qpos, u.klast) - k0;                       // visible: c <= hi
+      const int hi = (C::RAGGED ? min(qpos, u.klast) : qpos) - k0;  // visible: c <= hi
       const int lo = a.window > 0 ? qpos - a.window + 1 - k0 : -1;  // visible: c >= lo
       // Boundary blocks (the causal diagonal, a window's edge): softcap and the
       // band mask are applied in tensor memory first, 32 columns at a time in a
@@ -640,7 +643,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
     tmem_ld_row<C::DP>(lane_base + C::kOCol, o);
     tc::fence_before_sync();
     tc::mbar_arrive(&bars->o_free);
-    const bool real = qpos <= u.klast;
+    const bool real = !C::RAGGED || qpos <= u.klast;
     const float inv = real ? 1.0f / l : 0.f;
     store_rows(u, [&](int c) {
       return real ? make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv)
@@ -651,7 +654,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
     r = rn;
   }
   // Units with no real row (ragged batch): zeros.
-  if (ok && a.lengths) {
+  if (C::RAGGED && ok) {
     for (int r = 0;; ++r) {
       const int x = unit_of(blockIdx.x, r, gridDim.x);
       if (x >= a.units) break;
@@ -663,13 +666,13 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
   __syncwarp();
 }
 
-template <int DP, bool ROPE>
+template <int DP, bool ROPE, bool RAGGED>
 __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     prefill_tq_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o, const TcArgs a) {
-  using C = PCfg<DP>;
+  using C = PCfg<DP, RAGGED>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* skv = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -753,13 +756,13 @@ int sm_count() {
   return n;
 }
 
-template <int DP, bool ROPE>
+template <int DP, bool ROPE, bool RAGGED>
 cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
-  using C = PCfg<DP>;
+  using C = PCfg<DP, RAGGED>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tq_kernel<DP, ROPE>,
+    attr_err = cudaFuncSetAttribute(prefill_tq_kernel<DP, ROPE, RAGGED>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -793,8 +796,14 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   a.Lk = Lk;
   a.lengths = s.lengths;
   const int grid = a.units < sm_count() ? a.units : sm_count();
-  prefill_tq_kernel<DP, ROPE><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
+  prefill_tq_kernel<DP, ROPE, RAGGED><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
+}
+
+// The ragged instantiation only when the call has lengths.
+template <int DP, bool ROPE>
+cudaError_t launch_tq_r(const AttnShape& s, cudaStream_t stream) {
+  return s.lengths ? launch_tq<DP, ROPE, true>(s, stream) : launch_tq<DP, ROPE, false>(s, stream);
 }
 
 }  // namespace
@@ -807,10 +816,11 @@ bool prefill_tq_supports_kv_off(int D) { return D % 4 == 0 && D >= 32 && D <= 12
 cudaError_t launch_prefill_tq(const AttnShape& s, cudaStream_t stream) {
   switch ((s.D + 31) / 32) {
     // with q RoPE fused (R % 64 == 0, so D >= 64) or without
-    case 1: return s.rope.table ? cudaErrorNotSupported : launch_tq<32, false>(s, stream);
-    case 2: return s.rope.table ? launch_tq<64, true>(s, stream) : launch_tq<64, false>(s, stream);
-    case 3: return s.rope.table ? launch_tq<96, true>(s, stream) : launch_tq<96, false>(s, stream);
-    case 4: return s.rope.table ? launch_tq<128, true>(s, stream) : launch_tq<128, false>(s, stream);
+    case 1: return s.rope.table ? cudaErrorNotSupported : launch_tq_r<32, false>(s, stream);
+    case 2: return s.rope.table ? launch_tq_r<64, true>(s, stream) : launch_tq_r<64, false>(s, stream);
+    case 3: return s.rope.table ? launch_tq_r<96, true>(s, stream) : launch_tq_r<96, false>(s, stream);
+    case 4: return s.rope.table ? launch_tq_r<128, true>(s, stream)
+                                : launch_tq_r<128, false>(s, stream);
     default: return cudaErrorNotSupported;
   }
 }
