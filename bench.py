@@ -77,7 +77,7 @@ def peaks():
 # current kernels (profiles/); None where no capture of the timed kernel exists.
 # The decode capture ran on 16 of the 64 rows; its traffic scales with the
 # algorithmic bytes processed (ratio below).
-NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 350.916352e6 + 94.417408e6}
+NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 348.996352e6 + 96.940032e6}
 NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903360e6 + 4.927232e6) / 585572352.0
 
 
