@@ -59,7 +59,7 @@ struct AttnShape {
   float scale;              // > 0
   int32_t* status;
   QRope rope;               // rope.table == nullptr: q already rotated
-  // Continuing a cached prefix (D <= 128 kernel only): k and vt then hold Lk
+  // Continuing a cached prefix (persistent kernel, D <= 256): k and vt then hold Lk
   // key rows per head, kv_off[b] of them before query row 0 of row b.
   const int32_t* kv_off = nullptr;
   int Lk = 0;               // 0: the chunk's own keys (Lk = L)
@@ -100,7 +100,7 @@ struct GatherJob {
 cudaError_t launch_gather_kv(const GatherJob& j, cudaStream_t stream);
 bool prefill_tq_supports_kv_off(int D);
 int prefill_vt_pitch(int L);   // row pitch (floats) of the V^T workspace
-cudaError_t launch_prefill_tq(const AttnShape& a, cudaStream_t stream);  // D <= 128
+cudaError_t launch_prefill_tq(const AttnShape& a, cudaStream_t stream);  // 32 <= D <= 256
 bool prefill_fuses_rope(int D);  // the kernel taking D applies a.rope itself
 
 struct DecodeJob {

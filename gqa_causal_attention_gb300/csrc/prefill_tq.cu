@@ -1,15 +1,21 @@
-// Persistent tensor-core prefill for head dimensions up to 128.
+// Persistent tensor-core prefill for head dimensions 32..256 (multiples of 4).
 //
-// Same computation as prefill_tc.cu ("Core Layers -- Deep Reference", "Flash
-// Attention"; causal or windowed mask of "mojolearn.transformer"), organised
-// for GB300 throughput:
+// What it computes: "Core Layers -- Deep Reference", "Flash Attention" -- the
+// exact softmax(Q K^T) V of the causal (or windowed, "mojolearn.transformer"
+// window) mask without materialising the score matrix, the query heads of one
+// key/value head reading the same K and V ("MHA and GQA").
+//
+// How, on GB300:
 //  * One block per SM walks a list of work units (one 128-row query tile of
 //    one head each), heaviest tiles first, in snake order across blocks.
 //  * Q sits in tensor memory as the A operand of S = Q K^T, so the MMA reads
 //    only K (and later V^T) from shared memory; blocks of 128 keys give
-//    M128 N128 K8 TF32 instructions, which run at the full tensor rate.
+//    M128 N128 K8 TF32 instructions (kind::tf32: fp32 data, TF32 products,
+//    fp32 accumulation), which run at the full tensor rate.
 //    TMEM = Q | O | S0 | S1 (S double-buffered: S of the next key block is
-//    computed while softmax turns this one into P).
+//    computed while softmax turns this one into P). Head dims past 128 keep
+//    only Q's first 128 dims in tensor memory and the rest in shared memory
+//    (see PCfg), with 64-key blocks.
 //  * TMA streams Q tiles, K blocks and V^T blocks of successive units through
 //    one ring of stages; a unit's Q tile enters right after the previous
 //    unit's last K block. The S issuer moves it to tensor memory with
@@ -17,12 +23,15 @@
 //    stage early; the next unit's first S products then overlap the previous
 //    unit's last softmax and its epilogue. With q RoPE fused
 //    (gqa_attn_prefill_rope) the softmax warps normalise and rotate the tile in
-//    tensor memory after the previous unit's last P.
+//    tensor memory after the previous unit's last P. Out-of-range rows and
+//    columns arrive as zeros; key blocks outside the causal/window band are
+//    never loaded.
 //  * S = Q K^T and O += P V^T come from two issuing threads on different SM
 //    sub-partitions, each sharing its sub-partition with one softmax warp.
-//  * Softmax, masking, softcap, rescaling and the epilogue are those of the
-//    non-persistent kernel (one query row per thread, base-2 online softmax,
-//    P truncated to TF32 in place of S).
+//  * Four softmax warps own one query row per thread: they read S from tensor
+//    memory, apply scale, softcap and mask, keep the running maximum and sum
+//    (base 2), and write P (truncated to TF32) back over S. O is rescaled in
+//    tensor memory only when the running maximum grows by more than 2^8.
 //  * Every pipeline wait is bounded; a wait that runs out reports
 //    ATTN_DEV_TIMEOUT and the block winds down (drains its copies and MMAs,
 //    frees its tensor memory).
@@ -36,26 +45,50 @@ using namespace prefill;
 
 // RAGGED_: per-row lengths (gqa_attn_prefill_ragged); a separate instantiation,
 // so the other calls keep the code (and instruction-cache footprint) without it.
+// WIDE (head dims 160..256): Q and O of a whole head cannot both sit in the 512
+// TMEM columns, so Q is split: dims 0..127 (Q_a) in tensor memory and the rest
+// (Q_b) in a shared-memory buffer outside the ring, read as the A operand of the
+// second half of S = Q K^T. TMEM = Q_a 128 | O DP | S 2 x 64 columns (64-key
+// blocks). Ring stages are 32 KB: Q_a crosses as two 64-column parts, a K block
+// as two 128-column parts, V^T as one item per 32 keys.
 template <int DP_, bool RAGGED_ = false>
 struct PCfg {
-  static constexpr int DP = DP_;
+  static constexpr int DP = DP_;                        // head dim padded to 32: Q, K, O width
   static constexpr bool RAGGED = RAGGED_;
-  static constexpr int BK = 128;                        // keys per block
-  static constexpr int kChunks = DP / 32;
-  static constexpr int kKChunk = BK * 128;              // 128 rows x 128 B (K block or Q tile)
+  static constexpr bool WIDE = DP > 128;
+  static constexpr int BK = WIDE ? 64 : 128;            // keys per block
+  static constexpr int kChunks = DP / 32;               // 32-column chunks of Q and K
+  static constexpr int kQaChunks = WIDE ? 4 : kChunks;  // Q chunks in tensor memory
+  static constexpr int kQPC = WIDE ? 2 : kChunks;       // Q chunks per ring item
+  static constexpr int kKPC = WIDE ? 4 : kChunks;       // K chunks per ring item
+  static constexpr int kVPC = WIDE ? 1 : BK / 32;       // 32-key V^T chunks per ring item
+  static constexpr int QP = kQaChunks / kQPC;           // ring items per Q tile
+  static constexpr int KP = (kChunks + kKPC - 1) / kKPC;  // ring items per K block
+  static constexpr int VI = BK / 32 / kVPC;             // ring items per V^T block
+  static constexpr int kQChunk = kBM * 128;             // 128 rows x 128 B of Q
+  static constexpr int kKChunk = BK * 128;              // BK rows x 128 B of K
   static constexpr int kVtChunk = DP * 128;             // DP rows x 128 B (32 keys of V^T)
-  static constexpr int kStage = kChunks * kKChunk;      // one K block, V^T block or Q tile
+  static constexpr int kQBytes = kQPC * kQChunk;
+  static constexpr int kKBytes = kKPC * kKChunk;
+  static constexpr int kVBytes = kVPC * kVtChunk;
+  static constexpr int kStage =                         // one Q part, K part or V^T item
+      kQBytes > kKBytes ? (kQBytes > kVBytes ? kQBytes : kVBytes)
+                        : (kKBytes > kVBytes ? kKBytes : kVBytes);
+  static constexpr int kQb = (kChunks - kQaChunks) * kQChunk;   // Q_b buffer (WIDE)
   static constexpr int kEpi = 4 * 4096;                 // per-warp 32 x 32 output staging
-  static constexpr int kTab = 32 * 64 * 8;              // RoPE table rows 0..31, up to 64 pairs
-  static constexpr int kNSraw = (kSmemLimit - 2048 - kEpi - kTab) / kStage;
+  static constexpr int kTab = WIDE ? 0 : 32 * 64 * 8;   // RoPE table rows 0..31, up to 64 pairs
+  static constexpr int kNSraw = (kSmemLimit - 2048 - kEpi - kTab - kQb) / kStage;
   static constexpr int NS = kNSraw > 8 ? 8 : kNSraw;
   static constexpr int kThreads = 64 + 128 + 32;     // producer, S issuer, 4 softmax, P V issuer
-  static constexpr int kSmemNeed = NS * kStage + kEpi + kTab + 2048;
+  static constexpr int kSmemNeed = NS * kStage + kQb + kEpi + kTab + 2048;
   static constexpr int kSmem =
       kSmemNeed > kSmemLimit / 2 + 4096 ? kSmemNeed : kSmemLimit / 2 + 4096;
-  static constexpr int kQCol = 0, kOCol = DP, kSCol = 2 * DP;
-  static_assert(NS >= 3, "ring too short");
-  static_assert(DP % 32 == 0, "epilogue tiles alternate across units: DP / 16 must be even");
+  static constexpr int kQCol = 0, kOCol = kQaChunks * 32, kSCol = kOCol + DP;
+  // The issuers' ring waits stay alias-free (see the producer's ring order)
+  // from 3 stages with one-item Q tiles, K and V^T blocks, and from 4 with the
+  // WIDE parts.
+  static_assert(NS >= (WIDE ? 4 : 3), "ring too short");
+  static_assert(DP % 32 == 0 && DP <= 256, "head dim: 32-column chunks, an even number of output boxes");
   static_assert(kSCol + 2 * BK <= kTmemCols, "tensor memory budget");
   static_assert(kSmem <= kSmemLimit, "shared memory budget");
 };
@@ -70,6 +103,8 @@ struct PBars {
   uint64_t o_free;
   uint64_t q_copied;                           // a Q tile is in tensor memory (one phase per unit)
   uint64_t q_ready;                            // fused RoPE: that Q tile is rotated
+  uint64_t qb_full;                            // WIDE: a Q_b tile landed (one phase per tile)
+  uint64_t qb_empty;                           // WIDE: the S products reading Q_b are done
   uint64_t drain[2];                           // each issuer's MMAs and copies done
   uint32_t tmem_base;
   int abort;
@@ -119,12 +154,19 @@ __device__ __forceinline__ int next_live(const TcArgs& a, int r) {
 // ---------------------------------------------------------------- producer (one thread)
 // Ring order: the first unit's Q tile; then per unit K_0 .. K_{n-1} interleaved
 // with V^T_0 .. V^T_{n-1} as K_0, (K_{i+1}, V^T_i)..., with the next unit's Q
-// tile right after the last K block, so it lands while this unit's last P V
-// products are pending and the softmax warps can move it to tensor memory
-// before the next unit's first S = Q K^T.
+// tile right after the last K block (WIDE: its Q_a parts right before the last
+// V^T block), so it lands while this unit's last P V products are pending and
+// moves to tensor memory before the next unit's first S = Q K^T. WIDE: a Q_a
+// tile, K block or V^T block is several items, and the next Q_b tile is loaded
+// into its own buffer after the last V^T block, once the S products that read
+// the current one are done. These orders keep every issuer's ring wait
+// alias-free: when an issuer waits for the k-th fill of a stage, the (k-1)-th
+// has landed, either as one of its own items or as shown by the cross-role
+// barrier it waited on first (checked for all unit sequences of up to 4 units
+// of 1..5 blocks, 3..8 stages one-item, 4..6 stages WIDE).
 template <class C>
 __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtensorMap* tk,
-                            const CUtensorMap* tv, uint8_t* skv, PBars* bars) {
+                            const CUtensorMap* tv, uint8_t* skv, uint8_t* sqb, PBars* bars) {
   volatile int* abort = &bars->abort;
   tc::tma_prefetch(tq);
   tc::tma_prefetch(tk);
@@ -135,23 +177,27 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
   bool filled[8];
 #pragma unroll
   for (int s = 0; s < 8; ++s) filled[s] = false;
-  // kind: 0 = Q tile, 1 = K block, 2 = V^T block
-  auto load = [&](int kind, const PUnit& u, int j) -> bool {
+  // kind: 0 = Q part, 1 = K part, 2 = V^T item
+  auto load = [&](int kind, const PUnit& u, int j, int part) -> bool {
     if (!tc::mbar_wait(&bars->kv_empty[stage], phase ^ 1u, abort)) return false;
     uint64_t* full = &bars->kv_full[stage];
-    tc::mbar_arrive_expect_tx(full, C::kStage);
     uint8_t* dst = skv + stage * C::kStage;
     if (kind == 0) {
-      for (int c = 0; c < C::kChunks; ++c)
-        tc::tma_load_3d(dst + c * C::kKChunk, tq, full, 32 * c, u.q0, u.b * a.H + u.h);
+      const int c0 = part * C::kQPC;
+      tc::mbar_arrive_expect_tx(full, C::kQBytes);
+      for (int c = c0; c < c0 + C::kQPC; ++c)
+        tc::tma_load_3d(dst + (c - c0) * C::kQChunk, tq, full, 32 * c, u.q0, u.b * a.H + u.h);
     } else if (kind == 1) {
-      for (int c = 0; c < C::kChunks; ++c)
-        tc::tma_load_3d(dst + c * C::kKChunk, tk, full, 32 * c, j * C::BK,
+      const int c0 = part * C::kKPC, c1 = min(c0 + C::kKPC, C::kChunks);
+      tc::mbar_arrive_expect_tx(full, (c1 - c0) * C::kKChunk);
+      for (int c = c0; c < c1; ++c)
+        tc::tma_load_3d(dst + (c - c0) * C::kKChunk, tk, full, 32 * c, j * C::BK,
                         u.b * a.Hkv + u.h / a.G);
     } else {
-      for (int c = 0; c < C::BK / 32; ++c)
-        tc::tma_load_3d(dst + c * C::kVtChunk, tv, full, j * C::BK + 32 * c, 0,
-                        u.b * a.Hkv + u.h / a.G);
+      tc::mbar_arrive_expect_tx(full, C::kVBytes);
+      for (int c = 0; c < C::kVPC; ++c)
+        tc::tma_load_3d(dst + c * C::kVtChunk, tv, full, j * C::BK + 32 * (part * C::kVPC + c),
+                        0, u.b * a.Hkv + u.h / a.G);
     }
     filled[stage] = true;
     fill_parity[stage] = phase;
@@ -159,6 +205,22 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
       stage = 0;
       phase ^= 1u;
     }
+    return true;
+  };
+  auto load_items = [&](int kind, int items, const PUnit& u, int j) -> bool {
+    for (int p = 0; p < items; ++p)
+      if (!load(kind, u, j, p)) return false;
+    return true;
+  };
+  // WIDE: Q_b of the t-th tile, once the S products of tile t - 1 released the buffer.
+  uint32_t qb_loads = 0;
+  auto load_qb = [&](const PUnit& u) -> bool {
+    if (qb_loads > 0 && !tc::mbar_wait(&bars->qb_empty, (qb_loads - 1) & 1, abort)) return false;
+    tc::mbar_arrive_expect_tx(&bars->qb_full, C::kQb);
+    for (int c = C::kQaChunks; c < C::kChunks; ++c)
+      tc::tma_load_3d(sqb + (c - C::kQaChunks) * C::kQChunk, tq, &bars->qb_full, 32 * c, u.q0,
+                      u.b * a.H + u.h);
+    ++qb_loads;
     return true;
   };
   bool ok = true;
@@ -183,21 +245,27 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
         tc::bulk_prefetch_l2(a.rope_table + p0 * half, static_cast<uint32_t>((p1 - p0) * half * 8));
       }
     }
-    if (first) ok = load(0, u, 0);
-    if (ok) ok = load(1, u, u.jlo);
-    if (ok && u.n == 1 && has_next) ok = load(0, un, 0);
+    if (first) {
+      ok = load_items(0, C::QP, u, 0);
+      if (ok && C::WIDE) ok = load_qb(u);
+    }
+    if (ok) ok = load_items(1, C::KP, u, u.jlo);
+    if (ok && !C::WIDE && u.n == 1 && has_next) ok = load_items(0, C::QP, un, 0);
     for (int i = 0; ok && i < u.n; ++i) {
       if (i + 1 < u.n) {
-        ok = load(1, u, u.jlo + i + 1);
-        if (ok && i + 2 == u.n && has_next) ok = load(0, un, 0);
+        ok = load_items(1, C::KP, u, u.jlo + i + 1);
+        if (ok && !C::WIDE && i + 2 == u.n && has_next) ok = load_items(0, C::QP, un, 0);
       }
-      if (ok) ok = load(2, u, u.jlo + i);
+      if (ok && C::WIDE && i + 1 == u.n && has_next) ok = load_items(0, C::QP, un, 0);
+      if (ok) ok = load_items(2, C::VI, u, u.jlo + i);
     }
+    if (ok && C::WIDE && has_next) ok = load_qb(un);
     r = rn;
   }
   // Every copy this block started lands before the block may exit.
   for (int s = 0; s < C::NS; ++s)
     if (filled[s]) drain_wait(&bars->kv_full[s], fill_parity[s]);
+  if (qb_loads > 0) drain_wait(&bars->qb_full, (qb_loads - 1) & 1);
 }
 
 // ---------------------------------------------------------------- MMA issuers (two threads)
@@ -234,52 +302,71 @@ __device__ __forceinline__ uint64_t stage_desc(uint64_t base_desc, int st) {
 
 // The S issuer: Q tiles to tensor memory (tcgen05.cp) and S = Q K^T.
 template <class C>
-__device__ void tq_mma_s(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* bars) {
+__device__ void tq_mma_s(const TcArgs& a, uint32_t tmem, uint8_t* skv, uint8_t* sqb,
+                         PBars* bars) {
   volatile int* abort = &bars->abort;
   constexpr uint32_t id_s = tc::idesc_tf32(kBM, C::BK, false);
   // Descriptors are built once; an operand offset is added to the start-address
   // field (address >> 4), which stays below 2^14 for any shared-memory address.
   const uint64_t base_desc = tc::sdesc_sw128(tc::smem_u32(skv), 16, 1024);
+  const uint64_t qb_desc = tc::sdesc_sw128(tc::smem_u32(sqb), 16, 1024);
   RingCursor<C> ring;
-  // Q tile: shared -> tensor memory, in pipe order behind the last S that read
-  // the previous Q (so the next unit's S products follow without a wait); its
-  // stage is free once the copy is done.
+  // Q tile (WIDE: Q_a): shared -> tensor memory, in pipe order behind the last S
+  // that read the previous Q (so the next unit's S products follow without a
+  // wait); its stages are free once the copies are done.
   auto copy_q = [&]() -> bool {
-    int st = 0;
-    if (!ring.take(bars, abort, st)) return false;
-    const uint64_t qd = stage_desc<C>(base_desc, st);
 #pragma unroll
-    for (int kk = 0; kk < C::DP / 8; ++kk) {
-      const int c = kk / 4, j = kk % 4;
-      tc::tmem_cp_128x256b(tmem + C::kQCol + 8 * kk, qd + ((c * C::kKChunk + 32 * j) >> 4));
+    for (int p = 0; p < C::QP; ++p) {
+      int st = 0;
+      if (!ring.take(bars, abort, st)) return false;
+      const uint64_t qd = stage_desc<C>(base_desc, st);
+#pragma unroll
+      for (int c = 0; c < C::kQPC; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tc::tmem_cp_128x256b(tmem + C::kQCol + 32 * (p * C::kQPC + c) + 8 * j,
+                               qd + ((c * C::kQChunk + 32 * j) >> 4));
+      tc::mma_commit(&bars->kv_empty[st]);
     }
     tc::mma_commit(&bars->q_copied);
-    tc::mma_commit(&bars->kv_empty[st]);
     return true;
   };
   // S[G % 2] = Q K^T for global block G, once P V of block G - 2 has read that buffer.
   // The o_done wait comes before the ring wait: it also shows that the stage's
   // previous item (possibly a V^T this thread skipped) has landed, so the
-  // parity of the ring wait cannot alias an older fill.
+  // parity of the ring wait cannot alias an older fill. Q chunks past Q_a
+  // (WIDE) are read from the Q_b buffer.
   auto issue_s = [&](uint32_t G) -> bool {
     if (G >= 2 && !tc::mbar_wait(&bars->o_done[G & 1], ((G - 2) >> 1) & 1, abort)) return false;
-    int st = 0;
-    if (!ring.take(bars, abort, st)) return false;
-    tc::fence_after_sync();
     const uint32_t d = tmem + C::kSCol + (G & 1) * C::BK;
-    const uint64_t kd = stage_desc<C>(base_desc, st);
 #pragma unroll
-    for (int kk = 0; kk < C::DP / 8; ++kk) {
-      const int c = kk / 4, off = (kk % 4) * 32;
-      tc::mma_tf32_ts(d, tmem + C::kQCol + 8 * kk, kd + ((c * C::kKChunk + off) >> 4), id_s,
-                      kk > 0);
+    for (int p = 0; p < C::KP; ++p) {
+      int st = 0;
+      if (!ring.take(bars, abort, st)) return false;
+      tc::fence_after_sync();
+      const uint64_t kd = stage_desc<C>(base_desc, st);
+      const int c0 = p * C::kKPC, c1 = min(c0 + C::kKPC, C::kChunks);
+#pragma unroll
+      for (int c = c0; c < c1; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t b = kd + (((c - c0) * C::kKChunk + 32 * j) >> 4);
+          if (c < C::kQaChunks)
+            tc::mma_tf32_ts(d, tmem + C::kQCol + 32 * c + 8 * j, b, id_s, (c | j) != 0);
+          else
+            tc::mma_tf32_ss(d, qb_desc + (((c - C::kQaChunks) * C::kQChunk + 32 * j) >> 4), b,
+                            id_s, 1u);
+        }
+      tc::mma_commit(&bars->kv_empty[st]);
     }
     tc::mma_commit(&bars->s_full[G & 1]);
-    tc::mma_commit(&bars->kv_empty[st]);
     return true;
   };
+  auto skip = [&](int items) {
+    for (int e = 0; e < items; ++e) ring.skip();
+  };
 
-  uint32_t g = 0, uc = 0;       // key blocks and live units done so far by this block
+  uint32_t g = 0, tcnt = 0;     // key blocks and live units done so far by this block
   bool ok = true;
   for (int r = next_live<C>(a, 0); ok;) {
     const int x = unit_of(blockIdx.x, r, gridDim.x);
@@ -287,24 +374,40 @@ __device__ void tq_mma_s(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* ba
     const PUnit u = get_unit<C>(a, x);
     const int rn = next_live<C>(a, r + 1);
     const bool has_next = unit_of(blockIdx.x, rn, gridDim.x) < a.units;
-    if (uc == 0 && !(ok = copy_q())) break;
+    if (tcnt == 0 && !(ok = copy_q())) break;
     // With fused RoPE the softmax warps rotate Q in tensor memory first.
     if (a.rope_table) {
-      if (!(ok = tc::mbar_wait(&bars->q_ready, uc & 1, abort))) break;
+      if (!(ok = tc::mbar_wait(&bars->q_ready, tcnt & 1, abort))) break;
+      tc::fence_after_sync();
+    }
+    if (C::WIDE) {
+      if (!(ok = tc::mbar_wait(&bars->qb_full, tcnt & 1, abort))) break;
       tc::fence_after_sync();
     }
     if (!(ok = issue_s(g))) break;
-    if (u.n == 1 && has_next && !(ok = copy_q())) break;
+    if (!C::WIDE && u.n == 1 && has_next && !(ok = copy_q())) break;
     for (int i = 0; i < u.n; ++i) {
       if (i + 1 < u.n) {
         if (!(ok = issue_s(g + i + 1))) break;
-        if (i + 2 == u.n && has_next && !(ok = copy_q())) break;
+        if (!C::WIDE && i + 2 == u.n && has_next && !(ok = copy_q())) break;
       }
-      ring.skip();                                  // V^T_i: the P V issuer's
+      if (C::WIDE && i + 1 == u.n) {
+        // Q_b is free once this unit's S products are done.
+        tc::mma_commit(&bars->qb_empty);
+        if (has_next) {
+          // The stages the Q_a parts refill last held V^T items up to block
+          // g + i - 1: its P V (which the next S waits for anyway) shows they landed.
+          const uint32_t G = g + i - 1;
+          if (g + i >= 1 && !(ok = tc::mbar_wait(&bars->o_done[G & 1], (G >> 1) & 1, abort)))
+            break;
+          if (!(ok = copy_q())) break;
+        }
+      }
+      skip(C::VI);                                  // V^T_i: the P V issuer's
     }
     if (!ok) break;
     g += u.n;
-    ++uc;
+    ++tcnt;
     r = rn;
   }
   // No MMA or copy of this thread may still run when the block frees its TMEM.
@@ -319,6 +422,9 @@ __device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* b
   constexpr uint32_t id_pv = tc::idesc_tf32(kBM, C::DP, false);
   const uint64_t base_desc = tc::sdesc_sw128(tc::smem_u32(skv), 16, 1024);
   RingCursor<C> ring;
+  auto skip = [&](int items) {
+    for (int e = 0; e < items; ++e) ring.skip();
+  };
   uint32_t g = 0, uc = 0;
   bool ok = true;
   for (int r = next_live<C>(a, 0); ok;) {
@@ -327,32 +433,40 @@ __device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* b
     const PUnit u = get_unit<C>(a, x);
     const int rn = next_live<C>(a, r + 1);
     const bool has_next = unit_of(blockIdx.x, rn, gridDim.x) < a.units;
-    if (uc == 0) ring.skip();                       // the first Q tile
-    ring.skip();                                    // K_0
-    if (u.n == 1 && has_next) ring.skip();          // next Q
+    if (uc == 0) skip(C::QP);                       // the first Q tile
+    skip(C::KP);                                    // K_0
+    if (!C::WIDE && u.n == 1 && has_next) skip(C::QP);       // next Q
     for (int i = 0; i < u.n; ++i) {
       const uint32_t G = g + i;
       if (i + 1 < u.n) {
-        ring.skip();                                // K_{i+1}
-        if (i + 2 == u.n && has_next) ring.skip();  // next Q
+        skip(C::KP);                                // K_{i+1}
+        if (!C::WIDE && i + 2 == u.n && has_next) skip(C::QP);   // next Q
       }
-      // P of block G first: S of block G has then read K_G, the stage's previous
-      // item when no Q tile sits between, so the ring wait below cannot alias.
+      if (C::WIDE && i + 1 == u.n && has_next) skip(C::QP);      // next Q_a
+      // P of block G first: S of block G has then read K_G, so the stage's
+      // previous item has landed and the ring wait below cannot alias.
       if (!(ok = tc::mbar_wait(&bars->p_ready[G & 1], (G >> 1) & 1, abort))) break;
-      int st = 0;
-      if (!(ok = ring.take(bars, abort, st))) break;
-      if (i == 0 && uc > 0 && !(ok = tc::mbar_wait(&bars->o_free, (uc - 1) & 1, abort))) break;
-      tc::fence_after_sync();
-      const uint32_t d = tmem + C::kOCol;
-      const uint64_t vd = stage_desc<C>(base_desc, st);
 #pragma unroll
-      for (int kk = 0; kk < C::BK / 8; ++kk) {
-        const int c = kk / 4, off = (kk % 4) * 32;
-        tc::mma_tf32_ts(d, tmem + C::kSCol + (G & 1) * C::BK + 8 * kk,
-                        vd + ((c * C::kVtChunk + off) >> 4), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
+      for (int v = 0; v < C::VI; ++v) {
+        int st = 0;
+        if (!(ok = ring.take(bars, abort, st))) break;
+        if (v == 0 && i == 0 && uc > 0 &&
+            !(ok = tc::mbar_wait(&bars->o_free, (uc - 1) & 1, abort)))
+          break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + C::kOCol;
+        const uint64_t vd = stage_desc<C>(base_desc, st);
+#pragma unroll
+        for (int kk = 0; kk < 4 * C::kVPC; ++kk) {
+          const int kg = 4 * C::kVPC * v + kk;      // 8-key step within the block
+          const int c = kk / 4, off = (kk % 4) * 32;
+          tc::mma_tf32_ts(d, tmem + C::kSCol + (G & 1) * C::BK + 8 * kg,
+                          vd + ((c * C::kVtChunk + off) >> 4), id_pv, (i > 0 || kg > 0) ? 1u : 0u);
+        }
+        tc::mma_commit(&bars->kv_empty[st]);
       }
+      if (!ok) break;
       tc::mma_commit(&bars->o_done[G & 1]);
-      tc::mma_commit(&bars->kv_empty[st]);
     }
     if (!ok) break;
     tc::mma_commit(&bars->o_final);
@@ -471,11 +585,12 @@ template <class C, bool ROPE>
 __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quarter, int lane,
                            const CUtensorMap* tout, uint8_t* stage_out, const uint8_t* stage_tab) {
   constexpr int BK = C::BK;
+  static_assert(!(ROPE && C::WIDE), "q RoPE is fused for head dims up to 128");
   volatile int* abort = &bars->abort;
   const int row = quarter * 32 + lane;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const float cs = a.softcap_on ? 1.0f : a.c_score;   // raw score -> log2 units
-  uint32_t g = 0, uc = 0;
+  uint32_t g = 0, uc = 0;       // key blocks and live units done so far
   bool ok = true;
   // Fused RoPE: the first unit's Q is rotated up front, every later one right
   // after the previous unit's last P (before its epilogue), while the tensor
@@ -485,26 +600,24 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
     const PUnit u0 = get_unit<C>(a, unit_of(blockIdx.x, r0, gridDim.x));
     ok = tq_rotate_q<C>(a, lane_base, bars, stage_tab, u0, a.rope_start[u0.b], quarter, lane, 0);
   }
-  // One 32-row x DP-column box of this warp to the output: 16 columns at a
-  // time through two alternating 2 KB staging tiles (64-byte swizzle: 16-byte
-  // granule g of row r at g ^ ((r / 2) % 4)); a tile is rewritten once the
-  // store issued two steps earlier has read it. value(c) gives columns
-  // c .. c + 3 of this thread's row; rows past L are clipped.
-  auto store_rows = [&](const PUnit& uu, auto value) {
+  // The warp's 32 rows x 16 columns from column c0 to the output, through two
+  // alternating 2 KB staging tiles (64-byte swizzle: 16-byte granule g of row r
+  // at g ^ ((r / 2) % 4)); a tile is rewritten once the store issued two boxes
+  // earlier has read it: box c0 / 16 uses tile (c0 / 16) % 2, and a unit stores
+  // an even number of boxes. value(q) gives columns c0 + 4 q .. c0 + 4 q + 3 of
+  // this thread's row; rows past L and columns past D are clipped.
+  auto store_box = [&](const PUnit& uu, int c0, auto value) {
+    uint8_t* tile = stage_out + ((c0 / 16) & 1) * 2048;
+    if (lane == 0) tc::bulk_wait_read_all_but_one();
+    __syncwarp();
+    float4* row_out = reinterpret_cast<float4*>(tile + lane * 64);
 #pragma unroll
-    for (int c = 0; c < C::DP; c += 16) {
-      uint8_t* tile = stage_out + ((c / 16) & 1) * 2048;
-      if (lane == 0) tc::bulk_wait_read_all_but_one();
-      __syncwarp();
-      float4* row_out = reinterpret_cast<float4*>(tile + lane * 64);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) row_out[q ^ ((lane >> 1) & 3)] = value(c + 4 * q);
-      tc::fence_proxy_async();
-      __syncwarp();
-      if (lane == 0) {
-        tc::tma_store_3d(tout, tile, c, uu.q0 + quarter * 32, uu.b * a.H + uu.h);
-        tc::bulk_commit();
-      }
+    for (int q = 0; q < 4; ++q) row_out[q ^ ((lane >> 1) & 3)] = value(q);
+    tc::fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      tc::tma_store_3d(tout, tile, c0, uu.q0 + quarter * 32, uu.b * a.H + uu.h);
+      tc::bulk_commit();
     }
   };
   for (int r = r0; ok;) {
@@ -639,16 +752,37 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       break;
     }
     tc::fence_after_sync();
-    float o[C::DP];
-    tmem_ld_row<C::DP>(lane_base + C::kOCol, o);
-    tc::fence_before_sync();
-    tc::mbar_arrive(&bars->o_free);
     const bool real = !C::RAGGED || qpos <= u.klast;
     const float inv = real ? 1.0f / l : 0.f;
-    store_rows(u, [&](int c) {
-      return real ? make_float4(o[c] * inv, o[c + 1] * inv, o[c + 2] * inv, o[c + 3] * inv)
-                  : make_float4(0.f, 0.f, 0.f, 0.f);
-    });
+    if constexpr (!C::WIDE) {
+      float o[C::DP];
+      tmem_ld_row<C::DP>(lane_base + C::kOCol, o);
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->o_free);
+#pragma unroll
+      for (int c = 0; c < C::DP; c += 16)
+        store_box(u, c, [&](int q) {
+          const float* e = o + c + 4 * q;
+          return real ? make_float4(e[0] * inv, e[1] * inv, e[2] * inv, e[3] * inv)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        });
+    } else {
+      // 32 columns at a time: the whole row would not fit in registers.
+#pragma unroll 1
+      for (int c = 0; c < C::DP; c += 32) {
+        float o[32];
+        tc::tmem_ld32(lane_base + C::kOCol + c, o);
+#pragma unroll
+        for (int h = 0; h < 32; h += 16)
+          store_box(u, c + h, [&](int q) {
+            const float* e = o + h + 4 * q;
+            return real ? make_float4(e[0] * inv, e[1] * inv, e[2] * inv, e[3] * inv)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+          });
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&bars->o_free);
+    }
     g += u.n;
     ++uc;
     r = rn;
@@ -659,7 +793,10 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
       const int x = unit_of(blockIdx.x, r, gridDim.x);
       if (x >= a.units) break;
       const PUnit u = get_unit<C>(a, x);
-      if (u.n == 0) store_rows(u, [](int) { return make_float4(0.f, 0.f, 0.f, 0.f); });
+      if (u.n > 0) continue;
+#pragma unroll 1
+      for (int c = 0; c < C::DP; c += 16)
+        store_box(u, c, [](int) { return make_float4(0.f, 0.f, 0.f, 0.f); });
     }
   }
   if (lane == 0) tc::bulk_wait_all();           // output boxes written before the block exits
@@ -676,7 +813,8 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* skv = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sepi = skv + C::NS * C::kStage;      // 4 x 4 KB output staging tiles
+  uint8_t* sqb = skv + C::NS * C::kStage;       // Q_b (WIDE; 1024-byte aligned)
+  uint8_t* sepi = sqb + C::kQb;                 // 4 x 4 KB output staging tiles
   uint8_t* stab = sepi + C::kEpi;               // RoPE table rows 0..31 (ROPE)
   PBars* bars = reinterpret_cast<PBars*>(stab + C::kTab);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -696,6 +834,8 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     tc::mbar_init(&bars->o_free, 128);
     tc::mbar_init(&bars->q_copied, 1);
     tc::mbar_init(&bars->q_ready, 128);
+    tc::mbar_init(&bars->qb_full, 1);
+    tc::mbar_init(&bars->qb_empty, 1);
     tc::mbar_init(&bars->drain[0], 1);
     tc::mbar_init(&bars->drain[1], 1);
     bars->abort = 0;
@@ -725,10 +865,10 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) tq_producer<C>(a, &tm_q, &tm_k, &tm_v, skv, bars);
+    if (lane == 0) tq_producer<C>(a, &tm_q, &tm_k, &tm_v, skv, sqb, bars);
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) tq_mma_s<C>(a, tmem, skv, bars);
+    if (lane == 0) tq_mma_s<C>(a, tmem, skv, sqb, bars);
     __syncwarp();
   } else if (warp == 6) {
     if (lane == 0) tq_mma_pv<C>(a, tmem, skv, bars);
@@ -810,9 +950,10 @@ cudaError_t launch_tq_r(const AttnShape& s, cudaStream_t stream) {
 
 bool prefill_fuses_rope(int D) { return D % 32 == 0 && D <= 128; }
 
-bool prefill_tq_supports_kv_off(int D) { return D % 4 == 0 && D >= 32 && D <= 128; }
+bool prefill_tq_supports_kv_off(int D) { return D % 4 == 0 && D >= 32 && D <= 256; }
 
-// D <= 128; V^T must already be in s.vt (launch_prefill_tc runs the transpose first).
+// 32 <= D <= 256, D % 4 == 0; V^T must already be in s.vt (launch_prefill_tc runs
+// the transpose first). q RoPE is fused only for D <= 128.
 cudaError_t launch_prefill_tq(const AttnShape& s, cudaStream_t stream) {
   switch ((s.D + 31) / 32) {
     // with q RoPE fused (R % 64 == 0, so D >= 64) or without
@@ -821,6 +962,11 @@ cudaError_t launch_prefill_tq(const AttnShape& s, cudaStream_t stream) {
     case 3: return s.rope.table ? launch_tq_r<96, true>(s, stream) : launch_tq_r<96, false>(s, stream);
     case 4: return s.rope.table ? launch_tq_r<128, true>(s, stream)
                                 : launch_tq_r<128, false>(s, stream);
+    // two sub-units (output halves) per query tile, no fused RoPE
+    case 5: return s.rope.table ? cudaErrorNotSupported : launch_tq_r<160, false>(s, stream);
+    case 6: return s.rope.table ? cudaErrorNotSupported : launch_tq_r<192, false>(s, stream);
+    case 7: return s.rope.table ? cudaErrorNotSupported : launch_tq_r<224, false>(s, stream);
+    case 8: return s.rope.table ? cudaErrorNotSupported : launch_tq_r<256, false>(s, stream);
     default: return cudaErrorNotSupported;
   }
 }

@@ -219,7 +219,7 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
  *   start    [B] device int32, positions already cached; max_start bounds them
  *   workspace gqa_attn_prefill_cached_workspace_size bytes (the gathered keys,
  *            transposed values and, for some rope shapes, rotated q)
- * Head dims D % 4 == 0, 32 <= D <= 128 (ATTN_ERR_SHAPE otherwise). A start[b]
+ * Head dims D % 4 == 0, 32 <= D <= 256 (ATTN_ERR_SHAPE otherwise). A start[b]
  * outside [0, max_start] (or above capacity without a window) sets
  * ATTN_DEV_POSITION (ATTN_DEV_CAPACITY) and that row attends only to the chunk.
  * Cost: the gather reads the kept prefix of every (b, kv head) once per call.
@@ -253,7 +253,7 @@ int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, cons
  *            and is clamped to [0, L]
  *   workspace gqa_attn_prefill_ragged_workspace_size bytes
  * Other arguments as for gqa_attn_prefill_rope (rp, table, q_norm_w may be NULL
- * when rp is NULL). In the persistent kernel (D <= 128) query tiles with no
+ * when rp is NULL). In the persistent kernel (D % 4 == 0, D >= 32) query tiles with no
  * real row cost no attention work.
  */
 size_t gqa_attn_prefill_ragged_workspace_size(int B, int H, int Hkv, int L, int D,

@@ -222,7 +222,8 @@ def test_cached_prefill_refuses_before_launch():
                                            max_start, None, None, None, 1e-6, window, 0.0, 0.0,
                                            ws, wbytes, None, None)
 
-    assert call(D=256) == -2                      # head dims past the persistent kernel
+    assert call(D=260) == -2                      # head dims past 256
+    assert call(D=256) == -5                      # wide heads too (here: no workspace)
     assert call(D=20) == -2
     assert call(window=64, capacity=128) == -2    # a ring holds exactly window slots
     assert call(max_start=200) == -4              # prefix positions without cache slots

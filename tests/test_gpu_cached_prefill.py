@@ -32,6 +32,8 @@ CASES = [
     (2, 8, 2, 128, 128, (100, 40), 150, 64, 0.0, False, True),  # ring, chunk longer than W
     (1, 4, 2, 128, 64, (500,), 300, 256, 50.0, True, True),     # ring with softcap, q/k norm
     (2, 4, 2, 40, 40, (33, 7), 90, 0, 0.0, False, False),       # q pre-rotated, D % 32 != 0
+    (1, 4, 2, 256, 256, (300,), 130, 0, 50.0, True, True),      # two output halves per tile
+    (2, 4, 2, 192, 64, (200, 50), 100, 128, 0.0, False, False),  # halves over a ring
 ]
 
 

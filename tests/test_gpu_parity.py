@@ -152,6 +152,13 @@ PREFILL_CASES = [
     (2, 8, 1, 200, 128, 0, 30.0),
     (1, 8, 4, 333, 128, 64, 0.0),
     (1, 4, 2, 257, 256, 100, 50.0),
+    # D > 128: two output halves per query tile
+    (1, 4, 2, 200, 160, 0, 0.0),
+    (2, 8, 4, 300, 192, 64, 0.0),
+    (1, 6, 3, 260, 224, 0, 20.0),
+    (1, 4, 1, 333, 200, 0, 0.0),
+    (1, 4, 2, 129, 172, 40, 0.0),
+    (1, 2, 1, 1, 256, 0, 0.0),
     (1, 16, 2, 130, 128, 1, 0.0),
     (1, 2, 1, 1, 128, 0, 0.0),
     (2, 6, 3, 75, 6, 0, 5.0),

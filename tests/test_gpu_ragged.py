@@ -47,7 +47,8 @@ CASES = [
     (2, 6, 2, 200, 96, 64, (77, 200), 64, 0.0, False, True),
     (3, 8, 2, 384, 128, 128, (384, 256, 3), 0, 0.0, False, False),   # q rotated beforehand
     (2, 4, 2, 150, 40, 40, (150, 31), 0, 0.0, False, False),          # D % 32 != 0
-    (2, 4, 2, 200, 256, 256, (200, 70), 128, 50.0, True, False),      # the D > 128 kernel
+    (2, 4, 2, 200, 256, 256, (200, 70), 128, 50.0, True, False),      # two output halves
+    (3, 4, 2, 300, 200, 128, (1, 300, 150), 0, 0.0, False, False),    # halves, D % 32 != 0
     (2, 4, 2, 70, 6, 6, (70, 33), 0, 0.0, False, False),              # CUDA-core kernel
 ]
 
