@@ -77,7 +77,8 @@ def peaks():
 # current kernels (profiles/); None where no capture of the timed kernel exists.
 # The decode capture ran on 16 of the 64 rows; its traffic scales with the
 # algorithmic bytes processed (ratio below).
-NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 348.996352e6 + 96.940032e6}
+NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 348.996352e6 + 96.940032e6,
+                       ("gemma2_window", "fused"): 3360.615e6 + 247.863296e6}
 NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903360e6 + 4.927232e6) / 585572352.0
 
 
@@ -568,6 +569,12 @@ def main():
     fl = prefill_flops(w)
     value = world * fl / (pre["ms"] * 1e-3) / 1e12
     kern_tflops = fl / (pre["kernel_ms"] * 1e-3) / 1e12
+    # q RMSNorm/RoPE runs inside the attention kernel when the kernel takes it
+    # (no workspace needed), else as a pass over q inside the same call
+    q_fused = g.gqa_attn_prefill_rope_vt_workspace_size(
+        w.B, w.H, w.L, w.D, g.RopeParams.make(theta=w.theta, rope_dim=w.rope_dim,
+                                              max_positions=w.max_positions,
+                                              scaling=w.scaling)) <= 16
     dec = None
     if not args.no_decode:
         wd = syn.WORKLOADS["batched_decode"]
@@ -598,7 +605,8 @@ def main():
                             + ("attn_rope_apply (q) + gqa_attn_prefill (V^T pre-pass inside)"
                                if args.unfused_q_rope
                                else "gqa_attn_v_transpose + gqa_attn_prefill_rope_vt (q "
-                                    "RMSNorm/RoPE fused into the attention kernel)")
+                                    + ("RMSNorm/RoPE fused into the attention kernel)" if q_fused
+                                       else "RMSNorm/RoPE as a pass over q inside the call)"))
                             + ("" if args.no_graph else "; timed as CUDA graph replays")),
                    "ms_per_step_eager": pre["ms_eager"],
                    "l2": f"inputs larger than L2 ({prefill_bytes(w) / 2**20:.0f} MiB per step)",
@@ -610,7 +618,9 @@ def main():
                      "traffic_note": "ncu dram bytes of prefill_tq_kernel (one launch)",
                      "kernel": ("gqa_attn_prefill (V^T pre-pass + attention)"
                                 if args.unfused_q_rope else
-                                "gqa_attn_prefill_rope_vt (the attention kernel alone)"),
+                                "gqa_attn_prefill_rope_vt (the attention kernel alone)"
+                                if q_fused else
+                                "gqa_attn_prefill_rope_vt (q rotation pass + attention kernel)"),
                      "kernel_ms": pre["kernel_ms"],
                      "peak_note": "dense TF32 measured in this run: cuBLAS fp32 8192^3 "
                                   "with TF32 allowed, best of 10",
