@@ -14,6 +14,8 @@
 // split is finished by its split block directly.
 //
 // The work is HBM-bound: 2 * D * 4 bytes per cached position and KV head.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc_ptx.cuh"
@@ -481,6 +483,8 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
 // maximum, the sum and P V need no further exchange.
 // Shared memory per warp: its ring, at least the 36 floats per lane it hands to
 // warp 0 at the end.
+constexpr float kPairRescaleLog2 = 8.0f;   // O is rescaled when the max grows by > 2^8
+
 __host__ __device__ inline uint32_t pair_ring_stride(int nst, uint32_t part_bytes) {
   const uint32_t ring = static_cast<uint32_t>(nst) * 2 * part_bytes, merge = 36u * 32 * 4;
   return ((ring > merge ? ring : merge) + 127) / 128 * 128;
@@ -489,7 +493,7 @@ __host__ __device__ inline uint32_t pair_ring_stride(int nst, uint32_t part_byte
 // NW warps per block share one split: warp w takes batches w, w + NW, ... of
 // it through its own ring, and the warps' running (max, sum, O) are merged in
 // shared memory at the end, so a split costs one partial result whatever NW is.
-template <int NW, int KP>
+template <int NW, int KP, bool D128>
 __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int nst) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_all[NW][kBulkMaxStages];
@@ -502,7 +506,7 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
   const int ngroups = G / 8;
   const int hkv = blockIdx.y / ngroups;
   const int g0 = (blockIdx.y % ngroups) * 8;
-  const int D = j.D;
+  const int D = D128 ? 128 : j.D;            // D128: every lane's 16 dims are real
 
   const int n = j.cache_len[b];
   if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) {
@@ -547,11 +551,12 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
     for (int c = 0; c < 4; ++c) {
       const int d = 32 * c + 4 * grp;
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (d < D) t = *reinterpret_cast<const float4*>(row + d);
+      if (D128 || d < D) t = *reinterpret_cast<const float4*>(row + d);
       r[4 * c] = t.x; r[4 * c + 1] = t.y; r[4 * c + 2] = t.z; r[4 * c + 3] = t.w;
     }
   };
-  float q[2][16], o[2][16];
+  // q (pre-scaled) and O as pairs of adjacent dims: one paired FMA serves two.
+  uint64_t q2[2][8], o2[2][8];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const float* qr = j.q + ((long)b * j.H + hkv * G + g0 + 2 * pair + h) * D;
@@ -559,15 +564,19 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
     for (int c = 0; c < 4; ++c) {
       const int d = 32 * c + 4 * grp;
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (d < D) t = __ldg(reinterpret_cast<const float4*>(qr + d));
-      q[h][4 * c] = t.x * j.scale; q[h][4 * c + 1] = t.y * j.scale;
-      q[h][4 * c + 2] = t.z * j.scale; q[h][4 * c + 3] = t.w * j.scale;
+      if (D128 || d < D) t = __ldg(reinterpret_cast<const float4*>(qr + d));
+      q2[h][2 * c] = tc::pack2(t.x * j.scale, t.y * j.scale);
+      q2[h][2 * c + 1] = tc::pack2(t.z * j.scale, t.w * j.scale);
     }
 #pragma unroll
-    for (int e = 0; e < 16; ++e) o[h][e] = 0.f;
+    for (int e = 0; e < 8; ++e) o2[h][e] = tc::pack2(0.f, 0.f);
   }
   const bool capped = j.softcap > 0.f;
   const float cap_k = capped ? 2.0f * kLog2e / j.softcap : 0.f;
+  // Weights are taken against a reference maximum m_run (log2 units) that moves
+  // only when a score exceeds it by more than 2^kPairRescaleLog2; O and l are
+  // rescaled then. A weight is therefore at most 2^kPairRescaleLog2, and most
+  // batches need no rescale.
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
 
   int i = 0;
@@ -578,58 +587,79 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
     const int valid = min(KP, k1 - (k0 + (warp + NW * i) * KP));
     const float* sk = reinterpret_cast<const float*>(ring + 2 * s * part_bytes);
     const float* sv = reinterpret_cast<const float*>(ring + (2 * s + 1) * part_bytes);
-    float sc[2][KP];
-#pragma unroll
-    for (int u = 0; u < KP; ++u) {
-      float kr[16];
-      load16(sk + u * D, kr);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float a0 = 0.f, a1 = 0.f;             // two chains: half the dependent FMA depth
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          a0 = fmaf(q[h][e], kr[e], a0);
-          a1 = fmaf(q[h][e + 1], kr[e + 1], a1);
-        }
-        float acc = a0 + a1;
-#pragma unroll
-        for (int off = 1; off < 8; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (capped) acc = softcap_apply(acc, j.softcap, cap_k);
-        sc[h][u] = u < valid ? acc * kLog2e : -INFINITY;
-      }
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float mx = sc[h][0];
-#pragma unroll
-      for (int u = 1; u < KP; ++u) mx = fmaxf(mx, sc[h][u]);
-      const float m_new = fmaxf(m_run[h], mx);
-      const float corr = m_new == -INFINITY ? 1.f : exp2f(m_run[h] - m_new);
-      float ls = 0.f;
+    // Only a split's last batch can be partial: the full ones skip the key checks.
+    auto batch = [&](auto full_c) {
+      constexpr bool FULL = decltype(full_c)::value;
+      float sc[2][KP];
 #pragma unroll
       for (int u = 0; u < KP; ++u) {
-        sc[h][u] = m_new == -INFINITY ? 0.f : exp2f(sc[h][u] - m_new);
-        ls += sc[h][u];
+        float kr[16];
+        load16(sk + u * D, kr);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint64_t acc = tc::pack2(0.f, 0.f);   // even and odd dims: two FMA chains
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            acc = tc::fma2(q2[h][e], tc::pack2(kr[2 * e], kr[2 * e + 1]), acc);
+          float a0, a1;
+          tc::unpack2(acc, a0, a1);
+          float sum = a0 + a1;
+#pragma unroll
+          for (int off = 1; off < 8; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+          if (capped) sum = softcap_apply(sum, j.softcap, cap_k);
+          sc[h][u] = FULL || u < valid ? sum * kLog2e : -INFINITY;
+        }
       }
-      l_run[h] = l_run[h] * corr + ls;
-      m_run[h] = m_new;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) o[h][e] *= corr;
-    }
+      for (int h = 0; h < 2; ++h) {
+        float mx = sc[h][0];
 #pragma unroll
-    for (int u = 0; u < KP; ++u) {
-      if (u < valid) {                        // slots past the copied rows hold stale bytes
-        float vr[16];
-        load16(sv + u * D, vr);
+        for (int u = 1; u < KP; ++u) mx = fmaxf(mx, sc[h][u]);
+        const bool grow = mx > m_run[h] + kPairRescaleLog2;   // also the row's first finite score
+        if (__any_sync(0xffffffffu, grow)) {
+          const float corr = grow ? tc::ex2(m_run[h] - mx) : 1.f;   // 0 while O and l are 0
+          const uint64_t c2 = tc::pack2(corr, corr);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+          for (int e = 0; e < 8; ++e) o2[h][e] = tc::mul2(o2[h][e], c2);
+          l_run[h] *= corr;
+          if (grow) m_run[h] = mx;
+        }
+        const float mu = m_run[h] == -INFINITY ? 0.f : m_run[h];   // all keys so far masked
+        float ls = 0.f;
 #pragma unroll
-          for (int e = 0; e < 16; ++e) o[h][e] = fmaf(sc[h][u], vr[e], o[h][e]);
+        for (int u = 0; u < KP; ++u) {
+          sc[h][u] = tc::ex2(sc[h][u] - mu);
+          ls += sc[h][u];
+        }
+        l_run[h] += ls;
       }
-    }
+#pragma unroll
+      for (int u = 0; u < KP; ++u) {
+        if (FULL || u < valid) {              // slots past the copied rows hold stale bytes
+          float vr[16];
+          load16(sv + u * D, vr);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint64_t p2 = tc::pack2(sc[h][u], sc[h][u]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              o2[h][e] = tc::fma2(p2, tc::pack2(vr[2 * e], vr[2 * e + 1]), o2[h][e]);
+          }
+        }
+      }
+    };
+    if (valid == KP)
+      batch(std::true_type{});
+    else
+      batch(std::false_type{});
     __syncwarp();                             // every lane is done reading stage s
     if (lane == 0 && i + nst < nbw) issue(i + nst);
   }
+  float o[2][16];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) tc::unpack2(o2[h][e], o[h][2 * e], o[h][2 * e + 1]);
   const bool timed_out = i < nbw;
   if (timed_out && lane == 0) {
     // A wait ran out: let the copies already issued land, then report.
@@ -682,7 +712,7 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int d = 32 * c + 4 * grp;
-      if (d >= D) continue;
+      if (!D128 && d >= D) continue;
       if (single) {
         *reinterpret_cast<float4*>(j.out + hrow * D + d) =
             make_float4(o[h][4 * c] * inv, o[h][4 * c + 1] * inv, o[h][4 * c + 2] * inv,
@@ -757,8 +787,11 @@ cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream) {
     constexpr int NW = kPairWarps, KP = kPairKeys;
     const int nst = 2;
     const uint32_t smem = NW * pair_ring_stride(nst, KP * j.D * 4);
-    decode_pair_kernel<NW, KP>
-        <<<dim3(j.nsplit, j.Hkv * (G / 8), j.B), 32 * NW, smem, stream>>>(j, nst);
+    const dim3 grid(j.nsplit, j.Hkv * (G / 8), j.B);
+    if (j.D == 128)
+      decode_pair_kernel<NW, KP, true><<<grid, 32 * NW, smem, stream>>>(j, nst);
+    else
+      decode_pair_kernel<NW, KP, false><<<grid, 32 * NW, smem, stream>>>(j, nst);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || j.nsplit <= 1) return e;
     decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);
