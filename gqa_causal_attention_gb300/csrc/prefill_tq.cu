@@ -88,6 +88,7 @@ struct PCfg {
   // from 3 stages with one-item Q tiles, K and V^T blocks, and from 4 with the
   // WIDE parts.
   static_assert(NS >= (WIDE ? 4 : 3), "ring too short");
+  static_assert(VI == 1 || VI == 2, "V^T items per block: one, or one per half of P");
   static_assert(DP % 32 == 0 && DP <= 256, "head dim: 32-column chunks, an even number of output boxes");
   static_assert(kSCol + 2 * BK <= kTmemCols, "tensor memory budget");
   static_assert(kSmem <= kSmemLimit, "shared memory budget");
@@ -97,8 +98,9 @@ struct PBars {
   uint64_t kv_full[8];
   uint64_t kv_empty[8];
   uint64_t s_full[2];
-  uint64_t p_ready[2];
+  uint64_t p_ready[2][2];                      // [S buffer][half]: P of those columns written
   uint64_t o_done[2];                          // P V of block X done (X % 2)
+  uint64_t o_half[2];                          // P V of block X's first half done (X % 2)
   uint64_t o_final;
   uint64_t o_free;
   uint64_t q_copied;                           // a Q tile is in tensor memory (one phase per unit)
@@ -443,29 +445,36 @@ __device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* b
         if (!C::WIDE && i + 2 == u.n && has_next) skip(C::QP);   // next Q
       }
       if (C::WIDE && i + 1 == u.n && has_next) skip(C::QP);      // next Q_a
-      // P of block G first: S of block G has then read K_G, so the stage's
-      // previous item has landed and the ring wait below cannot alias.
-      if (!(ok = tc::mbar_wait(&bars->p_ready[G & 1], (G >> 1) & 1, abort))) break;
+      // P of block G arrives in two halves of BK / 2 keys; the products of the
+      // first half run while the softmax computes the second. P's first half
+      // comes before the ring wait: S of block G has then read K_G, so the
+      // stage's previous item has landed and the wait cannot alias.
+      constexpr int KH = C::BK / 16;              // 8-key steps per half
+      int st_item[2] = {0, 0};
 #pragma unroll
-      for (int v = 0; v < C::VI; ++v) {
-        int st = 0;
-        if (!(ok = ring.take(bars, abort, st))) break;
-        if (v == 0 && i == 0 && uc > 0 &&
-            !(ok = tc::mbar_wait(&bars->o_free, (uc - 1) & 1, abort)))
-          break;
+      for (int hh = 0; hh < 2; ++hh) {
+        if (!(ok = tc::mbar_wait(&bars->p_ready[G & 1][hh], (G >> 1) & 1, abort))) break;
+        if (C::VI == 2 || hh == 0) {              // this half's V^T item
+          if (!(ok = ring.take(bars, abort, st_item[hh]))) break;
+          if (hh == 0 && i == 0 && uc > 0 &&
+              !(ok = tc::mbar_wait(&bars->o_free, (uc - 1) & 1, abort)))
+            break;
+        }
         tc::fence_after_sync();
         const uint32_t d = tmem + C::kOCol;
-        const uint64_t vd = stage_desc<C>(base_desc, st);
+        const uint64_t vd = stage_desc<C>(base_desc, st_item[C::VI == 2 ? hh : 0]);
 #pragma unroll
-        for (int kk = 0; kk < 4 * C::kVPC; ++kk) {
-          const int kg = 4 * C::kVPC * v + kk;      // 8-key step within the block
-          const int c = kk / 4, off = (kk % 4) * 32;
-          tc::mma_tf32_ts(d, tmem + C::kSCol + (G & 1) * C::BK + 8 * kg,
-                          vd + ((c * C::kVtChunk + off) >> 4), id_pv, (i > 0 || kg > 0) ? 1u : 0u);
+        for (int kk = hh * KH; kk < (hh + 1) * KH; ++kk) {
+          const int kl = C::VI == 2 ? kk - hh * KH : kk;   // 8-key step within the item
+          const int c = kl / 4, off = (kl % 4) * 32;
+          tc::mma_tf32_ts(d, tmem + C::kSCol + (G & 1) * C::BK + 8 * kk,
+                          vd + ((c * C::kVtChunk + off) >> 4), id_pv, (i > 0 || kk > 0) ? 1u : 0u);
         }
-        tc::mma_commit(&bars->kv_empty[st]);
+        if (C::VI == 2) tc::mma_commit(&bars->kv_empty[st_item[hh]]);
+        if (hh == 0) tc::mma_commit(&bars->o_half[G & 1]);
       }
       if (!ok) break;
+      if (C::VI == 1) tc::mma_commit(&bars->kv_empty[st_item[0]]);
       tc::mma_commit(&bars->o_done[G & 1]);
     }
     if (!ok) break;
@@ -677,66 +686,77 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
           tc::tmem_st32(scol + c0, x);
         }
       }
-      float s[BK];
-      float lsum = 0.f;
-      // Pass 0, the common case: P against the running reference m_ref. It
-      // stands unless a score exceeds m_ref by more than 2^8 (where the
-      // reference is moved); then the block's sum of P exceeds 2^8 as well.
-      // Pass 1 (a row's first block, or pass 0 rejected): S read again, P
-      // against the block maximum. One copy of the code serves both passes:
-      // this kernel's code far exceeds the instruction caches, so every copy
-      // of an unrolled 128-column loop costs fetch stalls.
-      const bool fast = !__any_sync(0xffffffffu, m_ref == -INFINITY);
+      // P in two halves of H2 columns, each released to the P V issuer as soon
+      // as it is written (its products then overlap the second half's softmax).
+      // Per half, pass 0, the common case: P against the running reference
+      // m_ref. It stands unless a score exceeds m_ref by more than 2^8 (where
+      // the reference is moved); then the half's sum of P exceeds 2^8 as well.
+      // Pass 1 (a row's first visible keys, or pass 0 rejected): S read again,
+      // P against the new maximum, after O is rescaled once every product that
+      // wrote it is done: P V of block G - 1 for the first half, and P V of
+      // this block's first half for the second. One rolled copy of the code
+      // serves both halves and passes: this kernel's code far exceeds the
+      // instruction caches, so every copy of an unrolled loop costs fetch stalls.
+      constexpr int H2 = BK / 2;
 #pragma unroll 1
-      for (int pass = fast ? 0 : 1; pass < 2; ++pass) {
-        tmem_ld_row<BK>(scol, s);
-        // Softcap: log2(e) * cap * tanh(scale * s / cap) = c_out - 2 c_out / (2^(s c_in) + 1)
-        // (boundary blocks have it already).
-        if (a.softcap_on && !edge) {
-#pragma unroll
-          for (int c = 0; c < BK; ++c) {
-            const float e = tc::ex2(s[c] * a.c_cap_in);
-            s[c] = fmaf(-2.0f * a.c_cap_out, tc::rcp(e + 1.0f), a.c_cap_out);
-          }
-        }
-        float m_use = m_ref;
-        if (pass == 1) {
-          const float m_new = fmaxf(m_ref, tq_max<BK>(s) * cs);
-          // Rescale O only when the running maximum has grown a lot (warp-uniform).
-          const bool grow = m_ref != -INFINITY && m_new - m_ref > kRescaleLog2;
-          if (__any_sync(0xffffffffu, grow)) {
-            ok = tc::mbar_wait(&bars->o_done[(G - 1) & 1], ((G - 1) >> 1) & 1, abort);
-            if (__any_sync(0xffffffffu, !ok)) {
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            const float f = grow ? tc::ex2(m_ref - m_new) : 1.0f;
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t hcol = scol + hh * H2;
+        float s[H2];
+        float lsum = 0.f;
+        const bool fast = !__any_sync(0xffffffffu, m_ref == -INFINITY);
 #pragma unroll 1
-            for (int c = 0; c < C::DP; c += 32) {
-              float o[32];
-              tc::tmem_ld32(lane_base + C::kOCol + c, o);
+        for (int pass = fast ? 0 : 1; pass < 2; ++pass) {
+          tmem_ld_row<H2>(hcol, s);
+          // Softcap: log2(e) * cap * tanh(scale * s / cap) = c_out - 2 c_out / (2^(s c_in) + 1)
+          // (boundary blocks have it already).
+          if (a.softcap_on && !edge) {
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] *= f;
-              tc::tmem_st32(lane_base + C::kOCol + c, o);
-            }
-            if (grow) {
-              l *= f;
-              m_ref = m_new;
+            for (int c = 0; c < H2; ++c) {
+              const float e = tc::ex2(s[c] * a.c_cap_in);
+              s[c] = fmaf(-2.0f * a.c_cap_out, tc::rcp(e + 1.0f), a.c_cap_out);
             }
           }
-          if (m_ref == -INFINITY) m_ref = m_new;  // first visible keys of the row (O, l are 0)
-          // -inf only while every key so far was masked; then every score is -inf.
-          m_use = m_ref == -INFINITY ? 0.f : m_ref;
+          float m_use = m_ref;
+          if (pass == 1) {
+            const float m_new = fmaxf(m_ref, tq_max<H2>(s) * cs);
+            // Rescale O only when the running maximum has grown a lot (warp-uniform).
+            const bool grow = m_ref != -INFINITY && m_new - m_ref > kRescaleLog2;
+            if (__any_sync(0xffffffffu, grow)) {
+              ok = hh == 0 ? tc::mbar_wait(&bars->o_done[(G - 1) & 1], ((G - 1) >> 1) & 1, abort)
+                           : tc::mbar_wait(&bars->o_half[G & 1], (G >> 1) & 1, abort);
+              if (__any_sync(0xffffffffu, !ok)) {
+                ok = false;
+                break;
+              }
+              tc::fence_after_sync();
+              const float f = grow ? tc::ex2(m_ref - m_new) : 1.0f;
+#pragma unroll 1
+              for (int c = 0; c < C::DP; c += 32) {
+                float o[32];
+                tc::tmem_ld32(lane_base + C::kOCol + c, o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] *= f;
+                tc::tmem_st32(lane_base + C::kOCol + c, o);
+              }
+              if (grow) {
+                l *= f;
+                m_ref = m_new;
+              }
+            }
+            if (m_ref == -INFINITY) m_ref = m_new;  // first visible keys of the row (O, l are 0)
+            // -inf only while every key so far was masked; then every score is -inf.
+            m_use = m_ref == -INFINITY ? 0.f : m_ref;
+          }
+          lsum = tq_exp_sum<H2>(s, cs, m_use);
+          if (pass == 1 || !__any_sync(0xffffffffu, !(lsum <= kRescaleLimit))) break;
         }
-        lsum = tq_exp_sum<BK>(s, cs, m_use);
-        if (pass == 1 || !__any_sync(0xffffffffu, !(lsum <= kRescaleLimit))) break;
+        if (!ok) break;
+        l += lsum;
+        tmem_st_row<H2>(hcol, s);
+        tc::fence_before_sync();
+        tc::mbar_arrive(&bars->p_ready[buf][hh]);
       }
       if (!ok) break;
-      l += lsum;
-      tmem_st_row<BK>(scol, s);
-      tc::fence_before_sync();
-      tc::mbar_arrive(&bars->p_ready[buf]);
     }
     if (!ok) break;
     if (ROPE && xn < a.units &&
@@ -826,7 +846,9 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&bars->s_full[b], 1);
-      tc::mbar_init(&bars->p_ready[b], 128);
+      tc::mbar_init(&bars->p_ready[b][0], 128);
+      tc::mbar_init(&bars->p_ready[b][1], 128);
+      tc::mbar_init(&bars->o_half[b], 1);
     }
     tc::mbar_init(&bars->o_done[0], 1);
     tc::mbar_init(&bars->o_done[1], 1);
