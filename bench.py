@@ -77,8 +77,8 @@ def peaks():
 # current kernels (profiles/); None where no capture of the timed kernel exists.
 # The decode capture ran on 16 of the 64 rows; its traffic scales with the
 # algorithmic bytes processed (ratio below).
-NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 348.996352e6 + 96.940032e6,
-                       ("gemma2_window", "fused"): 3360.615e6 + 247.863296e6}
+NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 334.207232e6 + 96.35328e6,
+                       ("gemma2_window", "fused"): 2153.623e6 + 246.349568e6}
 NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903360e6 + 4.927232e6) / 585572352.0
 
 
