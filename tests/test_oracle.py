@@ -145,6 +145,16 @@ def test_rmsnorm_hand_case():
     np.testing.assert_allclose(y, [_eval(fx["y0"]), _eval(fx["y1"])], rtol=1e-15)
 
 
+def test_rmsnorm_eps_hand_case():
+    """eps sits inside the square root, added to the mean of squares."""
+    fx = _fixture("rmsnorm_eps_d2.txt")
+    x = np.array([float(t) for t in fx["x"].split()]).reshape(1, 1, 1, 2)
+    w = np.array([float(t) for t in fx["w"].split()])
+    cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=2, rope_dim=0, norm_eps=float(fx["eps"]))
+    y = oracle.rotate(x, [0], cfg, norm_w=w).reshape(-1)
+    np.testing.assert_allclose(y, [_eval(fx["y0"]), _eval(fx["y1"])], rtol=1e-14)
+
+
 def test_rmsnorm_unit_rms_and_scale_invariance():
     D = 64
     x = RNG.standard_normal((1, 2, 3, D))
@@ -238,6 +248,19 @@ def test_explicit_scale_matches_torch_sdpa():
     want = torch.nn.functional.scaled_dot_product_attention(
         torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), is_causal=True,
         enable_gqa=True, scale=0.3).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+def test_default_scale_under_partial_rotary_is_full_head_dim():
+    """Partial rotary narrows only the rotation: the default score scale stays 1/sqrt(D),
+    torch SDPA's default for head dimension D."""
+    B, H, Hkv, L, D = 1, 4, 2, 10, 16
+    q, k, v = (RNG.standard_normal((B, n, L, D)) for n in (H, Hkv, Hkv))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, rope_dim=4)
+    got = oracle.attention(q, k, v, [0], cfg)
+    want = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), is_causal=True,
+        enable_gqa=True).numpy()
     np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
 
 
