@@ -114,6 +114,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_attn_prefill_rope_vt": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, vp,
                                                ctypes.c_int32, rp, vp, vp, f, i32, f, f, vp, sz,
                                                vp, vp]),
+            "gqa_attn_prefill_from_host_workspace_size": (sz, [i32, i32, i32, i32, i32, i32,
+                                                               rp]),
+            "gqa_attn_prefill_from_host": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                                 i32, i32, vp, ctypes.c_int32, rp, vp, vp, vp, f,
+                                                 vp, vp, i32, i32, f, f, vp, sz, vp, vp]),
             "gqa_attn_prefill_cached_workspace_size": (sz, [i32, i32, i32, i32, i32,
                                                             ctypes.c_int32, i32, rp]),
             "gqa_attn_prefill_cached": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
@@ -399,6 +404,55 @@ def gqa_attn_prefill_rope_vt(q, k, vt, out, start, max_start: int, params: RopeP
                                          int(window), float(softcap), float(scale),
                                          _ptr(workspace), wbytes, _ptr(status), _stream(stream))
     _check("gqa_attn_prefill_rope_vt", rc)
+
+
+def gqa_attn_prefill_from_host_workspace_size(B: int, H: int, Hkv: int, L: int, D: int,
+                                              capacity: int, params: RopeParams) -> int:
+    return int(load().gqa_attn_prefill_from_host_workspace_size(B, H, Hkv, L, D, capacity,
+                                                                ctypes.byref(params)))
+
+
+def gqa_attn_prefill_from_host(q_host, k_host, v_host, out_host, q, k, v, out, k_cache, v_cache,
+                               start, max_start: int, params: RopeParams, table, q_norm_w=None,
+                               k_norm_w=None, norm_eps: float = 1e-6, window: int = 0,
+                               softcap: float = 0.0, scale: float = 0.0, workspace=None,
+                               status=None, stream=None) -> None:
+    """One prefill step from host memory: q_host, k_host, v_host (CPU float32, pinned for
+    the copies to overlap the kernels) are copied into the device buffers q, k, v row chunk
+    by row chunk, k/v are appended to the caches (k rotated in place), the attention with
+    q's RoPE fused writes out, and out is copied back into out_host. Returns once enqueued;
+    out_host is complete when `stream` has passed the call."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("k_cache", k_cache),
+                 ("v_cache", v_cache)):
+        _f32(n, t, 4)
+    for n, t, d in (("q_host", q_host, q), ("k_host", k_host, k), ("v_host", v_host, v),
+                    ("out_host", out_host, out)):
+        if t.dtype != torch.float32 or t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous CPU float32 tensor")
+        if t.shape != d.shape:
+            raise ValueError(f"{n} must have the shape of its device buffer {tuple(d.shape)}")
+    _f32("table", table); _f32("q_norm_w", q_norm_w); _f32("k_norm_w", k_norm_w)
+    _i32("start", start); _i32("status", status)
+    B, H, L, D = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, L, D) or v.shape != k.shape or out.shape != q.shape \
+            or k_cache.shape != v_cache.shape or tuple(k_cache.shape[:2]) != (B, Hkv) \
+            or k_cache.shape[3] != D:
+        raise ValueError("gqa_attn_prefill_from_host: inconsistent shapes")
+    cap = int(k_cache.shape[2])
+    if workspace is None:
+        n = gqa_attn_prefill_from_host_workspace_size(B, H, Hkv, L, D, cap, params)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().gqa_attn_prefill_from_host(
+        _ptr(q_host), _ptr(k_host), _ptr(v_host), _ptr(out_host), _ptr(q), _ptr(k), _ptr(v),
+        _ptr(out), B, H, Hkv, L, D, _ptr(start), int(max_start), ctypes.byref(params),
+        _ptr(table), _ptr(q_norm_w), _ptr(k_norm_w), float(norm_eps), _ptr(k_cache),
+        _ptr(v_cache), cap, int(window), float(softcap), float(scale), _ptr(workspace), wbytes,
+        _ptr(status), _stream(stream))
+    _check("gqa_attn_prefill_from_host", rc)
 
 
 def gqa_attn_prefill_cached_workspace_size(B: int, H: int, Hkv: int, L: int, D: int,

@@ -74,6 +74,8 @@ int cuda_status(cudaError_t e) {
 
 }  // namespace
 
+int gqa::record_cuda_error(cudaError_t e) { return cuda_status(e); }
+
 extern "C" {
 
 const char* attn_version(void) { return "0.1.0"; }

@@ -33,6 +33,10 @@ struct RopeJob {
   int window;
 };
 
+// ATTN_OK for cudaSuccess; otherwise remembers e for attn_last_cuda_error on this host
+// thread and returns ATTN_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 cudaError_t launch_rope_table(const InvFreq& inv, int R, int max_positions, float2* table,
                               cudaStream_t stream);
 cudaError_t launch_rope_rows(const RopeJob& job, cudaStream_t stream);

@@ -197,6 +197,42 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
                              int32_t* status, void* stream);
 
 /*
+ * One whole prefill step with q, k, v and the output in host memory
+ * ("mojolearn.transformer", TransformerBlock.forward: the caller hands in the
+ * step's tensors and reads the result back). For every batch row: q, k, v are
+ * copied to the caller's device buffers, kv_cache_append rotates k in place and
+ * stores k and v at their cache slots, gqa_attn_prefill_rope writes out, and out
+ * is copied back to out_host. Results equal those two calls over the whole batch.
+ *   q_host, out_host        host [B, H, L, D]; k_host, v_host  host [B, Hkv, L, D].
+ *                           Page-locked (cudaHostAlloc / cudaHostRegister) memory
+ *                           lets the copies overlap the kernels; pageable memory
+ *                           works but serialises them. Not read or written after
+ *                           the caller's stream has passed this call.
+ *   q, k, v, out            device buffers of the same shapes (overwritten; k ends
+ *                           up rotated, as kv_cache_append leaves it)
+ *   k_cache, v_cache, capacity, window, k_norm_w: as kv_cache_append;
+ *   start, max_start, rp, table, q_norm_w, norm_eps, softcap, scale: as
+ *   gqa_attn_prefill_rope; workspace: gqa_attn_prefill_from_host_workspace_size bytes.
+ * The batch is cut into at most 8 chunks of rows. Each chunk's host-to-device
+ * copies run on one library-owned stream, its kernels on `stream` and its
+ * device-to-host copy on another library-owned stream, so copies and kernels of
+ * different chunks overlap. The two copy streams of a device are created by the
+ * first call on it (with that device current) and kept until exit. The call
+ * returns once everything is enqueued; `stream` passes the call only after the
+ * last copy to out_host. All checks run before anything is enqueued.
+ */
+size_t gqa_attn_prefill_from_host_workspace_size(int B, int H, int Hkv, int L, int D,
+                                                 int capacity, const attn_rope_params* rp);
+int gqa_attn_prefill_from_host(const float* q_host, const float* k_host, const float* v_host,
+                               float* out_host, float* q, float* k, float* v, float* out, int B,
+                               int H, int Hkv, int L, int D, const int32_t* start,
+                               int32_t max_start, const attn_rope_params* rp, const float* table,
+                               const float* q_norm_w, const float* k_norm_w, float norm_eps,
+                               float* k_cache, float* v_cache, int capacity, int window,
+                               float softcap, float scale, void* workspace,
+                               size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * Prefill of a chunk that continues a carried cache ("mojolearn.transformer",
  * TransformerBlock.forward with a TransformerState): the chunk's L queries at
  * positions start[b] + l attend, causally, to the positions kept in the cache

@@ -309,3 +309,33 @@ def test_block_forward_refuses_before_launch():
     assert need >= 2 * 8 * (3 * 64 + 4 * 32 + 2 * 32) * 4
     w2 = g._BlockWeights(*([0x100000] * 8 + [0, 0, 0]))          # no down_proj
     assert call(weights=w2, ws=P, wbytes=need) == -1
+
+
+@no_device
+def test_prefill_from_host_refuses_before_any_copy():
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+    rp = g.RopeParams.make(theta=1e4, max_positions=64)
+    need = lib.gqa_attn_prefill_from_host_workspace_size(4, 8, 2, 16, 64, 64, ctypes.byref(rp))
+    # one row per chunk at these sizes: the workspace is the one-row prefill's
+    assert need == lib.gqa_attn_prefill_rope_workspace_size(1, 8, 2, 16, 64, ctypes.byref(rp))
+
+    def call(B=4, H=8, Hkv=2, L=16, D=64, max_start=0, capacity=64, window=0, ws=P,
+             wbytes=need, qh=P, table=P, dev_q=P, rpp=ctypes.byref(rp)):
+        return lib.gqa_attn_prefill_from_host(qh, P, P, P, dev_q, P, P, P, B, H, Hkv, L, D, P,
+                                              max_start, rpp, table, None, None, 1e-6, P, P,
+                                              capacity, window, 0.0, 0.0, ws, wbytes, None, None)
+
+    assert call(H=6, Hkv=4) == -2                 # H % Hkv != 0
+    assert call(D=7) == -2                        # odd head dim
+    assert call(window=32, capacity=64) == -2     # a ring holds exactly window slots
+    assert call(qh=None) == -1                    # host buffers are required
+    assert call(table=None) == -1
+    assert call(dev_q=ctypes.c_void_p(0x100004)) == -6
+    assert call(max_start=60) == -3               # positions reach max_positions
+    assert call(capacity=8) == -4                 # positions without cache slots
+    assert call(ws=None) == -5
+    assert call(wbytes=need - 4) == -5
+    bad = g.RopeParams.make(theta=1e4, rope_dim=66, max_positions=64)
+    assert call(rpp=ctypes.byref(bad)) == -7
+    assert call(B=0) == 0 and call(L=0) == 0      # empty: nothing to do
