@@ -324,9 +324,13 @@ def bench_prefill(w, args, dist, dev, rank):
         assert int(status.item()) == 0, f"device status {int(status.item())}"
         res["e2e_ms"] = ems / e_steps
         res["e2e_serial_ms"] = timed(e2e_serial_step, e_steps, 3, dist) / e_steps
-        rows = -(-w.B // 8)                     # the call's row chunks (at most 8)
-        res["e2e_launches"] = 3 * (-(-w.B // rows)) * e_steps + \
-            res["launches_per_step"] * e_steps
+        if w.B >= 16:                           # the call's chunks (at most 16)
+            chunks = -(-w.B // -(-w.B // 16))
+        else:
+            per_row = -(-w.Hkv // -(-w.Hkv // (16 // w.B)))
+            chunks = w.B * per_row
+        res["e2e_launches"] = 3 * chunks * e_steps + res["launches_per_step"] * e_steps
+        res["e2e_chunks"] = chunks
         res["h2d"] = sum(t.numel() * 4 for t in (hq, hk, hv))
         res["d2h"] = hout.numel() * 4
     return res
@@ -651,7 +655,7 @@ def main():
                        "h2d_bytes_per_step": pre["h2d"], "d2h_bytes_per_step": pre["d2h"],
                        "ms_per_step": pre["e2e_ms"],
                        "call": "gqa_attn_prefill_from_host (pinned host q, k, v in, out back; "
-                               "row chunks overlap copies and kernels)",
+                               f"{pre['e2e_chunks']} chunks overlap copies and kernels)",
                        "serial_ms_per_step": pre["e2e_serial_ms"]}
         line["gpu_launches"] += pre["e2e_launches"]
     if dec is not None:

@@ -418,8 +418,8 @@ def gqa_attn_prefill_from_host(q_host, k_host, v_host, out_host, q, k, v, out, k
                                softcap: float = 0.0, scale: float = 0.0, workspace=None,
                                status=None, stream=None) -> None:
     """One prefill step from host memory: q_host, k_host, v_host (CPU float32, pinned for
-    the copies to overlap the kernels) are copied into the device buffers q, k, v row chunk
-    by row chunk, k/v are appended to the caches (k rotated in place), the attention with
+    the copies to overlap the kernels) are copied into the device buffers q, k, v chunk by
+    chunk (rows, or kv-head slices of a row), k/v are appended to the caches (k rotated in place), the attention with
     q's RoPE fused writes out, and out is copied back into out_host. Returns once enqueued;
     out_host is complete when `stream` has passed the call."""
     for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("k_cache", k_cache),

@@ -2,14 +2,15 @@
 // host memory ("mojolearn.transformer", TransformerBlock.forward: the caller
 // hands in the step's tensors and reads the attention result back).
 //
-// The step is split into chunks of batch rows. Each chunk's q, k, v rows go to
+// The step is split into chunks: groups of batch rows, or slices of one row's kv
+// heads (with their query heads) when there are few rows. Each chunk's q, k, v go to
 // the device on one copy stream, its k/v cache append and its attention run on
-// the caller's stream once they have landed, and its output rows go back to
-// the host on a second copy stream once they are written. Host-to-device
-// copies, kernels and device-to-host copies of different chunks overlap, so
-// the step costs about the slower of the two copy directions rather than the
-// sum of copies and compute. Batch rows are independent in every kernel of the
-// path, so each row gets the same result as in one call over the whole batch.
+// the caller's stream once they have landed, and its output goes back to
+// the host on a second copy stream once it is written. Host-to-device copies,
+// kernels and device-to-host copies of different chunks overlap, so the step
+// costs about the copies alone rather than copies plus compute. Batch rows and kv-head groups are independent in
+// every kernel of the path, so each gets the same result as in one call over
+// the whole batch.
 //
 // The two copy streams belong to the library: one pair per device, created by
 // the first call on that device (with it current) and kept until exit.
@@ -23,7 +24,7 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kMaxChunks = 8;
+constexpr int kMaxChunks = 16;
 
 std::mutex g_mutex;
 cudaStream_t g_copy[kMaxDevices][2] = {};   // [device][0: host->device, 1: device->host]
@@ -50,14 +51,34 @@ int copy_streams(cudaStream_t* h2d, cudaStream_t* d2h) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Batch rows per chunk: at most kMaxChunks chunks. Chunk offsets must keep every
-// device pointer 16-byte aligned; when a row of k or of the cache is not a whole
-// number of 16-byte units the step runs as one chunk.
-int rows_per_chunk(int B, int Hkv, int L, int D, int capacity) {
-  const long long kv_row = (long long)Hkv * L * D;
-  const long long cache_row = (long long)Hkv * capacity * D;
-  if (B <= 0 || kv_row % 4 != 0 || cache_row % 4 != 0) return B > 0 ? B : 1;
-  return (B + kMaxChunks - 1) / kMaxChunks;
+// A chunk is nb whole batch rows from b0 (all kv heads), or, when there are
+// fewer rows than kMaxChunks, kv heads [h0, h0 + nh) of one row with their query
+// heads: in [B, heads, L, D] and [B, Hkv, capacity, D] either is one contiguous
+// run of memory, and either is a valid call of the kernels (B = nb, Hkv = nh).
+// Chunk offsets keep every device pointer 16-byte aligned only when one head's
+// rows (L * D and capacity * D floats) are whole 16-byte units; otherwise the
+// step runs as one chunk.
+struct Plan {
+  int rows;      // batch rows per chunk (1 when rows are sliced by heads)
+  int heads;     // kv heads per chunk
+  int slices;    // chunks per row
+  int chunks;
+};
+
+Plan plan_chunks(int B, int Hkv, int L, int D, int capacity) {
+  Plan p{B > 0 ? B : 1, Hkv, 1, 1};
+  if (B <= 0 || ((long long)L * D) % 4 != 0 || ((long long)capacity * D) % 4 != 0) return p;
+  if (B >= kMaxChunks) {
+    p.rows = (B + kMaxChunks - 1) / kMaxChunks;
+    p.chunks = (B + p.rows - 1) / p.rows;
+    return p;
+  }
+  p.rows = 1;
+  const int want = kMaxChunks / B;                      // slices per row, >= 1
+  p.heads = (Hkv + want - 1) / want;
+  p.slices = (Hkv + p.heads - 1) / p.heads;
+  p.chunks = B * p.slices;
+  return p;
 }
 
 }  // namespace
@@ -66,9 +87,9 @@ extern "C" {
 
 size_t gqa_attn_prefill_from_host_workspace_size(int B, int H, int Hkv, int L, int D,
                                                  int capacity, const attn_rope_params* rp) {
-  if (B < 0 || capacity < 1) return 0;
-  const int rows = rows_per_chunk(B, Hkv, L, D, capacity);
-  return gqa_attn_prefill_rope_workspace_size(rows, H, Hkv, L, D, rp);
+  if (B < 0 || capacity < 1 || Hkv < 1 || H % Hkv != 0) return 0;
+  const Plan p = plan_chunks(B, Hkv, L, D, capacity);
+  return gqa_attn_prefill_rope_workspace_size(p.rows, p.heads * (H / Hkv), p.heads, L, D, rp);
 }
 
 int gqa_attn_prefill_from_host(const float* q_host, const float* k_host, const float* v_host,
@@ -98,8 +119,10 @@ int gqa_attn_prefill_from_host(const float* q_host, const float* k_host, const f
   if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_positions)
     return ATTN_ERR_POSITION;
   if (window == 0 && (int64_t)max_start + L > (int64_t)capacity) return ATTN_ERR_CAPACITY;
-  const int rows = rows_per_chunk(B, Hkv, L, D, capacity);
-  const size_t need = gqa_attn_prefill_rope_workspace_size(rows, H, Hkv, L, D, rp);
+  const int G = H / Hkv;
+  const Plan plan = plan_chunks(B, Hkv, L, D, capacity);
+  const size_t need =
+      gqa_attn_prefill_rope_workspace_size(plan.rows, plan.heads * G, plan.heads, L, D, rp);
   if (need == 0) return ATTN_ERR_SHAPE;
   if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
@@ -107,7 +130,7 @@ int gqa_attn_prefill_from_host(const float* q_host, const float* k_host, const f
   cudaStream_t h2d = nullptr, d2h = nullptr;
   if (int rc = copy_streams(&h2d, &d2h); rc != ATTN_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int nchunks = (B + rows - 1) / rows;
+  const int nchunks = plan.chunks;
 
   // events: [0] entry, [1] host->device done, [2] device->host done,
   // [3 + c] chunk c landed, [3 + nchunks + c] chunk c's output written
@@ -130,44 +153,57 @@ int gqa_attn_prefill_from_host(const float* q_host, const float* k_host, const f
   if (rc == ATTN_OK) rc = gqa::record_cuda_error(cudaStreamWaitEvent(h2d, ev[0], 0));
   if (rc == ATTN_OK) rc = gqa::record_cuda_error(cudaStreamWaitEvent(d2h, ev[0], 0));
 
-  const size_t q_row = (size_t)H * L * D, kv_row = (size_t)Hkv * L * D;
-  const size_t cache_row = (size_t)Hkv * capacity * D;
+  // chunk c: rows [b0, b0 + nb), kv heads [h0, h0 + nh); element offsets of its
+  // q/out, k/v and cache runs
+  struct Chunk {
+    int b0, nb, h0, nh;
+    size_t q_off, kv_off, cache_off;
+  };
+  auto chunk = [&](int c) {
+    Chunk r{};
+    r.b0 = (c / plan.slices) * plan.rows;
+    r.nb = B - r.b0 < plan.rows ? B - r.b0 : plan.rows;
+    r.h0 = (c % plan.slices) * plan.heads;
+    r.nh = Hkv - r.h0 < plan.heads ? Hkv - r.h0 : plan.heads;
+    const size_t head = (size_t)L * D;
+    r.q_off = ((size_t)r.b0 * H + (size_t)r.h0 * G) * head;
+    r.kv_off = ((size_t)r.b0 * Hkv + r.h0) * head;
+    r.cache_off = ((size_t)r.b0 * Hkv + r.h0) * (size_t)capacity * D;
+    return r;
+  };
+  const size_t head_bytes = (size_t)L * D * sizeof(float);
   for (int c = 0; c < nchunks && rc == ATTN_OK; ++c) {
-    const size_t b0 = (size_t)c * rows;
-    const size_t nb = (size_t)((B - (int)b0) < rows ? (B - (int)b0) : rows);
-    rc = gqa::record_cuda_error(cudaMemcpyAsync(q + b0 * q_row, q_host + b0 * q_row,
-                                                nb * q_row * sizeof(float),
+    const Chunk ch = chunk(c);
+    const size_t kv_bytes = (size_t)ch.nb * ch.nh * head_bytes;
+    rc = gqa::record_cuda_error(cudaMemcpyAsync(q + ch.q_off, q_host + ch.q_off, kv_bytes * G,
                                                 cudaMemcpyHostToDevice, h2d));
     if (rc == ATTN_OK)
-      rc = gqa::record_cuda_error(cudaMemcpyAsync(k + b0 * kv_row, k_host + b0 * kv_row,
-                                                  nb * kv_row * sizeof(float),
+      rc = gqa::record_cuda_error(cudaMemcpyAsync(k + ch.kv_off, k_host + ch.kv_off, kv_bytes,
                                                   cudaMemcpyHostToDevice, h2d));
     if (rc == ATTN_OK)
-      rc = gqa::record_cuda_error(cudaMemcpyAsync(v + b0 * kv_row, v_host + b0 * kv_row,
-                                                  nb * kv_row * sizeof(float),
+      rc = gqa::record_cuda_error(cudaMemcpyAsync(v + ch.kv_off, v_host + ch.kv_off, kv_bytes,
                                                   cudaMemcpyHostToDevice, h2d));
     if (rc == ATTN_OK) rc = gqa::record_cuda_error(cudaEventRecord(ev[3 + c], h2d));
   }
   for (int c = 0; c < nchunks && rc == ATTN_OK; ++c) {
-    const size_t b0 = (size_t)c * rows;
-    const int nb = (B - (int)b0) < rows ? (B - (int)b0) : rows;
+    const Chunk ch = chunk(c);
     rc = gqa::record_cuda_error(cudaStreamWaitEvent(s, ev[3 + c], 0));
     if (rc == ATTN_OK)
-      rc = kv_cache_append(k + b0 * kv_row, v + b0 * kv_row, nb, Hkv, L, D, start + b0,
-                           max_start, rp, table, k_norm_w, norm_eps, k_cache + b0 * cache_row,
-                           v_cache + b0 * cache_row, capacity, window, status, s);
+      rc = kv_cache_append(k + ch.kv_off, v + ch.kv_off, ch.nb, ch.nh, L, D, start + ch.b0,
+                           max_start, rp, table, k_norm_w, norm_eps, k_cache + ch.cache_off,
+                           v_cache + ch.cache_off, capacity, window, status, s);
     if (rc == ATTN_OK)
-      rc = gqa_attn_prefill_rope(q + b0 * q_row, k + b0 * kv_row, v + b0 * kv_row,
-                                 out + b0 * q_row, nb, H, Hkv, L, D, start + b0, max_start, rp,
+      rc = gqa_attn_prefill_rope(q + ch.q_off, k + ch.kv_off, v + ch.kv_off, out + ch.q_off,
+                                 ch.nb, ch.nh * G, ch.nh, L, D, start + ch.b0, max_start, rp,
                                  table, q_norm_w, norm_eps, window, softcap, scale, workspace,
                                  workspace_bytes, status, s);
     if (rc == ATTN_OK) rc = gqa::record_cuda_error(cudaEventRecord(ev[3 + nchunks + c], s));
     if (rc == ATTN_OK)
       rc = gqa::record_cuda_error(cudaStreamWaitEvent(d2h, ev[3 + nchunks + c], 0));
     if (rc == ATTN_OK)
-      rc = gqa::record_cuda_error(cudaMemcpyAsync(out_host + b0 * q_row, out + b0 * q_row,
-                                                  (size_t)nb * q_row * sizeof(float),
-                                                  cudaMemcpyDeviceToHost, d2h));
+      rc = gqa::record_cuda_error(cudaMemcpyAsync(
+          out_host + ch.q_off, out + ch.q_off, (size_t)ch.nb * ch.nh * G * head_bytes,
+          cudaMemcpyDeviceToHost, d2h));
   }
 
   // Join: the caller's stream continues after every copy this call enqueued,

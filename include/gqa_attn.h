@@ -199,8 +199,8 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
 /*
  * One whole prefill step with q, k, v and the output in host memory
  * ("mojolearn.transformer", TransformerBlock.forward: the caller hands in the
- * step's tensors and reads the result back). For every batch row: q, k, v are
- * copied to the caller's device buffers, kv_cache_append rotates k in place and
+ * step's tensors and reads the result back). q, k, v are copied to the
+ * caller's device buffers, kv_cache_append rotates k in place and
  * stores k and v at their cache slots, gqa_attn_prefill_rope writes out, and out
  * is copied back to out_host. Results equal those two calls over the whole batch.
  *   q_host, out_host        host [B, H, L, D]; k_host, v_host  host [B, Hkv, L, D].
@@ -213,10 +213,12 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
  *   k_cache, v_cache, capacity, window, k_norm_w: as kv_cache_append;
  *   start, max_start, rp, table, q_norm_w, norm_eps, softcap, scale: as
  *   gqa_attn_prefill_rope; workspace: gqa_attn_prefill_from_host_workspace_size bytes.
- * The batch is cut into at most 8 chunks of rows. Each chunk's host-to-device
- * copies run on one library-owned stream, its kernels on `stream` and its
- * device-to-host copy on another library-owned stream, so copies and kernels of
- * different chunks overlap. The two copy streams of a device are created by the
+ * The step is cut into at most 16 chunks: groups of whole batch rows, or, with
+ * fewer than 16 rows, slices of a row's kv heads together with their query heads
+ * (one chunk when L * D or capacity * D is not a multiple of 4). Each chunk's
+ * host-to-device copies run on one library-owned stream, its kernels on `stream`
+ * and its device-to-host copy on another library-owned stream, so copies and
+ * kernels of different chunks overlap. The two copy streams of a device are created by the
  * first call on it (with that device current) and kept until exit. The call
  * returns once everything is enqueued; `stream` passes the call only after the
  * last copy to out_host. All checks run before anything is enqueued.

@@ -317,8 +317,13 @@ def test_prefill_from_host_refuses_before_any_copy():
     P = ctypes.c_void_p(0x100000)
     rp = g.RopeParams.make(theta=1e4, max_positions=64)
     need = lib.gqa_attn_prefill_from_host_workspace_size(4, 8, 2, 16, 64, 64, ctypes.byref(rp))
-    # one row per chunk at these sizes: the workspace is the one-row prefill's
-    assert need == lib.gqa_attn_prefill_rope_workspace_size(1, 8, 2, 16, 64, ctypes.byref(rp))
+    # 4 rows of 2 kv heads: 8 chunks of one kv head and its 4 query heads each
+    assert need == lib.gqa_attn_prefill_rope_workspace_size(1, 4, 1, 16, 64, ctypes.byref(rp))
+    # 32 rows: 16 chunks of 2 rows; L * D not a multiple of 4: one chunk of every row
+    assert lib.gqa_attn_prefill_from_host_workspace_size(32, 8, 2, 16, 64, 64, ctypes.byref(rp)) \
+        == lib.gqa_attn_prefill_rope_workspace_size(2, 8, 2, 16, 64, ctypes.byref(rp))
+    assert lib.gqa_attn_prefill_from_host_workspace_size(4, 8, 2, 3, 6, 64, ctypes.byref(rp)) \
+        == lib.gqa_attn_prefill_rope_workspace_size(4, 8, 2, 3, 6, ctypes.byref(rp))
 
     def call(B=4, H=8, Hkv=2, L=16, D=64, max_start=0, capacity=64, window=0, ws=P,
              wbytes=need, qh=P, table=P, dev_q=P, rpp=ctypes.byref(rp)):

@@ -1,11 +1,13 @@
 """gqa_attn_prefill_from_host: a prefill step whose inputs and output live in host memory.
 
-The call copies q, k, v in and the output back, chunk by chunk of batch rows, on two copy
-streams around the kernels. Checked against the fp64 oracle, and against the same kernels
-run over the whole batch from device-resident inputs (kv_cache_append then
-gqa_attn_prefill_rope): outputs within the parity bar, caches and rotated k bit for bit.
-Covers one-row chunks, several rows per chunk with a short last chunk, a single chunk
-(rows not a whole number of 16-byte units), a window ring and the CUDA-core head dims."""
+The call copies q, k, v in and the output back chunk by chunk (groups of batch rows, or
+slices of a row's kv heads) on two copy streams around the kernels. Checked against the
+fp64 oracle, and against the same kernels run over the whole batch from device-resident
+inputs (kv_cache_append then gqa_attn_prefill_rope): outputs within the parity bar, caches
+and rotated k bit for bit.
+Covers kv-head slices (a short last slice too), one-row chunks, two rows per chunk with a
+short last chunk, a single chunk (head rows not a whole number of 16-byte units), a window
+ring and the CUDA-core head dims."""
 import pytest
 import torch
 
@@ -22,6 +24,8 @@ CASES = [
     (3, 8, 2, 300, 128, 128, ("llama3", 8.0, 1.0, 4.0, 8192), True, 0, 30.0, (0, 5, 40), 400),
     (2, 4, 2, 130, 256, 256, None, True, 100, 50.0, (0, 7), 100),
     (9, 4, 4, 64, 64, 64, None, False, 0, 0.0, (0,) * 9, 64),
+    (3, 7, 7, 40, 64, 64, None, False, 0, 0.0, (0, 2, 9), 64),
+    (17, 2, 1, 33, 32, 32, None, True, 0, 0.0, tuple(range(17)), 64),
     (2, 2, 1, 3, 6, 6, None, False, 0, 0.0, (0, 1), 5),
 ]
 
