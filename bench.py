@@ -166,6 +166,18 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def reduce_max(ms, dist):
+    """The largest of the ranks' timings, returned on every rank (ms itself with no group).
+    The reduction runs on the GPU under NCCL and on the host under gloo."""
+    if not dist:
+        return ms
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def timed(fn, steps, warmup, dist, events_for=None):
     """Run fn() warmup + steps times; device time of the timed steps (ms, max over ranks)."""
     import torch
@@ -184,9 +196,7 @@ def timed(fn, steps, warmup, dist, events_for=None):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = reduce_max(ms, dist)
         dist.barrier()
     torch.cuda.synchronize()
     return ms
