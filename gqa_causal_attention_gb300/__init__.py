@@ -140,6 +140,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                       i32, i32, f, f, vp, sz, vp, vp]),
             "gqa_attn_decode_static": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32,
                                              i32, i32, i32, f, f, vp, vp]),
+            "attn_selftest_wait_timeout": (i32, [vp, vp]),
             "attn_status_string": (ctypes.c_char_p, [i32]),
             "attn_version": (ctypes.c_char_p, []),
             "attn_last_cuda_error": (ctypes.c_char_p, []),
@@ -198,6 +199,14 @@ def attn_version() -> str:
 def attn_last_cuda_error() -> str:
     """The CUDA error behind the last ATTN_ERR_CUDA on this thread."""
     return load().attn_last_cuda_error().decode()
+
+
+def attn_selftest_wait_timeout(status, stream=None) -> None:
+    """Run the kernels' bounded-wait failure path on purpose: after the wait limit (2 s)
+    the launched block ORs ATTN_DEV_TIMEOUT into status (device int32 [1])."""
+    _i32("status", status)
+    _check("attn_selftest_wait_timeout",
+           load().attn_selftest_wait_timeout(_ptr(status), _stream(stream)))
 
 
 def attn_rope_table_bytes(params: RopeParams, D: int) -> int:

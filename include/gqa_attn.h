@@ -431,6 +431,17 @@ int gqa_attn_decode_static(const float* q, const float* k_cache, const float* v_
                            int H, int Hkv, int D, int capacity, int window, float softcap,
                            float scale, int32_t* status, void* stream);
 
+/*
+ * Self-test of the failure path that every tensor-core kernel carries: one
+ * block waits on pipeline barriers that nothing signals. Its first wait gives
+ * up after the kernels' wait limit (2 s), raises the block's abort flag, the
+ * second wait returns on seeing it, and the block ORs ATTN_DEV_TIMEOUT into
+ * *status (device int32) -- the same code and the same report as a real stall,
+ * with no fault and the context left usable. Enqueued on `stream`; the pages
+ * have no counterpart to it.
+ */
+int attn_selftest_wait_timeout(int32_t* status, void* stream);
+
 /* A static string naming a return code (ATTN_OK / ATTN_ERR_*). */
 const char* attn_status_string(int code);
 

@@ -344,3 +344,7 @@ def test_prefill_from_host_refuses_before_any_copy():
     bad = g.RopeParams.make(theta=1e4, rope_dim=66, max_positions=64)
     assert call(rpp=ctypes.byref(bad)) == -7
     assert call(B=0) == 0 and call(L=0) == 0      # empty: nothing to do
+
+
+def test_wait_timeout_selftest_needs_a_status_word():
+    assert g.load().attn_selftest_wait_timeout(None, None) == -1      # ATTN_ERR_NULL
