@@ -488,29 +488,43 @@ def bench_chunked_prefill(args, dist, dev):
             "launches": 2}
 
 
-def cpu_baseline_prefill(w, budget_s=20.0):
-    """The oracle, as it stands, on a bounded sample of the prefill workload."""
+def cpu_baseline_prefill(w, budget_s=20.0, min_s=10.0):
+    """The oracle, as it stands, on the host cores: the whole prefill workload when it fits
+    the budget (run again until about min_s seconds have been timed), else a sample of
+    whole KV-head groups of batch row 0 at full length."""
     import oracle
     from gqa_causal_attention_gb300 import synthetic as syn
 
-    B1 = 1
-    inp = syn.prefill_inputs(w, B=B1)
-    cfg = oracle.Cfg(B=B1, H=w.H, Hkv=w.Hkv, L=w.L, D=w.D, rope_dim=w.R, theta=w.theta,
-                     scaling=w.scaling, norm_eps=w.norm_eps, window=w.window,
-                     softcap=w.softcap)
-    # calibrate on 2 heads (one KV head when G == 2), then size the sample
-    Hs = max(w.G, 2)
+    def cfg(B, H, Hkv):
+        return oracle.Cfg(B=B, H=H, Hkv=Hkv, L=w.L, D=w.D, rope_dim=w.R, theta=w.theta,
+                          scaling=w.scaling, norm_eps=w.norm_eps, window=w.window,
+                          softcap=w.softcap)
+
+    inp = syn.prefill_inputs(w, B=1)
+    # calibrate on one KV head and its query group of row 0
     t0 = time.perf_counter()
-    oracle.prefill(inp["q"][:, :Hs], inp["k"][:, :Hs // w.G], inp["v"][:, :Hs // w.G], [0],
-                   oracle.Cfg(**{**cfg.__dict__, "H": Hs, "Hkv": Hs // w.G}),
+    oracle.prefill(inp["q"][:, :w.G], inp["k"][:, :1], inp["v"][:, :1], [0], cfg(1, w.G, 1),
                    inp["q_norm_w"], inp["k_norm_w"])
     t1 = time.perf_counter() - t0
-    groups = max(1, min(w.Hkv, int(budget_s / max(t1, 1e-3) * (Hs // w.G))))
+    if t1 * w.B * w.Hkv <= budget_s:
+        full = syn.prefill_inputs(w)
+        runs, dt = 0, 0.0
+        while runs == 0 or (dt < min_s and dt * (runs + 1) / runs <= budget_s):
+            t0 = time.perf_counter()
+            oracle.prefill(full["q"], full["k"], full["v"], [0] * w.B, cfg(w.B, w.H, w.Hkv),
+                           full["q_norm_w"], full["k_norm_w"])
+            dt += time.perf_counter() - t0
+            runs += 1
+        fl = prefill_flops(w)
+        return {"value": fl * runs / dt / 1e12, "unit": "TFLOP/s",
+                "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": f"the whole {w.name} prefill (B={w.B}, H={w.H}, L={w.L}), "
+                          f"{fl:.3e} FLOP, run {runs} times in {dt:.1f} s"}
+    groups = max(1, min(w.Hkv, int(budget_s / max(t1, 1e-3))))
     H2, Hkv2 = groups * w.G, groups
-    sub = oracle.Cfg(**{**cfg.__dict__, "H": H2, "Hkv": Hkv2})
     t0 = time.perf_counter()
-    oracle.prefill(inp["q"][:, :H2], inp["k"][:, :Hkv2], inp["v"][:, :Hkv2], [0], sub,
-                   inp["q_norm_w"], inp["k_norm_w"])
+    oracle.prefill(inp["q"][:, :H2], inp["k"][:, :Hkv2], inp["v"][:, :Hkv2], [0],
+                   cfg(1, H2, Hkv2), inp["q_norm_w"], inp["k_norm_w"])
     dt = time.perf_counter() - t0
     fl = prefill_flops(w, B=1, H=H2)
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(),
