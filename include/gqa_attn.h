@@ -13,14 +13,18 @@
  * Conventions shared by every call
  * --------------------------------
  * - All tensors are fp32, contiguous, row-major, in DEVICE memory owned by the
- *   caller. The library never allocates, frees or keeps device memory.
+ *   caller, except the host buffers of gqa_attn_prefill_from_host. No call
+ *   allocates or frees device memory; the only device memory the library keeps
+ *   is the fixed scratch array of gqa_attn_decode_static, and the only other
+ *   state is the pair of copy streams per device of gqa_attn_prefill_from_host.
  *   Tensor pointers must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
  * - Shapes: Q and outputs [B, H, L, D]; K and V [B, Hkv, L, D]; caches
  *   [B, Hkv, capacity, D]. H % Hkv == 0; query head h reads key/value head
  *   h / (H / Hkv) (contiguous groups). D is even, 2 <= D <= 256.
  * - Positions are absolute: row b's token l sits at start[b] + l.
  * - stream is a cudaStream_t (NULL: the legacy default stream). Every call
- *   only enqueues work on it and returns; nothing is synchronised.
+ *   only enqueues work on it (and, for gqa_attn_prefill_from_host, on its copy
+ *   streams, joined back into it) and returns; nothing is synchronised.
  * - Errors: arguments are checked on the host before anything is launched,
  *   and a negative ATTN_ERR_* is returned with nothing enqueued. Values that
  *   live on the device (start, cache_len) are checked again by the kernels:
