@@ -58,6 +58,22 @@ def test_rope_partial_rotary_hand_case():
     np.testing.assert_allclose(y, want, rtol=0, atol=1e-14)
 
 
+def test_rope_two_dims_turn_by_the_absolute_position():
+    """At D = 2 the one pair has frequency theta^0 = 1, so the angle is the position itself:
+    (1, 0) at position p becomes (cos p, sin p), with p = start[b] + l for every row."""
+    B, H, L = 3, 2, 4
+    start = [0, 5, 11]
+    x = np.zeros((B, H, L, 2))
+    x[..., 0] = 1.0
+    y = oracle.rotate(x, start, oracle.Cfg(B=B, H=H, Hkv=H, L=L, D=2, theta=123.0))
+    for b in range(B):
+        for h in range(H):
+            for l in range(L):
+                p = start[b] + l
+                np.testing.assert_allclose(y[b, h, l], [math.cos(p), math.sin(p)], rtol=0,
+                                           atol=1e-15)
+
+
 @pytest.mark.parametrize("D,R", [(16, 16), (64, 32), (128, 64)])
 def test_rope_preserves_norm_and_position_zero_is_identity(D, R):
     L = 7
@@ -262,6 +278,22 @@ def test_default_scale_under_partial_rotary_is_full_head_dim():
         torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), is_causal=True,
         enable_gqa=True).numpy()
     np.testing.assert_allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+def test_sampled_rows_equal_the_full_prefill_rows():
+    """attention_rows computes chosen (b, h, l) rows alone; they equal those rows of the
+    whole prefill, with the query's batch row, head and position all taken from the triple."""
+    B, H, Hkv, L, D = 3, 6, 3, 13, 8
+    q = RNG.standard_normal((B, H, L, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    start = [0, 4, 9]
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=5, softcap=2.0)
+    full = oracle.attention(q, k, v, start, cfg)
+    rows = [(0, 0, 0), (2, 5, 12), (1, 3, 7), (2, 0, 4), (0, 4, 11), (1, 1, 0)]
+    got = oracle.attention_rows(q, k, v, start, cfg, rows)
+    for i, (b, h, l) in enumerate(rows):
+        np.testing.assert_array_equal(got[i], full[b, h, l])
 
 
 def test_gqa_equals_mha_over_repeated_kv():

@@ -95,6 +95,20 @@ MUTANTS = [
     ("decode_positions_are_slots", "oracle.c", "pos[n] = m;", "pos[n] = slot_of(m, W);"),
     ("decode_interleaved_groups", "oracle.c", "int b = (int)(r / H), h = (int)(r % H), hk = h / G;",
      "int b = (int)(r / H), h = (int)(r % H), hk = h % Hkv; (void)G;"),
+    ("sampled_rows_head_and_position_swapped", "oracle.c",
+     "rows[3 * i], rows[3 * i + 1], rows[3 * i + 2]",
+     "rows[3 * i], rows[3 * i + 2], rows[3 * i + 1]"),
+    ("rotate_rows_position_index", "oracle.c",
+     "int l = (int)(r % L);\n        const double* xr",
+     "int l = (int)((r / L) % L);\n        const double* xr"),
+    ("rotate_rows_first_batch_start", "oracle.c", "int b = (int)(r / ((long)NH * L));",
+     "int b = 0; (void)NH;"),
+    ("append_values_from_keys", "oracle.c", "memcpy(vc + dst, v + src, sizeof(double) * D);",
+     "memcpy(vc + dst, kr + src, sizeof(double) * D);"),
+    ("append_records_the_slot", "oracle.c",
+     "written[((long)b * Hkv + hk) * capacity + s] = m;",
+     "written[((long)b * Hkv + hk) * capacity + s] = s;"),
+    ("decode_values_from_key_cache", "oracle.c", "vp[n] = vc + off;", "vp[n] = kc + off;"),
     # the ragged batch and the decoder block (numpy, oracle/__init__.py)
     ("ragged_padding_keeps_full_length_rows", "__init__.py",
      "        out[b, :, :n] = o[0]\n",
