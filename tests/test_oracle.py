@@ -386,6 +386,33 @@ def test_carried_decode_equals_prefill(window, L):
         np.testing.assert_allclose(got[:, :, 0], want[:, :, t], rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("window", [0, 6])
+def test_decode_rows_each_use_their_own_cache_length(window):
+    """Rows of one decode call at different lengths: row b's query sits at cache_len[b] - 1
+    and sees only positions up to it, so it equals that position's row of the prefill over
+    the whole sequence (causality), whatever the other rows' lengths."""
+    B, H, Hkv, L, D = 3, 4, 2, 14, 8
+    q = RNG.standard_normal((B, H, L, D))
+    k = RNG.standard_normal((B, Hkv, L, D))
+    v = RNG.standard_normal((B, Hkv, L, D))
+    cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, theta=100.0, window=window, softcap=3.0)
+    want, qr, kr = oracle.prefill(q, k, v, [0] * B, cfg)
+    lens = [5, 14, 9]
+    # each row's cache after its first lens[b] tokens, filled here slot by slot (slot = m, or
+    # m mod W in a ring of W slots)
+    cap = window or L
+    kc = np.zeros((B, Hkv, cap, D))
+    vc = np.zeros((B, Hkv, cap, D))
+    for b, n in enumerate(lens):
+        for m in range(n):
+            kc[b, :, m % cap] = kr[b, :, m]
+            vc[b, :, m % cap] = v[b, :, m]
+    qsel = np.stack([qr[b, :, n - 1] for b, n in enumerate(lens)])[:, :, None]
+    got = oracle.decode(qsel, kc, vc, lens, oracle.Cfg(**{**cfg.__dict__, "L": 1}))
+    for b, n in enumerate(lens):
+        np.testing.assert_allclose(got[b, :, 0], want[b, :, n - 1], rtol=1e-12, atol=1e-13)
+
+
 def test_ring_slots_hold_the_last_window_positions():
     """Under a window the cache is a ring of W slots, slot = position % W
     ("mojolearn.transformer", TransformerState)."""

@@ -109,6 +109,8 @@ MUTANTS = [
      "written[((long)b * Hkv + hk) * capacity + s] = m;",
      "written[((long)b * Hkv + hk) * capacity + s] = s;"),
     ("decode_values_from_key_cache", "oracle.c", "vp[n] = vc + off;", "vp[n] = kc + off;"),
+    ("decode_rows_share_the_first_length", "oracle.c", "long p = (long)cache_len[b] - 1;",
+     "long p = (long)cache_len[0] - 1;"),
     # the ragged batch and the decoder block (numpy, oracle/__init__.py)
     ("ragged_padding_keeps_full_length_rows", "__init__.py",
      "        out[b, :, :n] = o[0]\n",
