@@ -243,6 +243,31 @@ def test_attention_matches_brute_force(H, Hkv, L, D, window, softcap, start):
     np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
 
 
+def test_attention_matches_brute_force_random_sweep():
+    """40 random small problems: head dims, group sizes, lengths (1 included), windows from 1
+    to past L, softcap on or off, explicit scales, per-row starts."""
+    rng = np.random.default_rng(77)
+    for _ in range(40):
+        D = int(rng.choice([2, 4, 6, 8, 10]))
+        Hkv = int(rng.integers(1, 3))
+        H = Hkv * int(rng.integers(1, 5))
+        L = int(rng.integers(1, 11))
+        B = int(rng.integers(1, 3))
+        window = int(rng.choice([0, 0, 1, 2, 3, L, L + 2]))
+        softcap = float(rng.choice([0.0, 0.0, 0.7, 4.0]))
+        scale = float(rng.choice([0.0, 0.0, 0.2, 1.3]))
+        start = [int(x) for x in rng.integers(0, 50, B)]
+        q = 2.0 * rng.standard_normal((B, H, L, D))
+        k = 2.0 * rng.standard_normal((B, Hkv, L, D))
+        v = rng.standard_normal((B, Hkv, L, D))
+        cfg = oracle.Cfg(B=B, H=H, Hkv=Hkv, L=L, D=D, window=window, softcap=softcap,
+                         scale=scale)
+        got = oracle.attention(q, k, v, start, cfg)
+        want = brute_force(q, k, v, start, H, Hkv, window, softcap,
+                           scale if scale > 0 else None)
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-13)
+
+
 @pytest.mark.parametrize("B,H,Hkv,L,D", [(2, 8, 2, 37, 16), (1, 4, 4, 20, 32), (1, 8, 1, 33, 8)])
 def test_attention_matches_torch_sdpa(B, H, Hkv, L, D):
     q = RNG.standard_normal((B, H, L, D))
