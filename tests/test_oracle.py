@@ -58,6 +58,28 @@ def test_rope_partial_rotary_hand_case():
     np.testing.assert_allclose(y, want, rtol=0, atol=1e-14)
 
 
+def test_rotate_half_is_the_printed_interleaved_rope_up_to_a_dim_permutation():
+    """"Core Layers -- Deep Reference", RoPE, prints pairs (2i, 2i+1) turned by p * theta_i;
+    the oracle pairs (i, i + R/2). Laying dims out so that interleaved dim 2i is half dim i and
+    2i+1 is half dim i + R/2 makes the two the same rotation, and since scores are dot
+    products, the same attention for q and k permuted alike."""
+    B, H, L, D, theta = 1, 2, 6, 8, 100.0
+    R = D
+    x_int = RNG.standard_normal((B, H, L, D))
+    perm = [2 * i for i in range(R // 2)] + [2 * i + 1 for i in range(R // 2)]
+    x_half = x_int[..., perm]                     # half dim j holds interleaved dim perm[j]
+    y_half = oracle.rotate(x_half, [3], oracle.Cfg(B=B, H=H, Hkv=H, L=L, D=D, theta=theta))
+    want = np.empty_like(x_int)                   # the printed interleaved form
+    for l in range(L):
+        p = 3 + l
+        for i in range(R // 2):
+            ang = p * theta ** (-2.0 * i / R)
+            a, b = x_int[..., l, 2 * i], x_int[..., l, 2 * i + 1]
+            want[..., l, 2 * i] = a * math.cos(ang) - b * math.sin(ang)
+            want[..., l, 2 * i + 1] = a * math.sin(ang) + b * math.cos(ang)
+    np.testing.assert_allclose(y_half, want[..., perm], rtol=0, atol=1e-13)
+
+
 def test_rope_two_dims_turn_by_the_absolute_position():
     """At D = 2 the one pair has frequency theta^0 = 1, so the angle is the position itself:
     (1, 0) at position p becomes (cos p, sin p), with p = start[b] + l for every row."""
