@@ -348,3 +348,46 @@ def test_prefill_from_host_refuses_before_any_copy():
 
 def test_wait_timeout_selftest_needs_a_status_word():
     assert g.load().attn_selftest_wait_timeout(None, None) == -1      # ATTN_ERR_NULL
+
+
+def test_no_cpu_fallback_host_tensors_are_refused():
+    """Every compute entry point of the binding takes device tensors only: host tensors are
+    refused with an error, never computed some other way."""
+    q = torch.zeros(1, 4, 8, 64)
+    k = torch.zeros(1, 2, 8, 64)
+    st = torch.zeros(1, dtype=torch.int32)
+    rp = g.RopeParams.make(theta=1e4, max_positions=64)
+    calls = [
+        lambda: g.gqa_attn_prefill(q, k, k, q),
+        lambda: g.attn_rope_apply(q, st, 0, rp, torch.zeros(64 * 32 * 2)),
+        lambda: g.kv_cache_append(k, k, st, 0, rp, torch.zeros(64 * 32 * 2), None, 1e-6,
+                                  torch.zeros(1, 2, 8, 64), torch.zeros(1, 2, 8, 64)),
+        lambda: g.gqa_attn_decode(q[:, :, :1], k, k, torch.ones(1, dtype=torch.int32), 1,
+                                  q[:, :, :1].clone()),
+        lambda: g.gqa_attn_decode_static(q[:, :, :1], k, k, torch.ones(1, dtype=torch.int32),
+                                         1, q[:, :, :1].clone()),
+    ]
+    for call in calls:
+        with pytest.raises((ValueError, TypeError)):
+            call()
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without the built CUDA library the package raises on load; nothing runs in its place."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "gqa_causal_attention_gb300"
+    shutil.copytree(os.path.join(ROOT, "gqa_causal_attention_gb300"), pkg,
+                    ignore=shutil.ignore_patterns("_build", "__pycache__", "*.so"))
+    code = ("import gqa_causal_attention_gb300 as g\n"
+            "try:\n"
+            "    g.load(build_if_missing=False)\n"
+            "except OSError as e:\n"
+            "    print('refused', type(e).__name__)\n"
+            "else:\n"
+            "    print('loaded')\n")
+    env = {k: v for k, v in os.environ.items() if k != "PYTHONPATH"}
+    out = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, env=env,
+                         capture_output=True, text=True, timeout=300)
+    assert out.stdout.strip() == "refused OSError", out.stdout + out.stderr
