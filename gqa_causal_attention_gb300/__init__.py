@@ -2,7 +2,8 @@
 
 Every function here has the name of the C entry point it wraps (see
 ``include/gqa_attn.h``) and does argument marshalling only: it checks dtypes,
-devices and contiguity, passes device pointers and the current CUDA stream,
+devices and contiguity, passes tensor pointers (device memory, and the host buffers
+of gqa_attn_prefill_from_host) and the current CUDA stream,
 and raises ``AttnError`` on a non-zero return code. All arithmetic runs in the
 library's CUDA kernels; there is no fallback of any kind. If the library is
 missing or cannot load, every call raises.
@@ -29,6 +30,8 @@ __all__ = [
     "gqa_attn_prefill_ragged", "gqa_attn_prefill_ragged_workspace_size",
     "gqa_attn_prefill_identical", "gqa_attn_decode_identical",
     "gqa_block_forward", "gqa_block_forward_workspace_size", "BLOCK_WEIGHT_NAMES",
+    "gqa_attn_prefill_from_host", "gqa_attn_prefill_from_host_workspace_size",
+    "attn_selftest_wait_timeout",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]

@@ -391,3 +391,9 @@ def test_missing_library_fails_loudly(tmp_path):
     out = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, env=env,
                          capture_output=True, text=True, timeout=300)
     assert out.stdout.strip() == "refused OSError", out.stdout + out.stderr
+
+
+def test_every_declared_function_has_a_binding_of_the_same_name():
+    missing = [f for f in declared_functions()
+               if f not in g.__all__ or not callable(getattr(g, f, None))]
+    assert not missing, missing
