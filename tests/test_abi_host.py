@@ -397,3 +397,32 @@ def test_every_declared_function_has_a_binding_of_the_same_name():
     missing = [f for f in declared_functions()
                if f not in g.__all__ or not callable(getattr(g, f, None))]
     assert not missing, missing
+
+
+def test_from_host_chunk_plan_follows_the_documented_rule():
+    """At most 16 chunks: groups of ceil(B / 16) rows when B >= 16; with fewer rows, slices of
+    ceil(Hkv / (16 // B)) kv heads of one row; one chunk of everything when a head's rows
+    (L * D or capacity * D floats) are not whole 16-byte units. Seen through the workspace
+    size, which is the prefill workspace of the largest chunk (rope_dim 32 < D keeps q's
+    rotation out of the kernel, so the size grows with the chunk's query heads)."""
+    lib = g.load()
+    G = 2
+    cases = [(64, g.RopeParams.make(theta=1e4, rope_dim=32, max_positions=4096),
+              ((64, 64), (33, 64), (3, 66), (64, 5))),
+             (6, g.RopeParams.make(theta=1e4, max_positions=4096),      # CUDA-core head dim
+              ((64, 64), (33, 64), (64, 33), (2, 2)))]
+    shapes = [(D, rp, L, cap, B, Hkv) for D, rp, sizes in cases for L, cap in sizes
+              for B in (1, 2, 3, 5, 8, 15, 16, 17, 40) for Hkv in (1, 2, 3, 8)]
+    for D, rp, L, cap, B, Hkv in shapes:
+        H = G * Hkv
+        if (L * D) % 4 or (cap * D) % 4:
+            rows, heads = B, Hkv
+        elif B >= 16:
+            rows, heads = -(-B // 16), Hkv
+        else:
+            rows, heads = 1, -(-Hkv // (16 // B))
+        want = lib.gqa_attn_prefill_rope_workspace_size(rows, heads * G, heads, L, D,
+                                                        ctypes.byref(rp))
+        got = lib.gqa_attn_prefill_from_host_workspace_size(B, H, Hkv, L, D, cap,
+                                                            ctypes.byref(rp))
+        assert got == want, (D, B, Hkv, L, cap, got, want)
