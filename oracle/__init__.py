@@ -151,8 +151,7 @@ def _ip(a: np.ndarray):
 
 
 def inv_freq(cfg: Cfg) -> np.ndarray:
-    """Rotary frequencies theta_i (with scaling), length R/2. Parity unpinned inside the
-    Llama-3 ramp (0 < s < 1): only its end points, continuity and bounds are pinned."""
+    """Rotary frequencies theta_i (with scaling), length R/2."""
     cc = cfg.c()
     out = np.zeros(max(cc.rope_dim // 2, 1), dtype=np.float64)
     lib().orc_inv_freq(ctypes.byref(cc), _dp(out))

@@ -30,11 +30,10 @@
  *   - softcap c*tanh(s/c) acts on the scaled score, before masking;
  *   - the default scale is 1/sqrt(D), with D the full head dimension.
  *
- * Parity unpinned: the interior of the Llama-3 ramp (0 < s < 1 in
- * orc_inv_freq). The pages name only its fields; the tests pin both ends of
- * the ramp, its continuity there, the interior lying between the two branches
- * and RoPE's relative-position invariance under the scaled frequencies, but no
- * independent value of an interior frequency.
+ * The interior of the Llama-3 ramp (0 < s < 1 in orc_inv_freq) is pinned by
+ * three frequencies of the Llama-3-8B-shaped workload worked by hand from the
+ * published Llama 3.1 rule (tests/golden/llama3_ramp_interior.txt) and by
+ * f'/f being affine in f there, besides both ends of the ramp.
  */
 #include <math.h>
 #include <stdlib.h>
@@ -76,8 +75,7 @@ int orc_num_threads(void)
  * "llama3"): a frequency whose wavelength 2*pi/f is shorter than
  * orig/high_freq_factor is kept, one longer than orig/low_freq_factor is
  * divided by the factor, and in between the two are blended linearly in
- * s = (orig/wavelength - low) / (high - low). (Parity unpinned inside the
- * ramp; see the header.)
+ * s = (orig/wavelength - low) / (high - low).
  */
 void orc_inv_freq(const orc_cfg* c, double* inv)
 {

@@ -171,6 +171,43 @@ def test_llama3_scaling_special_cases():
         assert abs(vals[0] - vals[1]) <= 1e-7 * abs(vals[0])
 
 
+def test_llama3_ramp_interior_hand_worked():
+    """Three frequencies inside the Llama-3 ramp of the Llama-3-8B-shaped
+    workload, worked by hand from the published Llama 3.1 rule (linear blend
+    in frequency), fix the interior arithmetic: a blend in wavelength or in
+    log-frequency stays continuous and bounded but misses these values."""
+    fx = _fixture("llama3_ramp_interior.txt")
+    cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=128, theta=5e5,
+                     scaling=("llama3", 8.0, 1.0, 4.0, 8192))
+    inv = oracle.inv_freq(cfg)
+    for i in (32, 29, 34):
+        want = float(fx[f"f{i}"])
+        assert abs(inv[i] - want) <= 1e-12 * want, (i, inv[i], want)
+
+
+def test_llama3_ramp_ratio_is_affine_in_frequency():
+    """Inside the ramp s is affine in 1/wavelength, i.e. in f, so the published
+    rule makes f'/f = 1/factor + (1 - 1/factor) * s an affine function of f.
+    Checked over every interior pair, for two bases (no fixed values)."""
+    for theta in (5e5, 2.5e5):
+        cfg = oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=128, theta=theta,
+                         scaling=("llama3", 8.0, 1.0, 4.0, 8192))
+        plain = oracle.inv_freq(oracle.Cfg(B=1, H=1, Hkv=1, L=1, D=128, theta=theta))
+        sc = oracle.inv_freq(cfg)
+        wl = 2 * math.pi / plain
+        mid = (wl >= 8192 / 4.0) & (wl <= 8192 / 1.0)
+        assert mid.sum() >= 4
+        f, ratio = plain[mid], sc[mid] / plain[mid]
+        slope, icpt = np.polyfit(f, ratio, 1)
+        np.testing.assert_allclose(ratio, slope * f + icpt, rtol=0, atol=1e-12)
+        # the line is fixed too: ratio 1/factor where s = 0 (f = 2*pi*low/orig) and
+        # 1 where s = 1 (f = 2*pi*high/orig)
+        np.testing.assert_allclose(slope * (2 * math.pi * 1.0 / 8192) + icpt, 1 / 8.0,
+                                   rtol=0, atol=1e-12)
+        np.testing.assert_allclose(slope * (2 * math.pi * 4.0 / 8192) + icpt, 1.0,
+                                   rtol=0, atol=1e-12)
+
+
 # ----------------------------------------------------------------------------- RMSNorm
 
 

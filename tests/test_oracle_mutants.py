@@ -46,6 +46,14 @@ MUTANTS = [
      "f = s * f / c->factor + (1.0 - s) * f;"),
     ("llama3_ramp_high_low_swapped", "oracle.c",
      "(c->high_freq_factor - c->low_freq_factor)", "(c->low_freq_factor - c->high_freq_factor)"),
+    ("llama3_ramp_blends_wavelengths", "oracle.c", "f = (1.0 - s) * f / c->factor + s * f;",
+     "f = 1.0 / ((1.0 - s) * c->factor / f + s / f);"),
+    ("llama3_ramp_blends_log_frequency", "oracle.c", "f = (1.0 - s) * f / c->factor + s * f;",
+     "f = exp((1.0 - s) * log(f / c->factor) + s * log(f));"),
+    ("llama3_ramp_s_linear_in_wavelength", "oracle.c",
+     "double s = (c->original_max_positions / wavelength - c->low_freq_factor) /\n"
+     "                           (c->high_freq_factor - c->low_freq_factor);",
+     "double s = (long_wl - wavelength) / (long_wl - short_wl);"),
     ("llama3_short_and_long_swapped", "oracle.c",
      "double short_wl = c->original_max_positions / c->high_freq_factor;",
      "double short_wl = c->original_max_positions / c->low_freq_factor;"),
