@@ -76,6 +76,25 @@ int cuda_status(cudaError_t e) {
 
 int gqa::record_cuda_error(cudaError_t e) { return cuda_status(e); }
 
+// Every host check of gqa_attn_decode except the workspace's: ATTN_OK (also for
+// B == 0, when there is nothing to do) or the ATTN_ERR_* the call would return.
+int gqa::decode_host_check(const float* q, const float* k_cache, const float* v_cache,
+                           const int32_t* cache_len, int32_t max_cache_len, const float* out,
+                           int B, int H, int Hkv, int D, int capacity, int window, float softcap,
+                           float scale) {
+  if (!dims_ok(B, H, 1, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || capacity < 1)
+    return ATTN_ERR_SHAPE;
+  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (B == 0) return ATTN_OK;
+  if (max_cache_len < 1) return ATTN_ERR_SHAPE;
+  if (window == 0 && max_cache_len > capacity) return ATTN_ERR_CAPACITY;
+  if (!q || !k_cache || !v_cache || !cache_len || !out) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return ATTN_ERR_ALIGN;
+  return ATTN_OK;
+}
+
 extern "C" {
 
 const char* attn_version(void) { return "0.1.0"; }
@@ -634,16 +653,9 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
                     const int32_t* cache_len, int32_t max_cache_len, float* out, int B, int H,
                     int Hkv, int D, int capacity, int window, float softcap, float scale,
                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
-  if (!dims_ok(B, H, 1, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || capacity < 1)
-    return ATTN_ERR_SHAPE;
-  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
-  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
-  if (B == 0) return ATTN_OK;
-  if (max_cache_len < 1) return ATTN_ERR_SHAPE;
-  if (window == 0 && max_cache_len > capacity) return ATTN_ERR_CAPACITY;
-  if (!q || !k_cache || !v_cache || !cache_len || !out) return ATTN_ERR_NULL;
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-    return ATTN_ERR_ALIGN;
+  const int rc = gqa::decode_host_check(q, k_cache, v_cache, cache_len, max_cache_len, out, B, H,
+                                        Hkv, D, capacity, window, softcap, scale);
+  if (rc != ATTN_OK || B == 0) return rc;
   gqa::DecodeJob j{};
   j.q = q; j.k_cache = k_cache; j.v_cache = v_cache; j.cache_len = cache_len;
   j.max_cache_len = max_cache_len; j.out = out;

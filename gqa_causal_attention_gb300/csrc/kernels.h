@@ -37,6 +37,13 @@ struct RopeJob {
 // thread and returns ATTN_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
 
+// The host checks of gqa_attn_decode other than its workspace (api.cu): ATTN_OK,
+// also when B == 0 (nothing to do), or the ATTN_ERR_* that call would return.
+int decode_host_check(const float* q, const float* k_cache, const float* v_cache,
+                      const int32_t* cache_len, int32_t max_cache_len, const float* out, int B,
+                      int H, int Hkv, int D, int capacity, int window, float softcap,
+                      float scale);
+
 cudaError_t launch_rope_table(const InvFreq& inv, int R, int max_positions, float2* table,
                               cudaStream_t stream);
 cudaError_t launch_rope_rows(const RopeJob& job, cudaStream_t stream);

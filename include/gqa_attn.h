@@ -423,8 +423,12 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
  * The call allocates nothing.
  *
  * - The first call on a device, with that device current, looks up the
- *   array's device address (cudaGetSymbolAddress) and keeps it; make that
- *   first call before any stream capture.
+ *   array's device address (cudaGetSymbolAddress) and keeps it for that
+ *   device's current context; after cudaDeviceReset (a new context) the next
+ *   call looks it up again. Make the first call on a device, and the first
+ *   after a reset, before any stream capture.
+ * - Host checks are those of gqa_attn_decode and come first, with its return
+ *   codes; only then is the scratch size compared with the array.
  * - All calls share the one array and it keeps the last call's contents;
  *   nothing in it has to start at zero. Calls whose work overlaps on the GPU
  *   (other streams, other host threads) race on it: order them on one stream.

@@ -346,6 +346,40 @@ def test_prefill_from_host_refuses_before_any_copy():
     assert call(B=0) == 0 and call(L=0) == 0      # empty: nothing to do
 
 
+@no_device
+def test_static_scratch_refuses_sizes_beyond_the_array():
+    # 64 rows x 256 heads x (tens of splits) x 258 floats: far more than 32 MiB
+    B, H, Hkv, D, maxlen = 64, 256, 8, 256, 8193
+    assert g.gqa_attn_decode_workspace_size(B, H, Hkv, D, maxlen, 0) > (32 << 20)
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)        # never dereferenced: refused before any launch
+    rc = lib.gqa_attn_decode_static(P, P, P, P, maxlen, P, B, H, Hkv, D, 8193, 0, 0.0, 0.0,
+                                    None, None)
+    assert rc == -5
+
+
+@no_device
+def test_static_scratch_refuses_like_the_workspace_decode():
+    """Host refusals come from gqa_attn_decode's own checks, before the size
+    check: a bad shape or capacity reports that, not the scratch size."""
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)        # never dereferenced: refused before any launch
+    big = (64, 256, 8, 256, 8193)        # scratch far beyond the array
+    B, H, Hkv, D, maxlen = big
+    # H % Hkv != 0 -> shape, even though the scratch would also be too large
+    assert lib.gqa_attn_decode_static(P, P, P, P, maxlen, P, B, H, 7, D, 8193, 0, 0.0, 0.0,
+                                      None, None) == -2
+    # positions beyond the capacity without a window -> capacity
+    assert lib.gqa_attn_decode_static(P, P, P, P, maxlen, P, B, H, Hkv, D, 100, 0, 0.0, 0.0,
+                                      None, None) == -4
+    # a NULL tensor -> null
+    assert lib.gqa_attn_decode_static(None, P, P, P, maxlen, P, B, H, Hkv, D, 8193, 0, 0.0,
+                                      0.0, None, None) == -1
+    # an empty batch is a no-op, as for the workspace decode
+    assert lib.gqa_attn_decode_static(None, None, None, None, 0, None, 0, H, Hkv, D, 8193, 0,
+                                      0.0, 0.0, None, None) == 0
+
+
 def test_wait_timeout_selftest_needs_a_status_word():
     assert g.load().attn_selftest_wait_timeout(None, None) == -1      # ATTN_ERR_NULL
 

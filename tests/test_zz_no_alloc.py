@@ -6,8 +6,9 @@ not allocate after start-up: its split-KV scratch is a fixed array inside the
 library. This file sorts last so that a run stopping at the first failure has
 already run every other test; it also passes on its own in a fresh process.
 
-Two calls in a row, through the C ABI, must match gqa_attn_decode (which uses
-a caller workspace) within the parity tolerance.
+Two calls in a row, through the C ABI, must give the bits of gqa_attn_decode
+(which uses a caller workspace): both run the same kernels with the same split
+plan, so any difference would mean a wrong plan or a stale scratch address.
 """
 import ctypes
 
@@ -17,7 +18,7 @@ import torch
 import gqa_causal_attention_gb300 as g
 from gqa_causal_attention_gb300 import synthetic as syn
 
-from gpu_util import TOL_MAX, TOL_MEAN, assert_close, dev
+from gpu_util import dev
 
 pytestmark = pytest.mark.gpu
 
@@ -57,17 +58,7 @@ def _decode_pair(B, H, Hkv, D, cap, window, softcap, lengths, seed):
 def test_static_scratch_decode_matches_workspace_decode(B, H, Hkv, D, cap, window, softcap,
                                                         lengths):
     ref, outs = _decode_pair(B, H, Hkv, D, cap, window, softcap, lengths, seed=41)
+    assert torch.isfinite(ref).all()
     for out in outs:
-        assert_close(out, ref.double().cpu().numpy(), "static vs workspace decode",
-                     max_tol=TOL_MAX, mean_tol=TOL_MEAN)
+        assert torch.equal(out, ref), (out - ref).abs().max().item()
 
-
-def test_static_scratch_refuses_sizes_beyond_the_array():
-    # 64 rows x 256 heads x (tens of splits) x 258 floats: far more than 32 MiB
-    B, H, Hkv, D, maxlen = 64, 256, 8, 256, 8193
-    assert g.gqa_attn_decode_workspace_size(B, H, Hkv, D, maxlen, 0) > (32 << 20)
-    lib = g.load()
-    P = ctypes.c_void_p(0x100000)        # never dereferenced: refused before any launch
-    rc = lib.gqa_attn_decode_static(P, P, P, P, maxlen, P, B, H, Hkv, D, 8193, 0, 0.0, 0.0,
-                                    None, None)
-    assert rc == -5
