@@ -30,6 +30,7 @@ __all__ = [
     "gqa_attn_prefill_ragged", "gqa_attn_prefill_ragged_workspace_size",
     "gqa_attn_prefill_identical", "gqa_attn_decode_identical",
     "gqa_block_forward", "gqa_block_forward_workspace_size", "BLOCK_WEIGHT_NAMES",
+    "attn_linear",
     "gqa_attn_prefill_from_host", "gqa_attn_prefill_from_host_workspace_size",
     "attn_selftest_wait_timeout",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
@@ -138,6 +139,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_block_forward_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, rp]),
             "gqa_block_forward": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, f, rp,
                                         vp, i32, f, f, vp, sz, vp, vp]),
+            "attn_linear": (i32, [vp, vp, vp, vp, ctypes.c_long, i32, i32, vp, vp]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -587,6 +589,21 @@ BLOCK_WEIGHT_NAMES = (
 
 class _BlockWeights(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f, _ in BLOCK_WEIGHT_NAMES]
+
+
+def attn_linear(x, w, y, residual=None, status=None, stream=None) -> None:
+    """y = x w^T (+ residual) on the tensor cores: x [T, K], w [N, K] (torch's [out, in]),
+    y and residual [T, N]; K and N multiples of 4."""
+    _f32("x", x, 2); _f32("w", w, 2); _f32("y", y, 2); _f32("residual", residual, 2)
+    _i32("status", status)
+    T, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or tuple(y.shape) != (T, N) or (
+            residual is not None and tuple(residual.shape) != (T, N)):
+        raise ValueError("attn_linear: x [T, K], w [N, K], y and residual [T, N]")
+    rc = load().attn_linear(_ptr(x), _ptr(w), _ptr(residual), _ptr(y), T, N, K, _ptr(status),
+                            _stream(stream))
+    _check("attn_linear", rc)
 
 
 def gqa_block_forward_workspace_size(B: int, L: int, H: int, Hkv: int, D: int, IT: int,

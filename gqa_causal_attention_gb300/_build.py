@@ -68,12 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if lg.strip():
                 print(f"--- {os.path.basename(s)}\n{lg}", file=sys.stderr)
     tmp = LIB + f".tmp{os.getpid()}"
-    # cuBLAS (the decoder block's fp32 projections) from the toolkit, found at run time
-    # through the toolkit's library directory.
-    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
-    link = ["-L", cuda_lib, "-lcublas", "-Xlinker", "-rpath," + cuda_lib] \
-        if os.path.isdir(cuda_lib) else ["-lcublas"]
-    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs + link
+    cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}{r.stderr}")

@@ -514,17 +514,40 @@ size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cach
   return (size_t)B * H * nsplit * (D + 2) * sizeof(float);
 }
 
+namespace {
+// Workspace of gqa_block_forward, in order (each part 256-byte aligned):
+// zero start [B] | normed rows [T, d_model] | q [B, H, L, D] | k, v [B, Hkv, L, D] |
+// attention output [B, H, L, D] | its token-major copy [T, d_model] (only when
+// D % 32 != 0) | SwiGLU activations [T, IT] | the attention's own workspace.
+struct BlockLayout {
+  size_t zs, nrm, qh, kh, vh, ao, aot, act, attn, total;
+};
+BlockLayout block_layout(int B, int L, int H, int Hkv, int D, int IT, size_t attn_bytes) {
+  const size_t T = (size_t)B * L, QW = (size_t)H * D, KW = (size_t)Hkv * D;
+  BlockLayout y{};
+  size_t p = 0;
+  auto take = [&](size_t bytes) { const size_t r = p; p += round256(bytes); return r; };
+  y.zs = take((size_t)B * 4);
+  y.nrm = take(T * QW * 4);
+  y.qh = take(T * QW * 4);
+  y.kh = take(T * KW * 4);
+  y.vh = take(T * KW * 4);
+  y.ao = take(T * QW * 4);
+  y.aot = D % 32 ? take(T * QW * 4) : p;
+  y.act = take(T * (size_t)IT * 4);
+  y.attn = take(attn_bytes);
+  y.total = p;
+  return y;
+}
+}  // namespace
+
 size_t gqa_block_forward_workspace_size(int B, int L, int H, int Hkv, int D, int IT,
                                         const attn_rope_params* rp) {
   if (B < 0 || L < 0 || H < 1 || Hkv < 1 || H % Hkv != 0 || IT < 1 || !rope_params_ok(rp, D))
     return 0;
-  const size_t T = (size_t)B * L, QW = (size_t)H * D, KW = (size_t)Hkv * D;
   const size_t attn = gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp);
   if (attn == 0) return 0;
-  // zero start [B] | normed rows [T, QW] | q, attention out [T, QW] x 2 | k, v token- and
-  // head-major [T, KW] x 4 | gate, up [T, IT] x 2 | the attention's own workspace
-  return round256((size_t)B * 4) + round256(T * QW * 4) * 3 + round256(T * KW * 4) * 4 +
-         round256(T * (size_t)IT * 4) * 2 + round256(attn);
+  return block_layout(B, L, H, Hkv, D, IT, attn).total;
 }
 
 int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, int D, int IT,
@@ -534,74 +557,122 @@ int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, 
                       void* stream) {
   if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || IT < 1 || window < 0)
     return ATTN_ERR_SHAPE;
+  if ((H * D) % 4 || IT % 4) return ATTN_ERR_SHAPE;   // 16-byte rows for the projections
   if (!isfinite(softcap) || !isfinite(scale) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
   if (!rp || !rope_params_ok(rp, D)) return rp ? ATTN_ERR_PARAM : ATTN_ERR_NULL;
   if (B == 0 || L == 0) return ATTN_OK;
   if (!x || !out || !w || !table || !w->input_norm || !w->post_norm || !w->wq || !w->wk ||
       !w->wv || !w->wo || !w->w_gate || !w->w_up || !w->w_down)
     return ATTN_ERR_NULL;
+  if (x == out) return ATTN_ERR_SHAPE;
   if ((int64_t)L - 1 >= (int64_t)max_pos_of(rp)) return ATTN_ERR_POSITION;
   const size_t need = gqa_block_forward_workspace_size(B, L, H, Hkv, D, IT, rp);
   if (need == 0) return ATTN_ERR_SHAPE;
   if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
-  if (!aligned16(workspace) || !aligned16(x) || !aligned16(out) || !aligned16(table))
-    return ATTN_ERR_ALIGN;
+  const float* ptrs[] = {x, out, table, w->input_norm, w->post_norm, w->wq, w->wk, w->wv,
+                         w->wo, w->w_gate, w->w_up, w->w_down, w->q_norm, w->k_norm};
+  for (const float* pp : ptrs)
+    if (pp && !aligned16(pp)) return ATTN_ERR_ALIGN;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const long T = (long)B * L;
   const int QW = H * D, KW = Hkv * D;
-  char* p = static_cast<char*>(workspace);
-  auto take = [&](size_t bytes) { char* r = p; p += round256(bytes); return r; };
-  int32_t* zero_start = reinterpret_cast<int32_t*>(take((size_t)B * 4));
-  float* nrm = reinterpret_cast<float*>(take((size_t)T * QW * 4));
-  float* qt = reinterpret_cast<float*>(take((size_t)T * QW * 4));   // token-major q, attn out
-  float* qh = reinterpret_cast<float*>(take((size_t)T * QW * 4));   // head-major q, attn out
-  float* kt = reinterpret_cast<float*>(take((size_t)T * KW * 4));
-  float* vt = reinterpret_cast<float*>(take((size_t)T * KW * 4));
-  float* kh = reinterpret_cast<float*>(take((size_t)T * KW * 4));
-  float* vh = reinterpret_cast<float*>(take((size_t)T * KW * 4));
-  float* gate = reinterpret_cast<float*>(take((size_t)T * IT * 4));
-  float* up = reinterpret_cast<float*>(take((size_t)T * IT * 4));
-  void* attn_ws = p;
-  const size_t attn_bytes = workspace_bytes - (size_t)(p - static_cast<char*>(workspace));
+  const size_t attn_need = gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp);
+  const BlockLayout lay = block_layout(B, L, H, Hkv, D, IT, attn_need);
+  char* ws = static_cast<char*>(workspace);
+  int32_t* zero_start = reinterpret_cast<int32_t*>(ws + lay.zs);
+  float* nrm = reinterpret_cast<float*>(ws + lay.nrm);
+  float* qh = reinterpret_cast<float*>(ws + lay.qh);
+  float* kh = reinterpret_cast<float*>(ws + lay.kh);
+  float* vh = reinterpret_cast<float*>(ws + lay.vh);
+  float* ao = reinterpret_cast<float*>(ws + lay.ao);
+  float* aot = reinterpret_cast<float*>(ws + lay.aot);
+  float* act = reinterpret_cast<float*>(ws + lay.act);
   const bool offset = norm_offset != 0;
   auto chk = [&](cudaError_t e) { return e == cudaSuccess ? ATTN_OK : cuda_status(e); };
+  auto gemm = [&](const gqa::GemmJob& j) {
+    return gqa::gemm_tc_supports(j) ? chk(gqa::launch_gemm_tc(j, s)) : ATTN_ERR_SHAPE;
+  };
   int rc;
   if ((rc = chk(cudaMemsetAsync(zero_start, 0, (size_t)B * 4, s)))) return rc;
-  // attention half: n1 = RMSNorm(x); q, k, v = n1 W^T; heads; k RoPE; attention; o_proj
-  if ((rc = chk(gqa::launch_rmsnorm_rows(x, w->input_norm, nrm, T, QW, norm_eps, offset, s))))
+  // attention half: n1 = RMSNorm(x); q, k, v = n1 W^T written head-major
+  if ((rc = chk(gqa::launch_rmsnorm_rows(x, w->input_norm, nrm, T, QW, norm_eps, offset, true,
+                                         s))))
     return rc;
-  if (gqa::gemm_xwt(nrm, w->wq, qt, T, QW, QW, 0.f, s) ||
-      gqa::gemm_xwt(nrm, w->wk, kt, T, KW, QW, 0.f, s) ||
-      gqa::gemm_xwt(nrm, w->wv, vt, T, KW, QW, 0.f, s))
-    return ATTN_ERR_CUDA;
-  if ((rc = chk(gqa::launch_swap_mid(qt, qh, B, L, H, D, s))) ||
-      (rc = chk(gqa::launch_swap_mid(kt, kh, B, L, Hkv, D, s))) ||
-      (rc = chk(gqa::launch_swap_mid(vt, vh, B, L, Hkv, D, s))))
-    return rc;
-  gqa::RopeJob j{};
-  j.x = kh; j.B = B; j.NH = Hkv; j.L = L; j.D = D; j.R = rope_dim_of(rp, D);
-  j.start = zero_start; j.max_positions = max_pos_of(rp);
-  j.table = reinterpret_cast<const float2*>(table);
-  j.norm_w = w->k_norm; j.norm_eps = norm_eps; j.status = status;
-  if ((rc = chk(gqa::launch_rope_rows(j, s)))) return rc;
-  rc = gqa_attn_prefill_rope(qh, kh, vh, qt, B, H, Hkv, L, D,
-                             zero_start, 0, rp, table, w->q_norm, norm_eps, window, softcap,
-                             scale, attn_ws, attn_bytes, status, stream);
+  {
+    gqa::GemmJob j{};
+    j.x = nrm; j.T = T; j.K = QW; j.L = L; j.D = D; j.status = status;
+    j.nseg = 3;
+    const float* wts[3] = {w->wq, w->wk, w->wv};
+    float* outs[3] = {qh, kh, vh};
+    const int ns[3] = {QW, KW, KW}, heads[3] = {H, Hkv, Hkv};
+    for (int i = 0; i < 3; ++i) {
+      j.seg[i].w = wts[i]; j.seg[i].n = ns[i]; j.seg[i].mode = 0;
+      j.seg[i].out = outs[i]; j.seg[i].out_heads = heads[i];
+    }
+    if ((rc = gemm(j))) return rc;
+  }
+  gqa::RopeJob rj{};
+  rj.x = kh; rj.B = B; rj.NH = Hkv; rj.L = L; rj.D = D; rj.R = rope_dim_of(rp, D);
+  rj.start = zero_start; rj.max_positions = max_pos_of(rp);
+  rj.table = reinterpret_cast<const float2*>(table);
+  rj.norm_w = w->k_norm; rj.norm_eps = norm_eps; rj.status = status;
+  if ((rc = chk(gqa::launch_rope_rows(rj, s)))) return rc;
+  rc = gqa_attn_prefill_rope(qh, kh, vh, ao, B, H, Hkv, L, D, zero_start, 0, rp, table,
+                             w->q_norm, norm_eps, window, softcap, scale, ws + lay.attn,
+                             workspace_bytes - lay.attn, status, stream);
   if (rc != ATTN_OK) return rc;
-  // qt now holds the attention output, head-major; back to token-major in qh
-  if ((rc = chk(gqa::launch_swap_mid(qt, qh, B, H, L, D, s)))) return rc;
-  if ((rc = chk(cudaMemcpyAsync(out, x, (size_t)T * QW * 4, cudaMemcpyDeviceToDevice, s))))
+  // h = x + o_proj(attention): the projection reads the head-major attention output
+  // directly when a 32-wide K block stays inside one head
+  {
+    gqa::GemmJob j{};
+    j.T = T; j.K = QW; j.L = L; j.D = D; j.status = status; j.nseg = 1;
+    if (D % 32 == 0) {
+      j.x = ao; j.x_heads = H;
+    } else {
+      if ((rc = chk(gqa::launch_swap_mid(ao, aot, B, H, L, D, s)))) return rc;
+      j.x = aot;
+    }
+    j.seg[0].w = w->wo; j.seg[0].n = QW; j.seg[0].mode = 1;
+    j.seg[0].out = out; j.seg[0].ldo = QW; j.seg[0].res = x; j.seg[0].ldr = QW;
+    if ((rc = gemm(j))) return rc;
+  }
+  // MLP half: n2 = RMSNorm(h); act = SiLU(n2 Wg^T) * (n2 Wu^T); out = h + act Wd^T
+  if ((rc = chk(gqa::launch_rmsnorm_rows(out, w->post_norm, nrm, T, QW, norm_eps, offset, true,
+                                         s))))
     return rc;
-  if (gqa::gemm_xwt(qh, w->wo, out, T, QW, QW, 1.f, s)) return ATTN_ERR_CUDA;   // h = x + o
-  // MLP half: n2 = RMSNorm(h); out = h + (SiLU(n2 Wg^T) * n2 Wu^T) Wd^T
-  if ((rc = chk(gqa::launch_rmsnorm_rows(out, w->post_norm, nrm, T, QW, norm_eps, offset, s))))
-    return rc;
-  if (gqa::gemm_xwt(nrm, w->w_gate, gate, T, IT, QW, 0.f, s) ||
-      gqa::gemm_xwt(nrm, w->w_up, up, T, IT, QW, 0.f, s))
-    return ATTN_ERR_CUDA;
-  if ((rc = chk(gqa::launch_swiglu(gate, up, T * IT, s)))) return rc;
-  if (gqa::gemm_xwt(gate, w->w_down, out, T, QW, IT, 1.f, s)) return ATTN_ERR_CUDA;
+  {
+    gqa::GemmJob j{};
+    j.x = nrm; j.T = T; j.K = QW; j.L = L; j.D = D; j.status = status; j.nseg = 1;
+    j.seg[0].w = w->w_gate; j.seg[0].w_up = w->w_up; j.seg[0].n = IT; j.seg[0].mode = 2;
+    j.seg[0].round_out = 1; j.seg[0].out = act; j.seg[0].ldo = IT;
+    if ((rc = gemm(j))) return rc;
+  }
+  {
+    gqa::GemmJob j{};
+    j.x = act; j.T = T; j.K = IT; j.L = L; j.D = D; j.status = status; j.nseg = 1;
+    j.seg[0].w = w->w_down; j.seg[0].n = QW; j.seg[0].mode = 1;
+    j.seg[0].out = out; j.seg[0].ldo = QW; j.seg[0].res = out; j.seg[0].ldr = QW;
+    if ((rc = gemm(j))) return rc;
+  }
   return ATTN_OK;
+}
+
+int attn_linear(const float* x, const float* w, const float* residual, float* y, long T, int N,
+                int K, int32_t* status, void* stream) {
+  if (T < 0 || N < 1 || K < 1) return ATTN_ERR_SHAPE;
+  if (K % 4 || N % 4) return ATTN_ERR_SHAPE;
+  if (T == 0) return ATTN_OK;
+  if (T > 0x7fffffffL) return ATTN_ERR_SHAPE;
+  if (!x || !w || !y) return ATTN_ERR_NULL;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (residual && !aligned16(residual)))
+    return ATTN_ERR_ALIGN;
+  gqa::GemmJob j{};
+  j.x = x; j.T = T; j.K = K; j.L = 1; j.D = 1; j.status = status; j.nseg = 1;
+  j.seg[0].w = w; j.seg[0].n = N; j.seg[0].mode = residual ? 1 : 0;
+  j.seg[0].out = y; j.seg[0].ldo = N; j.seg[0].res = residual; j.seg[0].ldr = N;
+  if (!gqa::gemm_tc_supports(j)) return ATTN_ERR_SHAPE;
+  return cuda_status(gqa::launch_gemm_tc(j, static_cast<cudaStream_t>(stream)));
 }
 
 int gqa_attn_prefill_identical(const float* q, const float* k, const float* v,

@@ -1,42 +1,60 @@
 // The decoder block around the attention ("mojolearn.transformer",
 // TransformerBlock.forward with state None, computing Hugging Face's
-// LlamaDecoderLayer.forward): input RMSNorm, q/k/v projections, (q/k norm,)
-// RoPE and causal GQA attention, output projection + residual,
-// post-attention RMSNorm, SiLU-gated MLP + residual.
-//
-// The projections are plain fp32 GEMMs (cuBLAS, default math: no TF32); the
-// attention is this library's prefill with q RMSNorm/RoPE fused; the rest are
-// the small memory-bound kernels below. Activations are token-major
-// [B * L, width] as the pages' (B, L, d_model) input; the attention's
-// head-major [B, heads, L, D] views come from one permute each way.
-#include <cublas_v2.h>
-
-#include <mutex>
-
+// LlamaDecoderLayer.forward): the memory-bound pieces around the tensor-core
+// projections of gemm_tc.cu -- RMSNorm of token rows and, for head dims that
+// the projection kernel cannot read head-major, the token-major <-> head-major
+// permute. Activations are token-major [B * L, width] as the pages' (B, L,
+// d_model) input.
 #include "common.cuh"
 #include "kernels.h"
+#include "tc_ptx.cuh"
 
 namespace gqa {
 
 namespace {
 
 // RMSNorm of each row of x [T, n] ("Core Layers -- Deep Reference", RMSNorm):
-// y = x / sqrt(mean x^2 + eps) * (w, or 1 + w). One warp per row.
+// y = x / sqrt(mean x^2 + eps) * (w, or 1 + w). One warp per row; 16-byte
+// accesses when n % 4 == 0. With round_out the results are rounded to the
+// nearest TF32 value (the projections read only those bits).
 __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* __restrict__ x,
                                                            const float* __restrict__ w,
                                                            float* __restrict__ y, long T, int n,
-                                                           float eps, int offset) {
+                                                           float eps, int offset, int round_out) {
   const int lane = threadIdx.x & 31;
   const long nw = static_cast<long>(gridDim.x) * 8;
+  const bool vec = (n % 4) == 0;
   for (long row = static_cast<long>(blockIdx.x) * 8 + threadIdx.x / 32; row < T; row += nw) {
     const float* xr = x + row * n;
+    float* yr = y + row * n;
     float ss = 0.f;
-    for (int i = lane; i < n; i += 32) ss = fmaf(xr[i], xr[i], ss);
+    if (vec) {
+      const float4* x4 = reinterpret_cast<const float4*>(xr);
+      for (int i = lane; i < n / 4; i += 32) {
+        const float4 v = x4[i];
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      }
+    } else {
+      for (int i = lane; i < n; i += 32) ss = fmaf(xr[i], xr[i], ss);
+    }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     const float inv = 1.0f / sqrtf(ss / static_cast<float>(n) + eps);
-    float* yr = y + row * n;
-    for (int i = lane; i < n; i += 32) yr[i] = xr[i] * inv * (offset ? 1.0f + w[i] : w[i]);
+    auto one = [&](float xv, float wv) {
+      const float r = xv * inv * (offset ? 1.0f + wv : wv);
+      return round_out ? tc::round_tf32(r) : r;
+    };
+    if (vec) {
+      const float4* x4 = reinterpret_cast<const float4*>(xr);
+      const float4* w4 = reinterpret_cast<const float4*>(w);
+      float4* y4 = reinterpret_cast<float4*>(yr);
+      for (int i = lane; i < n / 4; i += 32) {
+        const float4 v = x4[i], g = w4[i];
+        y4[i] = make_float4(one(v.x, g.x), one(v.y, g.y), one(v.z, g.z), one(v.w, g.w));
+      }
+    } else {
+      for (int i = lane; i < n; i += 32) yr[i] = one(xr[i], w[i]);
+    }
   }
 }
 
@@ -57,30 +75,18 @@ __global__ void __launch_bounds__(256) swap_mid_kernel(const float* __restrict__
   }
 }
 
-// gate <- SiLU(gate) * up, elementwise.
-__global__ void __launch_bounds__(256) swiglu_kernel(float* __restrict__ gate,
-                                                     const float* __restrict__ up, long n) {
-  for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<long>(gridDim.x) * blockDim.x) {
-    const float g = gate[i];
-    gate[i] = g / (1.0f + expf(-g)) * up[i];
-  }
-}
-
 unsigned grid_for(long n, int per_block) {
   long blocks = (n + per_block - 1) / per_block;
   if (blocks > 152L * 16) blocks = 152L * 16;
   return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
 }
 
-std::mutex g_blas_mutex;
-cublasHandle_t g_blas = nullptr;
-
 }  // namespace
 
 cudaError_t launch_rmsnorm_rows(const float* x, const float* w, float* y, long T, int n,
-                                float eps, bool offset, cudaStream_t stream) {
-  rmsnorm_rows_kernel<<<grid_for(T, 8), 256, 0, stream>>>(x, w, y, T, n, eps, offset ? 1 : 0);
+                                float eps, bool offset, bool round_out, cudaStream_t stream) {
+  rmsnorm_rows_kernel<<<grid_for(T, 8), 256, 0, stream>>>(x, w, y, T, n, eps, offset ? 1 : 0,
+                                                          round_out ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -89,28 +95,6 @@ cudaError_t launch_swap_mid(const float* in, float* out, int B, int P, int Q, in
   swap_mid_kernel<<<grid_for(static_cast<long>(B) * P * Q * D, 256), 256, 0, stream>>>(in, out, B,
                                                                                        P, Q, D);
   return cudaGetLastError();
-}
-
-cudaError_t launch_swiglu(float* gate, const float* up, long n, cudaStream_t stream) {
-  swiglu_kernel<<<grid_for(n, 256), 256, 0, stream>>>(gate, up, n);
-  return cudaGetLastError();
-}
-
-// Y [T, N] = X [T, K] . W^T (W [N, K], torch's [out, in]) + beta * Y, fp32.
-int gemm_xwt(const float* X, const float* W, float* Y, long T, int N, int K, float beta,
-             cudaStream_t stream) {
-  std::lock_guard<std::mutex> lock(g_blas_mutex);
-  if (!g_blas && cublasCreate(&g_blas) != CUBLAS_STATUS_SUCCESS) {
-    g_blas = nullptr;
-    return -1;
-  }
-  if (cublasSetStream(g_blas, stream) != CUBLAS_STATUS_SUCCESS) return -1;
-  const float alpha = 1.0f;
-  // Column-major view: Y^T [N, T] = W (as [K, N], transposed) . X^T [K, T].
-  return cublasSgemm(g_blas, CUBLAS_OP_T, CUBLAS_OP_N, N, static_cast<int>(T), K, &alpha, W, K, X,
-                     K, &beta, Y, N) == CUBLAS_STATUS_SUCCESS
-             ? 0
-             : -1;
 }
 
 }  // namespace gqa

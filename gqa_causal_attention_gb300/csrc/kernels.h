@@ -151,13 +151,36 @@ cudaError_t launch_identical(const IdentJob& j, cudaStream_t stream);
 
 // The decoder block around the attention (block.cu).
 cudaError_t launch_rmsnorm_rows(const float* x, const float* w, float* y, long T, int n,
-                                float eps, bool offset, cudaStream_t stream);
+                                float eps, bool offset, bool round_out, cudaStream_t stream);
 cudaError_t launch_swap_mid(const float* in, float* out, int B, int P, int Q, int D,
                             cudaStream_t stream);   // [B, P, Q, D] -> [B, Q, P, D]
-cudaError_t launch_swiglu(float* gate, const float* up, long n, cudaStream_t stream);
-// Y [T, N] = X [T, K] . W^T + beta * Y in fp32 (W in torch's [out, in] layout); 0 or -1.
-int gemm_xwt(const float* X, const float* W, float* Y, long T, int N, int K, float beta,
-             cudaStream_t stream);
+
+// Projections on the tensor cores (gemm_tc.cu): Y = X W^T, W in torch's [out, in]
+// layout, TF32 operands, fp32 accumulation. Up to three segments share X.
+struct GemmSegment {
+  const float* w;           // [n, K]; SwiGLU: gate_proj
+  const float* w_up;        // SwiGLU only: up_proj [n, K]
+  int n;                    // output columns
+  int mode;                 // 0 store, 1 out = res + X W^T, 2 out = SiLU(X Wg^T) * (X Wu^T)
+  int round_out;            // round outputs to the nearest TF32 value
+  float* out;               // row-major [T, ldo] (out_heads == 0) or head-major
+  long ldo;
+  int out_heads;            // > 0: out [T / L, out_heads, L, D], column h * D + d
+  const float* res;         // mode 1: [T, ldr] (may equal out)
+  long ldr;
+};
+struct GemmJob {
+  const float* x;           // [T, K] token-major, or head-major (x_heads > 0)
+  long T;
+  int K;
+  int x_heads;              // > 0: x is [T / L, x_heads, L, D] with K = x_heads * D, D % 32 == 0
+  int L, D;                 // tokens per batch row and head dim (head-major x or out)
+  int nseg;
+  GemmSegment seg[3];       // SwiGLU: one segment only
+  int32_t* status;
+};
+bool gemm_tc_supports(const GemmJob& j);
+cudaError_t launch_gemm_tc(const GemmJob& j, cudaStream_t stream);
 
 void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream);

@@ -322,8 +322,12 @@ int gqa_attn_prefill_ragged(const float* q, const float* k, const float* v, floa
  *            [IT, d_model], down_proj [d_model, IT]; norms [d_model]; q_norm,
  *            k_norm [D] or NULL
  *   workspace gqa_block_forward_workspace_size bytes
- * The projections are fp32 GEMMs (cuBLAS, no TF32; the library creates one
- * cuBLAS handle on first use). Returns ATTN_ERR_CUDA if a GEMM fails.
+ * The seven projections run as attn_linear does (tcgen05 tensor cores, TF32
+ * operands, fp32 accumulation): q, k and v in one launch writing head-major,
+ * o_proj reading the attention's head-major output (D % 32 == 0) and adding x,
+ * gate and up in one launch whose epilogue forms SiLU(gate) * up, down_proj
+ * adding h in place. d_model and IT must be multiples of 4 and x != out
+ * (ATTN_ERR_SHAPE otherwise).
  */
 typedef struct attn_block_weights {
     const float* input_norm;         /* input_layernorm.weight [d_model] */
@@ -346,6 +350,20 @@ int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, 
                       const attn_rope_params* rp, const float* table, int window, float softcap,
                       float scale, void* workspace, size_t workspace_bytes, int32_t* status,
                       void* stream);
+
+/*
+ * One bias-free linear map on the tcgen05 tensor cores ("mojolearn.transformer",
+ * TransformerBlock: q_proj ... down_proj are linear maps without bias, weights
+ * in torch's [out, in] layout):
+ *   y[t, n] = sum_k x[t, k] * w[n, k]  (+ residual[t, n] when residual != NULL)
+ *   x [T, K], w [N, K], y and residual [T, N]; fp32 in memory, TF32 operands
+ *   (the tensor core reads the top 19 bits of each value), fp32 accumulation.
+ *   residual may equal y (in-place add); x and w must not overlap y.
+ * K and N multiples of 4 (16-byte rows; ATTN_ERR_SHAPE otherwise). T == 0 is a
+ * no-op.
+ */
+int attn_linear(const float* x, const float* w, const float* residual, float* y, long T, int N,
+                int K, int32_t* status, void* stream);
 
 /*
  * The identical numeric mode ("mojolearn.transformer", TransformerBlock

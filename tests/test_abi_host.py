@@ -290,25 +290,46 @@ def test_identical_mode_refuses_before_launch():
 def test_block_forward_refuses_before_launch():
     lib = g.load()
     P = ctypes.c_void_p(0x100000)
+    P2 = ctypes.c_void_p(0x200000)
     rp = g.RopeParams.make(theta=1e4, max_positions=64)
     w = g._BlockWeights(*([0x100000] * 9 + [0, 0]))
 
-    def call(H=4, Hkv=2, D=16, IT=32, L=8, weights=w, params=rp, ws=None, wbytes=0):
-        return lib.gqa_block_forward(P, P, 2, L, H, Hkv, D, IT,
+    def call(H=4, Hkv=2, D=16, IT=32, L=8, weights=w, params=rp, ws=None, wbytes=0, out=P2):
+        return lib.gqa_block_forward(P, out, 2, L, H, Hkv, D, IT,
                                      None if weights is None else ctypes.byref(weights), 0, 1e-6,
                                      None if params is None else ctypes.byref(params), P, 0, 0.0,
                                      0.0, ws, wbytes, None, None)
 
     assert call(H=6, Hkv=4) == -2
     assert call(IT=0) == -2
+    assert call(IT=30) == -2                       # 16-byte rows for the projections
+    assert call(H=1, Hkv=1, D=2) == -2             # d_model = 2
     assert call(weights=None) == -1
     assert call(params=None) == -1
+    assert call(out=P) == -2                       # out must not be x
     assert call(L=65) == -3                        # positions reach max_positions
     assert call() == -5                            # no workspace
     need = lib.gqa_block_forward_workspace_size(2, 8, 4, 2, 16, 32, ctypes.byref(rp))
-    assert need >= 2 * 8 * (3 * 64 + 4 * 32 + 2 * 32) * 4
+    # normed rows, q, k, v, attention output, activations
+    assert need >= 2 * 8 * (3 * 64 + 2 * 32 + 32) * 4
     w2 = g._BlockWeights(*([0x100000] * 8 + [0, 0, 0]))          # no down_proj
     assert call(weights=w2, ws=P, wbytes=need) == -1
+    w3 = g._BlockWeights(*([0x100000] * 8 + [0x100004, 0, 0]))   # misaligned down_proj
+    assert call(weights=w3, ws=P, wbytes=need) == -6
+
+
+@no_device
+def test_linear_refuses_before_launch():
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+
+    def call(T=8, N=16, K=32, x=P, w=P, r=None, y=P):
+        return lib.attn_linear(x, w, r, y, T, N, K, None, None)
+
+    assert call(K=30) == -2 and call(N=6) == -2 and call(K=0) == -2 and call(T=-1) == -2
+    assert call(x=None) == -1 and call(w=None) == -1 and call(y=None) == -1
+    assert call(r=ctypes.c_void_p(0x100008)) == -6
+    assert call(T=0, x=None) == 0                  # empty: nothing to do
 
 
 @no_device

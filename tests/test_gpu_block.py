@@ -45,7 +45,10 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("B,L,H,Hkv,D,IT,R,window,softcap,qk_norm,offset", CASES)
+@pytest.mark.parametrize("B,L,H,Hkv,D,IT,R,window,softcap,qk_norm,offset", CASES + [
+    # the Llama-3-8B-shaped block: d_model 4096, 32 query / 8 kv heads, IT 14336
+    (1, 256, 32, 8, 128, 14336, 128, 0, 0.0, False, False),
+])
 def test_block_forward_matches_the_oracle(B, L, H, Hkv, D, IT, R, window, softcap, qk_norm,
                                           offset):
     dm = H * D
