@@ -30,14 +30,14 @@ __all__ = [
     "gqa_attn_prefill_ragged", "gqa_attn_prefill_ragged_workspace_size",
     "gqa_attn_prefill_identical", "gqa_attn_decode_identical",
     "gqa_block_forward", "gqa_block_forward_workspace_size", "BLOCK_WEIGHT_NAMES",
-    "attn_linear",
+    "attn_linear", "attn_set_check_finite", "DEV_NONFINITE",
     "gqa_attn_prefill_from_host", "gqa_attn_prefill_from_host_workspace_size",
     "attn_selftest_wait_timeout",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
     "DEV_POSITION", "DEV_CAPACITY", "DEV_LENGTH", "DEV_TIMEOUT",
 ]
 
-DEV_POSITION, DEV_CAPACITY, DEV_LENGTH, DEV_TIMEOUT = 1, 2, 4, 8
+DEV_POSITION, DEV_CAPACITY, DEV_LENGTH, DEV_TIMEOUT, DEV_NONFINITE = 1, 2, 4, 8, 16
 ROPE_SCALING = {None: 0, "none": 0, "linear": 1, "llama3": 2}
 
 
@@ -140,6 +140,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "gqa_block_forward": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, f, rp,
                                         vp, i32, f, f, vp, sz, vp, vp]),
             "attn_linear": (i32, [vp, vp, vp, vp, ctypes.c_long, i32, i32, vp, vp]),
+            "attn_set_check_finite": (i32, [i32]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
@@ -195,6 +196,12 @@ def _check(fn: str, rc: int):
 
 def attn_status_string(code: int) -> str:
     return load().attn_status_string(int(code)).decode()
+
+
+def attn_set_check_finite(on: int) -> int:
+    """Turn the non-finite input check on (1) or off (0), or query it (< 0); returns the
+    previous setting. With it on, every computing call needs a status tensor."""
+    return int(load().attn_set_check_finite(int(on)))
 
 
 def attn_version() -> str:

@@ -76,6 +76,30 @@ int cuda_status(cudaError_t e) {
 
 int gqa::record_cuda_error(cudaError_t e) { return cuda_status(e); }
 
+namespace {
+// The opt-in non-finite check. add() lists what a call reads; gate() then, with
+// the check on, requires a status word, enqueues the check and hands back the
+// status word as the kernels' skip flag (nullptr and nothing enqueued when off).
+struct Finite {
+  gqa::FiniteJob j{};
+  void add(const float* p, int B, int NH, long R, long C, int mode = gqa::kFiniteAll,
+           const int32_t* info = nullptr, int window = 0, long ld = 0) {
+    if (!p || B < 1 || NH < 1 || R < 1 || C < 1 || j.n >= gqa::kMaxFiniteRegions) return;
+    gqa::FiniteRegion& r = j.r[j.n++];
+    r.p = p; r.B = B; r.NH = NH; r.R = R; r.C = C; r.ld = ld > 0 ? ld : C;
+    r.mode = mode; r.info = info; r.window = window;
+  }
+  int gate(int32_t* status, cudaStream_t s, const int32_t** skip) {
+    *skip = nullptr;
+    if (!gqa::check_finite_enabled()) return ATTN_OK;
+    if (!status) return ATTN_ERR_NULL;
+    j.status = status;
+    *skip = status;
+    return cuda_status(gqa::launch_finite_check(j, s));
+  }
+};
+}  // namespace
+
 // Every host check of gqa_attn_decode except the workspace's: ATTN_OK (also for
 // B == 0, when there is nothing to do) or the ATTN_ERR_* the call would return.
 int gqa::decode_host_check(const float* q, const float* k_cache, const float* v_cache,
@@ -97,7 +121,9 @@ int gqa::decode_host_check(const float* q, const float* k_cache, const float* v_
 
 extern "C" {
 
-const char* attn_version(void) { return "0.1.0"; }
+const char* attn_version(void) { return "0.2.0"; }
+
+int attn_set_check_finite(int on) { return gqa::set_check_finite(on); }
 
 const char* attn_last_cuda_error(void) {
   return g_last_cuda_error == cudaSuccess ? "no CUDA error" : cudaGetErrorString(g_last_cuda_error);
@@ -148,12 +174,18 @@ int attn_rope_apply(float* x, int B, int Hx, int L, int D, const int32_t* start,
   if (!aligned16(x) || !aligned16(table) || (norm_w && !aligned16(norm_w))) return ATTN_ERR_ALIGN;
   if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_pos_of(rp))
     return ATTN_ERR_POSITION;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Finite fin;
+  fin.add(x, B, Hx, L, D);
+  fin.add(norm_w, 1, 1, 1, D);
+  const int32_t* skip = nullptr;
+  if (const int rc = fin.gate(status, s, &skip)) return rc;
   gqa::RopeJob j{};
   j.x = x; j.B = B; j.NH = Hx; j.L = L; j.D = D; j.R = rope_dim_of(rp, D);
   j.start = start; j.max_positions = max_pos_of(rp);
   j.table = reinterpret_cast<const float2*>(table);
-  j.norm_w = norm_w; j.norm_eps = norm_eps; j.status = status;
-  return cuda_status(gqa::launch_rope_rows(j, static_cast<cudaStream_t>(stream)));
+  j.norm_w = norm_w; j.norm_eps = norm_eps; j.status = status; j.skip = skip;
+  return cuda_status(gqa::launch_rope_rows(j, s));
 }
 
 int kv_cache_append(float* k, const float* v, int B, int Hkv, int L, int D,
@@ -174,13 +206,20 @@ int kv_cache_append(float* k, const float* v, int B, int Hkv, int L, int D,
   if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_positions)
     return ATTN_ERR_POSITION;
   if (window == 0 && (int64_t)max_start + L > (int64_t)capacity) return ATTN_ERR_CAPACITY;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Finite fin;
+  fin.add(k, B, Hkv, L, D);
+  fin.add(v, B, Hkv, L, D);
+  fin.add(k_norm_w, 1, 1, 1, D);
+  const int32_t* skip = nullptr;
+  if (const int rc = fin.gate(status, s, &skip)) return rc;
   gqa::RopeJob j{};
   j.x = k; j.B = B; j.NH = Hkv; j.L = L; j.D = D; j.R = rp ? rope_dim_of(rp, D) : D;
   j.start = start; j.max_positions = max_positions;
   j.table = reinterpret_cast<const float2*>(table);
-  j.norm_w = k_norm_w; j.norm_eps = norm_eps; j.status = status;
+  j.norm_w = k_norm_w; j.norm_eps = norm_eps; j.status = status; j.skip = skip;
   j.v = v; j.k_cache = k_cache; j.v_cache = v_cache; j.capacity = capacity; j.window = window;
-  return cuda_status(gqa::launch_rope_rows(j, static_cast<cudaStream_t>(stream)));
+  return cuda_status(gqa::launch_rope_rows(j, s));
 }
 
 size_t gqa_attn_prefill_workspace_size(int B, int Hkv, int L, int D) {
@@ -212,6 +251,16 @@ int prefill_impl(const float* q, const float* k, const float* v, float* out, int
     if (!workspace || workspace_bytes < gqa_attn_prefill_workspace_size(B, Hkv, L, D))
       return ATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  }
+  {
+    Finite fin;
+    const int mode = lengths ? gqa::kFiniteLen : gqa::kFiniteAll;
+    fin.add(q, B, H, L, D, mode, lengths);
+    fin.add(k, B, Hkv, L, D, mode, lengths);
+    fin.add(v, B, Hkv, L, D, mode, lengths);
+    if (const int rc = fin.gate(status, s, &a.skip)) return rc;
+  }
+  if (gqa::prefill_tc_supports(D)) {
     a.vt = static_cast<float*>(workspace);
     a.vt_pitch = gqa::prefill_vt_pitch(L);
     return cuda_status(gqa::launch_prefill_tc(a, s));
@@ -299,6 +348,16 @@ int prefill_rope_impl(const float* q, const float* k, const float* v, const floa
   a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   a.status = status;
   a.lengths = lengths;
+  {
+    Finite fin;
+    const int mode = lengths ? gqa::kFiniteLen : gqa::kFiniteAll;
+    fin.add(q, B, H, L, D, mode, lengths);
+    fin.add(k, B, Hkv, L, D, mode, lengths);
+    if (v) fin.add(v, B, Hkv, L, D, mode, lengths);
+    else fin.add(vt, B, Hkv, D, L, gqa::kFiniteAll, nullptr, 0, gqa::prefill_vt_pitch(L));
+    fin.add(q_norm_w, 1, 1, 1, D);
+    if (const int rc = fin.gate(status, s, &a.skip)) return rc;
+  }
   if (gqa::prefill_tc_supports(D)) {
     a.vt = vt ? const_cast<float*>(vt) : static_cast<float*>(workspace);
     a.vt_pitch = gqa::prefill_vt_pitch(L);
@@ -328,7 +387,7 @@ int prefill_rope_impl(const float* q, const float* k, const float* v, const floa
   j.B = B; j.NH = H; j.L = L; j.D = D; j.R = R;
   j.start = start; j.max_positions = max_pos_of(rp);
   j.table = reinterpret_cast<const float2*>(table);
-  j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status;
+  j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status; j.skip = a.skip;
   if (cudaError_t e = gqa::launch_rope_rows(j, s); e != cudaSuccess) return cuda_status(e);
   a.q = qrot;
   return attend();
@@ -463,6 +522,17 @@ int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, cons
   const CachedLayout lay = cached_layout(B, H, Hkv, L, D, max_start, window, rp && !fused);
   char* ws = static_cast<char*>(workspace);
   const int Lk = (int)cached_lk(max_start, window, L);
+  const int32_t* skip = nullptr;
+  {
+    Finite fin;
+    fin.add(q, B, H, L, D);
+    fin.add(k, B, Hkv, L, D);
+    fin.add(v, B, Hkv, L, D);
+    fin.add(k_cache, B, Hkv, capacity, D, gqa::kFinitePrefix, start, window);
+    fin.add(v_cache, B, Hkv, capacity, D, gqa::kFinitePrefix, start, window);
+    fin.add(q_norm_w, 1, 1, 1, D);
+    if (const int rc = fin.gate(status, s, &skip)) return rc;
+  }
 
   gqa::GatherJob gj{};
   gj.k = k; gj.v = v; gj.k_cache = k_cache; gj.v_cache = v_cache; gj.start = start;
@@ -472,6 +542,7 @@ int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, cons
   gj.B = B; gj.Hkv = Hkv; gj.L = L; gj.D = D; gj.capacity = capacity; gj.window = window;
   gj.Lk = Lk; gj.vt_pitch = gqa::prefill_vt_pitch(Lk); gj.max_start = max_start;
   gj.status = status;
+  gj.skip = skip;
   if (cudaError_t e = gqa::launch_gather_kv(gj, s); e != cudaSuccess) return cuda_status(e);
 
   gqa::AttnShape a{};
@@ -484,6 +555,7 @@ int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, cons
   a.kv_off = gj.pre;
   a.Lk = Lk;
   a.q = q;
+  a.skip = skip;
   if (fused) {
     a.rope.table = reinterpret_cast<const float2*>(table);
     a.rope.start = start;
@@ -498,7 +570,7 @@ int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, cons
     j.B = B; j.NH = H; j.L = L; j.D = D; j.R = R;
     j.start = start; j.max_positions = max_pos_of(rp);
     j.table = reinterpret_cast<const float2*>(table);
-    j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status;
+    j.norm_w = q_norm_w; j.norm_eps = norm_eps; j.status = status; j.skip = skip;
     if (cudaError_t e = gqa::launch_rope_rows(j, s); e != cudaSuccess) return cuda_status(e);
     a.q = qrot;
   }
@@ -589,15 +661,33 @@ int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, 
   float* aot = reinterpret_cast<float*>(ws + lay.aot);
   float* act = reinterpret_cast<float*>(ws + lay.act);
   const bool offset = norm_offset != 0;
+  const int32_t* skip = nullptr;
+  {
+    Finite fin;
+    fin.add(x, 1, 1, T, QW);
+    fin.add(w->input_norm, 1, 1, 1, QW);
+    fin.add(w->post_norm, 1, 1, 1, QW);
+    fin.add(w->wq, 1, 1, QW, QW);
+    fin.add(w->wk, 1, 1, KW, QW);
+    fin.add(w->wv, 1, 1, KW, QW);
+    fin.add(w->wo, 1, 1, QW, QW);
+    fin.add(w->w_gate, 1, 1, IT, QW);
+    fin.add(w->w_up, 1, 1, IT, QW);
+    fin.add(w->w_down, 1, 1, QW, IT);
+    fin.add(w->q_norm, 1, 1, 1, D);
+    fin.add(w->k_norm, 1, 1, 1, D);
+    if (const int rc = fin.gate(status, s, &skip)) return rc;
+  }
   auto chk = [&](cudaError_t e) { return e == cudaSuccess ? ATTN_OK : cuda_status(e); };
-  auto gemm = [&](const gqa::GemmJob& j) {
+  auto gemm = [&](gqa::GemmJob& j) {
+    j.skip = skip;
     return gqa::gemm_tc_supports(j) ? chk(gqa::launch_gemm_tc(j, s)) : ATTN_ERR_SHAPE;
   };
   int rc;
   if ((rc = chk(cudaMemsetAsync(zero_start, 0, (size_t)B * 4, s)))) return rc;
   // attention half: n1 = RMSNorm(x); q, k, v = n1 W^T written head-major
   if ((rc = chk(gqa::launch_rmsnorm_rows(x, w->input_norm, nrm, T, QW, norm_eps, offset, true,
-                                         s))))
+                                         s, skip))))
     return rc;
   {
     gqa::GemmJob j{};
@@ -616,7 +706,7 @@ int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, 
   rj.x = kh; rj.B = B; rj.NH = Hkv; rj.L = L; rj.D = D; rj.R = rope_dim_of(rp, D);
   rj.start = zero_start; rj.max_positions = max_pos_of(rp);
   rj.table = reinterpret_cast<const float2*>(table);
-  rj.norm_w = w->k_norm; rj.norm_eps = norm_eps; rj.status = status;
+  rj.norm_w = w->k_norm; rj.norm_eps = norm_eps; rj.status = status; rj.skip = skip;
   if ((rc = chk(gqa::launch_rope_rows(rj, s)))) return rc;
   rc = gqa_attn_prefill_rope(qh, kh, vh, ao, B, H, Hkv, L, D, zero_start, 0, rp, table,
                              w->q_norm, norm_eps, window, softcap, scale, ws + lay.attn,
@@ -630,7 +720,7 @@ int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, 
     if (D % 32 == 0) {
       j.x = ao; j.x_heads = H;
     } else {
-      if ((rc = chk(gqa::launch_swap_mid(ao, aot, B, H, L, D, s)))) return rc;
+      if ((rc = chk(gqa::launch_swap_mid(ao, aot, B, H, L, D, s, skip)))) return rc;
       j.x = aot;
     }
     j.seg[0].w = w->wo; j.seg[0].n = QW; j.seg[0].mode = 1;
@@ -639,7 +729,7 @@ int gqa_block_forward(const float* x, float* out, int B, int L, int H, int Hkv, 
   }
   // MLP half: n2 = RMSNorm(h); act = SiLU(n2 Wg^T) * (n2 Wu^T); out = h + act Wd^T
   if ((rc = chk(gqa::launch_rmsnorm_rows(out, w->post_norm, nrm, T, QW, norm_eps, offset, true,
-                                         s))))
+                                         s, skip))))
     return rc;
   {
     gqa::GemmJob j{};
@@ -672,7 +762,13 @@ int attn_linear(const float* x, const float* w, const float* residual, float* y,
   j.seg[0].w = w; j.seg[0].n = N; j.seg[0].mode = residual ? 1 : 0;
   j.seg[0].out = y; j.seg[0].ldo = N; j.seg[0].res = residual; j.seg[0].ldr = N;
   if (!gqa::gemm_tc_supports(j)) return ATTN_ERR_SHAPE;
-  return cuda_status(gqa::launch_gemm_tc(j, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Finite fin;
+  fin.add(x, 1, 1, T, K);
+  fin.add(w, 1, 1, N, K);
+  fin.add(residual, 1, 1, T, N);
+  if (const int rc = fin.gate(status, s, &j.skip)) return rc;
+  return cuda_status(gqa::launch_gemm_tc(j, s));
 }
 
 int gqa_attn_prefill_identical(const float* q, const float* k, const float* v,
@@ -695,7 +791,17 @@ int gqa_attn_prefill_identical(const float* q, const float* k, const float* v,
   j.softcap = softcap > 0.f ? softcap : 0.f;
   j.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   j.status = status;
-  return cuda_status(gqa::launch_identical(j, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Finite fin;
+  fin.add(q, B, H, L, D);
+  fin.add(k, B, Hkv, L, D);
+  fin.add(v, B, Hkv, L, D);
+  if (cached) {
+    fin.add(k_cache, B, Hkv, capacity, D, gqa::kFinitePrefix, start, window);
+    fin.add(v_cache, B, Hkv, capacity, D, gqa::kFinitePrefix, start, window);
+  }
+  if (const int rc = fin.gate(status, s, &j.skip)) return rc;
+  return cuda_status(gqa::launch_identical(j, s));
 }
 
 int gqa_attn_decode_identical(const float* q, const float* k_cache, const float* v_cache,
@@ -717,7 +823,13 @@ int gqa_attn_decode_identical(const float* q, const float* k_cache, const float*
   j.softcap = softcap > 0.f ? softcap : 0.f;
   j.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
   j.status = status;
-  return cuda_status(gqa::launch_identical(j, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Finite fin;
+  fin.add(q, B, H, 1, D);
+  fin.add(k_cache, B, Hkv, capacity, D, gqa::kFiniteCache, cache_len);
+  fin.add(v_cache, B, Hkv, capacity, D, gqa::kFiniteCache, cache_len);
+  if (const int rc = fin.gate(status, s, &j.skip)) return rc;
+  return cuda_status(gqa::launch_identical(j, s));
 }
 
 int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
@@ -741,7 +853,13 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
     if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
   }
   j.partial = static_cast<float*>(workspace);
-  return cuda_status(gqa::launch_decode(j, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Finite fin;
+  fin.add(q, B, H, 1, D);
+  fin.add(k_cache, B, Hkv, capacity, D, gqa::kFiniteCache, cache_len);
+  fin.add(v_cache, B, Hkv, capacity, D, gqa::kFiniteCache, cache_len);
+  if (const int rc = fin.gate(status, s, &j.skip)) return rc;
+  return cuda_status(gqa::launch_decode(j, s));
 }
 
 }  // extern "C"

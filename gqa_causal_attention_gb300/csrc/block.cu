@@ -20,7 +20,9 @@ namespace {
 __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* __restrict__ x,
                                                            const float* __restrict__ w,
                                                            float* __restrict__ y, long T, int n,
-                                                           float eps, int offset, int round_out) {
+                                                           float eps, int offset, int round_out,
+                                                           const int32_t* skip) {
+  if (gated_off(skip)) return;
   const int lane = threadIdx.x & 31;
   const long nw = static_cast<long>(gridDim.x) * 8;
   const bool vec = (n % 4) == 0;
@@ -61,7 +63,8 @@ __global__ void __launch_bounds__(256) rmsnorm_rows_kernel(const float* __restri
 // out[b, q, p, :] = in[b, p, q, :] for in [B, P, Q, D] (token-major <-> head-major).
 __global__ void __launch_bounds__(256) swap_mid_kernel(const float* __restrict__ in,
                                                        float* __restrict__ out, int B, int P, int Q,
-                                                       int D) {
+                                                       int D, const int32_t* skip) {
+  if (gated_off(skip)) return;
   const long total = static_cast<long>(B) * P * Q * D;
   for (long i = static_cast<long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<long>(gridDim.x) * blockDim.x) {
@@ -84,16 +87,17 @@ unsigned grid_for(long n, int per_block) {
 }  // namespace
 
 cudaError_t launch_rmsnorm_rows(const float* x, const float* w, float* y, long T, int n,
-                                float eps, bool offset, bool round_out, cudaStream_t stream) {
+                                float eps, bool offset, bool round_out, cudaStream_t stream,
+                                const int32_t* skip) {
   rmsnorm_rows_kernel<<<grid_for(T, 8), 256, 0, stream>>>(x, w, y, T, n, eps, offset ? 1 : 0,
-                                                          round_out ? 1 : 0);
+                                                          round_out ? 1 : 0, skip);
   return cudaGetLastError();
 }
 
 cudaError_t launch_swap_mid(const float* in, float* out, int B, int P, int Q, int D,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, const int32_t* skip) {
   swap_mid_kernel<<<grid_for(static_cast<long>(B) * P * Q * D, 256), 256, 0, stream>>>(in, out, B,
-                                                                                       P, Q, D);
+                                                                                       P, Q, D, skip);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,13 @@ __device__ __forceinline__ void report(int32_t* status, int32_t bits) {
   if (status) atomicOr(status, bits);
 }
 
+// True when the call's non-finite check found a bad input: every kernel of the
+// call then returns at once (skip is the caller's status word, or nullptr when
+// the check is off).
+__device__ __forceinline__ bool gated_off(const int32_t* skip) {
+  return skip && (*reinterpret_cast<const volatile int32_t*>(skip) & ATTN_DEV_NONFINITE);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

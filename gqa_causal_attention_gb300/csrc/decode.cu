@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeJob 
   __shared__ float sm_m[kDecodeWarps][GT];
   __shared__ float sm_l[kDecodeWarps][GT];
   __shared__ float sm_o[kDecodeWarps][GT][kMaxHeadDim];
+  if (gated_off(j.skip)) return;
 
   const int split = blockIdx.x, b = blockIdx.z;
   const int G = j.H / j.Hkv;
@@ -231,6 +232,7 @@ __global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
   extern __shared__ __align__(128) uint8_t ring[];
   __shared__ uint64_t full[kBulkMaxStages];
   __shared__ int abort_flag;
+  if (gated_off(j.skip)) return;
 
   const int lane = threadIdx.x;
   const int split = blockIdx.x, b = blockIdx.z;
@@ -435,6 +437,7 @@ __global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
 
 // out[b, h, :] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits of row b.
 __global__ void __launch_bounds__(128) decode_combine_kernel(DecodeJob j) {
+  if (gated_off(j.skip)) return;
   const int h = blockIdx.x, b = blockIdx.y;
   const int n = j.cache_len[b];
   if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) return;
@@ -498,6 +501,7 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_all[NW][kBulkMaxStages];
   __shared__ int abort_flag;
+  if (gated_off(j.skip)) return;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int pair = lane >> 3, grp = lane & 7;

@@ -19,6 +19,7 @@ namespace {
 
 __global__ void __launch_bounds__(256) gather_kv_kernel(GatherJob j) {
   __shared__ float tile[32][33];
+  if (gated_off(j.skip)) return;
   const int bh = blockIdx.z;
   const int b = bh / j.Hkv;
   const int r0 = blockIdx.x * 32, d0 = blockIdx.y * 32;

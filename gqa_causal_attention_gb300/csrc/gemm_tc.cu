@@ -76,6 +76,7 @@ struct GArgs {
   int nseg;
   GSeg seg[3];
   int32_t* status;
+  const int32_t* skip;
 };
 
 struct GBars {
@@ -319,6 +320,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                    const __grid_constant__ CUtensorMap tm_b0,
                    const __grid_constant__ CUtensorMap tm_b1,
                    const __grid_constant__ CUtensorMap tm_b2, const GArgs a) {
+  if (gated_off(a.skip)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -452,6 +454,7 @@ cudaError_t launch_gemm_tc(const GemmJob& j, cudaStream_t stream) {
   a.kblocks = (j.K + kGBK - 1) / kGBK;
   a.nseg = j.nseg;
   a.status = j.status;
+  a.skip = j.skip;
   CUtensorMap tb[3];
   int tiles_n = 0;
   for (int s = 0; s < j.nseg; ++s) {

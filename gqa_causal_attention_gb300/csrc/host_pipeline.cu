@@ -126,6 +126,8 @@ int gqa_attn_prefill_from_host(const float* q_host, const float* k_host, const f
   if (need == 0) return ATTN_ERR_SHAPE;
   if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  // The non-finite check, when on, runs inside each chunk's calls and needs a status word.
+  if (gqa::check_finite_enabled() && !status) return ATTN_ERR_NULL;
 
   cudaStream_t h2d = nullptr, d2h = nullptr;
   if (int rc = copy_streams(&h2d, &d2h); rc != ATTN_OK) return rc;

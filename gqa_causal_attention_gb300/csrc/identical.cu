@@ -30,6 +30,7 @@ namespace {
 constexpr int kWarps = 4;
 
 __global__ void __launch_bounds__(kWarps * 32) identical_attn_kernel(IdentJob j) {
+  if (gated_off(j.skip)) return;
   const int lane = threadIdx.x & 31;
   const long rows = static_cast<long>(j.B) * j.H * j.L;
   const long nwarps = static_cast<long>(gridDim.x) * kWarps;

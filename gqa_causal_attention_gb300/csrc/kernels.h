@@ -31,6 +31,7 @@ struct RopeJob {
   float* v_cache;
   int capacity;
   int window;
+  const int32_t* skip = nullptr;   // non-finite check on: return if *skip has ATTN_DEV_NONFINITE
 };
 
 // ATTN_OK for cudaSuccess; otherwise remembers e for attn_last_cuda_error on this host
@@ -78,6 +79,7 @@ struct AttnShape {
   // padding rows of out are written as +0.0 and padding keys are never seen.
   // nullptr: every row has length L. Not combined with kv_off.
   const int32_t* lengths = nullptr;
+  const int32_t* skip = nullptr;   // as RopeJob::skip
 };
 
 cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
@@ -89,7 +91,8 @@ cudaError_t launch_prefill_tc_vt(const AttnShape& a, cudaStream_t stream);   // 
 // in P V.
 cudaError_t launch_transpose_v(const float* v, float* vt, int BHkv, int L, int D, int vt_pitch,
                                cudaStream_t stream, const int32_t* lengths = nullptr,
-                               int Hkv = 1, int32_t* status = nullptr);
+                               int Hkv = 1, int32_t* status = nullptr,
+                               const int32_t* skip = nullptr);
 bool prefill_tc_supports(int D);
 // Keys for continuing a cached prefix: per (b, kv head), rows [0, pre_b) from the
 // cache (positions start[b] - pre_b .. start[b] - 1; slot = position, or position
@@ -107,6 +110,7 @@ struct GatherJob {
   float* vtg;
   int B, Hkv, L, D, capacity, window, Lk, vt_pitch, max_start;
   int32_t* status;
+  const int32_t* skip = nullptr;
 };
 cudaError_t launch_gather_kv(const GatherJob& j, cudaStream_t stream);
 bool prefill_tq_supports_kv_off(int D);
@@ -126,6 +130,7 @@ struct DecodeJob {
   float* partial;           // workspace [B, H, nsplit, D + 2]
   int nsplit, chunk;
   int32_t* status;
+  const int32_t* skip = nullptr;
 };
 
 // The identical numeric mode: one warp per query row, fixed arithmetic order
@@ -146,14 +151,17 @@ struct IdentJob {
   int B, H, Hkv, L, D, capacity, window;
   float softcap, scale;
   int32_t* status;
+  const int32_t* skip = nullptr;
 };
 cudaError_t launch_identical(const IdentJob& j, cudaStream_t stream);
 
 // The decoder block around the attention (block.cu).
 cudaError_t launch_rmsnorm_rows(const float* x, const float* w, float* y, long T, int n,
-                                float eps, bool offset, bool round_out, cudaStream_t stream);
+                                float eps, bool offset, bool round_out, cudaStream_t stream,
+                                const int32_t* skip = nullptr);
 cudaError_t launch_swap_mid(const float* in, float* out, int B, int P, int Q, int D,
-                            cudaStream_t stream);   // [B, P, Q, D] -> [B, Q, P, D]
+                            cudaStream_t stream,
+                            const int32_t* skip = nullptr);   // [B, P, Q, D] -> [B, Q, P, D]
 
 // Projections on the tensor cores (gemm_tc.cu): Y = X W^T, W in torch's [out, in]
 // layout, TF32 operands, fp32 accumulation. Up to three segments share X.
@@ -178,9 +186,36 @@ struct GemmJob {
   int nseg;
   GemmSegment seg[3];       // SwiGLU: one segment only
   int32_t* status;
+  const int32_t* skip = nullptr;
 };
 bool gemm_tc_supports(const GemmJob& j);
 cudaError_t launch_gemm_tc(const GemmJob& j, cudaStream_t stream);
+
+// The opt-in non-finite input check (finite.cu). A region is B * NH blocks of R
+// rows, C values of each row checked, rows ld floats apart (blocks R * ld apart);
+// the rows checked depend on the mode (info[b] per batch row b = block / NH).
+enum { kFiniteAll = 0,       // every row
+       kFiniteLen = 1,       // rows < info[b] (a ragged row's length)
+       kFiniteCache = 2,     // cache slots live at cache length info[b]: rows < min(info[b], R)
+       kFinitePrefix = 3 };  // slots of the positions a chunk at start info[b] reads from the
+                             // cache: all below it, or the last window - 1 of them in a ring
+struct FiniteRegion {
+  const float* p;
+  int B, NH;
+  long R, C, ld;
+  int mode;
+  const int32_t* info;
+  int window;
+};
+constexpr int kMaxFiniteRegions = 12;
+struct FiniteJob {
+  int n;
+  FiniteRegion r[kMaxFiniteRegions];
+  int32_t* status;
+};
+int check_finite_enabled();              // the process-wide switch (ATTN_CHECK_FINITE at first use)
+int set_check_finite(int on);            // on < 0: query only; returns the previous value
+cudaError_t launch_finite_check(const FiniteJob& j, cudaStream_t stream);
 
 void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream);

@@ -44,6 +44,7 @@ struct TcArgs {
   int Lk;
   // Ragged batch (nullptr: every row has length L): see AttnShape::lengths.
   const int32_t* lengths;
+  const int32_t* skip;                         // non-finite check: see common.cuh gated_off
 };
 
 // Real length of batch row b (lengths outside [0, L] are clamped; the V^T

@@ -23,6 +23,7 @@ template <int NE>
 __global__ void __launch_bounds__(kThreads) prefill_simt_kernel(AttnShape a) {
   __shared__ float sk[kBK][NE * kTPR];
   __shared__ float sv[kBK][NE * kTPR];
+  if (gated_off(a.skip)) return;
   const int D = a.D, L = a.L;
   const int G = a.H / a.Hkv;
   const int bh = blockIdx.y;                    // b * H + h

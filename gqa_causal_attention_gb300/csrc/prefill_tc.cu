@@ -19,8 +19,10 @@ using namespace prefill;
 __global__ void __launch_bounds__(256) transpose_v_kernel(const float* __restrict__ v,
                                                           float* __restrict__ vt, int L, int D,
                                                           int Lp, const int32_t* lengths,
-                                                          int Hkv, int32_t* status) {
+                                                          int Hkv, int32_t* status,
+                                                          const int32_t* skip) {
   __shared__ float tile[32][33];
+  if (gated_off(skip)) return;
   const long bh = blockIdx.z;
   const int l0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
   const int r = threadIdx.x / 8, q = threadIdx.x % 8;
@@ -60,16 +62,16 @@ int prefill_vt_pitch(int L) { return (L + 3) / 4 * 4; }
 
 cudaError_t launch_transpose_v(const float* v, float* vt, int BHkv, int L, int D, int vt_pitch,
                                cudaStream_t stream, const int32_t* lengths, int Hkv,
-                               int32_t* status) {
+                               int32_t* status, const int32_t* skip) {
   transpose_v_kernel<<<dim3((L + 31) / 32, (D + 31) / 32, BHkv), 256, 0, stream>>>(
-      v, vt, L, D, vt_pitch, lengths, Hkv, status);
+      v, vt, L, D, vt_pitch, lengths, Hkv, status, skip);
   return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_tc(const AttnShape& s, cudaStream_t stream) {
   if (!prefill_tc_supports(s.D)) return cudaErrorNotSupported;
   if (cudaError_t e = launch_transpose_v(s.v, s.vt, s.B * s.Hkv, s.L, s.D, s.vt_pitch, stream,
-                                         s.lengths, s.Hkv, s.status);
+                                         s.lengths, s.Hkv, s.status, s.skip);
       e != cudaSuccess)
     return e;
   return launch_prefill_tc_vt(s, stream);

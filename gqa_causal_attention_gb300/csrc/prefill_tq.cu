@@ -830,6 +830,7 @@ __global__ void __launch_bounds__(PCfg<DP>::kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v,
                       const __grid_constant__ CUtensorMap tm_o, const TcArgs a) {
   using C = PCfg<DP, RAGGED>;
+  if (gated_off(a.skip)) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* skv = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -957,6 +958,7 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   a.kv_off = s.kv_off;
   a.Lk = Lk;
   a.lengths = s.lengths;
+  a.skip = s.skip;
   const int grid = a.units < sm_count() ? a.units : sm_count();
   prefill_tq_kernel<DP, ROPE, RAGGED><<<grid, C::kThreads, C::kSmem, stream>>>(tq, tk, tv, to, a);
   return cudaGetLastError();

@@ -79,6 +79,7 @@ __device__ __forceinline__ void store_vec(float* p, const float* r) {
 template <int VEC, int RPW, bool APPEND, bool TAIL>
 __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
   constexpr int NP = 4 / VEC;            // R/2 <= 128  ->  <= 4/VEC vectors per lane
+  if (gated_off(j.skip)) return;
   const int lane = threadIdx.x & 31;
   const long warps = (long)gridDim.x * (blockDim.x >> 5);
   const long gwarp = (long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);

@@ -30,7 +30,8 @@
  *   live on the device (start, cache_len) are checked again by the kernels:
  *   a row that breaks a rule is skipped (its outputs are left untouched) and
  *   an ATTN_DEV_* bit is OR-ed into *status (a caller-owned device int32,
- *   which may be NULL to skip the report). Kernels never trap.
+ *   which may be NULL to skip the report, except with the non-finite check
+ *   on: see attn_set_check_finite). Kernels never trap.
  */
 #ifndef GQA_ATTN_H
 #define GQA_ATTN_H
@@ -59,6 +60,9 @@ extern "C" {
 #define ATTN_DEV_LENGTH    4   /* cache_len[b] outside [1, max_cache_len] or > capacity,
                                   or a ragged prefill's lengths[b] outside [1, L] */
 #define ATTN_DEV_TIMEOUT   8   /* a pipeline wait ran past its limit; outputs invalid */
+#define ATTN_DEV_NONFINITE 16  /* the opt-in check found an inf or NaN input; the call
+                                  (and every later checked call on this status word)
+                                  computed nothing, see attn_set_check_finite */
 
 /* RoPE frequency scaling ("mojolearn.transformer", rope_scaling). */
 #define ATTN_ROPE_SCALING_NONE   0
@@ -467,6 +471,30 @@ int gqa_attn_decode_static(const float* q, const float* k_cache, const float* v_
  * have no counterpart to it.
  */
 int attn_selftest_wait_timeout(int32_t* status, void* stream);
+
+/*
+ * The non-finite input check ("mojolearn.transformer", TransformerBlock:
+ * non-finite weights, inputs or cache values raise an error before any
+ * computation). Off by default; on when the environment variable
+ * ATTN_CHECK_FINITE is set to anything but "" or "0" at the library's first
+ * use, or after attn_set_check_finite(1). Process-wide.
+ *
+ * With the check on, every computing call (all of the above but the table
+ * calls, v_transpose and the self-test) first enqueues one read pass over the
+ * values it will read: its input tensors and weights, and of a cache only the
+ * slots it reads (decode: the live slots at cache_len[b]; a continued or
+ * identical prefill: the prefix its first query sees); of a ragged batch only
+ * the real rows. An inf or NaN ORs ATTN_DEV_NONFINITE into *status, and every
+ * kernel of the call -- and of any later checked call given the same status
+ * word while that bit stays set -- returns before writing anything: outputs,
+ * k rotated in place and caches are left as they were. The check needs a
+ * status word: such calls return ATTN_ERR_NULL for status == NULL.
+ * gqa_attn_prefill_from_host checks each chunk on its own: chunks before the
+ * one with the bad value are computed, the others are not, and the copies back
+ * to out_host still run.
+ * on: 1 turns the check on, 0 off, < 0 leaves it; returns the previous setting.
+ */
+int attn_set_check_finite(int on);
 
 /* A static string naming a return code (ATTN_OK / ATTN_ERR_*). */
 const char* attn_status_string(int code);

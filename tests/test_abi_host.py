@@ -481,3 +481,42 @@ def test_from_host_chunk_plan_follows_the_documented_rule():
         got = lib.gqa_attn_prefill_from_host_workspace_size(B, H, Hkv, L, D, cap,
                                                             ctypes.byref(rp))
         assert got == want, (D, B, Hkv, L, cap, got, want)
+
+
+def test_check_finite_switch_follows_the_environment(tmp_path):
+    """ATTN_CHECK_FINITE turns the non-finite check on at first use; unset, empty or "0"
+    leaves it off (fresh processes, so the process-wide switch starts unread)."""
+    import subprocess
+    import sys
+    code = ("import gqa_causal_attention_gb300 as g\n"
+            "print(g.attn_set_check_finite(-1))\n")
+    for val, want in ((None, "0"), ("", "0"), ("0", "0"), ("1", "1"), ("yes", "1")):
+        env = {k: v for k, v in os.environ.items() if k != "ATTN_CHECK_FINITE"}
+        if val is not None:
+            env["ATTN_CHECK_FINITE"] = val
+        env["PYTHONPATH"] = ROOT
+        out = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, env=env,
+                             capture_output=True, text=True, timeout=300)
+        assert out.stdout.strip() == want, (val, out.stdout, out.stderr)
+
+
+@no_device
+def test_check_finite_needs_a_status_word():
+    """With the check on, a computing call without a status word is refused before any
+    launch; with it off the same call goes on to launch (which fails here, with no GPU)."""
+    lib = g.load()
+    P = ctypes.c_void_p(0x100000)
+    prev = g.attn_set_check_finite(1)
+    try:
+        assert g.attn_set_check_finite(-1) == 1
+        assert lib.gqa_attn_decode(P, P, P, P, 10, P, 2, 4, 2, 64, 64, 0, 0.0, 0.0, P, 1 << 20,
+                                   None, None) == -1
+        assert lib.attn_linear(P, P, None, P, 8, 16, 32, None, None) == -1
+        rp = g.RopeParams.make(theta=1e4, max_positions=64)
+        assert lib.attn_rope_apply(P, 1, 2, 8, 16, P, 0, ctypes.byref(rp), P, None, 1e-6, None,
+                                   None) == -1
+        g.attn_set_check_finite(0)
+        assert lib.gqa_attn_decode(P, P, P, P, 10, P, 2, 4, 2, 64, 64, 0, 0.0, 0.0, P, 1 << 20,
+                                   None, None) == -8
+    finally:
+        g.attn_set_check_finite(prev)
