@@ -55,6 +55,12 @@ def parse():
                     help="time the steps as eager launches instead of CUDA graph replays")
     ap.add_argument("--unfused-q-rope", action="store_true",
                     help="time attn_rope_apply on q + gqa_attn_prefill instead of the fused call")
+    ap.add_argument("--no-gemma", action="store_true",
+                    help="skip the Gemma-2-shaped window prefill key")
+    ap.add_argument("--no-block", action="store_true",
+                    help="skip the decoder block and projection (attn_linear) keys")
+    ap.add_argument("--no-identical", action="store_true",
+                    help="skip the identical-numeric-mode timings")
     ap.add_argument("--decode-batch", type=int, default=0,
                     help="rows of the batched decode (default: the workload's 64; smaller "
                          "values are for profiling captures)")
@@ -77,8 +83,7 @@ def peaks():
 # current kernels (profiles/); None where no capture of the timed kernel exists.
 # The decode capture ran on 16 of the 64 rows; its traffic scales with the
 # algorithmic bytes processed (ratio below).
-NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 334.207232e6 + 96.35328e6,
-                       ("gemma2_window", "fused"): 2153.623e6 + 246.349568e6}
+NCU_PREFILL_TRAFFIC = {}
 NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903360e6 + 4.927232e6) / 585572352.0
 
 
@@ -202,6 +207,28 @@ def timed(fn, steps, warmup, dist, events_for=None):
     return ms
 
 
+def kernel_median(fn, iters=50, warm=10):
+    """Device time of one call of fn (ms): warm-up calls, then the median of `iters`
+    calls each bracketed by CUDA events on the launching stream."""
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    evs = []
+    for _ in range(iters):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+KERNEL_ITERS, KERNEL_WARM = 50, 10
+
+
 def graph_of(fn, warm=3):
     """fn's launches captured once into a CUDA graph (warmed up on a side stream
     first); replaying it takes the per-call host work out of the step."""
@@ -239,11 +266,12 @@ def prefill_bytes(w):
                 + 2 * w.B * w.Hkv * cap * w.D)
 
 
-def bench_prefill(w, args, dist, dev, rank):
+def bench_prefill(w, args, dist, dev, rank, steps=None, e2e=True):
     import torch
     import gqa_causal_attention_gb300 as g
     from gqa_causal_attention_gb300 import synthetic as syn
 
+    steps = args.steps if steps is None else steps
     inp = syn.prefill_inputs(w)
     rp = g.RopeParams.make(theta=w.theta, rope_dim=w.rope_dim, max_positions=w.max_positions,
                            scaling=w.scaling)
@@ -262,51 +290,65 @@ def bench_prefill(w, args, dist, dev, rank):
     vt = torch.empty(w.B * w.Hkv * w.D * g.gqa_attn_vt_pitch(w.L), device=dev)
     vws = torch.empty(max(4, g.gqa_attn_prefill_rope_vt_workspace_size(w.B, w.H, w.L, w.D, rp)
                           // 4), device=dev)
-    kern = []
+    # q's RMSNorm/RoPE runs inside the attention kernel when the kernel takes it (no
+    # workspace needed), else as a pass over q inside the call
+    q_fused = g.gqa_attn_prefill_rope_vt_workspace_size(w.B, w.H, w.L, w.D, rp) <= 16
 
-    def attention():
-        # the attention kernel alone (timed for the roofline): v arrives transposed
-        if args.unfused_q_rope:
-            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
-                               status=status)
-        else:
-            g.gqa_attn_prefill_rope_vt(q, k, vt, out, start, 0, rp, table, qn, w.norm_eps,
-                                       w.window, w.softcap, 0.0, workspace=vws, status=status)
-
-    def step(record=False):
+    def step():
         # k: RMSNorm + RoPE in place and into the cache; v transposed for the tensor cores;
-        # q: RMSNorm + RoPE inside the attention kernel
+        # q: RMSNorm + RoPE inside the attention kernel (or a pass inside the call)
         g.kv_cache_append(k, v, start, 0, rp, table, kn, w.norm_eps, kc, vc, w.window, status)
         if args.unfused_q_rope:
             g.attn_rope_apply(q, start, 0, rp, table, qn, w.norm_eps, status)
+            g.gqa_attn_prefill(q, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
+                               status=status)
         else:
             g.gqa_attn_v_transpose(v, vt)
-        if record:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            attention()
-            b.record()
-            kern.append((a, b))
-        else:
-            attention()
+            g.gqa_attn_prefill_rope_vt(q, k, vt, out, start, 0, rp, table, qn, w.norm_eps,
+                                       w.window, w.softcap, 0.0, workspace=vws, status=status)
 
-    # Eager launches, with CUDA events around the prefill call (kernel time).
-    ms_eager = timed(lambda: step(True), args.steps, args.warmup, dist)
-    kern = kern[args.warmup:]
-    kern_ms = sum(a.elapsed_time(b) for a, b in kern) / max(1, len(kern))
+    ms_eager = timed(step, steps, args.warmup, dist)
+    launches_per_step = 3 + (0 if q_fused or args.unfused_q_rope else 1)
     # The step as a CUDA graph: the whole-step time.
     with ClockSampler(torch.cuda.current_device()) as clk:
         if args.no_graph:
-            ms = timed(lambda: step(False), args.steps, args.warmup, dist)
+            ms = timed(step, steps, args.warmup, dist)
         else:
-            gr = graph_of(lambda: step(False))
-            ms = timed(gr.replay, args.steps, args.warmup, dist)
+            gr = graph_of(step)
+            ms = timed(gr.replay, steps, args.warmup, dist)
+    torch.cuda.synchronize()
+    # The attention kernel alone (the roofline): with q rotated in the kernel, the call
+    # itself; otherwise q rotated once beforehand and the call without RoPE.
+    if args.unfused_q_rope:
+        qrot = q
+    elif q_fused:
+        qrot = None
+    else:
+        qrot = q.clone()
+        g.attn_rope_apply(qrot, start, 0, rp, table, qn, w.norm_eps, status)
+
+    def attention():
+        if args.unfused_q_rope:
+            g.gqa_attn_prefill(qrot, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
+                               status=status)
+        elif q_fused:
+            g.gqa_attn_prefill_rope_vt(q, k, vt, out, start, 0, rp, table, qn, w.norm_eps,
+                                       w.window, w.softcap, 0.0, workspace=vws, status=status)
+        else:
+            g.gqa_attn_prefill_rope_vt(qrot, k, vt, out, None, 0, None, None, None, w.norm_eps,
+                                       w.window, w.softcap, 0.0, status=status)
+
+    kern_ms = kernel_median(attention, KERNEL_ITERS, KERNEL_WARM)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-    res = {"ms": ms / args.steps, "ms_eager": ms_eager / args.steps, "kernel_ms": kern_ms,
-           "clocks": clk.summary(), "launches_per_step": 4 if args.unfused_q_rope else 3}
+    kernel_launches = (2 if args.unfused_q_rope else 1) * KERNEL_ITERS
+    res = {"ms": ms / steps, "ms_eager": ms_eager / steps, "kernel_ms": kern_ms,
+           "clocks": clk.summary(), "launches_per_step": launches_per_step,
+           "q_fused": q_fused,
+           "launches": launches_per_step * 2 * steps + kernel_launches}
+    del qrot
 
-    if not args.no_e2e:
+    if e2e and not args.no_e2e:
         hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
         hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
         cap = kc.shape[2]
@@ -340,6 +382,7 @@ def bench_prefill(w, args, dist, dev, rank):
             per_row = -(-w.Hkv // -(-w.Hkv // (16 // w.B)))
             chunks = w.B * per_row
         res["e2e_launches"] = 3 * chunks * e_steps + res["launches_per_step"] * e_steps
+        res["launches"] += res["e2e_launches"]
         res["e2e_chunks"] = chunks
         res["h2d"] = sum(t.numel() * 4 for t in (hq, hk, hv))
         res["d2h"] = hout.numel() * 4
@@ -367,29 +410,25 @@ def bench_decode(w, args, dist, dev):
                                                              w.window) // 4), device=dev)
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    kern = []
 
-    def step(record=True):
+    def step():
+        # q and k are rotated in place at the same positions on every repeat: the work of
+        # a step does not depend on the values
         g.attn_rope_apply(q, pos, maxlen - 1, rp, table, None, w.norm_eps, status)
         g.kv_cache_append(k, v, pos, maxlen - 1, rp, table, None, w.norm_eps, kc, vc, 0, status)
-        if record:
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
         g.gqa_attn_decode(q, kc, vc, cl, maxlen, out, 0, w.softcap, 0.0, ws, status)
-        if record:
-            b.record()
-            kern.append((a, b))
 
     steps = args.decode_steps
     ms_eager = timed(step, steps, args.warmup, dist)
-    kern = kern[args.warmup:]
-    kern_ms = sum(a.elapsed_time(b) for a, b in kern) / max(1, len(kern))
     with ClockSampler(torch.cuda.current_device()) as clk:
         if args.no_graph:
-            ms = timed(lambda: step(False), steps, args.warmup, dist)
+            ms = timed(step, steps, args.warmup, dist)
         else:
-            gr = graph_of(lambda: step(False))
+            gr = graph_of(step)
             ms = timed(gr.replay, steps, args.warmup, dist)
+    kern_ms = kernel_median(
+        lambda: g.gqa_attn_decode(q, kc, vc, cl, maxlen, out, 0, w.softcap, 0.0, ws, status),
+        KERNEL_ITERS, KERNEL_WARM)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     nbytes = 2.0 * w.Hkv * w.D * 4 * float((n + 1).sum())
@@ -397,7 +436,8 @@ def bench_decode(w, args, dist, dev):
         else 1
     return {"ms": ms / steps, "ms_eager": ms_eager / steps, "kernel_ms": kern_ms, "bytes": nbytes,
             "clocks": clk.summary(),
-            "launches_per_step": 2 + ksplit}
+            "launches_per_step": 2 + ksplit,
+            "launches": (2 + ksplit) * 2 * steps + ksplit * KERNEL_ITERS}
 
 
 def bench_long_decode(w, args, dist, dev):
@@ -486,6 +526,110 @@ def bench_chunked_prefill(args, dist, dev):
     flops = 4.0 * B * H * D * sum(P + l + 1 for l in range(L))
     return {"config": dict(c), "ms": ms, "tflops": flops / (ms * 1e-3) / 1e12, "flops": flops,
             "launches": 2}
+
+
+BLOCK = {"B": 4, "L": 2048, "H": 32, "Hkv": 8, "D": 128, "IT": 14336, "theta": 5e5}
+
+
+def block_flops(c):
+    """Projection FLOP (q, k, v, o, gate, up, down) plus attention FLOP of one block."""
+    T, dm, kw = c["B"] * c["L"], c["H"] * c["D"], c["Hkv"] * c["D"]
+    proj = 2.0 * T * dm * (dm + 2 * kw + dm + 3 * c["IT"])
+    attn = 4.0 * c["B"] * c["H"] * c["D"] * visible_pairs(c["L"], 0)
+    return proj, attn
+
+
+def bench_block(args, dist, dev):
+    """The Llama-3-8B-shaped decoder block (gqa_block_forward: norms, the seven
+    projections on the tcgen05 GEMM kernel, RoPE, attention, SwiGLU, residuals) on
+    4 x 2048 tokens, and the projection kernel alone (attn_linear) at the down
+    projection's shape."""
+    import torch
+    import gqa_causal_attention_gb300 as g
+
+    c = BLOCK
+    B, L, H, Hkv, D, IT = c["B"], c["L"], c["H"], c["Hkv"], c["D"], c["IT"]
+    dm, kw, T = H * D, Hkv * D, B * L
+    gen = torch.Generator(device=dev).manual_seed(11)
+
+    def mat(rows, cols, gain=0.5):
+        return torch.randn(rows, cols, device=dev, generator=gen) * (gain / cols ** 0.5)
+
+    w = {"input_layernorm.weight": 1 + 0.1 * torch.randn(dm, device=dev, generator=gen),
+         "post_attention_layernorm.weight": 1 + 0.1 * torch.randn(dm, device=dev, generator=gen),
+         "q_proj.weight": mat(dm, dm, 1.0), "k_proj.weight": mat(kw, dm, 1.0),
+         "v_proj.weight": mat(kw, dm), "o_proj.weight": mat(dm, dm),
+         "gate_proj.weight": mat(IT, dm), "up_proj.weight": mat(IT, dm),
+         "down_proj.weight": mat(dm, IT)}
+    x = torch.randn(B, L, dm, device=dev, generator=gen)
+    out = torch.empty_like(x)
+    rp = g.RopeParams.make(theta=c["theta"], max_positions=8192,
+                           scaling=("llama3", 8.0, 1.0, 4.0, 8192))
+    table = g.rope_table(rp, D, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = torch.empty(g.gqa_block_forward_workspace_size(B, L, H, Hkv, D, IT, rp) // 4 + 4,
+                     device=dev)
+
+    def block():
+        g.gqa_block_forward(x, out, w, H, Hkv, rp, table, workspace=ws, status=status)
+
+    iters = 20
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        block_ms = kernel_median(block, iters, 3)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    del w, x, out, ws
+    torch.cuda.empty_cache()
+    # the projection kernel alone at the down projection's shape
+    xl = torch.randn(T, IT, device=dev, generator=gen)
+    wl = mat(dm, IT)
+    yl = torch.empty(T, dm, device=dev)
+    lin_ms = kernel_median(lambda: g.attn_linear(xl, wl, yl), KERNEL_ITERS, KERNEL_WARM)
+    del xl, wl, yl
+    torch.cuda.empty_cache()
+    proj, attn = block_flops(c)
+    return {"config": dict(c), "ms": block_ms, "proj_flops": proj, "attn_flops": attn,
+            "clocks": clk.summary(), "linear_ms": lin_ms,
+            "linear_shape": {"T": T, "N": dm, "K": IT},
+            "linear_flops": 2.0 * T * dm * IT,
+            # kernels per block: 2 RMSNorm, 4 projection launches, k RoPE, V^T, attention
+            "launches": 9 * (iters + 3) + KERNEL_ITERS + KERNEL_WARM}
+
+
+def bench_identical(args, dist, dev):
+    """The identical numeric mode's two calls on the Llama-3-8B-shaped prefill and on the
+    batched decode (CUDA cores, fixed summation order): what reproducibility costs."""
+    import torch
+    import gqa_causal_attention_gb300 as g
+    from gqa_causal_attention_gb300 import synthetic as syn
+
+    w = syn.WORKLOADS["llama3_8b_prefill"]
+    gen = torch.Generator(device=dev).manual_seed(13)
+    q = torch.randn(w.B, w.H, w.L, w.D, device=dev, generator=gen)
+    k = torch.randn(w.B, w.Hkv, w.L, w.D, device=dev, generator=gen)
+    v = torch.randn(w.B, w.Hkv, w.L, w.D, device=dev, generator=gen)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pre_ms = kernel_median(lambda: g.gqa_attn_prefill_identical(q, k, v, out, status=status),
+                           5, 1)
+    del q, k, v, out
+    wd = syn.WORKLOADS["batched_decode"]
+    n = syn.cache_lengths(wd.seed, wd.B, *wd.cache_len_range)
+    kc = torch.randn(wd.B, wd.Hkv, wd.capacity, wd.D, device=dev, generator=gen)
+    vc = torch.randn(wd.B, wd.Hkv, wd.capacity, wd.D, device=dev, generator=gen)
+    qd = torch.randn(wd.B, wd.H, 1, wd.D, device=dev, generator=gen)
+    od = torch.empty_like(qd)
+    cl = (n + 1).to(dev)
+    maxlen = int(n.max()) + 1
+    dec_ms = kernel_median(lambda: g.gqa_attn_decode_identical(qd, kc, vc, cl, maxlen, od,
+                                                               status=status), 5, 1)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    del kc, vc
+    torch.cuda.empty_cache()
+    return {"prefill_ms": pre_ms, "prefill_flops": prefill_flops(w),
+            "decode_ms": dec_ms, "decode_bytes": 2.0 * wd.Hkv * wd.D * 4 * float((n + 1).sum()),
+            "launches": 12}
 
 
 def cpu_baseline_prefill(w, budget_s=20.0, min_s=10.0):
@@ -614,12 +758,11 @@ def main():
     fl = prefill_flops(w)
     value = world * fl / (pre["ms"] * 1e-3) / 1e12
     kern_tflops = fl / (pre["kernel_ms"] * 1e-3) / 1e12
-    # q RMSNorm/RoPE runs inside the attention kernel when the kernel takes it
-    # (no workspace needed), else as a pass over q inside the same call
-    q_fused = g.gqa_attn_prefill_rope_vt_workspace_size(
-        w.B, w.H, w.L, w.D, g.RopeParams.make(theta=w.theta, rope_dim=w.rope_dim,
-                                              max_positions=w.max_positions,
-                                              scaling=w.scaling)) <= 16
+    q_fused = pre["q_fused"]
+    gem = None
+    if not args.no_gemma and w.name != "gemma2_window":
+        gem = bench_prefill(syn.WORKLOADS["gemma2_window"], args, dist, dev, rank,
+                            steps=max(5, min(args.steps, 50)), e2e=False)
     dec = None
     if not args.no_decode:
         wd = syn.WORKLOADS["batched_decode"]
@@ -631,6 +774,8 @@ def main():
     lng = None
     if not args.no_decode and not args.no_long_decode:
         lng = bench_long_decode(syn.WORKLOADS["long_decode"], args, dist, dev)
+    blk = None if args.no_block else bench_block(args, dist, dev)
+    idn = None if args.no_identical else bench_identical(args, dist, dev)
 
     if rank != 0:
         if dist:
@@ -663,15 +808,15 @@ def main():
                      "traffic_note": "ncu dram bytes of prefill_tq_kernel (one launch)",
                      "kernel": ("gqa_attn_prefill (V^T pre-pass + attention)"
                                 if args.unfused_q_rope else
-                                "gqa_attn_prefill_rope_vt (the attention kernel alone)"
-                                if q_fused else
-                                "gqa_attn_prefill_rope_vt (q rotation pass + attention kernel)"),
+                                "gqa_attn_prefill_rope_vt (the attention kernel alone)"),
                      "kernel_ms": pre["kernel_ms"],
+                     "kernel_timing": f"median of {KERNEL_ITERS} calls after {KERNEL_WARM} "
+                                      "warm-ups, CUDA events on the launching stream",
                      "peak_note": "dense TF32 measured in this run: cuBLAS fp32 8192^3 "
                                   "with TF32 allowed, best of 10",
                      "frac_of_tf32_nominal_ratio_peak": kern_tflops / pk["tf32_derived"],
                      "frac_of_bf16_peak": kern_tflops / pk["bf16_tflops"]},
-        "gpu_launches": pre["launches_per_step"] * args.steps,
+        "gpu_launches": pre["launches"],
         "clocks": pre["clocks"],
     }
     if "e2e_ms" in pre:
@@ -681,7 +826,7 @@ def main():
                        "call": "gqa_attn_prefill_from_host (pinned host q, k, v in, out back; "
                                f"{pre['e2e_chunks']} chunks overlap copies and kernels)",
                        "serial_ms_per_step": pre["e2e_serial_ms"]}
-        line["gpu_launches"] += pre["e2e_launches"]
+
     if dec is not None:
         gbs = dec["bytes"] / (dec["ms"] * 1e-3) / 1e9
         kgbs = dec["bytes"] / (dec["kernel_ms"] * 1e-3) / 1e9
@@ -694,7 +839,7 @@ def main():
                          "frac": kgbs / pk["hbm_gbs"],
                          "traffic": NCU_DECODE_TRAFFIC_PER_ALG_BYTE * dec["bytes"],
                          "kernel": "gqa_attn_decode", "kernel_ms": dec["kernel_ms"]},
-            "gpu_launches": dec["launches_per_step"] * args.decode_steps,
+            "gpu_launches": dec["launches"],
             "clocks": dec["clocks"]}
         line["gpu_launches"] += line["decode"]["gpu_launches"]
     if chk is not None:
@@ -719,6 +864,62 @@ def main():
             "note": "the cache (134 MB) is about L2-sized; part of each step's reads hit L2",
             "gpu_launches": lng["launches"], "clocks": lng["clocks"]}
         line["gpu_launches"] += lng["launches"]
+    if gem is not None:
+        wg = syn.WORKLOADS["gemma2_window"]
+        gfl = prefill_flops(wg)
+        gk = gfl / (gem["kernel_ms"] * 1e-3) / 1e12
+        line["gemma2_window"] = {
+            "workload": "gemma2_window",
+            "config": {"B": wg.B, "L": wg.L, "H": wg.H, "Hkv": wg.Hkv, "D": wg.D,
+                       "window": wg.window, "softcap": wg.softcap, "qk_norm": wg.qk_norm,
+                       "rope": f"theta {wg.theta:g}", "cache": f"ring of {wg.window}"},
+            "value": world * gfl / (gem["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": gem["ms"], "ms_per_step_eager": gem["ms_eager"],
+            "flops_per_step": gfl,
+            "step": "kv_cache_append (k RMSNorm/RoPE into the ring) + gqa_attn_v_transpose + "
+                    "gqa_attn_prefill_rope_vt (q RMSNorm/RoPE as a pass inside the call); "
+                    "CUDA graph replays",
+            "roofline": {"bound": "tensor", "achieved": gk, "peak": pk["tf32_tflops"],
+                         "unit": "TFLOP/s", "frac": gk / pk["tf32_tflops"],
+                         "traffic": NCU_PREFILL_TRAFFIC.get(("gemma2_window", "fused")),
+                         "kernel": "the attention kernel alone (q rotated beforehand; "
+                                   "gqa_attn_prefill_rope_vt without RoPE)",
+                         "kernel_ms": gem["kernel_ms"],
+                         "frac_of_bf16_peak": gk / pk["bf16_tflops"]},
+            "gpu_launches": gem["launches"], "clocks": gem["clocks"]}
+        line["gpu_launches"] += gem["launches"]
+    if blk is not None:
+        btot = blk["proj_flops"] + blk["attn_flops"]
+        lt = blk["linear_flops"] / (blk["linear_ms"] * 1e-3) / 1e12
+        line["block"] = {
+            "workload": "llama3_8b_block", "config": blk["config"],
+            "value": world * btot / (blk["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "ms_per_step": blk["ms"], "flops_per_step": btot,
+            "proj_flops": blk["proj_flops"], "attn_flops": blk["attn_flops"],
+            "step": "gqa_block_forward: RMSNorm, q/k/v projections (one launch, head-major "
+                    "out), k RoPE, V^T + attention (q RoPE fused), o_proj + residual, "
+                    "RMSNorm, gate/up with SwiGLU epilogue, down_proj + residual; "
+                    "median of 20 calls",
+            "roofline": {"bound": "tensor", "achieved": lt, "peak": pk["tf32_tflops"],
+                         "unit": "TFLOP/s", "frac": lt / pk["tf32_tflops"], "traffic": None,
+                         "kernel": "attn_linear (gemm_tc_kernel) at the down projection's "
+                                   f"shape T={blk['linear_shape']['T']} "
+                                   f"N={blk['linear_shape']['N']} K={blk['linear_shape']['K']}",
+                         "kernel_ms": blk["linear_ms"]},
+            "gpu_launches": blk["launches"], "clocks": blk["clocks"]}
+        line["gpu_launches"] += blk["launches"]
+    if idn is not None:
+        line["identical"] = {
+            "prefill": {"workload": "llama3_8b_prefill",
+                        "value": world * idn["prefill_flops"] / (idn["prefill_ms"] * 1e-3) / 1e12,
+                        "unit": "TFLOP/s", "ms": idn["prefill_ms"],
+                        "call": "gqa_attn_prefill_identical (median of 5)"},
+            "decode": {"workload": "batched_decode",
+                       "value": world * idn["decode_bytes"] / (idn["decode_ms"] * 1e-3) / 1e9,
+                       "unit": "GB/s", "ms": idn["decode_ms"],
+                       "call": "gqa_attn_decode_identical (median of 5)"},
+            "gpu_launches": idn["launches"]}
+        line["gpu_launches"] += idn["launches"]
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_prefill(w)
     print(json.dumps(line), flush=True)

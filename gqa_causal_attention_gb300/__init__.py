@@ -159,6 +159,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         return lib
 
 
+def _rp(params):
+    """RoPE parameters by reference, or NULL."""
+    return None if params is None else ctypes.byref(params)
+
+
 def _ptr(t) -> ctypes.c_void_p | None:
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -265,7 +270,7 @@ def kv_cache_append(k, v, start, max_start: int, params, table, k_norm_w, norm_e
             or tuple(k_cache.shape[:2]) != (B, Hkv) or k_cache.shape[3] != D:
         raise ValueError("kv_cache_append: inconsistent shapes")
     rc = load().kv_cache_append(_ptr(k), _ptr(v), B, Hkv, L, D, _ptr(start), int(max_start),
-                                None if params is None else ctypes.byref(params), _ptr(table),
+                                _rp(params), _ptr(table),
                                 _ptr(k_norm_w), float(norm_eps), _ptr(k_cache), _ptr(v_cache),
                                 int(k_cache.shape[2]), int(window), _ptr(status),
                                 _stream(stream))
@@ -304,7 +309,7 @@ def gqa_attn_prefill(q, k, v, out, window: int = 0, softcap: float = 0.0, scale:
 def gqa_attn_prefill_rope_workspace_size(B: int, H: int, Hkv: int, L: int, D: int,
                                          params: RopeParams) -> int:
     return int(load().gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D,
-                                                           ctypes.byref(params)))
+                                                           _rp(params)))
 
 
 def gqa_attn_prefill_rope(q, k, v, out, start, max_start: int, params: RopeParams, table,
@@ -328,7 +333,7 @@ def gqa_attn_prefill_rope(q, k, v, out, start, max_start: int, params: RopeParam
         raise ValueError("workspace must be a contiguous CUDA tensor")
     wbytes = workspace.numel() * workspace.element_size()
     rc = load().gqa_attn_prefill_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, L, D,
-                                      _ptr(start), int(max_start), ctypes.byref(params),
+                                      _ptr(start), int(max_start), _rp(params),
                                       _ptr(table), _ptr(q_norm_w), float(norm_eps), int(window),
                                       float(softcap), float(scale), _ptr(workspace), wbytes,
                                       _ptr(status), _stream(stream))
@@ -338,7 +343,7 @@ def gqa_attn_prefill_rope(q, k, v, out, start, max_start: int, params: RopeParam
 def gqa_attn_prefill_ragged_workspace_size(B: int, H: int, Hkv: int, L: int, D: int,
                                            params: RopeParams = None) -> int:
     return int(load().gqa_attn_prefill_ragged_workspace_size(
-        B, H, Hkv, L, D, None if params is None else ctypes.byref(params)))
+        B, H, Hkv, L, D, _rp(params)))
 
 
 def gqa_attn_prefill_ragged(q, k, v, out, lengths, params: RopeParams = None, table=None,
@@ -368,7 +373,7 @@ def gqa_attn_prefill_ragged(q, k, v, out, lengths, params: RopeParams = None, ta
     wbytes = workspace.numel() * workspace.element_size()
     rc = load().gqa_attn_prefill_ragged(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, L, D,
                                         _ptr(lengths),
-                                        None if params is None else ctypes.byref(params),
+                                        _rp(params),
                                         _ptr(table), _ptr(q_norm_w), float(norm_eps),
                                         int(window), float(softcap), float(scale),
                                         _ptr(workspace), wbytes, _ptr(status), _stream(stream))
@@ -394,7 +399,7 @@ def gqa_attn_v_transpose(v, vt, stream=None) -> None:
 
 def gqa_attn_prefill_rope_vt_workspace_size(B: int, H: int, L: int, D: int,
                                             params: RopeParams) -> int:
-    return int(load().gqa_attn_prefill_rope_vt_workspace_size(B, H, L, D, ctypes.byref(params)))
+    return int(load().gqa_attn_prefill_rope_vt_workspace_size(B, H, L, D, _rp(params)))
 
 
 def gqa_attn_prefill_rope_vt(q, k, vt, out, start, max_start: int, params: RopeParams, table,
@@ -420,7 +425,7 @@ def gqa_attn_prefill_rope_vt(q, k, vt, out, start, max_start: int, params: RopeP
         raise ValueError("workspace must be a contiguous CUDA tensor")
     wbytes = workspace.numel() * workspace.element_size()
     rc = load().gqa_attn_prefill_rope_vt(_ptr(q), _ptr(k), _ptr(vt), _ptr(out), B, H, Hkv, L, D,
-                                         _ptr(start), int(max_start), ctypes.byref(params),
+                                         _ptr(start), int(max_start), _rp(params),
                                          _ptr(table), _ptr(q_norm_w), float(norm_eps),
                                          int(window), float(softcap), float(scale),
                                          _ptr(workspace), wbytes, _ptr(status), _stream(stream))
@@ -481,7 +486,7 @@ def gqa_attn_prefill_cached_workspace_size(B: int, H: int, Hkv: int, L: int, D: 
                                            params: RopeParams = None) -> int:
     return int(load().gqa_attn_prefill_cached_workspace_size(
         B, H, Hkv, L, D, int(max_start), int(window),
-        None if params is None else ctypes.byref(params)))
+        _rp(params)))
 
 
 def gqa_attn_prefill_cached(q, k, v, k_cache, v_cache, out, start, max_start: int,
@@ -508,7 +513,7 @@ def gqa_attn_prefill_cached(q, k, v, k_cache, v_cache, out, start, max_start: in
     wbytes = workspace.numel() * workspace.element_size()
     rc = load().gqa_attn_prefill_cached(
         _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), cap, _ptr(out), B, H, Hkv, L, D,
-        _ptr(start), int(max_start), None if params is None else ctypes.byref(params),
+        _ptr(start), int(max_start), _rp(params),
         _ptr(table), _ptr(q_norm_w), float(norm_eps), int(window), float(softcap), float(scale),
         _ptr(workspace), wbytes, _ptr(status), _stream(stream))
     _check("gqa_attn_prefill_cached", rc)

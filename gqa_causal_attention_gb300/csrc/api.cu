@@ -287,8 +287,8 @@ size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 size_t gqa_attn_prefill_rope_workspace_size(int B, int H, int Hkv, int L, int D,
                                             const attn_rope_params* rp) {
   const size_t base = gqa_attn_prefill_workspace_size(B, Hkv, L, D);
-  if (base == 0 || H < 1 || !rope_params_ok(rp, D)) return 0;
-  if (rope_fused(D, rope_dim_of(rp, D))) return base;
+  if (base == 0 || H < 1 || (rp && !rope_params_ok(rp, D))) return 0;
+  if (!rp || rope_fused(D, rope_dim_of(rp, D))) return base;
   return round256(base) + (size_t)B * H * L * D * sizeof(float);
 }
 
@@ -305,9 +305,9 @@ int gqa_attn_v_transpose(const float* v, float* vt, int B, int Hkv, int L, int D
 
 size_t gqa_attn_prefill_rope_vt_workspace_size(int B, int H, int L, int D,
                                                const attn_rope_params* rp) {
-  if (B < 0 || H < 1 || L < 0 || !gqa::prefill_tc_supports(D) || !rope_params_ok(rp, D))
+  if (B < 0 || H < 1 || L < 0 || !gqa::prefill_tc_supports(D) || (rp && !rope_params_ok(rp, D)))
     return 0;
-  if (rope_fused(D, rope_dim_of(rp, D)) || B == 0 || L == 0) return 16;
+  if (!rp || rope_fused(D, rope_dim_of(rp, D)) || B == 0 || L == 0) return 16;
   return (size_t)B * H * L * D * sizeof(float);
 }
 
@@ -324,17 +324,19 @@ int prefill_rope_impl(const float* q, const float* k, const float* v, const floa
   if (vt && !gqa::prefill_tc_supports(D)) return ATTN_ERR_SHAPE;
   if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
   if (B == 0 || L == 0) return ATTN_OK;
-  if (!q || !k || !(v || vt) || !out || !start || !rp || !table) return ATTN_ERR_NULL;
-  if (!rope_params_ok(rp, D) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
+  if (!q || !k || !(v || vt) || !out) return ATTN_ERR_NULL;
+  if (!rp && (table || q_norm_w)) return ATTN_ERR_PARAM;     // no RoPE: q arrives rotated
+  if (rp && (!start || !table)) return ATTN_ERR_NULL;
+  if ((rp && !rope_params_ok(rp, D)) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
   if (!aligned16(q) || !aligned16(k) || (v && !aligned16(v)) || (vt && !aligned16(vt)) ||
-      !aligned16(out) || !aligned16(table) || (q_norm_w && !aligned16(q_norm_w)))
+      !aligned16(out) || (table && !aligned16(table)) || (q_norm_w && !aligned16(q_norm_w)))
     return ATTN_ERR_ALIGN;
-  if (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_pos_of(rp))
+  if (rp && (max_start < 0 || (int64_t)max_start + L - 1 >= (int64_t)max_pos_of(rp)))
     return ATTN_ERR_POSITION;
   const size_t need = vt ? gqa_attn_prefill_rope_vt_workspace_size(B, H, L, D, rp)
                          : gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp);
-  const int R = rope_dim_of(rp, D);
-  const bool fused = rope_fused(D, R);
+  const int R = rp ? rope_dim_of(rp, D) : 0;
+  const bool fused = !rp || rope_fused(D, R);
   const bool needs_ws = !vt || !fused;
   if (needs_ws) {
     if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -367,6 +369,10 @@ int prefill_rope_impl(const float* q, const float* k, const float* v, const floa
     if (!gqa::prefill_tc_supports(D)) return cuda_status(gqa::launch_prefill_simt(a, s));
     return cuda_status(vt ? gqa::launch_prefill_tc_vt(a, s) : gqa::launch_prefill_tc(a, s));
   };
+  if (!rp) {
+    a.q = q;
+    return attend();
+  }
   if (fused) {
     a.q = q;
     a.rope.table = reinterpret_cast<const float2*>(table);

@@ -165,6 +165,8 @@ int gqa_attn_prefill(const float* q, const float* k, const float* v, float* out,
  * rope_dim % 64 == 0 the rotation happens inside the tensor-core kernel, in
  * tensor memory after the Q tile's copy there; other shapes rotate q into the
  * workspace first. Positions are start[b] + l; max_start bounds every start[b].
+ * rp == NULL (then table and q_norm_w must be NULL; start is not read): q is
+ * already rotated and the call is gqa_attn_prefill.
  */
 size_t gqa_attn_prefill_rope_workspace_size(int B, int H, int Hkv, int L, int D,
                                             const attn_rope_params* rp);
