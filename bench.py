@@ -53,6 +53,9 @@ def parse():
                     help="skip the carried-cache decode (1024 steps after a 1024-token prefill)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the steps as eager launches instead of CUDA graph replays")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="time kv_cache_append + gqa_attn_v_transpose + gqa_attn_prefill_rope_vt "
+                         "as the step instead of the fused gqa_attn_prefill_step")
     ap.add_argument("--unfused-q-rope", action="store_true",
                     help="time attn_rope_apply on q + gqa_attn_prefill instead of the fused call")
     ap.add_argument("--no-gemma", action="store_true",
@@ -290,11 +293,22 @@ def bench_prefill(w, args, dist, dev, rank, steps=None, e2e=True):
     vt = torch.empty(w.B * w.Hkv * w.D * g.gqa_attn_vt_pitch(w.L), device=dev)
     vws = torch.empty(max(4, g.gqa_attn_prefill_rope_vt_workspace_size(w.B, w.H, w.L, w.D, rp)
                           // 4), device=dev)
+    sws = torch.empty(max(4, g.gqa_attn_prefill_step_workspace_size(w.B, w.H, w.Hkv, w.L, w.D,
+                                                                    w.window, rp) // 4),
+                      device=dev)
     # q's RMSNorm/RoPE runs inside the attention kernel when the kernel takes it (no
     # workspace needed), else as a pass over q inside the call
     q_fused = g.gqa_attn_prefill_rope_vt_workspace_size(w.B, w.H, w.L, w.D, rp) <= 16
+    separate = args.separate_append or args.unfused_q_rope
 
     def step():
+        if not separate:
+            # one call: k RMSNorm/RoPE into the cache, v into the cache and transposed
+            # (one memory pass over k and v), then attention with q's RMSNorm/RoPE fused,
+            # reading the rotated keys from the cache
+            g.gqa_attn_prefill_step(q, k, v, out, kc, vc, rp, table, qn, kn, w.norm_eps,
+                                    w.window, w.softcap, 0.0, workspace=sws, status=status)
+            return
         # k: RMSNorm + RoPE in place and into the cache; v transposed for the tensor cores;
         # q: RMSNorm + RoPE inside the attention kernel (or a pass inside the call)
         g.kv_cache_append(k, v, start, 0, rp, table, kn, w.norm_eps, kc, vc, w.window, status)
@@ -308,7 +322,8 @@ def bench_prefill(w, args, dist, dev, rank, steps=None, e2e=True):
                                        w.window, w.softcap, 0.0, workspace=vws, status=status)
 
     ms_eager = timed(step, steps, args.warmup, dist)
-    launches_per_step = 3 + (0 if q_fused or args.unfused_q_rope else 1)
+    launches_per_step = (2 if not separate else 3) + (0 if q_fused or args.unfused_q_rope
+                                                      else 1)
     # The step as a CUDA graph: the whole-step time.
     with ClockSampler(torch.cuda.current_device()) as clk:
         if args.no_graph:
@@ -317,8 +332,16 @@ def bench_prefill(w, args, dist, dev, rank, steps=None, e2e=True):
             gr = graph_of(step)
             ms = timed(gr.replay, steps, args.warmup, dist)
     torch.cuda.synchronize()
-    # The attention kernel alone (the roofline): with q rotated in the kernel, the call
-    # itself; otherwise q rotated once beforehand and the call without RoPE.
+    # The attention kernel alone (the roofline): rotated keys and V^T prepared once; with
+    # q rotated in the kernel, the call itself; otherwise q rotated once beforehand and
+    # the call without RoPE.
+    if not separate:
+        krot = k.clone()
+        g.kv_cache_append(krot, v, start, 0, rp, table, kn, w.norm_eps, kc, vc, w.window,
+                          status)
+        g.gqa_attn_v_transpose(v, vt)
+    else:
+        krot = k
     if args.unfused_q_rope:
         qrot = q
     elif q_fused:
@@ -329,24 +352,24 @@ def bench_prefill(w, args, dist, dev, rank, steps=None, e2e=True):
 
     def attention():
         if args.unfused_q_rope:
-            g.gqa_attn_prefill(qrot, k, v, out, w.window, w.softcap, 0.0, workspace=pws,
+            g.gqa_attn_prefill(qrot, krot, v, out, w.window, w.softcap, 0.0, workspace=pws,
                                status=status)
         elif q_fused:
-            g.gqa_attn_prefill_rope_vt(q, k, vt, out, start, 0, rp, table, qn, w.norm_eps,
+            g.gqa_attn_prefill_rope_vt(q, krot, vt, out, start, 0, rp, table, qn, w.norm_eps,
                                        w.window, w.softcap, 0.0, workspace=vws, status=status)
         else:
-            g.gqa_attn_prefill_rope_vt(qrot, k, vt, out, None, 0, None, None, None, w.norm_eps,
-                                       w.window, w.softcap, 0.0, status=status)
+            g.gqa_attn_prefill_rope_vt(qrot, krot, vt, out, None, 0, None, None, None,
+                                       w.norm_eps, w.window, w.softcap, 0.0, status=status)
 
     kern_ms = kernel_median(attention, KERNEL_ITERS, KERNEL_WARM)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-    kernel_launches = (2 if args.unfused_q_rope else 1) * KERNEL_ITERS
+    kernel_launches = (2 if args.unfused_q_rope else 1) * (KERNEL_ITERS + KERNEL_WARM)
     res = {"ms": ms / steps, "ms_eager": ms_eager / steps, "kernel_ms": kern_ms,
            "clocks": clk.summary(), "launches_per_step": launches_per_step,
            "q_fused": q_fused,
            "launches": launches_per_step * 2 * steps + kernel_launches}
-    del qrot
+    del qrot, krot
 
     if e2e and not args.no_e2e:
         hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
@@ -791,12 +814,15 @@ def main():
                                                    if w.scaling else ""),
                    "mask": f"window {w.window}" if w.window else "causal",
                    "softcap": w.softcap, "qk_norm": w.qk_norm,
-                   "step": ("kv_cache_append (k RMSNorm/RoPE + cache) + "
-                            + ("attn_rope_apply (q) + gqa_attn_prefill (V^T pre-pass inside)"
-                               if args.unfused_q_rope
-                               else "gqa_attn_v_transpose + gqa_attn_prefill_rope_vt (q "
-                                    + ("RMSNorm/RoPE fused into the attention kernel)" if q_fused
-                                       else "RMSNorm/RoPE as a pass over q inside the call)"))
+                   "step": ((("kv_cache_append (k RMSNorm/RoPE + cache) + "
+                              + ("attn_rope_apply (q) + gqa_attn_prefill (V^T pre-pass inside)"
+                                 if args.unfused_q_rope
+                                 else "gqa_attn_v_transpose + gqa_attn_prefill_rope_vt"))
+                             if args.separate_append or args.unfused_q_rope else
+                             "gqa_attn_prefill_step: one pass writes rotated k and v into the "
+                             "cache and V^T, then the attention kernel reads k from the cache")
+                            + (" (q RMSNorm/RoPE fused into the attention kernel)" if q_fused
+                               else " (q RMSNorm/RoPE as a pass over q inside the call)")
                             + ("" if args.no_graph else "; timed as CUDA graph replays")),
                    "ms_per_step_eager": pre["ms_eager"],
                    "l2": f"inputs larger than L2 ({prefill_bytes(w) / 2**20:.0f} MiB per step)",
@@ -876,8 +902,8 @@ def main():
             "value": world * gfl / (gem["ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
             "ms_per_step": gem["ms"], "ms_per_step_eager": gem["ms_eager"],
             "flops_per_step": gfl,
-            "step": "kv_cache_append (k RMSNorm/RoPE into the ring) + gqa_attn_v_transpose + "
-                    "gqa_attn_prefill_rope_vt (q RMSNorm/RoPE as a pass inside the call); "
+            "step": "gqa_attn_prefill_step: one pass writes rotated k (ring + a rotated copy), "
+                    "v and V^T; q RMSNorm/RoPE as a pass; then the attention kernel; "
                     "CUDA graph replays",
             "roofline": {"bound": "tensor", "achieved": gk, "peak": pk["tf32_tflops"],
                          "unit": "TFLOP/s", "frac": gk / pk["tf32_tflops"],

@@ -422,6 +422,150 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
                            status, stream);
 }
 
+namespace {
+// Workspace of gqa_attn_prefill_step, in order: V^T | rotated keys (a ring shorter
+// than the chunk) | rotated q (shapes whose kernel does not rotate q) -- or, for
+// head dims the tensor cores do not take, rotated keys | rotated q.
+struct StepLayout {
+  bool tc;
+  size_t vt, kr, qrot, total;
+};
+StepLayout step_layout(int B, int H, int Hkv, int L, int D, int window,
+                       const attn_rope_params* rp) {
+  StepLayout y{};
+  y.tc = gqa::prefill_tc_supports(D) && gqa::append_vt_supports(D);
+  const size_t kv = (size_t)B * Hkv * L * D * sizeof(float);
+  size_t p = 0;
+  if (y.tc) {
+    y.vt = p;
+    p += round256((size_t)B * Hkv * D * gqa::prefill_vt_pitch(L) * sizeof(float));
+    y.kr = p;
+    if (window > 0 && L > window) p += round256(kv);
+    y.qrot = p;
+    if (!rope_fused(D, rope_dim_of(rp, D))) p += round256((size_t)B * H * L * D * sizeof(float));
+  } else {
+    y.kr = p;
+    p += round256(kv);
+    y.qrot = p;
+    p += round256((size_t)B * H * L * D * sizeof(float));
+  }
+  y.total = p;
+  return y;
+}
+}  // namespace
+
+size_t gqa_attn_prefill_step_workspace_size(int B, int H, int Hkv, int L, int D, int window,
+                                            const attn_rope_params* rp) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || !rope_params_ok(rp, D))
+    return 0;
+  if (B == 0 || L == 0) return 16;
+  return step_layout(B, H, Hkv, L, D, window, rp).total;
+}
+
+int gqa_attn_prefill_step(const float* q, const float* k, const float* v, float* out, int B,
+                          int H, int Hkv, int L, int D, const attn_rope_params* rp,
+                          const float* table, const float* q_norm_w, const float* k_norm_w,
+                          float norm_eps, float* k_cache, float* v_cache, int capacity,
+                          int window, float softcap, float scale, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream) {
+  if (!dims_ok(B, H, L, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || capacity < 1)
+    return ATTN_ERR_SHAPE;
+  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (!rp) return ATTN_ERR_NULL;
+  if (!rope_params_ok(rp, D) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
+  if (B == 0 || L == 0) return ATTN_OK;
+  if (!q || !k || !v || !out || !table || !k_cache || !v_cache) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(table) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || (q_norm_w && !aligned16(q_norm_w)) ||
+      (k_norm_w && !aligned16(k_norm_w)))
+    return ATTN_ERR_ALIGN;
+  if ((int64_t)L - 1 >= (int64_t)max_pos_of(rp)) return ATTN_ERR_POSITION;
+  if (window == 0 && L > capacity) return ATTN_ERR_CAPACITY;
+  if ((int64_t)B * Hkv > 65535) return ATTN_ERR_SHAPE;
+  const StepLayout lay = step_layout(B, H, Hkv, L, D, window, rp);
+  if (!workspace || workspace_bytes < lay.total) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int R = rope_dim_of(rp, D);
+  const int32_t* skip = nullptr;
+  {
+    Finite fin;
+    fin.add(q, B, H, L, D);
+    fin.add(k, B, Hkv, L, D);
+    fin.add(v, B, Hkv, L, D);
+    fin.add(q_norm_w, 1, 1, 1, D);
+    fin.add(k_norm_w, 1, 1, 1, D);
+    if (const int rc = fin.gate(status, s, &skip)) return rc;
+  }
+  // RoPE jobs at positions 0 .. L-1 (no start array)
+  auto rope_job = [&](float* x, float* y, int NH, const float* nw) {
+    gqa::RopeJob j{};
+    j.x = x; j.y = y; j.B = B; j.NH = NH; j.L = L; j.D = D; j.R = R;
+    j.start = nullptr; j.max_positions = max_pos_of(rp);
+    j.table = reinterpret_cast<const float2*>(table);
+    j.norm_w = nw; j.norm_eps = norm_eps; j.status = status; j.skip = skip;
+    return j;
+  };
+  gqa::AttnShape a{};
+  a.out = out; a.v = v;
+  a.B = B; a.H = H; a.Hkv = Hkv; a.L = L; a.D = D;
+  a.window = window; a.softcap = softcap > 0.f ? softcap : 0.f;
+  a.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  a.status = status;
+  a.skip = skip;
+  if (!lay.tc) {
+    // head dims off the tensor cores: rotate a copy of k (into the cache as well) and
+    // q, then the CUDA-core prefill
+    float* kr = reinterpret_cast<float*>(ws + lay.kr);
+    float* qrot = reinterpret_cast<float*>(ws + lay.qrot);
+    if (cudaError_t e = cudaMemcpyAsync(kr, k, (size_t)B * Hkv * L * D * sizeof(float),
+                                        cudaMemcpyDeviceToDevice, s);
+        e != cudaSuccess)
+      return cuda_status(e);
+    gqa::RopeJob kj = rope_job(kr, nullptr, Hkv, k_norm_w);
+    kj.v = v; kj.k_cache = k_cache; kj.v_cache = v_cache; kj.capacity = capacity;
+    kj.window = window;
+    if (cudaError_t e = gqa::launch_rope_rows(kj, s); e != cudaSuccess) return cuda_status(e);
+    const gqa::RopeJob qj = rope_job(const_cast<float*>(q), qrot, H, q_norm_w);
+    if (cudaError_t e = gqa::launch_rope_rows(qj, s); e != cudaSuccess) return cuda_status(e);
+    a.q = qrot; a.k = kr;
+    return cuda_status(gqa::launch_prefill_simt(a, s));
+  }
+  // one memory pass: rotated k into the cache (and kr for a ring shorter than the
+  // chunk), v into the cache, V^T into the workspace; then the tensor-core kernel
+  // reads the rotated keys from the cache
+  float* vt = reinterpret_cast<float*>(ws + lay.vt);
+  float* kr = window > 0 && L > window ? reinterpret_cast<float*>(ws + lay.kr) : nullptr;
+  gqa::AppendVtJob aj{};
+  aj.k = k; aj.v = v; aj.k_cache = k_cache; aj.v_cache = v_cache; aj.kr = kr; aj.vt = vt;
+  aj.B = B; aj.Hkv = Hkv; aj.L = L; aj.D = D; aj.R = R;
+  aj.table = reinterpret_cast<const float2*>(table);
+  aj.norm_w = k_norm_w; aj.norm_eps = norm_eps; aj.start = nullptr;
+  aj.max_positions = max_pos_of(rp); aj.capacity = capacity; aj.window = window;
+  aj.vt_pitch = gqa::prefill_vt_pitch(L); aj.status = status; aj.skip = skip;
+  if (cudaError_t e = gqa::launch_append_vt(aj, s); e != cudaSuccess) return cuda_status(e);
+  a.k = kr ? kr : k_cache;
+  a.k_head_rows = kr ? 0 : capacity;
+  a.vt = vt; a.vt_pitch = aj.vt_pitch;
+  if (rope_fused(D, R)) {
+    a.q = q;
+    a.rope.table = reinterpret_cast<const float2*>(table);
+    a.rope.start = nullptr;
+    a.rope.norm_w = q_norm_w;
+    a.rope.norm_eps = norm_eps;
+    a.rope.R = R;
+    a.rope.max_positions = max_pos_of(rp);
+  } else {
+    float* qrot = reinterpret_cast<float*>(ws + lay.qrot);
+    const gqa::RopeJob qj = rope_job(const_cast<float*>(q), qrot, H, q_norm_w);
+    if (cudaError_t e = gqa::launch_rope_rows(qj, s); e != cudaSuccess) return cuda_status(e);
+    a.q = qrot;
+  }
+  return cuda_status(gqa::launch_prefill_tc_vt(a, s));
+}
+
 size_t gqa_attn_prefill_ragged_workspace_size(int B, int H, int Hkv, int L, int D,
                                               const attn_rope_params* rp) {
   const size_t base = rp ? gqa_attn_prefill_rope_workspace_size(B, H, Hkv, L, D, rp)

@@ -19,7 +19,7 @@ struct RopeJob {
   float* x;                 // [B, NH, L, D], rotated in place (or read only, see y)
   float* y;                 // nullptr: in place; else rotated rows go here ([B, NH, L, D])
   int B, NH, L, D, R;
-  const int32_t* start;     // [B]
+  const int32_t* start;     // [B], or nullptr: every row starts at 0
   int max_positions;
   const float2* table;      // [max_positions][R/2] (cos, sin), or nullptr: no rotation
   const float* norm_w;      // [D] or nullptr
@@ -52,7 +52,7 @@ cudaError_t launch_rope_rows(const RopeJob& job, cudaStream_t stream);
 // Fused q RMSNorm + RoPE inside the tensor-core prefill (q is then the raw query).
 struct QRope {
   const float2* table;      // [max_positions][R/2] (cos, sin); nullptr: q already rotated
-  const int32_t* start;     // [B]
+  const int32_t* start;     // [B], or nullptr: every row starts at 0
   const float* norm_w;      // [D] or nullptr
   float norm_eps;
   int R, max_positions;
@@ -80,6 +80,9 @@ struct AttnShape {
   // nullptr: every row has length L. Not combined with kv_off.
   const int32_t* lengths = nullptr;
   const int32_t* skip = nullptr;   // as RopeJob::skip
+  // Rows between consecutive heads of k (0: Lk, i.e. contiguous heads); lets the
+  // kernel read rotated keys from a cache whose heads hold `capacity` rows.
+  int k_head_rows = 0;
 };
 
 cudaError_t launch_prefill_simt(const AttnShape& a, cudaStream_t stream);
@@ -190,6 +193,27 @@ struct GemmJob {
 };
 bool gemm_tc_supports(const GemmJob& j);
 cudaError_t launch_gemm_tc(const GemmJob& j, cudaStream_t stream);
+
+// The memory pass of a prefill step (step.cu): k RMSNorm + RoPE into the cache
+// (and into kr when given), v into the cache, V^T into vt; k and v are read only.
+struct AppendVtJob {
+  const float* k;           // [B, Hkv, L, D]
+  const float* v;
+  float* k_cache;           // [B, Hkv, capacity, D]: slot = position, or position mod window
+  float* v_cache;
+  float* kr;                // [B, Hkv, L, D] rotated keys, or nullptr
+  float* vt;                // [B * Hkv, D, vt_pitch]
+  int B, Hkv, L, D, R;
+  const float2* table;      // [max_positions][R/2] (cos, sin); nullptr: no rotation
+  const float* norm_w;      // [D] or nullptr
+  float norm_eps;
+  const int32_t* start;     // [B] or nullptr (0)
+  int max_positions, capacity, window, vt_pitch;
+  int32_t* status;
+  const int32_t* skip = nullptr;
+};
+bool append_vt_supports(int D);
+cudaError_t launch_append_vt(const AppendVtJob& j, cudaStream_t stream);
 
 // The opt-in non-finite input check (finite.cu). A region is B * NH blocks of R
 // rows, C values of each row checked, rows ld floats apart (blocks R * ld apart);

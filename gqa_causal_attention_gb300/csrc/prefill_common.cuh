@@ -27,7 +27,7 @@ struct TcArgs {
   int units;                                   // persistent kernel: B * H * QT query tiles
   // Fused q RMSNorm + RoPE (persistent kernel): rope_table == nullptr means q is rotated.
   const float2* rope_table;                    // [max_positions][R/2] (cos, sin)
-  const int32_t* rope_start;                   // [B]
+  const int32_t* rope_start;                   // [B], or nullptr: every row starts at 0
   const float* qnorm_w;                        // [D] or nullptr
   float qnorm_eps;
   int rope_R, rope_max_positions;
@@ -53,6 +53,11 @@ __device__ __forceinline__ int row_len(const TcArgs& a, int b) {
   if (!a.lengths) return a.L;
   const int v = a.lengths[b];
   return v < 0 ? 0 : (v > a.L ? a.L : v);
+}
+
+// Position of query row 0 of batch row b (fused RoPE); no start array: 0.
+__device__ __forceinline__ int start_of(const TcArgs& a, int b) {
+  return a.rope_start ? a.rope_start[b] : 0;
 }
 
 // Timeout-only wait used while winding down after an abort.
@@ -150,13 +155,15 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // [NH, L, D] fp32 rows as a 3-D tensor map; boxes of 32 columns x box_rows rows.
-inline bool make_map(CUtensorMap* m, const float* base, int D, int L, int NH, int box_rows) {
+// Heads are head_rows rows apart (0: L, contiguous).
+inline bool make_map(CUtensorMap* m, const float* base, int D, int L, int NH, int box_rows,
+                     long head_rows = 0) {
   auto enc = encode_fn();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(L),
                               static_cast<cuuint64_t>(NH)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4,
-                                 static_cast<cuuint64_t>(L) * D * 4};
+                                 static_cast<cuuint64_t>(head_rows > 0 ? head_rows : L) * D * 4};
   const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,

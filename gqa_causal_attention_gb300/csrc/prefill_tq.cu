@@ -241,7 +241,7 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
         tc::tma_prefetch_l2_3d(tq, 32 * c, un.q0, un.b * a.H + un.h);
       if (a.rope_table) {
         const long half = a.rope_R / 2;
-        const long p0 = min(max(static_cast<long>(a.rope_start[un.b]) + un.q0, 0L),
+        const long p0 = min(max(static_cast<long>(start_of(a, un.b)) + un.q0, 0L),
                             static_cast<long>(a.rope_max_positions - 1));
         const long p1 = min(p0 + kBM, static_cast<long>(a.rope_max_positions));
         tc::bulk_prefetch_l2(a.rope_table + p0 * half, static_cast<uint32_t>((p1 - p0) * half * 8));
@@ -607,7 +607,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
   const int r0 = next_live<C>(a, 0);
   if (ROPE && unit_of(blockIdx.x, r0, gridDim.x) < a.units) {
     const PUnit u0 = get_unit<C>(a, unit_of(blockIdx.x, r0, gridDim.x));
-    ok = tq_rotate_q<C>(a, lane_base, bars, stage_tab, u0, a.rope_start[u0.b], quarter, lane, 0);
+    ok = tq_rotate_q<C>(a, lane_base, bars, stage_tab, u0, start_of(a, u0.b), quarter, lane, 0);
   }
   // The warp's 32 rows x 16 columns from column c0 to the output, through two
   // alternating 2 KB staging tiles (64-byte swizzle: 16-byte granule g of row r
@@ -637,7 +637,7 @@ __device__ void tq_softmax(const TcArgs& a, uint32_t tmem, PBars* bars, int quar
     const int xn = unit_of(blockIdx.x, rn, gridDim.x);
     // start[b] of the next unit, read now so that its latency is not on the
     // path of that unit's rotation.
-    const int next_start = ROPE && xn < a.units ? a.rope_start[get_unit<C>(a, xn).b] : 0;
+    const int next_start = ROPE && xn < a.units ? start_of(a, get_unit<C>(a, xn).b) : 0;
     const int qpos = u.qk0 + row;               // the query's own key index
     float m_ref = -INFINITY, l = 0.f;         // running max (log2 units) and sum
 
@@ -932,7 +932,7 @@ cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   const int Lk = s.Lk > 0 ? s.Lk : s.L;
   CUtensorMap tq, tk, tv, to;
   if (!make_map(&tq, s.q, s.D, s.L, s.B * s.H, kBM) ||
-      !make_map(&tk, s.k, s.D, Lk, s.B * s.Hkv, C::BK) ||
+      !make_map(&tk, s.k, s.D, Lk, s.B * s.Hkv, C::BK, s.k_head_rows) ||
       !make_map_vt(&tv, s.vt, s.D, Lk, s.vt_pitch, s.B * s.Hkv, C::DP) ||
       !make_map_out16(&to, s.out, s.D, s.L, s.B * s.H))
     return cudaErrorInvalidValue;

@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
       if (!live[r]) continue;
       const int b = (int)(row / ((long)j.NH * j.L));
       const int l = (int)(row % j.L);
-      const int s0 = j.start[b];
+      const int s0 = j.start ? j.start[b] : 0;
       // Device-side re-check of the positions the host could not see.
       if (s0 < 0 || (long)s0 + j.L - 1 >= (long)j.max_positions) {
         if (lane == 0 && l == 0) report(j.status, ATTN_DEV_POSITION);

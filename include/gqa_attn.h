@@ -207,6 +207,34 @@ int gqa_attn_prefill_rope_vt(const float* q, const float* k, const float* vt, fl
                              int32_t* status, void* stream);
 
 /*
+ * One whole prefill step from a fresh cache ("mojolearn.transformer",
+ * TransformerBlock.forward with an empty TransformerState): for positions
+ * 0 .. L-1 the keys and values enter the cache and attention runs over them,
+ *   k_cache, v_cache  <- as kv_cache_append with start 0 would write them;
+ *   out               <- as gqa_attn_prefill_rope with start 0 computes it.
+ * Unlike kv_cache_append, k and v are only read (k is not rotated in place).
+ *   q [B, H, L, D] raw; k, v [B, Hkv, L, D] raw; out [B, H, L, D];
+ *   caches [B, Hkv, capacity, D]: capacity >= L without a window, a ring of
+ *   capacity == window slots with one (of a chunk longer than the ring only
+ *   its last window positions are stored).
+ * For D % 4 == 0 and D >= 32 one memory pass reads k and v once and writes the
+ * rotated keys into the cache, v into the cache and v transposed into the
+ * workspace; the tensor-core kernel then reads the keys from the cache (from a
+ * rotated copy in the workspace when a ring is shorter than L), with q's RMSNorm
+ * and RoPE fused as in gqa_attn_prefill_rope. Other even D run on the CUDA
+ * cores. B * Hkv <= 65535.
+ *   workspace  gqa_attn_prefill_step_workspace_size bytes
+ */
+size_t gqa_attn_prefill_step_workspace_size(int B, int H, int Hkv, int L, int D, int window,
+                                            const attn_rope_params* rp);
+int gqa_attn_prefill_step(const float* q, const float* k, const float* v, float* out, int B,
+                          int H, int Hkv, int L, int D, const attn_rope_params* rp,
+                          const float* table, const float* q_norm_w, const float* k_norm_w,
+                          float norm_eps, float* k_cache, float* v_cache, int capacity,
+                          int window, float softcap, float scale, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * One whole prefill step with q, k, v and the output in host memory
  * ("mojolearn.transformer", TransformerBlock.forward: the caller hands in the
  * step's tensors and reads the result back). q, k, v are copied to the
