@@ -87,7 +87,7 @@ def peaks():
 # The decode capture ran on 16 of the 64 rows; its traffic scales with the
 # algorithmic bytes processed (ratio below).
 NCU_PREFILL_TRAFFIC = {}
-NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903360e6 + 4.927232e6) / 585572352.0
+NCU_DECODE_TRAFFIC_PER_ALG_BYTE = None
 
 
 def measure_tf32_peak(dev):
@@ -434,12 +434,17 @@ def bench_decode(w, args, dist, dev):
     out = torch.empty_like(q)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
+    sws = torch.empty(g.gqa_attn_decode_step_workspace_size(w.B, w.H, w.Hkv, w.D, maxlen - 1,
+                                                            w.window) // 4 + 4, device=dev)
+    qrot = q.clone()
+    g.attn_rope_apply(qrot, pos, maxlen - 1, rp, table, None, w.norm_eps, status)
+
     def step():
-        # q and k are rotated in place at the same positions on every repeat: the work of
-        # a step does not depend on the values
-        g.attn_rope_apply(q, pos, maxlen - 1, rp, table, None, w.norm_eps, status)
-        g.kv_cache_append(k, v, pos, maxlen - 1, rp, table, None, w.norm_eps, kc, vc, 0, status)
-        g.gqa_attn_decode(q, kc, vc, cl, maxlen, out, 0, w.softcap, 0.0, ws, status)
+        # one call: q and k rotated at position n_b, k and v appended, then the split-KV
+        # decode whose last block per row and head group merges the splits
+        g.gqa_attn_decode_step(q, k, v, out, pos, maxlen - 1, kc, vc, rp, table, None, None,
+                               w.norm_eps, w.window, w.softcap, 0.0, workspace=sws,
+                               status=status)
 
     steps = args.decode_steps
     ms_eager = timed(step, steps, args.warmup, dist)
@@ -450,17 +455,18 @@ def bench_decode(w, args, dist, dev):
             gr = graph_of(step)
             ms = timed(gr.replay, steps, args.warmup, dist)
     kern_ms = kernel_median(
-        lambda: g.gqa_attn_decode(q, kc, vc, cl, maxlen, out, 0, w.softcap, 0.0, ws, status),
+        lambda: g.gqa_attn_decode(qrot, kc, vc, cl, maxlen, out, 0, w.softcap, 0.0, ws, status),
         KERNEL_ITERS, KERNEL_WARM)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     nbytes = 2.0 * w.Hkv * w.D * 4 * float((n + 1).sum())
     ksplit = 2 if g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, maxlen, w.window) > 16 \
         else 1
+    per_step = 2 + ksplit
     return {"ms": ms / steps, "ms_eager": ms_eager / steps, "kernel_ms": kern_ms, "bytes": nbytes,
             "clocks": clk.summary(),
-            "launches_per_step": 2 + ksplit,
-            "launches": (2 + ksplit) * 2 * steps + ksplit * KERNEL_ITERS}
+            "launches_per_step": per_step,
+            "launches": per_step * 2 * steps + ksplit * (KERNEL_ITERS + KERNEL_WARM)}
 
 
 def bench_long_decode(w, args, dist, dev):
@@ -488,16 +494,15 @@ def bench_long_decode(w, args, dist, dev):
     out = torch.empty(w.B, w.H, 1, w.D, device=dev)
     pos = torch.arange(w.L, w.L + n, dtype=torch.int32, device=dev).repeat(w.B, 1).t().contiguous()
     cl = (pos + 1).contiguous()
-    ws = torch.empty(max(4, g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, w.L + n, 0)
-                         // 4), device=dev)
+    ws = torch.empty(max(4, g.gqa_attn_decode_step_workspace_size(w.B, w.H, w.Hkv, w.D,
+                                                                   w.L + n - 1, 0) // 4),
+                     device=dev)
 
     def steps():
         for t in range(n):
             p = w.L + t
-            g.attn_rope_apply(qs[t], pos[t], p, rp, table, None, w.norm_eps, status)
-            g.kv_cache_append(ks[t], vs[t], pos[t], p, rp, table, None, w.norm_eps, kc, vc, 0,
-                              status)
-            g.gqa_attn_decode(qs[t], kc, vc, cl[t], p + 1, out, 0, 0.0, 0.0, ws, status)
+            g.gqa_attn_decode_step(qs[t], ks[t], vs[t], out, pos[t], p, kc, vc, rp, table, None,
+                                   None, w.norm_eps, 0, 0.0, 0.0, workspace=ws, status=status)
 
     gr = graph_of(steps, warm=1)
     with ClockSampler(torch.cuda.current_device()) as clk:
@@ -506,7 +511,7 @@ def bench_long_decode(w, args, dist, dev):
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     nbytes = 2.0 * w.Hkv * w.D * 4 * w.B * sum(w.L + t + 1 for t in range(n))
     launches = sum(3 if g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, w.L + t + 1, 0)
-                   <= 16 else 4 for t in range(n))
+                   > 16 else 2 for t in range(n))
     return {"steps": n, "ms_per_step": ms / n, "us_per_token_step": 1e3 * ms / n,
             "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "launches": launches,
             "clocks": clk.summary()}
@@ -861,9 +866,12 @@ def main():
             "ms_per_step": dec["ms"], "ms_per_step_eager": dec["ms_eager"],
             "bytes_per_step": dec["bytes"],
             "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+            "step": "gqa_attn_decode_step: q, k RMSNorm/RoPE at n_b + append (one pass), then "
+                    "the split-KV decode and its combine; CUDA graph replays",
             "roofline": {"bound": "hbm", "achieved": kgbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": kgbs / pk["hbm_gbs"],
-                         "traffic": NCU_DECODE_TRAFFIC_PER_ALG_BYTE * dec["bytes"],
+                         "traffic": (NCU_DECODE_TRAFFIC_PER_ALG_BYTE * dec["bytes"]
+                                     if NCU_DECODE_TRAFFIC_PER_ALG_BYTE else None),
                          "kernel": "gqa_attn_decode", "kernel_ms": dec["kernel_ms"]},
             "gpu_launches": dec["launches"],
             "clocks": dec["clocks"]}
@@ -885,8 +893,8 @@ def main():
                                                    "prefill": wl.L, "steps": wl.decode_steps},
             "value": world * lng["gbs"], "unit": "GB/s",
             "us_per_step": lng["us_per_token_step"], "bytes_total": lng["bytes"],
-            "step": "attn_rope_apply (q) + kv_cache_append + gqa_attn_decode, 1024 steps in one "
-                    "CUDA graph",
+            "step": "gqa_attn_decode_step (one pass: q, k RoPE + append; split-KV decode; "
+                    "combine), 1024 steps in one CUDA graph",
             "note": "the cache (134 MB) is about L2-sized; part of each step's reads hit L2",
             "gpu_launches": lng["launches"], "clocks": lng["clocks"]}
         line["gpu_launches"] += lng["launches"]

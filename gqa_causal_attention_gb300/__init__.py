@@ -32,6 +32,7 @@ __all__ = [
     "gqa_block_forward", "gqa_block_forward_workspace_size", "BLOCK_WEIGHT_NAMES",
     "attn_linear", "attn_set_check_finite", "DEV_NONFINITE",
     "gqa_attn_prefill_step", "gqa_attn_prefill_step_workspace_size",
+    "gqa_attn_decode_step", "gqa_attn_decode_step_workspace_size",
     "gqa_attn_prefill_from_host", "gqa_attn_prefill_from_host_workspace_size",
     "attn_selftest_wait_timeout",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
@@ -142,6 +143,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                         vp, i32, f, f, vp, sz, vp, vp]),
             "attn_linear": (i32, [vp, vp, vp, vp, ctypes.c_long, i32, i32, vp, vp]),
             "gqa_attn_prefill_step_workspace_size": (sz, [i32, i32, i32, i32, i32, i32, rp]),
+            "gqa_attn_decode_step_workspace_size": (sz, [i32, i32, i32, i32, ctypes.c_int32,
+                                                         i32]),
+            "gqa_attn_decode_step": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, vp,
+                                           ctypes.c_int32, rp, vp, vp, vp, f, vp, vp, i32, i32,
+                                           f, f, vp, sz, vp, vp]),
             "gqa_attn_prefill_step": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, rp, vp, vp,
                                             vp, f, vp, vp, i32, i32, f, f, vp, sz, vp, vp]),
             "attn_set_check_finite": (i32, [i32]),
@@ -642,6 +648,44 @@ def gqa_attn_prefill_step(q, k, v, out, k_cache, v_cache, params: RopeParams, ta
                                       int(window), float(softcap), float(scale),
                                       _ptr(workspace), wbytes, _ptr(status), _stream(stream))
     _check("gqa_attn_prefill_step", rc)
+
+
+def gqa_attn_decode_step_workspace_size(B: int, H: int, Hkv: int, D: int, max_pos: int,
+                                        window: int = 0) -> int:
+    return int(load().gqa_attn_decode_step_workspace_size(B, H, Hkv, D, int(max_pos),
+                                                          int(window)))
+
+
+def gqa_attn_decode_step(q, k, v, out, pos, max_pos: int, k_cache, v_cache, params: RopeParams,
+                         table, q_norm_w=None, k_norm_w=None, norm_eps: float = 1e-6,
+                         window: int = 0, softcap: float = 0.0, scale: float = 0.0,
+                         workspace=None, status=None, stream=None) -> None:
+    """One decode step: the new token of row b (raw q [B,H,1,D], k, v [B,Hkv,1,D], read only)
+    at position pos[b] enters the caches and out = its attention over the cache."""
+    for n, t in (("q", q), ("k", k), ("v", v), ("out", out), ("k_cache", k_cache),
+                 ("v_cache", v_cache)):
+        _f32(n, t, 4)
+    _f32("table", table); _f32("q_norm_w", q_norm_w); _f32("k_norm_w", k_norm_w)
+    _i32("pos", pos); _i32("status", status)
+    B, H, one, D = q.shape
+    Hkv, cap = k_cache.shape[1], k_cache.shape[2]
+    if one != 1 or tuple(k.shape) != (B, Hkv, 1, D) or v.shape != k.shape or \
+            out.shape != q.shape or tuple(k_cache.shape) != (B, Hkv, cap, D) or \
+            v_cache.shape != k_cache.shape or pos.numel() != B:
+        raise ValueError("gqa_attn_decode_step: inconsistent shapes")
+    if workspace is None:
+        n = gqa_attn_decode_step_workspace_size(B, H, Hkv, D, max_pos, window)
+        workspace = torch.empty(max(4, n // 4), dtype=torch.float32, device=q.device)
+    elif not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    wbytes = workspace.numel() * workspace.element_size()
+    rc = load().gqa_attn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, H, Hkv, D,
+                                     _ptr(pos), int(max_pos), _rp(params), _ptr(table),
+                                     _ptr(q_norm_w), _ptr(k_norm_w), float(norm_eps),
+                                     _ptr(k_cache), _ptr(v_cache), cap, int(window),
+                                     float(softcap), float(scale), _ptr(workspace), wbytes,
+                                     _ptr(status), _stream(stream))
+    _check("gqa_attn_decode_step", rc)
 
 
 def attn_linear(x, w, y, residual=None, status=None, stream=None) -> None:

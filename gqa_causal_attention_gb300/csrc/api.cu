@@ -1012,4 +1012,93 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
   return cuda_status(gqa::launch_decode(j, s));
 }
 
+namespace {
+// Workspace of gqa_attn_decode_step: rotated q [B, H, D] | cache lengths [B] | the
+// split partials.
+struct DecodeStepLayout {
+  size_t qrot, cl, part, total;
+};
+DecodeStepLayout decode_step_layout(int B, int H, int Hkv, int D, int max_len, int window) {
+  DecodeStepLayout y{};
+  size_t p = 0;
+  y.qrot = p;
+  p += round256((size_t)B * H * D * sizeof(float));
+  y.cl = p;
+  p += round256((size_t)B * sizeof(int32_t));
+  y.part = p;
+  p += round256(gqa_attn_decode_workspace_size(B, H, Hkv, D, max_len, window));
+  y.total = p;
+  return y;
+}
+}  // namespace
+
+size_t gqa_attn_decode_step_workspace_size(int B, int H, int Hkv, int D, int32_t max_pos,
+                                           int window) {
+  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv || D < 2 || D % 2 || D > gqa::kMaxHeadDim ||
+      max_pos < 0 || max_pos == 0x7fffffff || window < 0)
+    return 0;
+  return decode_step_layout(B, H, Hkv, D, max_pos + 1, window).total;
+}
+
+int gqa_attn_decode_step(const float* q, const float* k, const float* v, float* out, int B,
+                         int H, int Hkv, int D, const int32_t* pos, int32_t max_pos,
+                         const attn_rope_params* rp, const float* table, const float* q_norm_w,
+                         const float* k_norm_w, float norm_eps, float* k_cache, float* v_cache,
+                         int capacity, int window, float softcap, float scale, void* workspace,
+                         size_t workspace_bytes, int32_t* status, void* stream) {
+  if (!dims_ok(B, H, 1, D) || Hkv < 1 || H % Hkv != 0 || window < 0 || capacity < 1)
+    return ATTN_ERR_SHAPE;
+  if (window > 0 && capacity != window) return ATTN_ERR_SHAPE;
+  if (!isfinite(softcap) || !isfinite(scale)) return ATTN_ERR_PARAM;
+  if (!rp) return ATTN_ERR_NULL;
+  if (!rope_params_ok(rp, D) || !(norm_eps >= 0.f)) return ATTN_ERR_PARAM;
+  if (B == 0) return ATTN_OK;
+  if (!q || !k || !v || !out || !pos || !table || !k_cache || !v_cache) return ATTN_ERR_NULL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(table) ||
+      !aligned16(k_cache) || !aligned16(v_cache) || (q_norm_w && !aligned16(q_norm_w)) ||
+      (k_norm_w && !aligned16(k_norm_w)))
+    return ATTN_ERR_ALIGN;
+  if (max_pos < 0 || (int64_t)max_pos >= (int64_t)max_pos_of(rp)) return ATTN_ERR_POSITION;
+  if (window == 0 && max_pos >= capacity) return ATTN_ERR_CAPACITY;
+  const DecodeStepLayout lay = decode_step_layout(B, H, Hkv, D, max_pos + 1, window);
+  if (!workspace || workspace_bytes < lay.total) return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int32_t* skip = nullptr;
+  {
+    Finite fin;
+    fin.add(q, B, H, 1, D);
+    fin.add(k, B, Hkv, 1, D);
+    fin.add(v, B, Hkv, 1, D);
+    fin.add(k_cache, B, Hkv, capacity, D, gqa::kFiniteCache, pos);
+    fin.add(v_cache, B, Hkv, capacity, D, gqa::kFiniteCache, pos);
+    fin.add(q_norm_w, 1, 1, 1, D);
+    fin.add(k_norm_w, 1, 1, 1, D);
+    if (const int rc = fin.gate(status, s, &skip)) return rc;
+  }
+  gqa::DecodePrepJob pj{};
+  pj.q = q; pj.k = k; pj.v = v;
+  pj.qrot = reinterpret_cast<float*>(ws + lay.qrot);
+  pj.k_cache = k_cache; pj.v_cache = v_cache;
+  pj.cache_len = reinterpret_cast<int32_t*>(ws + lay.cl);
+  pj.B = B; pj.H = H; pj.Hkv = Hkv; pj.D = D; pj.R = rope_dim_of(rp, D);
+  pj.pos = pos; pj.max_positions = max_pos_of(rp); pj.capacity = capacity; pj.window = window;
+  pj.table = reinterpret_cast<const float2*>(table);
+  pj.q_norm_w = q_norm_w; pj.k_norm_w = k_norm_w; pj.norm_eps = norm_eps;
+  pj.status = status; pj.skip = skip;
+  if (cudaError_t e = gqa::launch_decode_prep(pj, s); e != cudaSuccess) return cuda_status(e);
+  gqa::DecodeJob j{};
+  j.q = pj.qrot; j.k_cache = k_cache; j.v_cache = v_cache; j.cache_len = pj.cache_len;
+  j.max_cache_len = max_pos + 1; j.out = out;
+  j.B = B; j.H = H; j.Hkv = Hkv; j.D = D; j.capacity = capacity; j.window = window;
+  j.softcap = softcap > 0.f ? softcap : 0.f;
+  j.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)D);
+  j.status = status;
+  j.skip = skip;
+  gqa::decode_split_plan(B, Hkv, max_pos + 1, window, &j.nsplit, &j.chunk);
+  j.partial = reinterpret_cast<float*>(ws + lay.part);
+  return cuda_status(gqa::launch_decode(j, s));
+}
+
 }  // extern "C"

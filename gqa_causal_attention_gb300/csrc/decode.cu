@@ -781,6 +781,69 @@ static cudaError_t launch_gt(const DecodeJob& j, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// One decode step's prep pass: a warp per q or k row (RMSNorm, RoPE at the row's
+// position), v rows copied beside their k rows, cache lengths set.
+__global__ void __launch_bounds__(256) decode_prep_kernel(DecodePrepJob j) {
+  if (gated_off(j.skip)) return;
+  const int lane = threadIdx.x & 31;
+  const long nwarps = gridDim.x * 8L, gw = blockIdx.x * 8L + threadIdx.x / 32;
+  const long qrows = (long)j.B * j.H, rows = qrows + (long)j.B * j.Hkv;
+  const int D = j.D, R = j.R, half = R / 2;
+  for (long row = gw; row < rows; row += nwarps) {
+    const bool isq = row < qrows;
+    const long r = isq ? row : row - qrows;
+    const int nh = isq ? j.H : j.Hkv;
+    const int b = static_cast<int>(r / nh);
+    const int p = j.pos[b];
+    const bool in_table = p >= 0 && p < j.max_positions;
+    const bool has_slot = j.window > 0 || p < j.capacity;
+    const bool lead = isq && r % nh == 0 && lane == 0;     // one report per batch row
+    if (lead) {
+      if (!in_table) report(j.status, ATTN_DEV_POSITION);
+      else if (!has_slot) report(j.status, ATTN_DEV_CAPACITY);
+      j.cache_len[b] = in_table && has_slot ? p + 1 : 0;
+    }
+    if (!in_table || !has_slot) continue;
+    const float* x = (isq ? j.q : j.k) + r * D;
+    const float* nw = isq ? j.q_norm_w : j.k_norm_w;
+    const long slot = j.window > 0 ? p % j.window : p;
+    float* y = isq ? j.qrot + r * D : j.k_cache + (r * j.capacity + slot) * D;
+    float inv = 1.0f;
+    if (nw) {
+      float ss = 0.f;
+      for (int i = lane; i < D; i += 32) ss = fmaf(x[i], x[i], ss);
+      ss = warp_sum(ss);
+      inv = 1.0f / sqrtf(ss / static_cast<float>(D) + j.norm_eps);
+    }
+    const float2* tab = j.table + static_cast<long>(p) * half;
+    for (int i = lane; i < half; i += 32) {
+      float a = x[i], c = x[i + half];
+      if (nw) {
+        a = a * inv * nw[i];
+        c = c * inv * nw[i + half];
+      }
+      const float2 cs = tab[i];
+      y[i] = fmaf(a, cs.x, -c * cs.y);
+      y[i + half] = fmaf(a, cs.y, c * cs.x);
+    }
+    for (int i = R + lane; i < D; i += 32) y[i] = nw ? x[i] * inv * nw[i] : x[i];
+    if (!isq) {
+      const float* vr = j.v + r * D;
+      float* vd = j.v_cache + (r * j.capacity + slot) * D;
+      for (int i = lane; i < D; i += 32) vd[i] = vr[i];
+    }
+  }
+}
+
+cudaError_t launch_decode_prep(const DecodePrepJob& j, cudaStream_t stream) {
+  const long rows = (long)j.B * (j.H + j.Hkv);
+  long blocks = (rows + 7) / 8;
+  if (blocks > 152L * 8) blocks = 152L * 8;
+  if (blocks < 1) blocks = 1;
+  decode_prep_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(j);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream) {
   const int G = j.H / j.Hkv;
   if (G % 8 == 0 && j.D % 4 == 0 && j.D <= 128) {

@@ -136,6 +136,29 @@ struct DecodeJob {
   const int32_t* skip = nullptr;
 };
 
+// One decode step's prep pass (decode.cu): q RMSNorm + RoPE into qrot, k RMSNorm +
+// RoPE and v into their cache slots, cache_len[b] = pos[b] + 1 (0 for a row whose
+// position fails the device check).
+struct DecodePrepJob {
+  const float* q;           // [B, H, D] raw
+  const float* k;           // [B, Hkv, D] raw
+  const float* v;
+  float* qrot;              // [B, H, D]
+  float* k_cache;           // [B, Hkv, capacity, D]
+  float* v_cache;
+  int32_t* cache_len;       // [B]
+  int B, H, Hkv, D, R;
+  const int32_t* pos;       // [B] tokens already cached = the new token's position
+  int max_positions, capacity, window;
+  const float2* table;
+  const float* q_norm_w;
+  const float* k_norm_w;
+  float norm_eps;
+  int32_t* status;
+  const int32_t* skip = nullptr;
+};
+cudaError_t launch_decode_prep(const DecodePrepJob& j, cudaStream_t stream);
+
 // The identical numeric mode: one warp per query row, fixed arithmetic order
 // (identical.cu). Keys at positions >= s0 come from k / v (the chunk), below
 // s0 from the cache. Prefill: s0 = start[b] (nullptr: 0), query row l at

@@ -461,6 +461,32 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
                     void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
+ * One whole decode step ("mojolearn.transformer", TransformerBlock.step: the new
+ * token of each row at position cached_tokens): for row b the token sits at
+ * p = pos[b] (the number of positions already cached), and
+ *   k_cache, v_cache slot(p) <- RoPE(RMSNorm(k)), v    (as kv_cache_append at p)
+ *   out[b,h,0,:] <- attention of RoPE(RMSNorm(q)) over positions max(0, p-W+1) .. p
+ *                   (as gqa_attn_decode with cache_len[b] = p + 1).
+ * q, k and v are only read. q [B, H, 1, D], k, v [B, Hkv, 1, D] raw; out [B, H, 1, D];
+ * caches as gqa_attn_decode (capacity > every p without a window).
+ *   pos      device int32 [B]; max_pos bounds every pos[b] (host), < max_positions
+ *   workspace gqa_attn_decode_step_workspace_size bytes
+ * One pass rotates q and k and stores k and v at their slots; then the
+ * split-KV decode of gqa_attn_decode (and its combine kernel when a row has
+ * several splits). A pos[b] outside
+ * the table (or the capacity, without a window) sets ATTN_DEV_POSITION
+ * (ATTN_DEV_CAPACITY) and ATTN_DEV_LENGTH, and the row is skipped.
+ */
+size_t gqa_attn_decode_step_workspace_size(int B, int H, int Hkv, int D, int32_t max_pos,
+                                           int window);
+int gqa_attn_decode_step(const float* q, const float* k, const float* v, float* out, int B,
+                         int H, int Hkv, int D, const int32_t* pos, int32_t max_pos,
+                         const attn_rope_params* rp, const float* table, const float* q_norm_w,
+                         const float* k_norm_w, float norm_eps, float* k_cache, float* v_cache,
+                         int capacity, int window, float softcap, float scale, void* workspace,
+                         size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * gqa_attn_decode without a caller workspace, for callers that cannot
  * allocate device memory: code running where cudaMalloc is not allowed (a
  * plug-in inside a host framework that owns all device memory, a serving path
