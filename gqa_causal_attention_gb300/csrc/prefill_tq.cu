@@ -491,7 +491,7 @@ __device__ void tq_mma_pv(const TcArgs& a, uint32_t tmem, uint8_t* skv, PBars* b
 // Rotates the next unit's Q tile where the MMA reads it, in tensor memory:
 // thread = query row, as in the softmax. RMSNorm (if q_norm_w) over the row
 // first, then RoPE at the row's absolute position p = start[b] + q0 + row,
-// pairs (i, i + R/2) taken 16 at a time with tcgen05.ld / tcgen05.st; requires
+// pairs (i, i + R/2) taken 32 at a time with tcgen05.ld / tcgen05.st; requires
 // D % 32 == 0, D <= 128 and R % 64 == 0. Rows past L hold zeros (TMA fill).
 // The angle of row 32 w + l of warp w is split as (B + l) theta_i with
 // B = start[b] + q0 + 32 w, and its cosine and sine are formed by the
@@ -554,34 +554,30 @@ __device__ bool tq_rotate_q(const TcArgs& a, uint32_t lane_base, PBars* bars,
     }
   }
   const float4* lrow = reinterpret_cast<const float4*>(stage_tab) + lane * 32;
+  // 32 pairs per round (one paired TMEM load and store, one wait each)
 #pragma unroll 1
-  for (int j = 0; j < half / 16; ++j) {
-    // (cos, sin) of (B + l) theta for pairs 16 j + 2 g, + 1 (in t[g])
-    float4 t[8];
+  for (int j = 0; j < half / 32; ++j) {
+    float x0[32], x1[32];
+    tc::tmem_ld32x2(qa + 32 * j, qa + 32 * j + half, x0, x1);
+    if (a.qnorm_w) {
+      scale(x0, 32 * j, 32);
+      scale(x1, 32 * j + half, 32);
+    }
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const int src = 8 * j + g;
+    for (int g = 0; g < 16; ++g) {
+      // (cos, sin) of (B + l) theta for pairs 32 j + 2 g, + 1
+      const int src = 16 * j + g;
       const float4 cb = __ldg(brow + src);                 // row B (the same for every lane)
       const float4 cl = lrow[src ^ lane];                  // row l (swizzled granules)
-      t[g] = make_float4(fmaf(cb.x, cl.x, -cb.y * cl.y), fmaf(cb.y, cl.x, cb.x * cl.y),
-                         fmaf(cb.z, cl.z, -cb.w * cl.w), fmaf(cb.w, cl.z, cb.z * cl.w));
+      const float4 cs = make_float4(fmaf(cb.x, cl.x, -cb.y * cl.y), fmaf(cb.y, cl.x, cb.x * cl.y),
+                                    fmaf(cb.z, cl.z, -cb.w * cl.w), fmaf(cb.w, cl.z, cb.z * cl.w));
+      const float a0 = x0[2 * g], b0 = x1[2 * g], a1 = x0[2 * g + 1], b1 = x1[2 * g + 1];
+      x0[2 * g] = fmaf(a0, cs.x, -b0 * cs.y);
+      x1[2 * g] = fmaf(a0, cs.y, b0 * cs.x);
+      x0[2 * g + 1] = fmaf(a1, cs.z, -b1 * cs.w);
+      x1[2 * g + 1] = fmaf(a1, cs.w, b1 * cs.z);
     }
-    float x0[16], x1[16];
-    tc::tmem_ld16x2(qa + 16 * j, qa + 16 * j + half, x0, x1);
-    if (a.qnorm_w) {
-      scale(x0, 16 * j, 16);
-      scale(x1, 16 * j + half, 16);
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const float4 cs = t[e];
-      const float a0 = x0[2 * e], b0 = x1[2 * e], a1 = x0[2 * e + 1], b1 = x1[2 * e + 1];
-      x0[2 * e] = fmaf(a0, cs.x, -b0 * cs.y);
-      x1[2 * e] = fmaf(a0, cs.y, b0 * cs.x);
-      x0[2 * e + 1] = fmaf(a1, cs.z, -b1 * cs.w);
-      x1[2 * e + 1] = fmaf(a1, cs.w, b1 * cs.z);
-    }
-    tc::tmem_st16x2(qa + 16 * j, qa + 16 * j + half, x0, x1);
+    tc::tmem_st32x2(qa + 32 * j, qa + 32 * j + half, x0, x1);
   }
   tc::fence_before_sync();
   tc::mbar_arrive(&bars->q_ready);
