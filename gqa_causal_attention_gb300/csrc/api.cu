@@ -213,6 +213,18 @@ int kv_cache_append(float* k, const float* v, int B, int Hkv, int L, int D,
   fin.add(k_norm_w, 1, 1, 1, D);
   const int32_t* skip = nullptr;
   if (const int rc = fin.gate(status, s, &skip)) return rc;
+  if (gqa::append_vt_supports(D) && (int64_t)B * Hkv <= 65535) {
+    // 32-row tiles through shared memory: the rotated keys go to the cache and back
+    // over k (each tile is read whole before any of it is written)
+    gqa::AppendVtJob aj{};
+    aj.k = k; aj.v = v; aj.k_cache = k_cache; aj.v_cache = v_cache; aj.kr = k; aj.vt = nullptr;
+    aj.B = B; aj.Hkv = Hkv; aj.L = L; aj.D = D; aj.R = rp ? rope_dim_of(rp, D) : D;
+    aj.table = reinterpret_cast<const float2*>(table);
+    aj.norm_w = k_norm_w; aj.norm_eps = norm_eps; aj.start = start;
+    aj.max_positions = max_positions; aj.capacity = capacity; aj.window = window;
+    aj.vt_pitch = 0; aj.status = status; aj.skip = skip;
+    return cuda_status(gqa::launch_append_vt(aj, s));
+  }
   gqa::RopeJob j{};
   j.x = k; j.B = B; j.NH = Hkv; j.L = L; j.D = D; j.R = rp ? rope_dim_of(rp, D) : D;
   j.start = start; j.max_positions = max_positions;

@@ -224,8 +224,8 @@ struct AppendVtJob {
   const float* v;
   float* k_cache;           // [B, Hkv, capacity, D]: slot = position, or position mod window
   float* v_cache;
-  float* kr;                // [B, Hkv, L, D] rotated keys, or nullptr
-  float* vt;                // [B * Hkv, D, vt_pitch]
+  float* kr;                // [B, Hkv, L, D] rotated keys (may be k itself), or nullptr
+  float* vt;                // [B * Hkv, D, vt_pitch], or nullptr
   int B, Hkv, L, D, R;
   const float2* table;      // [max_positions][R/2] (cos, sin); nullptr: no rotation
   const float* norm_w;      // [D] or nullptr

@@ -8,6 +8,8 @@
 // its cache slots, and v transposed (V^T, the K-major operand of the tensor
 // core's P V product) into the workspace. k and v themselves are only read.
 // The tensor-core prefill then reads the rotated keys straight from the cache.
+// kv_cache_append uses the same pass with the rotated keys written back over k
+// (every row of a tile is in shared memory before any is written) and no V^T.
 //
 // A block takes 32 consecutive rows of one (b, kv head): both 32 x D tiles go
 // through shared memory (rows padded to an odd number of floats so that the
@@ -77,9 +79,11 @@ __global__ void __launch_bounds__(kStepThreads) append_vt_kernel(AppendVtJob j) 
                                c) = make_float4(vr[0], vr[1], vr[2], vr[3]);
   }
   // V^T rows: 32 keys of dim d, one 128-byte store per warp
-  for (int d = warp; d < D; d += kStepThreads / 32) {
-    if (lane < rows)
-      j.vt[(static_cast<long>(bh) * D + d) * j.vt_pitch + l0 + lane] = vs[lane * S + d];
+  if (j.vt) {
+    for (int d = warp; d < D; d += kStepThreads / 32) {
+      if (lane < rows)
+        j.vt[(static_cast<long>(bh) * D + d) * j.vt_pitch + l0 + lane] = vs[lane * S + d];
+    }
   }
   // keys: RMSNorm (optional) then RoPE, one warp per row
   const int R = j.R, half = R / 2;

@@ -7,7 +7,7 @@ inputs (kv_cache_append then gqa_attn_prefill_rope): outputs within the parity b
 and rotated k bit for bit.
 Covers kv-head slices (a short last slice too), one-row chunks, two rows per chunk with a
 short last chunk, a single chunk (head rows not a whole number of 16-byte units), a window
-ring and the CUDA-core head dims."""
+ring, the CUDA-core head dims, and longer sequences with every start 0."""
 import pytest
 import torch
 
@@ -27,6 +27,10 @@ CASES = [
     (3, 7, 7, 40, 64, 64, None, False, 0, 0.0, (0, 2, 9), 64),
     (17, 2, 1, 33, 32, 32, None, True, 0, 0.0, tuple(range(17)), 64),
     (2, 2, 1, 3, 6, 6, None, False, 0, 0.0, (0, 1), 5),
+    (4, 8, 2, 200, 128, 128, ("llama3", 8.0, 1.0, 4.0, 8192), True, 0, 0.0, (0,) * 4, 256),
+    (2, 4, 2, 130, 256, 256, None, True, 64, 50.0, (0, 0), 64),
+    (2, 8, 2, 700, 128, 64, None, True, 0, 20.0, (0, 0), 700),
+    (1, 4, 1, 2100, 64, 64, ("llama3", 8.0, 1.0, 4.0, 8192), False, 0, 0.0, (0,), 2200),
 ]
 
 
