@@ -90,16 +90,18 @@ __global__ void __launch_bounds__(pow2_threads<D>(), D > 128 ? 2 : 4) append_vt_
   if (gated_off(j.skip)) return;
   float4* ks = sm4;
   float4* vs = sm4 + kStepRows * D4;
+  __shared__ float inv_row[kStepRows];                       // 1 / rms of each key row
   const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  // 32-bit tile indices (the host bounds the tile count below 2^31).
   const int tph = (j.L + kStepRows - 1) / kStepRows;        // tiles per (b, kv head)
-  const long ntiles = static_cast<long>(tph) * j.B * j.Hkv;
+  const int ntiles = tph * j.B * j.Hkv;
   auto at = [](int r, int u) { return r * D4 + (u ^ (r % SW)); };
   float4 pk[NV], pv[NV];
-  auto fetch = [&](long t) {
-    const long bh = t / tph;
-    const int l0 = static_cast<int>(t % tph) * kStepRows;
+  auto fetch = [&](int t) {
+    const int bh = t / tph;
+    const int l0 = (t - bh * tph) * kStepRows;
     const int nv = min(kStepRows, j.L - l0) * D4;
-    const long src0 = (bh * j.L + l0) * D4;                  // in 16-byte units
+    const long src0 = (static_cast<long>(bh) * j.L + l0) * D4;   // in 16-byte units
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int e = tid + i * kThreads;
@@ -113,12 +115,12 @@ __global__ void __launch_bounds__(pow2_threads<D>(), D > 128 ? 2 : 4) append_vt_
   // earlier ones would land on the same slots).
   const int first_kept = j.window > 0 ? j.L - j.window : 0;
 
-  long t = blockIdx.x;
+  int t = blockIdx.x;
   if (t < ntiles) fetch(t);
   for (; t < ntiles; t += gridDim.x) {
-    const int bh = static_cast<int>(t / tph);
+    const int bh = t / tph;
     const int b = bh / j.Hkv;
-    const int l0 = static_cast<int>(t % tph) * kStepRows;
+    const int l0 = (t - bh * tph) * kStepRows;
     const int rows = min(kStepRows, j.L - l0);
     const int nv = rows * D4;
     __syncthreads();                                         // the previous tile is written out
@@ -167,15 +169,83 @@ __global__ void __launch_bounds__(pow2_threads<D>(), D > 128 ? 2 : 4) append_vt_
         dst[3 * j.vt_pitch] = x.w;
       }
     }
-    // keys: RMSNorm (optional) then RoPE, one warp per row
-    const float* kf = reinterpret_cast<const float*>(ks);
-    for (int r = warp; r < rows; r += kThreads / 32) {
-      const int l = l0 + r;
-      float* kc = l >= first_kept ? j.k_cache + (static_cast<long>(bh) * j.capacity + slot_of(l)) * D
-                                  : nullptr;
-      float* kr = j.kr ? j.kr + (static_cast<long>(bh) * j.L + l) * D : nullptr;
-      auto x = [&](int i) { return kf[4 * at(r, i / 4) + i % 4]; };
-      rotate_key_row(j, x, D, lane, s0 + l, kc, kr);
+    // keys: RMSNorm (optional) then RoPE
+    if (j.R % 8 == 0) {
+      // 16-byte units: item k < hu rotates units k and k + hu (pairs 4k..4k+3),
+      // item k >= hu passes unit k + hu (dims past R) through the norm only.
+      const int hu = j.R / 8, ni = D4 - hu, half = j.R / 2;
+      if (j.norm_w) {
+        for (int r = warp; r < rows; r += kThreads / 32) {
+          float ss = 0.f;
+#pragma unroll
+          for (int u = lane; u < D4; u += 32) {
+            const float4 x = ks[at(r, u)];
+            ss = fmaf(x.x, x.x, fmaf(x.y, x.y, fmaf(x.z, x.z, fmaf(x.w, x.w, ss))));
+          }
+          ss = warp_sum(ss);
+          if (lane == 0) inv_row[r] = 1.0f / sqrtf(ss / static_cast<float>(D) + j.norm_eps);
+        }
+        __syncthreads();
+      }
+      const float4* w4 = reinterpret_cast<const float4*>(j.norm_w);
+      for (int idx = tid; idx < rows * ni; idx += kThreads) {
+        const int r = idx / ni, k = idx - r * ni;
+        const int l = l0 + r;
+        float4* kc = l >= first_kept ? reinterpret_cast<float4*>(
+                                           j.k_cache + (static_cast<long>(bh) * j.capacity + slot_of(l)) * D)
+                                     : nullptr;
+        float4* kr = j.kr ? reinterpret_cast<float4*>(j.kr + (static_cast<long>(bh) * j.L + l) * D)
+                          : nullptr;
+        const float inv = j.norm_w ? inv_row[r] : 1.0f;
+        if (k < hu) {
+          float4 a = ks[at(r, k)], c = ks[at(r, k + hu)];
+          if (j.norm_w) {
+            const float4 wa = __ldg(w4 + k), wc = __ldg(w4 + k + hu);
+            a = make_float4(a.x * inv * wa.x, a.y * inv * wa.y, a.z * inv * wa.z, a.w * inv * wa.w);
+            c = make_float4(c.x * inv * wc.x, c.y * inv * wc.y, c.z * inv * wc.z, c.w * inv * wc.w);
+          }
+          float4 t0 = make_float4(1.f, 0.f, 1.f, 0.f), t1 = t0;   // (cos, sin) of pairs 4k..4k+3
+          if (j.table) {
+            const float4* tb =
+                reinterpret_cast<const float4*>(j.table + static_cast<long>(s0 + l) * half + 4 * k);
+            t0 = __ldg(tb);
+            t1 = __ldg(tb + 1);
+          }
+          const float4 y0 = make_float4(fmaf(a.x, t0.x, -c.x * t0.y), fmaf(a.y, t0.z, -c.y * t0.w),
+                                        fmaf(a.z, t1.x, -c.z * t1.y), fmaf(a.w, t1.z, -c.w * t1.w));
+          const float4 y1 = make_float4(fmaf(a.x, t0.y, c.x * t0.x), fmaf(a.y, t0.w, c.y * t0.z),
+                                        fmaf(a.z, t1.y, c.z * t1.x), fmaf(a.w, t1.w, c.w * t1.z));
+          if (kc) {
+            kc[k] = y0;
+            kc[k + hu] = y1;
+          }
+          if (kr) {
+            kr[k] = y0;
+            kr[k + hu] = y1;
+          }
+        } else {
+          const int u = k + hu;
+          float4 x = ks[at(r, u)];
+          if (j.norm_w) {
+            const float4 wx = __ldg(w4 + u);
+            x = make_float4(x.x * inv * wx.x, x.y * inv * wx.y, x.z * inv * wx.z, x.w * inv * wx.w);
+          }
+          if (kc) kc[u] = x;
+          if (kr) kr[u] = x;
+        }
+      }
+    } else {
+      // one warp per row, scalar pairs
+      const float* kf = reinterpret_cast<const float*>(ks);
+      for (int r = warp; r < rows; r += kThreads / 32) {
+        const int l = l0 + r;
+        float* kc = l >= first_kept
+                        ? j.k_cache + (static_cast<long>(bh) * j.capacity + slot_of(l)) * D
+                        : nullptr;
+        float* kr = j.kr ? j.kr + (static_cast<long>(bh) * j.L + l) * D : nullptr;
+        auto x = [&](int i) { return kf[4 * at(r, i / 4) + i % 4]; };
+        rotate_key_row(j, x, D, lane, s0 + l, kc, kr);
+      }
     }
   }
 }
@@ -320,6 +390,7 @@ cudaError_t launch_pow2(const AppendVtJob& j, cudaStream_t stream) {
     grid = grid_of[dev];
   }
   const long ntiles = static_cast<long>((j.L + kStepRows - 1) / kStepRows) * j.B * j.Hkv;
+  if (ntiles + grid > 0x7fffffffL) return cudaErrorInvalidValue;   // 32-bit tile indices
   if (ntiles < grid) grid = static_cast<int>(ntiles);
   append_vt_pow2_kernel<D><<<grid, pow2_threads<D>(), smem, stream>>>(j);
   return cudaGetLastError();
