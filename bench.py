@@ -89,8 +89,8 @@ def peaks():
 NCU_PREFILL_TRAFFIC = {("llama3_8b_prefill", "fused"): 347.001088e6 + 96.9472e6,
                        ("gemma2_window", "fused"): 1915.213e6 + 244.01664e6}
 NCU_DECODE_TRAFFIC_PER_ALG_BYTE = (585.903872e6 + 4.77312e6) / 585572352.0
-# gemm_tc_kernel at the down projection's shape (T=8192, N=4096, K=14336), one launch.
-NCU_GEMM_TRAFFIC = 2100.046e6 + 122.840576e6
+# gemm_tc2_kernel (the CTA-pair projection kernel) at the down projection's shape (T=8192, N=4096, K=14336), one launch.
+NCU_GEMM_TRAFFIC = 2422.774e6 + 122.948352e6
 
 
 def measure_tf32_peak(dev):
@@ -940,8 +940,8 @@ def main():
             "roofline": {"bound": "tensor", "achieved": lt, "peak": pk["tf32_tflops"],
                          "unit": "TFLOP/s", "frac": lt / pk["tf32_tflops"],
                          "traffic": NCU_GEMM_TRAFFIC,
-                         "traffic_note": "ncu dram bytes of gemm_tc_kernel (one launch)",
-                         "kernel": "attn_linear (gemm_tc_kernel) at the down projection's "
+                         "traffic_note": "ncu dram bytes of gemm_tc2_kernel (one launch)",
+                         "kernel": "attn_linear (gemm_tc2_kernel) at the down projection's "
                                    f"shape T={blk['linear_shape']['T']} "
                                    f"N={blk['linear_shape']['N']} K={blk['linear_shape']['K']}",
                          "kernel_ms": blk["linear_ms"]},

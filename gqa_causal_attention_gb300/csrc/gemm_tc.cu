@@ -365,6 +365,268 @@ __global__ void __launch_bounds__(kGThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- CTA-pair kernel
+// Tiles of 256 rows x 256 columns on a cluster of two CTAs (one per SM). CTA r
+// of the pair holds rows 128 r .. 128 r + 127 of the tile in its tensor memory
+// and stages, per K block, its 128 X rows and weight rows 128 r .. 128 r + 127
+// of the tile's 256 (32 KB per stage, 6 stages). The even CTA issues
+// tcgen05.mma.cta_group::2 M256 N256 K8 products, which read each CTA's X rows
+// and both CTAs' weight rows from their shared memory: an SM streams 32 KB from
+// L2 per 512 tensor cycles instead of 48 KB. Both CTAs' copies complete on the
+// even CTA's `full` barrier; its commits arrive on both CTAs' `empty`,
+// `acc_full` and `drain` barriers; each epilogue warp of either CTA hands the
+// accumulator back with one arrive on the even CTA's `acc_empty`.
+constexpr int kG2M = 2 * kGBM;                  // tile rows
+constexpr int kG2NS = 6;                        // ring stages
+constexpr int kG2Stage = kGAStage + kGBHalf;    // 32 KB
+constexpr int kG2Smem = kG2NS * kG2Stage + 1024 + 512;
+
+struct G2Bars {
+  uint64_t full[kG2NS];       // even CTA: both CTAs' copies of a stage have landed
+  uint64_t empty[kG2NS];      // each CTA: the products reading a stage are done
+  uint64_t acc_full[2];       // each CTA: an accumulator is complete
+  uint64_t acc_empty[2];      // even CTA: all eight epilogue warps have read it
+  uint64_t drain;             // each CTA: every product has completed
+  uint32_t tmem_base;
+  int abort;
+};
+
+// First row of this CTA's half of m-tile m, and its batch row (head-major X).
+__device__ __forceinline__ void g2_rows(const GArgs& a, int m, uint32_t rank, int& b, int& row0) {
+  const int half = kGBM * static_cast<int>(rank & 1u);
+  if (a.batched) {
+    b = m / a.mt_per_b;
+    row0 = (m % a.mt_per_b) * kG2M + half;
+  } else {
+    b = 0;
+    row0 = m * kG2M + half;
+  }
+}
+
+__device__ void g2_producer(const GArgs& a, uint32_t rank, const CUtensorMap* ta,
+                            const CUtensorMap* tb0, const CUtensorMap* tb1,
+                            const CUtensorMap* tb2, uint8_t* ring, G2Bars* bars) {
+  volatile int* abort = &bars->abort;
+  const CUtensorMap* tb[3] = {tb0, tb1, tb2};
+  tc::tma_prefetch(ta);
+  for (int s = 0; s < a.nseg; ++s) tc::tma_prefetch(tb[s]);
+  const bool odd = rank & 1u;
+  const uint32_t lead = rank & ~1u;
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t fill_parity[kG2NS];
+  bool filled[kG2NS];
+#pragma unroll
+  for (int s = 0; s < kG2NS; ++s) filled[s] = false;
+  bool ok = true;
+  for (int x = blockIdx.x / 2; x < a.tiles && ok; x += gridDim.x / 2) {
+    const GTile t = tile_of(a, x);
+    const GSeg& sg = a.seg[t.s];
+    int b, row0;
+    g2_rows(a, t.m, rank, b, row0);
+    const CUtensorMap* tw = tb[odd ? sg.map_hi : sg.map_lo];
+    const int wrow = t.n0 + (odd ? sg.hi_off : 0);
+    for (int kb = 0; kb < a.kblocks; ++kb) {
+      if (!(ok = tc::mbar_wait(&bars->empty[stage], phase ^ 1u, abort))) break;
+      uint8_t* dst = ring + stage * kG2Stage;
+      const uint32_t full = tc::cluster_addr(tc::smem_u32(&bars->full[stage]), lead);
+      if (!odd) tc::mbar_arrive_expect_tx(&bars->full[stage], 2 * kG2Stage);
+      const int k0 = kb * kGBK;
+      if (a.batched)
+        tc::tma_load_4d_pair(dst, ta, full, k0 % a.D, row0, k0 / a.D, b);
+      else
+        tc::tma_load_3d_pair(dst, ta, full, k0, row0, 0);
+      tc::tma_load_3d_pair(dst + kGAStage, tw, full, k0, wrow, 0);
+      fill_parity[stage] = phase;
+      filled[stage] = true;
+      if (++stage == kG2NS) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  if (!ok && !odd) {
+    // Copies still in flight (both CTAs') land before the pair may exit.
+    for (int s = 0; s < kG2NS; ++s)
+      if (filled[s]) prefill::drain_wait(&bars->full[s], fill_parity[s]);
+  }
+}
+
+// The even CTA's issuing thread.
+__device__ void g2_mma(const GArgs& a, uint32_t tmem, uint8_t* ring, G2Bars* bars) {
+  volatile int* abort = &bars->abort;
+  constexpr uint32_t idesc = tc::idesc_tf32(kG2M, kGBN, false);
+  const uint64_t base = tc::sdesc_sw128(tc::smem_u32(ring), 16, 1024);
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int x = blockIdx.x / 2; x < a.tiles && ok; x += gridDim.x / 2, ++it) {
+    const uint32_t acc = it & 1u;
+    if (!(ok = tc::mbar_wait_cluster(&bars->acc_empty[acc], ((it >> 1) & 1u) ^ 1u, abort)))
+      break;
+    tc::fence_after_sync();
+    const uint32_t d = tmem + acc * kGBN;
+    for (int kb = 0; kb < a.kblocks; ++kb) {
+      if (!(ok = tc::mbar_wait_cluster(&bars->full[stage], phase, abort))) break;
+      tc::fence_after_sync();
+      const uint64_t ad = base + static_cast<uint32_t>((stage * kG2Stage) >> 4);
+      const uint64_t bd = base + static_cast<uint32_t>((stage * kG2Stage + kGAStage) >> 4);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        tc::mma_tf32_ss_pair(d, ad + ((32 * j) >> 4), bd + ((32 * j) >> 4), idesc, (kb | j) != 0);
+      tc::mma_commit_pair(&bars->empty[stage]);
+      if (++stage == kG2NS) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    if (ok) tc::mma_commit_pair(&bars->acc_full[acc]);
+  }
+  // Every product issued has completed before either CTA releases its tensor memory.
+  tc::mma_commit_pair(&bars->drain);
+  prefill::drain_wait(&bars->drain, 0);
+}
+
+__device__ void g2_epilogue(const GArgs& a, uint32_t rank, uint32_t tmem, G2Bars* bars,
+                            int quarter, int lane) {
+  volatile int* abort = &bars->abort;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+  const uint32_t lead = rank & ~1u;
+  uint32_t it = 0;
+  for (int x = blockIdx.x / 2; x < a.tiles; x += gridDim.x / 2, ++it) {
+    const uint32_t acc = it & 1u;
+    if (!tc::mbar_wait_cluster(&bars->acc_full[acc], (it >> 1) & 1u, abort)) break;
+    tc::fence_after_sync();
+    const GTile t = tile_of(a, x);
+    const GSeg& sg = a.seg[t.s];
+    int b, row0;
+    g2_rows(a, t.m, rank, b, row0);
+    const int r = row0 + quarter * 32 + lane;
+    int l;
+    long row;
+    bool valid;
+    if (a.batched) {
+      l = r;
+      valid = l < a.L;
+      row = static_cast<long>(b) * a.L + l;
+    } else {
+      row = r;
+      valid = row < a.T;
+      b = valid ? static_cast<int>(row / a.L) : 0;
+      l = valid ? static_cast<int>(row % a.L) : 0;
+    }
+    const uint32_t col = lane_base + acc * kGBN;
+    // the warp's loads of this accumulator are done: one arrive for the warp
+    auto release = [&]() {
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0)
+        tc::mbar_arrive_cluster(tc::cluster_addr(tc::smem_u32(&bars->acc_empty[acc]), lead));
+    };
+    if (sg.mode == kEpiSwiglu) {
+      for (int c = 0; c < kGBN / 2; c += 32) {
+        float gt[32], u[32];
+        __syncwarp();
+        tc::tmem_ld32(col + c, gt);
+        tc::tmem_ld32(col + kGBN / 2 + c, u);
+        if (c + 32 >= kGBN / 2) release();
+        if (valid && t.n0 + c < sg.n) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) gt[i] = silu_mul(gt[i], u[i]);
+          g_store32(a, sg, row, b, l, t.n0 + c, gt);
+        }
+      }
+    } else {
+      for (int c = 0; c < kGBN; c += 32) {
+        float v[32];
+        __syncwarp();
+        tc::tmem_ld32(col + c, v);
+        if (c + 32 >= kGBN) release();
+        const int n = t.n0 + c;
+        if (valid && n < sg.n) {
+          if (sg.mode == kEpiAdd) {
+            const float* rs = sg.res + row * sg.ldr + n;
+            if (n + 32 <= sg.n) {
+              const float4* r4 = reinterpret_cast<const float4*>(rs);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 q = r4[i];
+                v[4 * i] += q.x;
+                v[4 * i + 1] += q.y;
+                v[4 * i + 2] += q.z;
+                v[4 * i + 3] += q.w;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (n + i < sg.n) v[i] += rs[i];
+            }
+          }
+          g_store32(a, sg, row, b, l, n, v);
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tm_a,
+                    const __grid_constant__ CUtensorMap tm_b0,
+                    const __grid_constant__ CUtensorMap tm_b1,
+                    const __grid_constant__ CUtensorMap tm_b2, const GArgs a) {
+  if (gated_off(a.skip)) return;                // both CTAs of a pair read the same word
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  G2Bars* bars = reinterpret_cast<G2Bars*>(ring + kG2NS * kG2Stage);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = tc::cluster_rank();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kG2NS; ++s) {
+      tc::mbar_init(&bars->full[s], 1);
+      tc::mbar_init(&bars->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&bars->acc_full[i], 1);
+      tc::mbar_init(&bars->acc_empty[i], 8);
+    }
+    tc::mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc_pair(&bars->tmem_base, 2 * kGBN);
+    tc::tmem_relinquish_pair();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::cluster_sync();                           // both CTAs' barriers exist before any remote use
+  tc::fence_after_sync();
+  const uint32_t tmem = bars->tmem_base;
+  if (warp == 0) {
+    if (lane == 0) g2_producer(a, rank, &tm_a, &tm_b0, &tm_b1, &tm_b2, ring, bars);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && (rank & 1u) == 0) g2_mma(a, tmem, ring, bars);
+    __syncwarp();
+  } else {
+    g2_epilogue(a, rank, tmem, bars, warp % 4, lane);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && bars->abort) report(a.status, ATTN_DEV_TIMEOUT);
+  if (warp == 1) {
+    // The odd CTA's tensor memory is written by the even CTA's products.
+    if ((rank & 1u) && lane == 0) prefill::drain_wait(&bars->drain, 0);
+    __syncwarp();
+    tc::fence_after_sync();
+    tc::tmem_dealloc_pair(tmem, 2 * kGBN);
+  }
+  tc::cluster_sync();                           // neither CTA leaves while the other may use its memory
+}
+
 // rows x K fp32, K contiguous, as a 3-D map {K, rows, 1} with 32 x 128 boxes.
 bool map_rows(CUtensorMap* m, const float* base, int K, long rows) {
   auto enc = prefill::encode_fn();
@@ -393,6 +655,41 @@ bool map_heads(CUtensorMap* m, const float* base, int B, int H, int L, int D) {
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box,
              es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Clusters of two that fit on the current device at once (cached per device),
+// after setting the pair kernel's shared-memory size; -1 on a CUDA error.
+int pair_clusters() {
+  static std::mutex mu;
+  static int cached[64];
+  static bool known[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev]) {
+    if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kG2Smem) != cudaSuccess)
+      return -1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kG2Smem;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    cached[dev] = n;
+    known[dev] = true;
+  }
+  return cached[dev];
 }
 
 int g_sm_count() {
@@ -494,6 +791,34 @@ cudaError_t launch_gemm_tc(const GemmJob& j, cudaStream_t stream) {
   const bool ok = a.batched ? map_heads(&ta, j.x, static_cast<int>(j.T / j.L), j.x_heads, j.L, j.D)
                             : map_rows(&ta, j.x, j.K, j.T);
   if (!ok) return cudaErrorInvalidValue;
+  // The pair kernel, one tile per cluster of two SMs (as many clusters as fit at
+  // once, found per device); the one-SM kernel only if no such cluster can run.
+  int clusters = pair_clusters();
+  if (clusters < 0) return cudaErrorUnknown;
+  if (clusters > 0) {
+    GArgs p = a;
+    if (p.batched) {
+      p.mt_per_b = (j.L + kG2M - 1) / kG2M;
+      p.m_tiles = static_cast<int>(j.T / j.L) * p.mt_per_b;
+    } else {
+      p.m_tiles = static_cast<int>((j.T + kG2M - 1) / kG2M);
+    }
+    p.tiles = p.m_tiles * p.n_tiles;
+    if (p.tiles < clusters) clusters = p.tiles;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kGThreads);
+    cfg.dynamicSmemBytes = kG2Smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr{};
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ta, tb[0], tb[1], tb[2], p);
+  }
   const int sms = g_sm_count();
   const int grid = a.tiles < sms ? a.tiles : sms;
   gemm_tc_kernel<<<grid, kGThreads, kGSmem, stream>>>(ta, tb[0], tb[1], tb[2], a);
