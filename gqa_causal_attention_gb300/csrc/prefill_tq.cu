@@ -272,10 +272,9 @@ __device__ void tq_producer(const TcArgs& a, const CUtensorMap* tq, const CUtens
 
 // ---------------------------------------------------------------- MMA issuers (two threads)
 // S = Q K^T and O += P V^T are issued by two threads on different SM
-// sub-partitions (warps 1 and 6). Each sub-partition also runs a softmax warp,
-// and a busy neighbour slows one issuer's M128 N128 instructions to ~110
-// cycles; two issuers in parallel keep the tensor pipe at its 64-cycle rate.
-// Both walk the producer's ring order, each taking its own items and stepping
+// sub-partitions (warps 1 and 6), so that neither stream's waits (for a free S
+// buffer, for the softmax's P) hold back the other's products; measured, this
+// kept the tensor pipe busier than one issuing thread. Both walk the producer's ring order, each taking its own items and stepping
 // over the other's; P V of block X signals o_done[X % 2], so every wait on it
 // (S of block X + 2 overwrites X's P; a rescale of O in block X + 1) names a
 // phase that cannot be two behind.
