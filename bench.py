@@ -444,7 +444,7 @@ def bench_decode(w, args, dist, dev):
 
     def step():
         # one call: q and k rotated at position n_b, k and v appended, then the split-KV
-        # decode whose last block per row and head group merges the splits
+        # decode and the combine of its splits
         g.gqa_attn_decode_step(q, k, v, out, pos, maxlen - 1, kc, vc, rp, table, None, None,
                                w.norm_eps, w.window, w.softcap, 0.0, workspace=sws,
                                status=status)
@@ -465,11 +465,21 @@ def bench_decode(w, args, dist, dev):
     nbytes = 2.0 * w.Hkv * w.D * 4 * float((n + 1).sum())
     ksplit = 2 if g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, maxlen, w.window) > 16 \
         else 1
-    per_step = 2 + ksplit
+    per_step = decode_step_launches(w, maxlen)
     return {"ms": ms / steps, "ms_eager": ms_eager / steps, "kernel_ms": kern_ms, "bytes": nbytes,
             "clocks": clk.summary(),
             "launches_per_step": per_step,
             "launches": per_step * 2 * steps + ksplit * (KERNEL_ITERS + KERNEL_WARM)}
+
+
+def decode_step_launches(w, cache_len):
+    """Kernels of one gqa_attn_decode_step: the prep pass (folded into the split kernel
+    for 8 query heads per KV head at D = 128 with rotary dims 64 or 128), the split
+    pass, and the combine when there is more than one split."""
+    import gqa_causal_attention_gb300 as g
+    fused = (w.H // w.Hkv) % 8 == 0 and w.D == 128 and w.R in (64, 128)
+    multi = g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, cache_len, w.window) > 16
+    return (0 if fused else 1) + 1 + (1 if multi else 0)
 
 
 def bench_long_decode(w, args, dist, dev):
@@ -513,8 +523,7 @@ def bench_long_decode(w, args, dist, dev):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     nbytes = 2.0 * w.Hkv * w.D * 4 * w.B * sum(w.L + t + 1 for t in range(n))
-    launches = sum(3 if g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, w.L + t + 1, 0)
-                   > 16 else 2 for t in range(n))
+    launches = sum(decode_step_launches(w, w.L + t + 1) for t in range(n))
     return {"steps": n, "ms_per_step": ms / n, "us_per_token_step": 1e3 * ms / n,
             "bytes": nbytes, "gbs": nbytes / (ms * 1e-3) / 1e9, "launches": launches,
             "clocks": clk.summary()}
@@ -896,8 +905,8 @@ def main():
                                                    "prefill": wl.L, "steps": wl.decode_steps},
             "value": world * lng["gbs"], "unit": "GB/s",
             "us_per_step": lng["us_per_token_step"], "bytes_total": lng["bytes"],
-            "step": "gqa_attn_decode_step (one pass: q, k RoPE + append; split-KV decode; "
-                    "combine), 1024 steps in one CUDA graph",
+            "step": "gqa_attn_decode_step (q, k RoPE and the append folded into the split-KV "
+                    "kernel; combine), 1024 steps in one CUDA graph",
             "note": "the cache (134 MB) is about L2-sized; part of each step's reads hit L2",
             "gpu_launches": lng["launches"], "clocks": lng["clocks"]}
         line["gpu_launches"] += lng["launches"]

@@ -1099,8 +1099,18 @@ int gqa_attn_decode_step(const float* q, const float* k, const float* v, float* 
   pj.table = reinterpret_cast<const float2*>(table);
   pj.q_norm_w = q_norm_w; pj.k_norm_w = k_norm_w; pj.norm_eps = norm_eps;
   pj.status = status; pj.skip = skip;
-  if (cudaError_t e = gqa::launch_decode_prep(pj, s); e != cudaSuccess) return cuda_status(e);
   gqa::DecodeJob j{};
+  // The split kernel rotates q and appends k, v itself where it can (one launch fewer).
+  const bool fused = gqa::decode_step_fuses(H, Hkv, D, pj.R);
+  gqa::DecodeStepArgs st{};
+  if (fused) {
+    st.q_raw = q; st.k_new = k; st.v_new = v; st.pos = pos;
+    st.table = pj.table; st.R = pj.R; st.max_positions = pj.max_positions;
+    st.q_norm_w = q_norm_w; st.k_norm_w = k_norm_w; st.norm_eps = norm_eps;
+    st.cache_len = pj.cache_len;
+  } else if (cudaError_t e = gqa::launch_decode_prep(pj, s); e != cudaSuccess) {
+    return cuda_status(e);
+  }
   j.q = pj.qrot; j.k_cache = k_cache; j.v_cache = v_cache; j.cache_len = pj.cache_len;
   j.max_cache_len = max_pos + 1; j.out = out;
   j.B = B; j.H = H; j.Hkv = Hkv; j.D = D; j.capacity = capacity; j.window = window;
@@ -1110,7 +1120,7 @@ int gqa_attn_decode_step(const float* q, const float* k, const float* v, float* 
   j.skip = skip;
   gqa::decode_split_plan(B, Hkv, max_pos + 1, window, &j.nsplit, &j.chunk);
   j.partial = reinterpret_cast<float*>(ws + lay.part);
-  return cuda_status(gqa::launch_decode(j, s));
+  return cuda_status(gqa::launch_decode(j, s, fused ? &st : nullptr));
 }
 
 }  // extern "C"

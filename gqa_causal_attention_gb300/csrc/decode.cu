@@ -488,6 +488,58 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
 // warp 0 at the end.
 constexpr float kPairRescaleLog2 = 8.0f;   // O is rescaled when the max grows by > 2^8
 
+// A fused step's RMSNorm (optional) and RoPE at position p of one 128-dim row, in
+// the head-pair lane map: lane group grp holds dims 32 c + 4 grp .. + 3 (c < 4);
+// the 8 lanes of a group reduce the sum of squares together. With R = 128 or 64
+// the partner dim i + R/2 of every rotated dim i sits in the same lane (c + 2 or
+// c + 1). Every lane must call it (the reduction shuffles over the whole warp).
+__device__ __forceinline__ void pair_rotate_row(const DecodeStepArgs& j, const float* row,
+                                                const float* nw, int p, int grp, float* x) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float4 t = __ldg(reinterpret_cast<const float4*>(row + 32 * c + 4 * grp));
+    x[4 * c] = t.x; x[4 * c + 1] = t.y; x[4 * c + 2] = t.z; x[4 * c + 3] = t.w;
+  }
+  if (nw) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) ss = fmaf(x[e], x[e], ss);
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    const float inv = 1.0f / sqrtf(ss / 128.0f + j.norm_eps);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 w = __ldg(reinterpret_cast<const float4*>(nw + 32 * c + 4 * grp));
+      x[4 * c] = x[4 * c] * inv * w.x; x[4 * c + 1] = x[4 * c + 1] * inv * w.y;
+      x[4 * c + 2] = x[4 * c + 2] * inv * w.z; x[4 * c + 3] = x[4 * c + 3] * inv * w.w;
+    }
+  }
+  const int half = j.R / 2;
+  const float4* tab = reinterpret_cast<const float4*>(j.table + static_cast<long>(p) * half);
+  // dims of chunk c pair with those of chunk c2 (c2 = c + R / 64); both compile-time
+  auto rot = [&](auto cc, auto cc2) {
+    constexpr int c = decltype(cc)::value, c2 = decltype(cc2)::value;
+    const float4 t0 = __ldg(tab + (32 * c + 4 * grp) / 2), t1 = __ldg(tab + (32 * c + 4 * grp) / 2 + 1);
+    const float cs[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = x[4 * c + e], o = x[4 * c2 + e];
+      x[4 * c + e] = fmaf(a, cs[2 * e], -o * cs[2 * e + 1]);
+      x[4 * c2 + e] = fmaf(a, cs[2 * e + 1], o * cs[2 * e]);
+    }
+  };
+  using I0 = std::integral_constant<int, 0>;
+  using I1 = std::integral_constant<int, 1>;
+  using I2 = std::integral_constant<int, 2>;
+  using I3 = std::integral_constant<int, 3>;
+  if (half == 64) {
+    rot(I0{}, I2{});
+    rot(I1{}, I3{});
+  } else {
+    rot(I0{}, I1{});
+  }
+}
+
 __host__ __device__ inline uint32_t pair_ring_stride(int nst, uint32_t part_bytes) {
   const uint32_t ring = static_cast<uint32_t>(nst) * 2 * part_bytes, merge = 36u * 32 * 4;
   return ((ring > merge ? ring : merge) + 127) / 128 * 128;
@@ -496,8 +548,11 @@ __host__ __device__ inline uint32_t pair_ring_stride(int nst, uint32_t part_byte
 // NW warps per block share one split: warp w takes batches w, w + NW, ... of
 // it through its own ring, and the warps' running (max, sum, O) are merged in
 // shared memory at the end, so a split costs one partial result whatever NW is.
-template <int NW, int KP, bool D128>
-__global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int nst) {
+// FUSED (D128 only): the whole decode step (st), a separate instantiation so
+// that the plain kernel's code is not touched by the step's prologue.
+template <int NW, int KP, bool D128, bool FUSED = false>
+__global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int nst,
+                                                              DecodeStepArgs st) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_all[NW][kBulkMaxStages];
   __shared__ int abort_flag;
@@ -512,7 +567,20 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
   const int g0 = (blockIdx.y % ngroups) * 8;
   const int D = D128 ? 128 : j.D;            // D128: every lane's 16 dims are real
 
-  const int n = j.cache_len[b];
+  int n;
+  if (FUSED) {
+    const int p = st.pos[b];
+    const bool in_table = p >= 0 && p < st.max_positions;
+    const bool has_slot = j.window > 0 || p < j.capacity;
+    n = in_table && has_slot ? p + 1 : 0;
+    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) {   // one block per batch row
+      if (!in_table) report(j.status, ATTN_DEV_POSITION);
+      else if (!has_slot) report(j.status, ATTN_DEV_CAPACITY);
+      st.cache_len[b] = n;                                    // for the combine pass
+    }
+  } else {
+    n = j.cache_len[b];
+  }
   if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) {
     if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) report(j.status, ATTN_DEV_LENGTH);
     return;                                   // the whole block leaves together
@@ -523,6 +591,31 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
   if (k0 >= nlive) return;
   const int k1 = min(k0 + j.chunk, nlive);
   const int nb = (k1 - k0 + KP - 1) / KP;                 // batches of the split
+  if (FUSED && warp == 0) {
+    // The split holding the new position's slot writes its rotated k and its v
+    // there first (every group of a KV head writes the same values); the proxy
+    // fence orders those writes before this block's bulk copies read them.
+    const int p = n - 1;
+    const int slot = j.window > 0 ? p % j.window : p;
+    if (slot >= k0 && slot < k1) {
+      const long src = (long)b * j.Hkv + hkv;
+      float x[16];
+      pair_rotate_row(st, st.k_new + src * 128, st.k_norm_w, p, grp, x);
+      // a step's cache is the caller's writable cache (DecodeJob holds it read-only)
+      float* kd = const_cast<float*>(j.k_cache) + (src * j.capacity + slot) * 128;
+      float* vd = const_cast<float*>(j.v_cache) + (src * j.capacity + slot) * 128;
+      const float* vs = st.v_new + src * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d = 32 * c + 4 * grp;
+        if (pair == 0)
+          *reinterpret_cast<float4*>(kd + d) = make_float4(x[4 * c], x[4 * c + 1], x[4 * c + 2], x[4 * c + 3]);
+        else if (pair == 1)
+          *reinterpret_cast<float4*>(vd + d) = __ldg(reinterpret_cast<const float4*>(vs + d));
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+  }
   const int nbw = nb > warp ? (nb - warp + NW - 1) / NW : 0;   // this warp's: warp + NW i
 
   const long head_off = ((long)b * j.Hkv + hkv) * j.capacity * D;
@@ -563,14 +656,22 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
   uint64_t q2[2][8], o2[2][8];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const float* qr = j.q + ((long)b * j.H + hkv * G + g0 + 2 * pair + h) * D;
+    const long qrow = (long)b * j.H + hkv * G + g0 + 2 * pair + h;
+    if (FUSED) {
+      float x[16];
+      pair_rotate_row(st, st.q_raw + qrow * 128, st.q_norm_w, n - 1, grp, x);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int d = 32 * c + 4 * grp;
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (D128 || d < D) t = __ldg(reinterpret_cast<const float4*>(qr + d));
-      q2[h][2 * c] = tc::pack2(t.x * j.scale, t.y * j.scale);
-      q2[h][2 * c + 1] = tc::pack2(t.z * j.scale, t.w * j.scale);
+      for (int e = 0; e < 8; ++e) q2[h][e] = tc::pack2(x[2 * e] * j.scale, x[2 * e + 1] * j.scale);
+    } else {
+      const float* qr = j.q + qrow * D;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int d = 32 * c + 4 * grp;
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (D128 || d < D) t = __ldg(reinterpret_cast<const float4*>(qr + d));
+        q2[h][2 * c] = tc::pack2(t.x * j.scale, t.y * j.scale);
+        q2[h][2 * c + 1] = tc::pack2(t.z * j.scale, t.w * j.scale);
+      }
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) o2[h][e] = tc::pack2(0.f, 0.f);
@@ -844,7 +945,11 @@ cudaError_t launch_decode_prep(const DecodePrepJob& j, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream) {
+bool decode_step_fuses(int H, int Hkv, int D, int R) {
+  return Hkv > 0 && (H / Hkv) % 8 == 0 && D == 128 && (R == 64 || R == 128);
+}
+
+cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream, const DecodeStepArgs* step) {
   const int G = j.H / j.Hkv;
   if (G % 8 == 0 && j.D % 4 == 0 && j.D <= 128) {
     // One warp per split with a 2-stage ring of 8-key batches (16 KB at D = 128).
@@ -855,10 +960,13 @@ cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream) {
     const int nst = 2;
     const uint32_t smem = NW * pair_ring_stride(nst, KP * j.D * 4);
     const dim3 grid(j.nsplit, j.Hkv * (G / 8), j.B);
-    if (j.D == 128)
-      decode_pair_kernel<NW, KP, true><<<grid, 32 * NW, smem, stream>>>(j, nst);
+    const DecodeStepArgs none{};
+    if (step)
+      decode_pair_kernel<NW, KP, true, true><<<grid, 32 * NW, smem, stream>>>(j, nst, *step);
+    else if (j.D == 128)
+      decode_pair_kernel<NW, KP, true><<<grid, 32 * NW, smem, stream>>>(j, nst, none);
     else
-      decode_pair_kernel<NW, KP, false><<<grid, 32 * NW, smem, stream>>>(j, nst);
+      decode_pair_kernel<NW, KP, false><<<grid, 32 * NW, smem, stream>>>(j, nst, none);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || j.nsplit <= 1) return e;
     decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);

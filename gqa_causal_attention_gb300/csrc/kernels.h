@@ -135,6 +135,29 @@ struct DecodeJob {
   int32_t* status;
   const int32_t* skip = nullptr;
 };
+// (Kept at this size: the split kernels read it through references, and
+// growing it by 72 bytes measured 20 % slower on the long carried decode.)
+
+// A whole decode step in the head-pair split kernel (decode_step_fuses): q and
+// the new k, v raw, positions pos[b]; each block rotates its heads' q, the block
+// whose slots hold position pos[b] writes the rotated k and v there before
+// reading them, and one block per row writes cache_len[b] = pos[b] + 1 (0 for a
+// position without a table row or slot) for the combine. DecodeJob::q is unused.
+struct DecodeStepArgs {
+  const float* q_raw;       // [B, H, D]
+  const float* k_new;       // [B, Hkv, D]
+  const float* v_new;
+  const int32_t* pos;       // [B]
+  const float2* table;      // [max_positions][R / 2] (cos, sin)
+  const float* q_norm_w;
+  const float* k_norm_w;
+  float norm_eps;
+  int R, max_positions;
+  int32_t* cache_len;       // [B], written (DecodeJob::cache_len points here too)
+};
+// Whether a decode step of this shape runs as one split pass (+ combine) with
+// the prep fused in: 8 query heads per group, D = 128, rotary dims 64 or 128.
+bool decode_step_fuses(int H, int Hkv, int D, int R);
 
 // One decode step's prep pass (decode.cu): q RMSNorm + RoPE into qrot, k RMSNorm +
 // RoPE and v into their cache slots, cache_len[b] = pos[b] + 1 (0 for a row whose
@@ -265,6 +288,7 @@ int set_check_finite(int on);            // on < 0: query only; returns the prev
 cudaError_t launch_finite_check(const FiniteJob& j, cudaStream_t stream);
 
 void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
-cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream,
+                          const DecodeStepArgs* step = nullptr);
 
 }  // namespace gqa

@@ -108,8 +108,9 @@ def test_prefill_step_then_decode_steps_equal_one_prefill(window):
     assert_close(torch.cat(outs, dim=2), want, "prefill + decode steps")
 
 
-def test_decode_step_reports_positions_past_the_table():
-    B, H, Hkv, D, cap = 2, 8, 2, 64, 64
+@pytest.mark.parametrize("H,Hkv,D", [(8, 2, 64), (16, 2, 128)])   # prep pass; fused into the split
+def test_decode_step_reports_positions_past_the_table(H, Hkv, D):
+    B, cap = 2, 64
     rp = g.RopeParams.make(theta=1e4, max_positions=64)
     table = g.rope_table(rp, D, dev())
     q = syn.normal(3, "q", (B, H, 1, D)).to(dev())
