@@ -223,8 +223,40 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_split_kernel(DecodeJob 
 // lanes of one head; P V needs each p broadcast once.
 constexpr int kBulkMaxStages = 4;
 
-template <int GT, int NC, int KW>
-__global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
+// A fused step's RMSNorm (optional) and RoPE at position p of one 128-dim row in
+// the bulk lane map (lane l holds dims 4l .. 4l + 3): the partner of a rotated dim
+// i < R/2 is i + R/2, R/8 lanes away (R % 8 == 0). Every lane must call it.
+__device__ __forceinline__ void bulk_rotate_row(const DecodeStepArgs& st, const float* row,
+                                                const float* nw, int p, int lane, float* x) {
+  const float4 t = __ldg(reinterpret_cast<const float4*>(row) + lane);
+  x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+  if (nw) {
+    float ss = fmaf(x[0], x[0], fmaf(x[1], x[1], fmaf(x[2], x[2], x[3] * x[3])));
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / 128.0f + st.norm_eps);
+    const float4 w = __ldg(reinterpret_cast<const float4*>(nw) + lane);
+    x[0] = x[0] * inv * w.x; x[1] = x[1] * inv * w.y; x[2] = x[2] * inv * w.z; x[3] = x[3] * inv * w.w;
+  }
+  const int hl = st.R / 8;                    // lanes per half of the rotated dims
+  const bool low = lane < hl;
+  float o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) o[e] = __shfl_sync(0xffffffffu, x[e], low ? lane + hl : lane - hl);
+  if (lane < 2 * hl) {
+    const int i = 4 * (low ? lane : lane - hl);       // pairs i .. i + 3
+    const float4* tab = reinterpret_cast<const float4*>(st.table + static_cast<long>(p) * (st.R / 2) + i);
+    const float4 t0 = __ldg(tab), t1 = __ldg(tab + 1);
+    const float cs[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)                      // low: a = x, c = o; high: a = o, c = x
+      x[e] = low ? fmaf(x[e], cs[2 * e], -o[e] * cs[2 * e + 1])
+                 : fmaf(o[e], cs[2 * e + 1], x[e] * cs[2 * e]);
+  }
+}
+
+// FUSED (NC == 1, D == 128): the whole decode step (st), a separate instantiation.
+template <int GT, int NC, int KW, bool FUSED = false>
+__global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst, DecodeStepArgs st) {
   constexpr int NVAL = KW * GT;               // scores per batch
   constexpr int RL = 32 / NVAL;               // lanes holding each reduced score
   static_assert(NVAL <= 32 && 32 % NVAL == 0, "batch shape");
@@ -240,9 +272,22 @@ __global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
   const int ngroups = (G + GT - 1) / GT;
   const int hkv = blockIdx.y / ngroups;
   const int g0 = (blockIdx.y % ngroups) * GT;
-  const int D = j.D;
+  const int D = FUSED ? 128 : j.D;
 
-  const int n = j.cache_len[b];
+  int n;
+  if (FUSED) {
+    const int p = st.pos[b];
+    const bool in_table = p >= 0 && p < st.max_positions;
+    const bool has_slot = j.window > 0 || p < j.capacity;
+    n = in_table && has_slot ? p + 1 : 0;
+    if (lane == 0 && split == 0 && blockIdx.y == 0) {       // one block per batch row
+      if (!in_table) report(j.status, ATTN_DEV_POSITION);
+      else if (!has_slot) report(j.status, ATTN_DEV_CAPACITY);
+      st.cache_len[b] = n;                                   // for the combine pass
+    }
+  } else {
+    n = j.cache_len[b];
+  }
   if (n < 1 || n > j.max_cache_len || (j.window == 0 && n > j.capacity)) {
     if (lane == 0 && split == 0 && blockIdx.y == 0) report(j.status, ATTN_DEV_LENGTH);
     return;
@@ -253,6 +298,25 @@ __global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
   if (k0 >= nlive) return;
   const int k1 = min(k0 + j.chunk, nlive);
   const int nb = (k1 - k0 + KW - 1) / KW;    // batches of this block
+  if (FUSED) {
+    // The split holding the new position's slot writes its rotated k and its v
+    // there first (every head group of the KV head writes the same values); the
+    // proxy fence orders those writes before this block's bulk copies read them.
+    const int p = n - 1;
+    const int slot = j.window > 0 ? p % j.window : p;
+    if (slot >= k0 && slot < k1) {
+      const long src = (long)b * j.Hkv + hkv;
+      float x[4];
+      bulk_rotate_row(st, st.k_new + src * 128, st.k_norm_w, p, lane, x);
+      // a step's cache is the caller's writable cache (DecodeJob holds it read-only)
+      float4* kd = reinterpret_cast<float4*>(const_cast<float*>(j.k_cache) + (src * j.capacity + slot) * 128);
+      float4* vd = reinterpret_cast<float4*>(const_cast<float*>(j.v_cache) + (src * j.capacity + slot) * 128);
+      kd[lane] = make_float4(x[0], x[1], x[2], x[3]);
+      vd[lane] = __ldg(reinterpret_cast<const float4*>(st.v_new + src * 128) + lane);
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    __syncwarp();
+  }
 
   const long head_off = ((long)b * j.Hkv + hkv) * j.capacity * D;
   const float* kbase = j.k_cache + head_off;
@@ -283,7 +347,16 @@ __global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
   // Queries of the GT heads (scaled), this lane's dimensions.
   float q[GT][NV];
 #pragma unroll
-  for (int g = 0; g < GT; ++g)
+  for (int g = 0; g < GT; ++g) {
+    if (FUSED) {
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      if (g0 + g < G)                          // warp-uniform
+        bulk_rotate_row(st, st.q_raw + ((long)b * j.H + hkv * G + g0 + g) * 128, st.q_norm_w,
+                        n - 1, lane, x);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q[g][e] = x[e] * j.scale;
+      continue;
+    }
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const int d = 4 * lane + 128 * c;
@@ -293,6 +366,7 @@ __global__ void __launch_bounds__(32) decode_bulk_kernel(DecodeJob j, int nst) {
       q[g][4 * c] = t.x * j.scale; q[g][4 * c + 1] = t.y * j.scale;
       q[g][4 * c + 2] = t.z * j.scale; q[g][4 * c + 3] = t.w * j.scale;
     }
+  }
   const bool capped = j.softcap > 0.f;
   const float cap_k = capped ? 2.0f * kLog2e / j.softcap : 0.f;
   auto load_row = [&](const float* row, float* r) {
@@ -846,23 +920,30 @@ constexpr int kBulkStageBudget = 16 * 1024;   // ring bytes per block (at least 
 constexpr int kPairWarps = 1, kPairKeys = 8;   // head-pair kernel: warps per split, keys per batch
 
 template <int GT, int NC>
-static cudaError_t launch_bulk(const DecodeJob& j, dim3 grid, cudaStream_t stream) {
+static cudaError_t launch_bulk(const DecodeJob& j, dim3 grid, cudaStream_t stream,
+                               const DecodeStepArgs* step) {
   constexpr int KW = GT * kBulkKeys > 32 ? 32 / GT : kBulkKeys;
   const int stage = 2 * KW * j.D * 4;
   int nst = kBulkStageBudget / stage;
   nst = nst < 2 ? 2 : (nst > kBulkMaxStages ? kBulkMaxStages : nst);
-  decode_bulk_kernel<GT, NC, KW><<<grid, 32, nst * stage, stream>>>(j, nst);
+  if constexpr (NC == 1) {                    // a fused step has D = 128
+    if (step) {
+      decode_bulk_kernel<GT, NC, KW, true><<<grid, 32, nst * stage, stream>>>(j, nst, *step);
+      return cudaSuccess;
+    }
+  }
+  decode_bulk_kernel<GT, NC, KW><<<grid, 32, nst * stage, stream>>>(j, nst, DecodeStepArgs{});
   return cudaSuccess;
 }
 
 template <int GT>
-static cudaError_t launch_gt(const DecodeJob& j, cudaStream_t stream) {
+static cudaError_t launch_gt(const DecodeJob& j, cudaStream_t stream, const DecodeStepArgs* step) {
   const int G = j.H / j.Hkv;
   const int ngroups = (G + GT - 1) / GT;
   dim3 grid(j.nsplit, j.Hkv * ngroups, j.B);
   if (j.D % 4 == 0) {
-    cudaError_t e = j.D <= 128 ? launch_bulk<GT, 1>(j, grid, stream)
-                               : launch_bulk<GT, 2>(j, grid, stream);
+    cudaError_t e = j.D <= 128 ? launch_bulk<GT, 1>(j, grid, stream, step)
+                               : launch_bulk<GT, 2>(j, grid, stream, step);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess || j.nsplit <= 1) return e;
     decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);
@@ -946,7 +1027,10 @@ cudaError_t launch_decode_prep(const DecodePrepJob& j, cudaStream_t stream) {
 }
 
 bool decode_step_fuses(int H, int Hkv, int D, int R) {
-  return Hkv > 0 && (H / Hkv) % 8 == 0 && D == 128 && (R == 64 || R == 128);
+  if (Hkv < 1 || D != 128 || R < 8 || R > 128 || R % 8 != 0) return false;
+  // the head-pair kernel (8 heads per group) holds dims 32 c + 4 g: R = 64 or 128;
+  // the bulk kernel (other groups) holds dims 4 l .. 4 l + 3: any R % 8 == 0
+  return (H / Hkv) % 8 == 0 ? (R == 64 || R == 128) : true;
 }
 
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream, const DecodeStepArgs* step) {
@@ -972,10 +1056,10 @@ cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream, const DecodeS
     decode_combine_kernel<<<dim3(j.H, j.B), 128, 0, stream>>>(j);
     return cudaGetLastError();
   }
-  if (G == 1) return launch_gt<1>(j, stream);
-  if (G == 2) return launch_gt<2>(j, stream);
-  if (G <= 4) return launch_gt<4>(j, stream);
-  return launch_gt<8>(j, stream);
+  if (G == 1) return launch_gt<1>(j, stream, step);
+  if (G == 2) return launch_gt<2>(j, stream, step);
+  if (G <= 4) return launch_gt<4>(j, stream, step);
+  return launch_gt<8>(j, stream, step);
 }
 
 }  // namespace gqa

@@ -156,7 +156,8 @@ struct DecodeStepArgs {
   int32_t* cache_len;       // [B], written (DecodeJob::cache_len points here too)
 };
 // Whether a decode step of this shape runs as one split pass (+ combine) with
-// the prep fused in: 8 query heads per group, D = 128, rotary dims 64 or 128.
+// the prep fused in: D = 128 and rotary dims R % 8 == 0 (64 or 128 with 8 query
+// heads per KV head).
 bool decode_step_fuses(int H, int Hkv, int D, int R);
 
 // One decode step's prep pass (decode.cu): q RMSNorm + RoPE into qrot, k RMSNorm +

@@ -108,7 +108,8 @@ def test_prefill_step_then_decode_steps_equal_one_prefill(window):
     assert_close(torch.cat(outs, dim=2), want, "prefill + decode steps")
 
 
-@pytest.mark.parametrize("H,Hkv,D", [(8, 2, 64), (16, 2, 128)])   # prep pass; fused into the split
+# the prep pass (D = 64); folded into the bulk (4 heads per KV head) and head-pair splits
+@pytest.mark.parametrize("H,Hkv,D", [(8, 2, 64), (8, 2, 128), (16, 2, 128)])
 def test_decode_step_reports_positions_past_the_table(H, Hkv, D):
     B, cap = 2, 64
     rp = g.RopeParams.make(theta=1e4, max_positions=64)
