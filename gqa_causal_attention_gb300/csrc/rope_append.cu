@@ -87,7 +87,42 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
   const int D = j.D, R = j.R, half = R / 2;
   const int ntail = (D - R) / 2;
   constexpr bool append = APPEND;             // key rows: also store k and v in the cache
-  constexpr bool need_tail = TAIL;            // dims past R are read (norm or cache copy)
+  // The norm weights of this lane's dims, loaded once (every row uses the same).
+  float wlo[NP * VEC], whi[NP * VEC];
+  float2 wtl[TAIL ? 4 : 1];
+  if (j.norm_w) {
+#pragma unroll
+    for (int k = 0; k < NP; ++k) {
+      const int i = (lane + 32 * k) * VEC;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        wlo[k * VEC + e] = i < half ? __ldg(j.norm_w + i + e) : 0.f;
+        whi[k * VEC + e] = i < half ? __ldg(j.norm_w + i + half + e) : 0.f;
+      }
+    }
+    if constexpr (TAIL) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int t = lane + 32 * k;
+        wtl[k] = t < ntail ? make_float2(__ldg(j.norm_w + R + 2 * t), __ldg(j.norm_w + R + 2 * t + 1))
+                           : make_float2(0.f, 0.f);
+      }
+    }
+  }
+  // Row indices in 32 bits where they fit (the 64-bit division is a long
+  // instruction sequence, paid per row).
+  const bool narrow = rows < (1L << 31);
+  auto split_row = [&](long row, long& hrow, int& l) {
+    if (narrow) {
+      const uint32_t rr = static_cast<uint32_t>(row), L = static_cast<uint32_t>(j.L);
+      const uint32_t h = rr / L;
+      hrow = h;
+      l = static_cast<int>(rr - h * L);
+    } else {
+      hrow = row / j.L;
+      l = static_cast<int>(row - hrow * j.L);
+    }
+  };
 
   for (long row0 = gwarp * RPW; row0 < rows; row0 += warps * RPW) {
     float lo[RPW][NP * VEC], hi[RPW][NP * VEC];
@@ -101,8 +136,11 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
       live[r] = row < rows;
       pos[r] = 0;
       if (!live[r]) continue;
-      const int b = (int)(row / ((long)j.NH * j.L));
-      const int l = (int)(row % j.L);
+      long hrow;
+      int l;
+      split_row(row, hrow, l);
+      const int b = static_cast<int>(narrow ? static_cast<uint32_t>(hrow) / static_cast<uint32_t>(j.NH)
+                                            : hrow / j.NH);
       const int s0 = j.start ? j.start[b] : 0;
       // Device-side re-check of the positions the host could not see.
       if (s0 < 0 || (long)s0 + j.L - 1 >= (long)j.max_positions) {
@@ -130,9 +168,19 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
 #pragma unroll
         for (int k = 0; k < NP; ++k) {
           const int i = (lane + 32 * k) * VEC;
-          if (i < half)
+          if (i < half) {
+            if constexpr (VEC == 4) {                // two 16-byte loads (half % 4 == 0)
+              const float4 t0 = __ldg(reinterpret_cast<const float4*>(tab + i));
+              const float4 t1 = __ldg(reinterpret_cast<const float4*>(tab + i) + 1);
+              cs[r][k * 4] = make_float2(t0.x, t0.y);
+              cs[r][k * 4 + 1] = make_float2(t0.z, t0.w);
+              cs[r][k * 4 + 2] = make_float2(t1.x, t1.y);
+              cs[r][k * 4 + 3] = make_float2(t1.z, t1.w);
+            } else {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) cs[r][k * VEC + e] = tab[i + e];
+              for (int e = 0; e < VEC; ++e) cs[r][k * VEC + e] = tab[i + e];
+            }
+          }
         }
       }
       if constexpr (TAIL) {
@@ -156,7 +204,7 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
     for (int r = 0; r < RPW; ++r) {
       if (!live[r]) continue;
       const long row = row0 + r;
-      if (TAIL && j.norm_w) {
+      if (j.norm_w) {
         float ss = 0.f;
 #pragma unroll
         for (int k = 0; k < NP; ++k)
@@ -164,9 +212,11 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e)
               ss += lo[r][k * VEC + e] * lo[r][k * VEC + e] + hi[r][k * VEC + e] * hi[r][k * VEC + e];
+        if constexpr (TAIL) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (lane + 32 * k < ntail) ss += tl[r][k].x * tl[r][k].x + tl[r][k].y * tl[r][k].y;
+          for (int k = 0; k < 4; ++k)
+            if (lane + 32 * k < ntail) ss += tl[r][k].x * tl[r][k].x + tl[r][k].y * tl[r][k].y;
+        }
         ss = warp_sum(ss);
         const float inv_rms = 1.0f / sqrtf(ss / (float)D + j.norm_eps);
 #pragma unroll
@@ -175,17 +225,19 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
           if (i < half) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-              lo[r][k * VEC + e] = lo[r][k * VEC + e] * inv_rms * j.norm_w[i + e];
-              hi[r][k * VEC + e] = hi[r][k * VEC + e] * inv_rms * j.norm_w[i + half + e];
+              lo[r][k * VEC + e] = lo[r][k * VEC + e] * inv_rms * wlo[k * VEC + e];
+              hi[r][k * VEC + e] = hi[r][k * VEC + e] * inv_rms * whi[k * VEC + e];
             }
           }
         }
+        if constexpr (TAIL) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int t = lane + 32 * k;
-          if (t < ntail) {
-            tl[r][k].x = tl[r][k].x * inv_rms * j.norm_w[R + 2 * t];
-            tl[r][k].y = tl[r][k].y * inv_rms * j.norm_w[R + 2 * t + 1];
+          for (int k = 0; k < 4; ++k) {
+            const int t = lane + 32 * k;
+            if (t < ntail) {
+              tl[r][k].x = tl[r][k].x * inv_rms * wtl[k].x;
+              tl[r][k].y = tl[r][k].y * inv_rms * wtl[k].y;
+            }
           }
         }
       }
@@ -225,12 +277,13 @@ __global__ void __launch_bounds__(256) rope_rows_kernel(RopeJob j) {
       }
       // ... and, for key rows, into the cache next to the value row.
       if constexpr (APPEND) {
-        const int l = (int)(row % j.L);
+        long hrow;                                        // b * NH + head
+        int l;
+        split_row(row, hrow, l);
         // Of a chunk longer than the ring only its last W positions survive;
         // writing the earlier ones would race on the same slots.
         if (j.window > 0 && l < j.L - j.window) continue;
         const long slot = j.window > 0 ? (long)(pos[r] % j.window) : (long)pos[r];
-        const long hrow = row / j.L;                      // b * NH + head
         const long dst = (hrow * j.capacity + slot) * D;
         float* kc = j.k_cache + dst;
 #pragma unroll
@@ -281,7 +334,8 @@ cudaError_t launch_rope_rows(const RopeJob& j, cudaStream_t stream) {
   const long cap = 152L * 8;                    // one full wave of 8 blocks per SM
   if (blocks > cap) blocks = cap;
   const bool append = j.k_cache != nullptr;
-  const bool tail = append || j.norm_w != nullptr || (j.y != nullptr && j.R < j.D);
+  // dims past R read only where there are any (the norm over full rotary needs none)
+  const bool tail = append || (j.R < j.D && (j.norm_w != nullptr || j.y != nullptr));
   if (half % 4 == 0 && half >= 128)
     return launch_rows<4>(j, append, tail, blocks, stream);
   if (half % 2 == 0) return launch_rows<2>(j, append, tail, blocks, stream);
