@@ -24,6 +24,8 @@ CASES = [
     (2, 4, 2, 256, 0, 64, 64, 50.0, True, (10, 700)),               # ring, wrapped row
     (2, 4, 2, 40, 0, 0, 600, 0.0, False, (3, 599)),                 # CUDA-core head dim
     (1, 16, 2, 128, 0, 300, 300, 0.0, True, (1000,)),               # ring, 8 heads per KV head
+    (2, 32, 2, 128, 64, 0, 600, 0.0, True, (5, 599)),               # 16 heads: two groups write
+    (2, 8, 2, 128, 0, 100, 100, 0.0, False, (7, 250)),              # 4 heads, wrapped ring
 ]
 
 
