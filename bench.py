@@ -473,14 +473,11 @@ def bench_decode(w, args, dist, dev):
 
 
 def decode_step_launches(w, cache_len):
-    """Kernels of one gqa_attn_decode_step: the prep pass (folded into the split kernel
-    at D = 128 with rotary dims R % 8 == 0, R = 64 or 128 for 8 query heads per KV
-    head), the split pass, and the combine when there is more than one split."""
+    """Kernels of one gqa_attn_decode_step over cache_len positions, as the library
+    reports them: the RoPE/append pass unless the decode kernel does it, the decode
+    kernel, and the combine of a row's splits unless a cluster merges them."""
     import gqa_causal_attention_gb300 as g
-    G, R = w.H // w.Hkv, w.R
-    fused = w.D == 128 and 8 <= R <= 128 and R % 8 == 0 and (G % 8 != 0 or R in (64, 128))
-    multi = g.gqa_attn_decode_workspace_size(w.B, w.H, w.Hkv, w.D, cache_len, w.window) > 16
-    return (0 if fused else 1) + 1 + (1 if multi else 0)
+    return g.gqa_attn_decode_launches(w.B, w.H, w.Hkv, w.D, cache_len, w.window, w.R)
 
 
 def bench_long_decode(w, args, dist, dev):

@@ -32,7 +32,7 @@ __all__ = [
     "gqa_block_forward", "gqa_block_forward_workspace_size", "BLOCK_WEIGHT_NAMES",
     "attn_linear", "attn_set_check_finite", "DEV_NONFINITE",
     "gqa_attn_prefill_step", "gqa_attn_prefill_step_workspace_size",
-    "gqa_attn_decode_step", "gqa_attn_decode_step_workspace_size",
+    "gqa_attn_decode_step", "gqa_attn_decode_step_workspace_size", "gqa_attn_decode_launches",
     "gqa_attn_prefill_from_host", "gqa_attn_prefill_from_host_workspace_size",
     "attn_selftest_wait_timeout",
     "attn_status_string", "attn_version", "attn_last_cuda_error", "rope_table", "ROPE_SCALING",
@@ -152,6 +152,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                             vp, f, vp, vp, i32, i32, f, f, vp, sz, vp, vp]),
             "attn_set_check_finite": (i32, [i32]),
             "gqa_attn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+            "gqa_attn_decode_launches": (i32, [i32, i32, i32, i32, ctypes.c_int32, i32, i32]),
             "gqa_attn_decode": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32, i32,
                                       i32, i32, f, f, vp, sz, vp, vp]),
             "gqa_attn_decode_static": (i32, [vp, vp, vp, vp, ctypes.c_int32, vp, i32, i32, i32,
@@ -648,6 +649,16 @@ def gqa_attn_prefill_step(q, k, v, out, k_cache, v_cache, params: RopeParams, ta
                                       int(window), float(softcap), float(scale),
                                       _ptr(workspace), wbytes, _ptr(status), _stream(stream))
     _check("gqa_attn_prefill_step", rc)
+
+
+def gqa_attn_decode_launches(B: int, H: int, Hkv: int, D: int, max_cache_len: int,
+                             window: int = 0, step_rope_dim: int = -1) -> int:
+    """Kernels one gqa_attn_decode call (step_rope_dim < 0) or one gqa_attn_decode_step
+    call (step_rope_dim = its rope_dim, 0 meaning D; max_cache_len = max_pos + 1) launches."""
+    n = int(load().gqa_attn_decode_launches(B, H, Hkv, D, int(max_cache_len), int(window),
+                                            int(step_rope_dim)))
+    _check("gqa_attn_decode_launches", min(n, 0))
+    return n
 
 
 def gqa_attn_decode_step_workspace_size(B: int, H: int, Hkv: int, D: int, max_pos: int,

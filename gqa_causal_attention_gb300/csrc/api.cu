@@ -1024,6 +1024,20 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
   return cuda_status(gqa::launch_decode(j, s));
 }
 
+int gqa_attn_decode_launches(int B, int H, int Hkv, int D, int32_t max_cache_len, int window,
+                             int step_rope_dim) {
+  if (B < 1 || H < 1 || Hkv < 1 || H % Hkv || D < 2 || D % 2 || D > gqa::kMaxHeadDim ||
+      max_cache_len < 1 || window < 0 ||
+      (step_rope_dim >= 0 && (step_rope_dim > D || step_rope_dim % 2)))
+    return ATTN_ERR_SHAPE;
+  gqa::DecodeJob j{};
+  j.B = B; j.H = H; j.Hkv = Hkv; j.D = D; j.window = window; j.max_cache_len = max_cache_len;
+  gqa::decode_split_plan(B, Hkv, max_cache_len, window, &j.nsplit, &j.chunk);
+  if (step_rope_dim < 0) return gqa::decode_launches(j, false);
+  const bool fused = gqa::decode_step_fuses(H, Hkv, D, step_rope_dim ? step_rope_dim : D);
+  return (fused ? 0 : 1) + gqa::decode_launches(j, fused);
+}
+
 namespace {
 // Workspace of gqa_attn_decode_step: rotated q [B, H, D] | cache lengths [B] | the
 // split partials.

@@ -559,7 +559,8 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
 // lanes of its pair (3 shuffles), which then all hold it, so the running
 // maximum, the sum and P V need no further exchange.
 // Shared memory per warp: its ring, at least the 36 floats per lane it hands to
-// warp 0 at the end.
+// warp 0 at the end (which also covers warp 0's 8 D + 17 floats for a cluster
+// merge).
 constexpr float kPairRescaleLog2 = 8.0f;   // O is rescaled when the max grows by > 2^8
 
 // A fused step's RMSNorm (optional) and RoPE at position p of one 128-dim row, in
@@ -624,7 +625,11 @@ __host__ __device__ inline uint32_t pair_ring_stride(int nst, uint32_t part_byte
 // shared memory at the end, so a split costs one partial result whatever NW is.
 // FUSED (D128 only): the whole decode step (st), a separate instantiation so
 // that the plain kernel's code is not touched by the step's prologue.
-template <int NW, int KP, bool D128, bool FUSED = false>
+// CL > 1: the grid's x is one cluster of CL blocks per (row, group of 8 heads);
+// block r takes the r-th of CL equal runs of whole batches of the row's cached
+// keys, and the blocks merge their (max, sum, O) through distributed shared
+// memory and write the output themselves (no partials, no combine pass).
+template <int NW, int KP, bool D128, bool FUSED = false, int CL = 1>
 __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int nst,
                                                               DecodeStepArgs st) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -661,9 +666,18 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
   }
   const int nlive = j.window > 0 ? min(n, j.window) : n;
   const int nsplit_b = (nlive + j.chunk - 1) / j.chunk;
-  const int k0 = split * j.chunk;
-  if (k0 >= nlive) return;
-  const int k1 = min(k0 + j.chunk, nlive);
+  int k0, k1;
+  if constexpr (CL > 1) {
+    // Every block of the cluster stays to the end (the merge's barriers), also
+    // one whose run is empty.
+    const int per = (nlive + CL * KP - 1) / (CL * KP) * KP;
+    k0 = min(split * per, nlive);
+    k1 = min(k0 + per, nlive);
+  } else {
+    k0 = split * j.chunk;
+    if (k0 >= nlive) return;
+    k1 = min(k0 + j.chunk, nlive);
+  }
   const int nb = (k1 - k0 + KP - 1) / KP;                 // batches of the split
   if (FUSED && warp == 0) {
     // The split holding the new position's slot writes its rotated k and its v
@@ -865,8 +879,8 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
       }
     }
     __syncthreads();
-    if (warp > 0) return;
-    for (int w = 1; w < NW; ++w) {
+    if (CL == 1 && warp > 0) return;
+    for (int w = 1; warp == 0 && w < NW; ++w) {
       const float* ys = reinterpret_cast<const float*>(smem + w * stride) + lane * 36;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -880,6 +894,63 @@ __global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int n
         m_run[h] = M;
       }
     }
+  }
+  if constexpr (CL > 1) {
+    // Warp 0 leaves the block's (m, l, O) and its abort flag in its own ring
+    // (idle now; 8 D + 17 floats, within pair_ring_stride's merge area): O of
+    // head hh at [hh D, hh D + D), m at 8 D + hh, l at 8 D + 8 + hh, the flag at
+    // 8 D + 16. After the cluster barrier, thread t of block r merges output
+    // elements e = r 32 NW + t (+ multiples of CL 32 NW) over the CL blocks.
+    float* ex = reinterpret_cast<float*>(smem);
+    if (warp == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int hh = 2 * pair + h;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int d = 32 * c + 4 * grp;
+          if (D128 || d < D)
+            *reinterpret_cast<float4*>(ex + hh * D + d) =
+                make_float4(o[h][4 * c], o[h][4 * c + 1], o[h][4 * c + 2], o[h][4 * c + 3]);
+        }
+        if (grp == 0) {
+          ex[8 * D + hh] = m_run[h];
+          ex[8 * D + 8 + hh] = l_run[h];
+        }
+      }
+      if (lane == 0) ex[8 * D + 16] = abort_flag ? 1.f : 0.f;
+    }
+    tc::cluster_sync();                       // every block's export is written
+    const uint32_t ex_a = tc::smem_u32(ex);
+    const long orow = (long)b * j.H + hkv * G + g0;
+    for (int e = split * NW * 32 + threadIdx.x; e < 8 * D; e += CL * NW * 32) {
+      const int hh = e / D, d = e - hh * D;
+      float mv[CL], lv[CL], ov[CL];
+      float bad = 0.f;
+#pragma unroll
+      for (int r = 0; r < CL; ++r) {
+        const uint32_t base = tc::cluster_addr(ex_a, r);
+        mv[r] = tc::ld_cluster_f32(base + 4u * (8 * D + hh));
+        lv[r] = tc::ld_cluster_f32(base + 4u * (8 * D + 8 + hh));
+        ov[r] = tc::ld_cluster_f32(base + 4u * e);
+        bad += tc::ld_cluster_f32(base + 4u * (8 * D + 16));
+      }
+      float M = mv[0];
+#pragma unroll
+      for (int r = 1; r < CL; ++r) M = fmaxf(M, mv[r]);
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < CL; ++r) {
+          const float f = exp2f(mv[r] - M);   // 0 for a block without keys
+          L = fmaf(lv[r], f, L);
+          O = fmaf(ov[r], f, O);
+        }
+      }
+      if (bad == 0.f) j.out[(orow + hh) * D + d] = L > 0.f ? O / L : 0.f;
+    }
+    tc::cluster_sync();                       // no block leaves while its export is read
+    return;
   }
   if (__any_sync(0xffffffffu, timed_out) || abort_flag) return;
 
@@ -1033,8 +1104,93 @@ bool decode_step_fuses(int H, int Hkv, int D, int R) {
   return (H / Hkv) % 8 == 0 ? (R == 64 || R == 128) : true;
 }
 
+// The clustered head-pair kernel: one cluster of kPairClusterBlocks blocks of
+// 2 warps (6-key batches, 12 KB of ring per warp) per (row, group of 8 heads).
+// With 16 such warps per SM a cluster per group keeps the GPU in one wave up to
+// ~70 groups, and the merge through distributed shared memory replaces the
+// partial results and the combine launch.
+// Measured on the long carried decode (B = 8, 64 query heads over 8 KV heads):
+// 6-key batches beat 4 by 2-5 % from 1.5 k cached positions on; a third ring
+// stage was 1-2 % slower.
+constexpr int kPairClusterBlocks = 16, kPairClusterWarps = 2, kPairClusterKeys = 6,
+              kPairClusterStages = 2;
+
+template <bool FUSED>
+static cudaLaunchConfig_t pair_cluster_config(const DecodeJob& j, cudaStream_t stream,
+                                              cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(kPairClusterBlocks, j.Hkv * (j.H / j.Hkv / 8), j.B);
+  cfg.blockDim = dim3(32 * kPairClusterWarps);
+  cfg.dynamicSmemBytes =
+      kPairClusterWarps * pair_ring_stride(kPairClusterStages, kPairClusterKeys * 128 * 4);
+  cfg.stream = stream;
+  attr->id = cudaLaunchAttributeClusterDimension;
+  attr->val.clusterDim.x = kPairClusterBlocks;
+  attr->val.clusterDim.y = 1;
+  attr->val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Clusters of the clustered kernel that fit on the current device at once
+// (cached per device; 0 when clusters of that size cannot be launched).
+template <bool FUSED>
+static int pair_cluster_capacity(const DecodeJob& j) {
+  static std::mutex mu;
+  static int cached[64];
+  static bool known[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev]) {
+    auto kern = decode_pair_kernel<kPairClusterWarps, kPairClusterKeys, true, FUSED,
+                                   kPairClusterBlocks>;
+    int n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchAttribute attr{};
+      const cudaLaunchConfig_t cfg = pair_cluster_config<FUSED>(j, nullptr, &attr);
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    cached[dev] = n;
+    known[dev] = true;
+  }
+  return cached[dev];
+}
+
+template <bool FUSED>
+static cudaError_t launch_pair_cluster(const DecodeJob& j, const DecodeStepArgs& st,
+                                       cudaStream_t stream) {
+  cudaLaunchAttribute attr{};
+  const cudaLaunchConfig_t cfg = pair_cluster_config<FUSED>(j, stream, &attr);
+  return cudaLaunchKernelEx(&cfg,
+                            decode_pair_kernel<kPairClusterWarps, kPairClusterKeys, true, FUSED,
+                                               kPairClusterBlocks>,
+                            j, kPairClusterStages, st);
+}
+
+// 8 heads per group at D = 128: one cluster per group when they all fit at once.
+static bool use_pair_cluster(const DecodeJob& j, bool step) {
+  const int G = j.H / j.Hkv;
+  if (G % 8 != 0 || j.D != 128) return false;
+  const long groups = (long)j.B * j.Hkv * (G / 8);
+  return groups <= (step ? pair_cluster_capacity<true>(j) : pair_cluster_capacity<false>(j));
+}
+
+int decode_launches(const DecodeJob& j, bool step) {
+  return use_pair_cluster(j, step) ? 1 : (j.nsplit > 1 ? 2 : 1);
+}
+
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream, const DecodeStepArgs* step) {
   const int G = j.H / j.Hkv;
+  if (use_pair_cluster(j, step != nullptr))
+    return step ? launch_pair_cluster<true>(j, *step, stream)
+                : launch_pair_cluster<false>(j, DecodeStepArgs{}, stream);
   if (G % 8 == 0 && j.D % 4 == 0 && j.D <= 128) {
     // One warp per split with a 2-stage ring of 8-key batches (16 KB at D = 128).
     // Measured on the long carried decode (B = 8, 64 query heads over 8 KV heads,

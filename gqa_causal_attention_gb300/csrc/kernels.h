@@ -291,5 +291,6 @@ cudaError_t launch_finite_check(const FiniteJob& j, cudaStream_t stream);
 void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream,
                           const DecodeStepArgs* step = nullptr);
+int decode_launches(const DecodeJob& j, bool step);   // kernels launch_decode launches
 
 }  // namespace gqa

@@ -265,10 +265,17 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) 
   return r;
 }
 
-// Every thread of both CTAs (all must arrive).
+// Every thread of every CTA of the cluster (all must arrive).
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// A float from another CTA's shared memory (shared::cluster address).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
+  return v;
 }
 
 // Arrive on an mbarrier of either CTA (shared::cluster address), releasing this

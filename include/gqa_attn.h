@@ -472,8 +472,9 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
  *   pos      device int32 [B]; max_pos bounds every pos[b] (host), < max_positions
  *   workspace gqa_attn_decode_step_workspace_size bytes
  * One pass rotates q and k and stores k and v at their slots; then the
- * split-KV decode of gqa_attn_decode (and its combine kernel when a row has
- * several splits). A pos[b] outside
+ * split-KV decode of gqa_attn_decode. At D = 128 (rotary dims a multiple of 8;
+ * 64 or 128 with 8 query heads per KV head) that pass is folded into the decode
+ * kernel. A pos[b] outside
  * the table (or the capacity, without a window) sets ATTN_DEV_POSITION
  * (ATTN_DEV_CAPACITY) and ATTN_DEV_LENGTH, and the row is skipped.
  */
@@ -485,6 +486,19 @@ int gqa_attn_decode_step(const float* q, const float* k, const float* v, float* 
                          const float* k_norm_w, float norm_eps, float* k_cache, float* v_cache,
                          int capacity, int window, float softcap, float scale, void* workspace,
                          size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Kernels that one call with these sizes launches, with the non-finite check
+ * off: gqa_attn_decode (step_rope_dim < 0; max_cache_len as passed to it) or
+ * gqa_attn_decode_step (step_rope_dim = its rope_dim, 0 meaning D; max_cache_len
+ * = max_pos + 1). Between one and three: the decode kernel (split-KV, or with
+ * 8 query heads per KV head at D = 128 one cluster of blocks per head group
+ * when all groups fit on the current device at once), the combine of a row's
+ * splits, and the step's separate RoPE/append pass. Reads the current device's
+ * properties; ATTN_ERR_SHAPE for sizes no call accepts.
+ */
+int gqa_attn_decode_launches(int B, int H, int Hkv, int D, int32_t max_cache_len, int window,
+                             int step_rope_dim);
 
 /*
  * gqa_attn_decode without a caller workspace, for callers that cannot

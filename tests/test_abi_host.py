@@ -401,6 +401,17 @@ def test_static_scratch_refuses_like_the_workspace_decode():
                                       0.0, 0.0, None, None) == 0
 
 
+def test_decode_launch_count_refuses_sizes_no_call_accepts():
+    lib = g.load()
+    assert lib.gqa_attn_decode_launches(0, 8, 2, 128, 100, 0, -1) == -2     # no rows
+    assert lib.gqa_attn_decode_launches(2, 8, 3, 128, 100, 0, -1) == -2     # H % Hkv
+    assert lib.gqa_attn_decode_launches(2, 8, 2, 7, 100, 0, -1) == -2       # odd D
+    assert lib.gqa_attn_decode_launches(2, 8, 2, 128, 0, 0, -1) == -2       # no positions
+    assert lib.gqa_attn_decode_launches(2, 8, 2, 128, 100, -1, -1) == -2    # window
+    assert lib.gqa_attn_decode_launches(2, 8, 2, 64, 100, 0, 66) == -2      # rotary dims > D
+    assert lib.gqa_attn_decode_launches(2, 8, 2, 64, 100, 0, 5) == -2       # odd rotary dims
+
+
 def test_wait_timeout_selftest_needs_a_status_word():
     assert g.load().attn_selftest_wait_timeout(None, None) == -1      # ATTN_ERR_NULL
 

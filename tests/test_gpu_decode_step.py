@@ -26,6 +26,8 @@ CASES = [
     (1, 16, 2, 128, 0, 300, 300, 0.0, True, (1000,)),               # ring, 8 heads per KV head
     (2, 32, 2, 128, 64, 0, 600, 0.0, True, (5, 599)),               # 16 heads: two groups write
     (2, 8, 2, 128, 0, 100, 100, 0.0, False, (7, 250)),              # 4 heads, wrapped ring
+    # 96 groups of 8 heads: more than fit on the GPU at once as clusters
+    (12, 64, 8, 128, 64, 0, 400, 0.0, False, (3, 399, 1, 200, 64, 65, 300, 0, 128, 129, 250, 333)),
 ]
 
 
@@ -130,3 +132,40 @@ def test_decode_step_reports_positions_past_the_table(H, Hkv, D):
     assert st & g.DEV_POSITION and st & g.DEV_LENGTH
     assert bool((out[1] == 7.0).all()) and torch.isfinite(out[0]).all()
     assert bool((kc[1] == 0).all())
+
+
+def test_clustered_decode_step_reports_positions_past_the_table():
+    """8 heads per KV head with a row split several ways (the clustered kernel): a row
+    whose position is past the table is reported and left alone, the other finished."""
+    B, H, Hkv, D, cap = 2, 16, 2, 128, 200
+    rp = g.RopeParams.make(theta=1e4, max_positions=256)
+    table = g.rope_table(rp, D, dev())
+    q = syn.normal(4, "q", (B, H, 1, D)).to(dev())
+    k = syn.normal(4, "k", (B, Hkv, 1, D)).to(dev())
+    v = syn.normal(4, "v", (B, Hkv, 1, D)).to(dev())
+    kc = syn.normal(4, "kc", (B, Hkv, cap, D)).to(dev())
+    vc = syn.normal(4, "vc", (B, Hkv, cap, D)).to(dev())
+    kc1 = kc[1].clone()
+    out = torch.full_like(q, 7.0)
+    pos = torch.tensor([150, 300], dtype=torch.int32, device=dev())   # 300 >= 256: device check
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    g.gqa_attn_decode_step(q, k, v, out, pos, 150, kc, vc, rp, table, status=status)
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st & g.DEV_POSITION and st & g.DEV_LENGTH
+    assert bool((out[1] == 7.0).all()) and torch.isfinite(out[0]).all()
+    assert torch.equal(kc[1], kc1)
+
+
+def test_decode_launch_counts():
+    """The kernels a decode call and a decode step launch, as the library reports them
+    (the bench counts its launches with this)."""
+    # 8 heads per KV head at D = 128, 64 groups: one cluster per group, one kernel
+    assert g.gqa_attn_decode_launches(8, 64, 8, 128, 1536, 0, 64) == 1
+    assert g.gqa_attn_decode_launches(8, 64, 8, 128, 1536, 0) == 1
+    # 4 heads per KV head: the split kernel (RoPE/append folded in) and the combine
+    assert g.gqa_attn_decode_launches(32, 32, 8, 128, 8192, 0, 128) == 2
+    # rotary dims that the split kernel does not fold in: a separate pass first
+    assert g.gqa_attn_decode_launches(32, 32, 8, 128, 8192, 0, 4) == 3
+    # one split per row: no combine
+    assert g.gqa_attn_decode_launches(2, 8, 2, 64, 64, 0) == 1
