@@ -904,7 +904,9 @@ def main():
             "value": world * lng["gbs"], "unit": "GB/s",
             "us_per_step": lng["us_per_token_step"], "bytes_total": lng["bytes"],
             "step": "gqa_attn_decode_step (q, k RoPE and the append folded into the split-KV "
-                    "kernel; combine), 1024 steps in one CUDA graph",
+                    "kernel; one cluster per (row, KV head) merges its splits in distributed "
+                    "shared memory, or a combine pass when the groups do not fit at once), "
+                    "1024 steps in one CUDA graph",
             "note": "the cache (134 MB) is about L2-sized; part of each step's reads hit L2",
             "gpu_launches": lng["launches"], "clocks": lng["clocks"]}
         line["gpu_launches"] += lng["launches"]
