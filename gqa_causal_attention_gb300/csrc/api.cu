@@ -742,10 +742,7 @@ int gqa_attn_prefill_cached(const float* q, const float* k, const float* v, cons
 size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cache_len,
                                       int window) {
   if (B < 1 || H < 1 || Hkv < 1 || H % Hkv || D < 2 || max_cache_len < 1 || window < 0) return 0;
-  int nsplit, chunk;
-  gqa::decode_split_plan(B, Hkv, max_cache_len, window, &nsplit, &chunk);
-  if (nsplit <= 1) return 16;      // never read; a non-empty buffer keeps the rule simple
-  return (size_t)B * H * nsplit * (D + 2) * sizeof(float);
+  return gqa::decode_partial_bytes(B, H, Hkv, D, max_cache_len, window, true);
 }
 
 namespace {
@@ -1010,7 +1007,7 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
   j.status = status;
   gqa::decode_split_plan(B, Hkv, max_cache_len, window, &j.nsplit, &j.chunk);
   if (j.nsplit > 1) {
-    const size_t need = gqa_attn_decode_workspace_size(B, H, Hkv, D, max_cache_len, window);
+    const size_t need = gqa::decode_partial_bytes(B, H, Hkv, D, max_cache_len, window, false);
     if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
     if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
   }
@@ -1044,7 +1041,8 @@ namespace {
 struct DecodeStepLayout {
   size_t qrot, cl, part, total;
 };
-DecodeStepLayout decode_step_layout(int B, int H, int Hkv, int D, int max_len, int window) {
+DecodeStepLayout decode_step_layout(int B, int H, int Hkv, int D, int max_len, int window,
+                                    bool bound) {
   DecodeStepLayout y{};
   size_t p = 0;
   y.qrot = p;
@@ -1052,7 +1050,7 @@ DecodeStepLayout decode_step_layout(int B, int H, int Hkv, int D, int max_len, i
   y.cl = p;
   p += round256((size_t)B * sizeof(int32_t));
   y.part = p;
-  p += round256(gqa_attn_decode_workspace_size(B, H, Hkv, D, max_len, window));
+  p += round256(gqa::decode_partial_bytes(B, H, Hkv, D, max_len, window, bound));
   y.total = p;
   return y;
 }
@@ -1063,7 +1061,7 @@ size_t gqa_attn_decode_step_workspace_size(int B, int H, int Hkv, int D, int32_t
   if (B < 1 || H < 1 || Hkv < 1 || H % Hkv || D < 2 || D % 2 || D > gqa::kMaxHeadDim ||
       max_pos < 0 || max_pos == 0x7fffffff || window < 0)
     return 0;
-  return decode_step_layout(B, H, Hkv, D, max_pos + 1, window).total;
+  return decode_step_layout(B, H, Hkv, D, max_pos + 1, window, true).total;
 }
 
 int gqa_attn_decode_step(const float* q, const float* k, const float* v, float* out, int B,
@@ -1086,7 +1084,7 @@ int gqa_attn_decode_step(const float* q, const float* k, const float* v, float* 
     return ATTN_ERR_ALIGN;
   if (max_pos < 0 || (int64_t)max_pos >= (int64_t)max_pos_of(rp)) return ATTN_ERR_POSITION;
   if (window == 0 && max_pos >= capacity) return ATTN_ERR_CAPACITY;
-  const DecodeStepLayout lay = decode_step_layout(B, H, Hkv, D, max_pos + 1, window);
+  const DecodeStepLayout lay = decode_step_layout(B, H, Hkv, D, max_pos + 1, window, false);
   if (!workspace || workspace_bytes < lay.total) return ATTN_ERR_WORKSPACE;
   if (!aligned16(workspace)) return ATTN_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -548,6 +548,31 @@ void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nspli
   *nsplit = (eff + c - 1) / c;
 }
 
+// The plan's split count is not monotone in the length: it peaks at per_row at
+// the end of each chunk band (64 per_row, 128 per_row, ... positions) and drops
+// when the chunk grows. The largest count over every length up to
+// max_cache_len is therefore per_row once the first band is passed.
+int decode_split_bound(int B, int Hkv, int max_cache_len, int window) {
+  int nsplit, chunk;
+  decode_split_plan(B, Hkv, max_cache_len, window, &nsplit, &chunk);
+  const int eff = window > 0 ? (max_cache_len < window ? max_cache_len : window) : max_cache_len;
+  const int units = B * Hkv;
+  const int per_row = (4096 + units - 1) / units;
+  if (eff > 64 * per_row && nsplit < per_row) nsplit = per_row;
+  return nsplit;
+}
+
+size_t decode_partial_bytes(int B, int H, int Hkv, int D, int max_cache_len, int window,
+                            bool bound) {
+  int nsplit, chunk;
+  if (bound)
+    nsplit = decode_split_bound(B, Hkv, max_cache_len, window);
+  else
+    decode_split_plan(B, Hkv, max_cache_len, window, &nsplit, &chunk);
+  if (nsplit <= 1) return 16;      // never read; a non-empty buffer keeps the rule simple
+  return (size_t)B * H * nsplit * (D + 2) * sizeof(float);
+}
+
 // ---------------------------------------------------------------- head-pair split kernel
 // Groups of 8 query heads per key/value head (G % 8 == 0), D % 4 == 0, D <= 128:
 // the same split-KV reduction and the same bulk-copy ring, with a lane map that

@@ -105,7 +105,7 @@ extern "C" int gqa_attn_decode_static(const float* q, const float* k_cache,
   const int rc = gqa::decode_host_check(q, k_cache, v_cache, cache_len, max_cache_len, out, B, H,
                                         Hkv, D, capacity, window, softcap, scale);
   if (rc != ATTN_OK || B == 0) return rc;
-  const size_t need = gqa_attn_decode_workspace_size(B, H, Hkv, D, max_cache_len, window);
+  const size_t need = gqa::decode_partial_bytes(B, H, Hkv, D, max_cache_len, window, false);
   if (need == 0 || need > kStaticScratchBytes) return ATTN_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (const int r = scratch_for_current_device(&scratch); r != ATTN_OK) return r;

@@ -289,6 +289,10 @@ int set_check_finite(int on);            // on < 0: query only; returns the prev
 cudaError_t launch_finite_check(const FiniteJob& j, cudaStream_t stream);
 
 void decode_split_plan(int B, int Hkv, int max_cache_len, int window, int* nsplit, int* chunk);
+// Split partials in bytes: for exactly this max_cache_len (what a call uses), or
+// (bound) the largest over every max_cache_len up to it (what a caller allocates).
+size_t decode_partial_bytes(int B, int H, int Hkv, int D, int max_cache_len, int window,
+                            bool bound);
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream,
                           const DecodeStepArgs* step = nullptr);
 int decode_launches(const DecodeJob& j, bool step);   // kernels launch_decode launches

@@ -439,7 +439,10 @@ int gqa_attn_decode_identical(const float* q, const float* k_cache, const float*
 
 /*
  * Bytes of scratch gqa_attn_decode needs for these sizes (split-KV partial
- * results). max_cache_len bounds every cache_len[b].
+ * results). max_cache_len bounds every cache_len[b]. The size never shrinks as
+ * max_cache_len grows, so a buffer sized for the largest length serves every
+ * call with a smaller one (a call itself needs only the bytes its own split
+ * plan uses, which can be fewer).
  */
 size_t gqa_attn_decode_workspace_size(int B, int H, int Hkv, int D, int max_cache_len,
                                       int window);
@@ -470,7 +473,8 @@ int gqa_attn_decode(const float* q, const float* k_cache, const float* v_cache,
  * q, k and v are only read. q [B, H, 1, D], k, v [B, Hkv, 1, D] raw; out [B, H, 1, D];
  * caches as gqa_attn_decode (capacity > every p without a window).
  *   pos      device int32 [B]; max_pos bounds every pos[b] (host), < max_positions
- *   workspace gqa_attn_decode_step_workspace_size bytes
+ *   workspace gqa_attn_decode_step_workspace_size bytes (never shrinking as max_pos
+ *            grows: one buffer sized for the largest position serves every step)
  * One pass rotates q and k and stores k and v at their slots; then the
  * split-KV decode of gqa_attn_decode. At D = 128 (rotary dims a multiple of 8;
  * 64 or 128 with 8 query heads per KV head) that pass is folded into the decode

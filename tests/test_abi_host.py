@@ -401,6 +401,22 @@ def test_static_scratch_refuses_like_the_workspace_decode():
                                       0.0, 0.0, None, None) == 0
 
 
+def test_decode_workspace_sizes_never_shrink_as_the_length_grows():
+    """One buffer sized for the largest length must serve every shorter one: the split
+    plan's chunk grows in steps, which drops the split count, but the sizes do not."""
+    for B, H, Hkv, D, window in ((8, 64, 8, 128, 0), (1, 32, 8, 128, 0), (32, 32, 8, 128, 0),
+                                 (3, 12, 3, 96, 0), (2, 16, 2, 256, 1500)):
+        prev = prev_step = 0
+        for n in list(range(1, 9000, 7)) + [16384, 16385, 40000, 100000]:
+            size = g.gqa_attn_decode_workspace_size(B, H, Hkv, D, n, window)
+            step = g.gqa_attn_decode_step_workspace_size(B, H, Hkv, D, n - 1, window)
+            assert size >= prev and step >= prev_step, (B, H, Hkv, D, window, n)
+            prev, prev_step = size, step
+    # at the edge of a chunk band the plan's own need drops; the reported size does not
+    assert g.gqa_attn_decode_workspace_size(8, 64, 8, 128, 4097, 0) == \
+        g.gqa_attn_decode_workspace_size(8, 64, 8, 128, 4096, 0)
+
+
 def test_decode_launch_count_refuses_sizes_no_call_accepts():
     lib = g.load()
     assert lib.gqa_attn_decode_launches(0, 8, 2, 128, 100, 0, -1) == -2     # no rows
