@@ -654,8 +654,9 @@ __host__ __device__ inline uint32_t pair_ring_stride(int nst, uint32_t part_byte
 // block r takes the r-th of CL equal runs of whole batches of the row's cached
 // keys, and the blocks merge their (max, sum, O) through distributed shared
 // memory and write the output themselves (no partials, no combine pass).
+// Clustered blocks: registers for 16 warps per SM (no bound otherwise).
 template <int NW, int KP, bool D128, bool FUSED = false, int CL = 1>
-__global__ void __launch_bounds__(32 * NW) decode_pair_kernel(DecodeJob j, int nst,
+__global__ void __launch_bounds__(32 * NW, CL > 1 ? 16 / NW : 0) decode_pair_kernel(DecodeJob j, int nst,
                                                               DecodeStepArgs st) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full_all[NW][kBulkMaxStages];
@@ -1129,28 +1130,36 @@ bool decode_step_fuses(int H, int Hkv, int D, int R) {
   return (H / Hkv) % 8 == 0 ? (R == 64 || R == 128) : true;
 }
 
-// The clustered head-pair kernel: one cluster of kPairClusterBlocks blocks of
-// 2 warps (6-key batches, 12 KB of ring per warp) per (row, group of 8 heads).
-// With 16 such warps per SM a cluster per group keeps the GPU in one wave up to
-// ~70 groups, and the merge through distributed shared memory replaces the
-// partial results and the combine launch.
-// Measured on the long carried decode (B = 8, 64 query heads over 8 KV heads):
-// 6-key batches beat 4 by 2-5 % from 1.5 k cached positions on; a third ring
-// stage was 1-2 % slower.
-constexpr int kPairClusterBlocks = 16, kPairClusterWarps = 2, kPairClusterKeys = 6,
-              kPairClusterStages = 2;
+// The clustered head-pair kernel: one cluster per (row, group of 8 heads), in
+// one of two shapes, both 16 warps per SM with 2-stage rings: up to
+// kPairShortKeys live positions 8 blocks x 4 warps with 4-key batches (8 KB of
+// ring per warp; half the blocks to merge, so a shorter fixed cost), beyond that
+// 16 blocks x 2 warps with 6-key batches (12 KB per warp). With a cluster per
+// group a row's splits merge through distributed shared memory instead of
+// partial results and a combine launch; it is used when every group fits on the
+// GPU at once. Measured on the carried-decode shape (B = 8, 64 query heads over
+// 8 KV heads, graph-timed steps) at 64 / 512 / 1024 / 1536 / 2048 / 8192 cached
+// positions: 8 x 4 x 4 keys 7.8 / 12.9 / 19.0 / 26.7 / 33.3 / 106.2 us, 16 x 2 x
+// 6 keys 10.4 / 14.5 / 20.3 / 26.2 / 32.7 / 101.5 us; a third ring stage was
+// 1-2 % slower, 8 x 4 with 6-key batches did not fit one wave.
+template <int CL_, int NW_, int KP_>
+struct PairCluster {
+  static constexpr int CL = CL_, NW = NW_, KP = KP_, NST = 2;
+};
+using PairShort = PairCluster<8, 4, 4>;
+using PairLong = PairCluster<16, 2, 6>;
+constexpr int kPairShortKeys = 1280;
 
-template <bool FUSED>
+template <class P, bool FUSED>
 static cudaLaunchConfig_t pair_cluster_config(const DecodeJob& j, cudaStream_t stream,
                                               cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(kPairClusterBlocks, j.Hkv * (j.H / j.Hkv / 8), j.B);
-  cfg.blockDim = dim3(32 * kPairClusterWarps);
-  cfg.dynamicSmemBytes =
-      kPairClusterWarps * pair_ring_stride(kPairClusterStages, kPairClusterKeys * 128 * 4);
+  cfg.gridDim = dim3(P::CL, j.Hkv * (j.H / j.Hkv / 8), j.B);
+  cfg.blockDim = dim3(32 * P::NW);
+  cfg.dynamicSmemBytes = P::NW * pair_ring_stride(P::NST, P::KP * 128 * 4);
   cfg.stream = stream;
   attr->id = cudaLaunchAttributeClusterDimension;
-  attr->val.clusterDim.x = kPairClusterBlocks;
+  attr->val.clusterDim.x = P::CL;
   attr->val.clusterDim.y = 1;
   attr->val.clusterDim.z = 1;
   cfg.attrs = attr;
@@ -1158,9 +1167,9 @@ static cudaLaunchConfig_t pair_cluster_config(const DecodeJob& j, cudaStream_t s
   return cfg;
 }
 
-// Clusters of the clustered kernel that fit on the current device at once
-// (cached per device; 0 when clusters of that size cannot be launched).
-template <bool FUSED>
+// Clusters of this shape that fit on the current device at once (cached per
+// device; 0 when clusters of that size cannot be launched).
+template <class P, bool FUSED>
 static int pair_cluster_capacity(const DecodeJob& j) {
   static std::mutex mu;
   static int cached[64];
@@ -1172,13 +1181,12 @@ static int pair_cluster_capacity(const DecodeJob& j) {
   }
   std::lock_guard<std::mutex> lock(mu);
   if (!known[dev]) {
-    auto kern = decode_pair_kernel<kPairClusterWarps, kPairClusterKeys, true, FUSED,
-                                   kPairClusterBlocks>;
+    auto kern = decode_pair_kernel<P::NW, P::KP, true, FUSED, P::CL>;
     int n = 0;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess) {
       cudaLaunchAttribute attr{};
-      const cudaLaunchConfig_t cfg = pair_cluster_config<FUSED>(j, nullptr, &attr);
+      const cudaLaunchConfig_t cfg = pair_cluster_config<P, FUSED>(j, nullptr, &attr);
       if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
@@ -1188,34 +1196,48 @@ static int pair_cluster_capacity(const DecodeJob& j) {
   return cached[dev];
 }
 
-template <bool FUSED>
+template <class P, bool FUSED>
 static cudaError_t launch_pair_cluster(const DecodeJob& j, const DecodeStepArgs& st,
                                        cudaStream_t stream) {
   cudaLaunchAttribute attr{};
-  const cudaLaunchConfig_t cfg = pair_cluster_config<FUSED>(j, stream, &attr);
-  return cudaLaunchKernelEx(&cfg,
-                            decode_pair_kernel<kPairClusterWarps, kPairClusterKeys, true, FUSED,
-                                               kPairClusterBlocks>,
-                            j, kPairClusterStages, st);
+  const cudaLaunchConfig_t cfg = pair_cluster_config<P, FUSED>(j, stream, &attr);
+  return cudaLaunchKernelEx(&cfg, decode_pair_kernel<P::NW, P::KP, true, FUSED, P::CL>, j,
+                            P::NST, st);
 }
 
-// 8 heads per group at D = 128: one cluster per group when they all fit at once.
-static bool use_pair_cluster(const DecodeJob& j, bool step) {
+// 8 heads per group at D = 128 and every group fitting at once: 1 for the short
+// shape, 2 for the long one; 0 otherwise.
+static int pair_cluster_kind(const DecodeJob& j, bool step) {
   const int G = j.H / j.Hkv;
-  if (G % 8 != 0 || j.D != 128) return false;
+  if (G % 8 != 0 || j.D != 128) return 0;
   const long groups = (long)j.B * j.Hkv * (G / 8);
-  return groups <= (step ? pair_cluster_capacity<true>(j) : pair_cluster_capacity<false>(j));
+  const int eff = j.window > 0 ? min(j.max_cache_len, j.window) : j.max_cache_len;
+  if (eff <= kPairShortKeys &&
+      groups <= (step ? pair_cluster_capacity<PairShort, true>(j)
+                      : pair_cluster_capacity<PairShort, false>(j)))
+    return 1;
+  if (groups <= (step ? pair_cluster_capacity<PairLong, true>(j)
+                      : pair_cluster_capacity<PairLong, false>(j)))
+    return 2;
+  return 0;
 }
 
 int decode_launches(const DecodeJob& j, bool step) {
-  return use_pair_cluster(j, step) ? 1 : (j.nsplit > 1 ? 2 : 1);
+  return pair_cluster_kind(j, step) ? 1 : (j.nsplit > 1 ? 2 : 1);
 }
 
 cudaError_t launch_decode(const DecodeJob& j, cudaStream_t stream, const DecodeStepArgs* step) {
   const int G = j.H / j.Hkv;
-  if (use_pair_cluster(j, step != nullptr))
-    return step ? launch_pair_cluster<true>(j, *step, stream)
-                : launch_pair_cluster<false>(j, DecodeStepArgs{}, stream);
+  switch (pair_cluster_kind(j, step != nullptr)) {
+    case 1:
+      return step ? launch_pair_cluster<PairShort, true>(j, *step, stream)
+                  : launch_pair_cluster<PairShort, false>(j, DecodeStepArgs{}, stream);
+    case 2:
+      return step ? launch_pair_cluster<PairLong, true>(j, *step, stream)
+                  : launch_pair_cluster<PairLong, false>(j, DecodeStepArgs{}, stream);
+    default:
+      break;
+  }
   if (G % 8 == 0 && j.D % 4 == 0 && j.D <= 128) {
     // One warp per split with a 2-stage ring of 8-key batches (16 KB at D = 128).
     // Measured on the long carried decode (B = 8, 64 query heads over 8 KV heads,
