@@ -26,6 +26,7 @@ CASES = [
     (1, 16, 2, 128, 0, 300, 300, 0.0, True, (1000,)),               # ring, 8 heads per KV head
     (2, 32, 2, 128, 64, 0, 600, 0.0, True, (5, 599)),               # 16 heads: two groups write
     (2, 8, 2, 128, 0, 100, 100, 0.0, False, (7, 250)),              # 4 heads, wrapped ring
+    (2, 32, 4, 128, 64, 0, 900, 50.0, True, (5, 899)),              # 8 heads, softcap, norms
     # 96 groups of 8 heads: more than fit on the GPU at once as clusters
     (12, 64, 8, 128, 64, 0, 400, 0.0, False, (3, 399, 1, 200, 64, 65, 300, 0, 128, 129, 250, 333)),
 ]

@@ -213,6 +213,9 @@ DECODE_CASES = [
     (2, 16, 2, 64, 256, 256, 30.0, (1000, 3)),
     (3, 32, 2, 128, 600, 0, 0.0, (600, 1, 65)),
     (2, 64, 8, 128, 3000, 0, 0.0, (2999, 1400)),              # past 1280 positions
+    (2, 64, 8, 128, 1500, 0, 30.0, (1500, 700)),              # softcap, 16-block clusters
+    (2, 64, 8, 128, 1000, 0, 30.0, (1000, 300)),              # softcap, 8-block clusters
+    (2, 16, 2, 128, 2000, 2000, 0.0, (3000, 1500)),           # wrapped ring past 1280 slots
     (2, 8, 1, 40, 90, 0, 0.0, (90, 9)),
     # 96 groups of 8 heads (more than fit at once as clusters: the one-warp splits)
     (12, 64, 8, 128, 300, 0, 0.0, (300, 1, 129, 64, 65, 200, 2, 299, 150, 100, 33, 257)),
