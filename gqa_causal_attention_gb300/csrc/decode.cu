@@ -1171,29 +1171,21 @@ static cudaLaunchConfig_t pair_cluster_config(const DecodeJob& j, cudaStream_t s
 // device; 0 when clusters of that size cannot be launched).
 template <class P, bool FUSED>
 static int pair_cluster_capacity(const DecodeJob& j) {
-  static std::mutex mu;
-  static int cached[64];
-  static bool known[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    cudaGetLastError();
-    return 0;
-  }
-  std::lock_guard<std::mutex> lock(mu);
-  if (!known[dev]) {
-    auto kern = decode_pair_kernel<P::NW, P::KP, true, FUSED, P::CL>;
-    int n = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-        cudaSuccess) {
-      cudaLaunchAttribute attr{};
-      const cudaLaunchConfig_t cfg = pair_cluster_config<P, FUSED>(j, nullptr, &attr);
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
-    }
-    cudaGetLastError();
-    cached[dev] = n;
-    known[dev] = true;
-  }
-  return cached[dev];
+  static PerContext<int> cache;           // the cluster-size permission is per context
+  return cache.get(
+      [&j] {
+        auto kern = decode_pair_kernel<P::NW, P::KP, true, FUSED, P::CL>;
+        int n = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess) {
+          cudaLaunchAttribute attr{};
+          const cudaLaunchConfig_t cfg = pair_cluster_config<P, FUSED>(j, nullptr, &attr);
+          if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+        }
+        cudaGetLastError();
+        return n;
+      },
+      0);
 }
 
 template <class P, bool FUSED>

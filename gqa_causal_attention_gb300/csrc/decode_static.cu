@@ -24,24 +24,9 @@
 #include "../../include/gqa_attn.h"
 #include "kernels.h"
 
-namespace {
-
-constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // GQA_ATTN_STATIC_SCRATCH_BYTES
-static_assert(kStaticScratchBytes == GQA_ATTN_STATIC_SCRATCH_BYTES, "header and array agree");
-
-__device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
-
-struct Entry {
-  unsigned long long ctx_id;   // process-unique id of the context the address belongs to
-  void* addr;
-};
-
-std::mutex g_mutex;
-std::map<int, Entry> g_scratch;   // device ordinal -> address in its current context
-
 // Process-unique id of the calling thread's current context, or 0 when the
-// driver does not offer the query (then the address is looked up every call).
-unsigned long long current_context_id() {
+// driver does not offer the query or no context is current.
+unsigned long long gqa::current_context_id() {
   static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
   static PFN_cuCtxGetId_v12000 get_id = nullptr;
   static std::once_flag once;
@@ -66,6 +51,21 @@ unsigned long long current_context_id() {
   return id;
 }
 
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // GQA_ATTN_STATIC_SCRATCH_BYTES
+static_assert(kStaticScratchBytes == GQA_ATTN_STATIC_SCRATCH_BYTES, "header and array agree");
+
+__device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+struct Entry {
+  unsigned long long ctx_id;   // process-unique id of the context the address belongs to
+  void* addr;
+};
+
+std::mutex g_mutex;
+std::map<int, Entry> g_scratch;   // device ordinal -> address in its current context
+
 // Device address of g_decode_scratch on the current device: looked up on the
 // first call in the device's current context, then reused.
 int scratch_for_current_device(void** out) {
@@ -76,7 +76,7 @@ int scratch_for_current_device(void** out) {
   }
   // Before the runtime's first use on this device no context is current (id 0);
   // the symbol lookup below creates it, and the id is read again after it.
-  unsigned long long id = current_context_id();
+  unsigned long long id = gqa::current_context_id();
   std::lock_guard<std::mutex> lock(g_mutex);
   auto it = g_scratch.find(dev);
   if (id != 0 && it != g_scratch.end() && it->second.ctx_id == id) {
@@ -88,7 +88,7 @@ int scratch_for_current_device(void** out) {
     cudaGetLastError();
     return gqa::record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
   }
-  if (id == 0) id = current_context_id();   // the lookup has made the context current
+  if (id == 0) id = gqa::current_context_id();   // the lookup has made the context current
   if (id != 0) g_scratch[dev] = Entry{id, p};
   *out = p;
   return ATTN_OK;

@@ -657,39 +657,36 @@ bool map_heads(CUtensorMap* m, const float* base, int B, int H, int L, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Clusters of two that fit on the current device at once (cached per device),
-// after setting the pair kernel's shared-memory size; -1 on a CUDA error.
+// Clusters of two that fit on the current device at once (per device and
+// context), after setting the pair kernel's shared-memory size; -1 on a CUDA error.
 int pair_clusters() {
-  static std::mutex mu;
-  static int cached[64];
-  static bool known[64] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!known[dev]) {
-    if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kG2Smem) != cudaSuccess)
-      return -1;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2);
-    cfg.blockDim = dim3(kGThreads);
-    cfg.dynamicSmemBytes = kG2Smem;
-    cudaLaunchAttribute attr{};
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = 2;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) != cudaSuccess) {
-      cudaGetLastError();
-      n = 0;
-    }
-    cached[dev] = n;
-    known[dev] = true;
-  }
-  return cached[dev];
+  static PerContext<int> cache;
+  return cache.get(
+      [] {
+        if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kG2Smem) != cudaSuccess) {
+          cudaGetLastError();
+          return -1;
+        }
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kGThreads);
+        cfg.dynamicSmemBytes = kG2Smem;
+        cudaLaunchAttribute attr{};
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) != cudaSuccess) {
+          cudaGetLastError();
+          n = 0;
+        }
+        return n;
+      },
+      -1, [](int n) { return n >= 0; });
 }
 
 int g_sm_count() {
@@ -720,21 +717,15 @@ bool gemm_tc_supports(const GemmJob& j) {
 
 cudaError_t launch_gemm_tc(const GemmJob& j, cudaStream_t stream) {
   if (!gemm_tc_supports(j)) return cudaErrorInvalidValue;
-  static std::mutex mu;
-  static bool attr_done[64] = {};
-  {
-    int dev = 0;
-    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!attr_done[dev]) {
-      if (cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
-          e != cudaSuccess)
-        return e;
-      attr_done[dev] = true;
-    }
-  }
+  static PerContext<cudaError_t> attr;
+  if (const cudaError_t e = attr.get(
+          [] {
+            return cudaFuncSetAttribute(gemm_tc_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
+          },
+          cudaErrorInvalidDevice, [](cudaError_t r) { return r == cudaSuccess; });
+      e != cudaSuccess)
+    return e;
   GArgs a{};
   a.T = static_cast<int>(j.T);
   a.K = j.K;

@@ -26,26 +26,37 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int kMaxChunks = 16;
 
-std::mutex g_mutex;
-cudaStream_t g_copy[kMaxDevices][2] = {};   // [device][0: host->device, 1: device->host]
+// The two copy streams of a device ([0] host to device, [1] device to host), made
+// by the first call in the device's current context (streams belong to it).
+struct CopyStreams {
+  cudaStream_t s[2];
+  cudaError_t err;
+};
+gqa::PerContext<CopyStreams> g_copy;
 
 int copy_streams(cudaStream_t* h2d, cudaStream_t* d2h) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return gqa::record_cuda_error(e);
   if (dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  for (int i = 0; i < 2; ++i) {
-    if (!g_copy[dev][i]) {
-      e = cudaStreamCreateWithFlags(&g_copy[dev][i], cudaStreamNonBlocking);
-      if (e != cudaSuccess) {
-        g_copy[dev][i] = nullptr;
-        return gqa::record_cuda_error(e);
-      }
-    }
-  }
-  *h2d = g_copy[dev][0];
-  *d2h = g_copy[dev][1];
+  const CopyStreams cs = g_copy.get(
+      [] {
+        CopyStreams c{};
+        for (int i = 0; i < 2 && c.err == cudaSuccess; ++i)
+          c.err = cudaStreamCreateWithFlags(&c.s[i], cudaStreamNonBlocking);
+        if (c.err != cudaSuccess) {
+          // nothing half made is kept: the next call tries again in a clean state
+          for (int i = 0; i < 2; ++i)
+            if (c.s[i]) cudaStreamDestroy(c.s[i]);
+          c.s[0] = c.s[1] = nullptr;
+        }
+        return c;
+      },
+      CopyStreams{}, [](const CopyStreams& c) { return c.err == cudaSuccess; });
+  if (cs.err != cudaSuccess) return gqa::record_cuda_error(cs.err);
+  if (!cs.s[0] || !cs.s[1]) return ATTN_ERR_CUDA;
+  *h2d = cs.s[0];
+  *d2h = cs.s[1];
   return ATTN_OK;
 }
 

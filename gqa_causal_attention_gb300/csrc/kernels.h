@@ -6,7 +6,54 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace gqa {
+
+// Process-unique id of the calling thread's current CUDA context; 0 when the
+// driver does not offer the query or no context is current yet.
+unsigned long long current_context_id();
+
+// A value worked out once per device and context. Function attributes set with
+// cudaFuncSetAttribute, occupancy answers and streams belong to a device's
+// context: another device, or the context created again after cudaDeviceReset,
+// works them out again. (Without the context query the value is kept per
+// device.) compute() runs with the device current; a value that keep() turns
+// down is returned but not kept (the next call computes again); on_error is
+// returned when the current device cannot be read.
+template <class T>
+class PerContext {
+ public:
+  template <class F, class K>
+  T get(F compute, T on_error, K keep) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kSlots) {
+      cudaGetLastError();
+      return on_error;
+    }
+    const unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!known_[dev] || (id != 0 && id != ctx_[dev])) {
+      const T v = compute();
+      if (!keep(v)) return v;
+      value_[dev] = v;
+      ctx_[dev] = id != 0 ? id : current_context_id();   // compute() may have made it
+      known_[dev] = true;
+    }
+    return value_[dev];
+  }
+  template <class F>
+  T get(F compute, T on_error) {
+    return get(compute, on_error, [](const T&) { return true; });
+  }
+
+ private:
+  static constexpr int kSlots = 64;
+  std::mutex mu_;
+  unsigned long long ctx_[kSlots] = {};
+  T value_[kSlots] = {};
+  bool known_[kSlots] = {};
+};
 
 constexpr int kMaxHeadDim = 256;
 constexpr int kMaxRopeHalf = kMaxHeadDim / 2;

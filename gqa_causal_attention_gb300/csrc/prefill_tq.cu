@@ -917,12 +917,14 @@ int sm_count() {
 template <int DP, bool ROPE, bool RAGGED>
 cudaError_t launch_tq(const AttnShape& s, cudaStream_t stream) {
   using C = PCfg<DP, RAGGED>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tq_kernel<DP, ROPE, RAGGED>,
+  // The shared-memory allowance is a function attribute of each device's context.
+  static PerContext<cudaError_t> attr;
+  const cudaError_t attr_err = attr.get(
+      [] {
+        return cudaFuncSetAttribute(prefill_tq_kernel<DP, ROPE, RAGGED>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-  });
+      },
+      cudaErrorInvalidDevice, [](cudaError_t e) { return e == cudaSuccess; });
   if (attr_err != cudaSuccess) return attr_err;
   const int Lk = s.Lk > 0 ? s.Lk : s.L;
   CUtensorMap tq, tk, tv, to;

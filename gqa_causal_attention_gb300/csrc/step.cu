@@ -359,36 +359,32 @@ namespace {
 
 template <int D>
 cudaError_t launch_pow2(const AppendVtJob& j, cudaStream_t stream) {
-  // Per device: the dynamic shared memory allowed once, and the grid of one
-  // wave (SMs x resident blocks).
-  static std::mutex mu;
-  static int grid_of[64] = {};
+  // Per device and context: the dynamic shared memory allowed, and the grid of
+  // one wave (SMs x resident blocks); a CUDA error as its negative code.
   constexpr int smem = 2 * kStepRows * D * static_cast<int>(sizeof(float));
-  int dev = 0;
-  if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  int grid = 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (grid_of[dev] == 0) {
-      if (smem > 48 * 1024) {
-        if (cudaError_t e = cudaFuncSetAttribute(append_vt_pow2_kernel<D>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerContext<int> wave;
+  int grid = wave.get(
+      [] {
+        if (smem > 48 * 1024) {
+          if (cudaError_t e = cudaFuncSetAttribute(append_vt_pow2_kernel<D>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   smem);
+              e != cudaSuccess)
+            return -static_cast<int>(e);
+        }
+        int dev = 0, sms = 0, per_sm = 0;
+        if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return -static_cast<int>(e);
+        if (cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             e != cudaSuccess)
-          return e;
-      }
-      int sms = 0, per_sm = 0;
-      if (cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-          e != cudaSuccess)
-        return e;
-      if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-              &per_sm, append_vt_pow2_kernel<D>, pow2_threads<D>(), smem);
-          e != cudaSuccess)
-        return e;
-      grid_of[dev] = sms * (per_sm > 0 ? per_sm : 1);
-    }
-    grid = grid_of[dev];
-  }
+          return -static_cast<int>(e);
+        if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm, append_vt_pow2_kernel<D>, pow2_threads<D>(), smem);
+            e != cudaSuccess)
+          return -static_cast<int>(e);
+        return sms * (per_sm > 0 ? per_sm : 1);
+      },
+      -static_cast<int>(cudaErrorInvalidDevice), [](int g) { return g > 0; });
+  if (grid <= 0) return static_cast<cudaError_t>(-grid);
   const long ntiles = static_cast<long>((j.L + kStepRows - 1) / kStepRows) * j.B * j.Hkv;
   if (ntiles + grid > 0x7fffffffL) return cudaErrorInvalidValue;   // 32-bit tile indices
   if (ntiles < grid) grid = static_cast<int>(ntiles);
@@ -400,21 +396,17 @@ cudaError_t launch_any(const AppendVtJob& j, cudaStream_t stream) {
   if (static_cast<long>(j.B) * j.Hkv > 65535) return cudaErrorInvalidValue;
   const int smem = 2 * kStepRows * (j.D + 1) * static_cast<int>(sizeof(float));
   if (smem > 48 * 1024) {
-    // the larger dynamic shared memory is allowed once per device
-    static std::mutex mu;
-    static bool done[64] = {};
-    int dev = 0;
-    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done[dev]) {
-      if (cudaError_t e = cudaFuncSetAttribute(append_vt_any_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               2 * kStepRows * (kMaxHeadDim + 1) * 4);
-          e != cudaSuccess)
-        return e;
-      done[dev] = true;
-    }
+    // the larger dynamic shared memory is allowed once per device and context
+    static PerContext<cudaError_t> attr;
+    if (const cudaError_t e = attr.get(
+            [] {
+              return cudaFuncSetAttribute(append_vt_any_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          2 * kStepRows * (kMaxHeadDim + 1) * 4);
+            },
+            cudaErrorInvalidDevice, [](cudaError_t r) { return r == cudaSuccess; });
+        e != cudaSuccess)
+      return e;
   }
   const dim3 grid((j.L + kStepRows - 1) / kStepRows, j.B * j.Hkv);
   append_vt_any_kernel<<<grid, kStepThreads, smem, stream>>>(j);

@@ -16,7 +16,10 @@
  *   caller, except the host buffers of gqa_attn_prefill_from_host. No call
  *   allocates or frees device memory; the only device memory the library keeps
  *   is the fixed scratch array of gqa_attn_decode_static, and the only other
- *   state is the pair of copy streams per device of gqa_attn_prefill_from_host.
+ *   state is the pair of copy streams per device of gqa_attn_prefill_from_host
+ *   and, per device and context, the kernels' function attributes (shared
+ *   memory sizes, cluster sizes) set on first use with the occupancy figures
+ *   worked out then; a new context (after cudaDeviceReset) sets them again.
  *   Tensor pointers must be 16-byte aligned (ATTN_ERR_ALIGN otherwise).
  * - Shapes: Q and outputs [B, H, L, D]; K and V [B, Hkv, L, D]; caches
  *   [B, Hkv, capacity, D]. H % Hkv == 0; query head h reads key/value head
@@ -257,7 +260,8 @@ int gqa_attn_prefill_step(const float* q, const float* k, const float* v, float*
  * host-to-device copies run on one library-owned stream, its kernels on `stream`
  * and its device-to-host copy on another library-owned stream, so copies and
  * kernels of different chunks overlap. The two copy streams of a device are created by the
- * first call on it (with that device current) and kept until exit. The call
+ * first call on it (with that device current) and kept for that device's context (made
+ * again after cudaDeviceReset). The call
  * returns once everything is enqueued; `stream` passes the call only after the
  * last copy to out_host. All checks run before anything is enqueued.
  */
