@@ -767,6 +767,10 @@ __global__ void __launch_bounds__(32 * NW, CL > 1 ? 16 / NW : 0) decode_pair_ker
     }
   };
   // q (pre-scaled) and O as pairs of adjacent dims: one paired FMA serves two.
+  // Scores come out in log2 units: q carries scale * log2(e), and the softcap
+  // runs on the scaled score with the cap scaled alike (L c tanh(s / c) =
+  // (L c) tanh(L s / (L c)), L = log2 e).
+  const float qscale = j.scale * kLog2e;
   uint64_t q2[2][8], o2[2][8];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -775,7 +779,7 @@ __global__ void __launch_bounds__(32 * NW, CL > 1 ? 16 / NW : 0) decode_pair_ker
       float x[16];
       pair_rotate_row(st, st.q_raw + qrow * 128, st.q_norm_w, n - 1, grp, x);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) q2[h][e] = tc::pack2(x[2 * e] * j.scale, x[2 * e + 1] * j.scale);
+      for (int e = 0; e < 8; ++e) q2[h][e] = tc::pack2(x[2 * e] * qscale, x[2 * e + 1] * qscale);
     } else {
       const float* qr = j.q + qrow * D;
 #pragma unroll
@@ -783,15 +787,16 @@ __global__ void __launch_bounds__(32 * NW, CL > 1 ? 16 / NW : 0) decode_pair_ker
         const int d = 32 * c + 4 * grp;
         float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
         if (D128 || d < D) t = __ldg(reinterpret_cast<const float4*>(qr + d));
-        q2[h][2 * c] = tc::pack2(t.x * j.scale, t.y * j.scale);
-        q2[h][2 * c + 1] = tc::pack2(t.z * j.scale, t.w * j.scale);
+        q2[h][2 * c] = tc::pack2(t.x * qscale, t.y * qscale);
+        q2[h][2 * c + 1] = tc::pack2(t.z * qscale, t.w * qscale);
       }
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) o2[h][e] = tc::pack2(0.f, 0.f);
   }
   const bool capped = j.softcap > 0.f;
-  const float cap_k = capped ? 2.0f * kLog2e / j.softcap : 0.f;
+  const float cap_l2 = j.softcap * kLog2e;                  // the cap in log2 units
+  const float cap_k = capped ? 2.0f / j.softcap : 0.f;      // 2 log2(e) / cap_l2
   // Weights are taken against a reference maximum m_run (log2 units) that moves
   // only when a score exceeds it by more than 2^kPairRescaleLog2; O and l are
   // rescaled then. A weight is therefore at most 2^kPairRescaleLog2, and most
@@ -825,9 +830,21 @@ __global__ void __launch_bounds__(32 * NW, CL > 1 ? 16 / NW : 0) decode_pair_ker
           float sum = a0 + a1;
 #pragma unroll
           for (int off = 1; off < 8; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-          if (capped) sum = softcap_apply(sum, j.softcap, cap_k);
-          sc[h][u] = FULL || u < valid ? sum * kLog2e : -INFINITY;
+          sc[h][u] = sum;
         }
+      }
+      if (capped) {                           // one branch per batch
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int u = 0; u < KP; ++u) sc[h][u] = softcap_apply(sc[h][u], cap_l2, cap_k);
+      }
+      if (!FULL) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int u = 0; u < KP; ++u)
+            if (u >= valid) sc[h][u] = -INFINITY;
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
